@@ -1,0 +1,387 @@
+"""Plain, slow, fp64 CPU statement of one DSpark draft-head round.
+
+TEST INFRASTRUCTURE.  This oracle exists to check the CUDA path.  Only tests/,
+__graft_entry__.smoke() and bench.py's CPU-baseline leg may import or call it;
+the product path never does, and it shares no code with the CUDA library.
+
+Pages followed (by title and section):
+  [DD]  "大模型推理的'免费加速'还能怎么卷？DSpark 深度解读" (zhichai.net)
+        §二 设计一: Markov head  B(x_{k-1},.) = W1[x_{k-1}] W2, W1: V x r, W2: r x V
+        §二 设计二: confidence head c_k = sigmoid(w^T [h_k; W1[x_{k-1}]]),
+              label c* = 1 - 1/2 ||p_d - p_t||_1, Sequential Temperature Scaling,
+              hardware-aware prefix scheduler Theta = tau * SPS(B),
+              B = sum(1 + l_r), tau = sum(1 + sum_j a_{r,j}), a_{r,j} = prod_i c_{r,i},
+              global descending sort, greedy admission with a break
+        §三 挑战1/挑战2: asynchronous top-K, unconstrained search without the break
+  [AR]  "DSpark整体架构" (10100.com), Fig. 1 and the semi-autoregressive stages:
+        the anchor is itself the first prediction position; verification keeps
+        the accepted run and emits one corrected token.
+  [V4]  DeepSeek-V4-Pro-0813 DSpark article (demingchina.com), config table:
+        block size 5, markov rank 512, noise token 128799, fp32 confidence.
+
+Readings where the pages are silent (each listed in the design notes):
+  * x_0 = anchor: bias and confidence at position 1 use the anchor's W1 row.
+  * T_k divides the confidence logit: c_k = sigmoid(z_k / T_k).  No bias term.
+  * Sampling temperature tau divides (base + bias); tau = 0 means greedy argmax
+    (ties to the lowest vocabulary id); tau > 0 samples by Gumbel-max with the
+    Philox layout of oracle.philox.  The target uses the same tau.
+  * Base logits are materialised in bf16 (the LM head's output type); every
+    later step accumulates in float64 here.
+  * Confidences are float32; survival products a_{r,j} are float32 products
+    taken left to right (the scheduler's sort is decided in that precision);
+    Theta is evaluated in float64.
+  * Sort order: a descending, ties by (request, position) ascending.
+    Theta argmax ties go to the smallest K; the break mode admits K+1 only if
+    Theta(K+1) > Theta(K) strictly.
+  * Verification is standard speculative sampling: accept x_j iff
+    u * p_d(x_j) < p_t(x_j); on the first rejection sample from
+    norm(max(0, p_t - p_d)); if every draft is accepted, sample the bonus from
+    target row l_r + 1.  Greedy: accept iff x_j = argmax t_j.
+"""
+from __future__ import annotations
+
+from typing import Dict, Optional
+
+import numpy as np
+
+from . import philox
+
+UNCONSTRAINED = 0
+BREAK = 1
+FIXED_K = 2
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def to_f64(x) -> np.ndarray:
+    """Accept numpy arrays or torch tensors (any float dtype) and return float64."""
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu")
+        if str(x.dtype) == "torch.bfloat16":
+            x = x.float()
+        x = x.numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def to_i64(x) -> np.ndarray:
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu").numpy()
+    return np.asarray(x, dtype=np.int64)
+
+
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Round to bfloat16 (via float32, round-to-nearest-even), returned in float64."""
+    f = np.asarray(x, dtype=np.float32)
+    b = f.view(np.uint32).astype(np.uint64)
+    b = (b + np.uint64(0x7FFF) + ((b >> np.uint64(16)) & np.uint64(1))) & np.uint64(0xFFFF0000)
+    return b.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def logsumexp(x: np.ndarray, axis: int = -1) -> np.ndarray:
+    m = np.max(x, axis=axis, keepdims=True)
+    return (m + np.log(np.sum(np.exp(x - m), axis=axis, keepdims=True))).squeeze(axis)
+
+
+def sigmoid(z):
+    return 1.0 / (1.0 + np.exp(-z))
+
+
+def top2_margin(score: np.ndarray) -> np.ndarray:
+    """Difference between the largest and second-largest entry of each row."""
+    part = np.partition(score, -2, axis=-1)
+    return part[..., -1] - part[..., -2]
+
+
+# ---------------------------------------------------------------------------
+# a1: base logits through the shared, frozen LM head   [DD §二 architecture; AR]
+# ---------------------------------------------------------------------------
+
+def base_logits(h, W_lm, bf16_out: bool = True, vocab_chunk: int = 0) -> np.ndarray:
+    """l0[m, v] = sum_i h[m, i] W_lm[v, i]  (W_lm stored [V, d]).
+
+    h is [..., d]; the result is [..., V].  `vocab_chunk` > 0 only splits the
+    vocabulary into slices to bound host memory; each slice is the same matmul.
+    """
+    h = to_f64(h)
+    lead = h.shape[:-1]
+    h2 = h.reshape(-1, h.shape[-1])
+    if vocab_chunk and vocab_chunk < W_lm.shape[0]:
+        parts = []
+        for v0 in range(0, W_lm.shape[0], vocab_chunk):
+            parts.append(h2 @ to_f64(W_lm[v0:v0 + vocab_chunk]).T)
+        out = np.concatenate(parts, axis=1)
+    else:
+        out = h2 @ to_f64(W_lm).T
+    if bf16_out:
+        out = round_bf16(out)
+    return out.reshape(*lead, -1)
+
+
+# ---------------------------------------------------------------------------
+# a2-a4: gamma-step Markov-head loop with the confidence head
+#        [DD §二 设计一 and 设计二 confidence head; AR semi-autoregressive stage 2]
+# ---------------------------------------------------------------------------
+
+def markov_draft(base, h, anchor, W1, W2, w_conf, T, tau: float, seed: int,
+                 forced=None, keep_logits: bool = False,
+                 requests: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
+    """Run the sequential head for k = 1..gamma.
+
+    base [R, gamma, V] base logits; h [R, gamma, d]; anchor [R]; W1 [V, r];
+    W2 [r, V]; w_conf [d + r]; T [gamma]; tau sampling temperature (0 = greedy).
+    `forced` [R, gamma]: when given, step k conditions on forced[:, k-1] instead
+    of the oracle's own x_k (teacher forcing), so each step can be checked on
+    the path another implementation took.  `requests` gives the request ids used
+    for the random streams (default 0..R-1).
+
+    Returns tokens (the oracle's own choice at each step), conf, z, margin (top-2
+    gap of the decision score), and in sampling mode lse = logsumexp(l_k / tau)
+    and logp = l_k[x_k] / tau - lse for the token that conditions the next step.
+    """
+    base = to_f64(base)
+    h = to_f64(h)
+    anchor = to_i64(anchor)
+    W1 = to_f64(W1)
+    W2 = to_f64(W2)
+    w_conf = to_f64(w_conf)
+    T = to_f64(T)
+    R, G, V = base.shape
+    d = h.shape[-1]
+    w_h, w_e = w_conf[:d], w_conf[d:]
+    req = np.arange(R) if requests is None else to_i64(requests)
+    vocab = np.arange(V, dtype=np.uint64)
+
+    tokens = np.zeros((R, G), dtype=np.int64)
+    conf = np.zeros((R, G))
+    z_out = np.zeros((R, G))
+    margin = np.zeros((R, G))
+    lse = np.zeros((R, G))
+    logp = np.zeros((R, G))
+    path = np.zeros((R, G), dtype=np.int64)
+    logits = np.zeros((R, G, V)) if keep_logits else None
+    forced = None if forced is None else to_i64(forced)
+
+    prev = anchor.copy()
+    for k in range(1, G + 1):
+        e = W1[prev]                                   # [R, r]  W1[x_{k-1}]
+        ell = base[:, k - 1, :] + e @ W2               # base + B(x_{k-1}, .)
+        z = h[:, k - 1, :] @ w_h + e @ w_e             # w^T [h_k; W1[x_{k-1}]]
+        conf[:, k - 1] = sigmoid(z / T[k - 1])
+        z_out[:, k - 1] = z
+        if tau == 0.0:
+            score = ell
+        else:
+            g = philox.gumbel(seed, k, req[:, None], philox.STREAM_DRAFT, vocab[None, :])
+            score = ell / tau + g
+        x = np.argmax(score, axis=1)                   # first maximum: lowest id
+        tokens[:, k - 1] = x
+        margin[:, k - 1] = top2_margin(score)
+        nxt = x if forced is None else forced[:, k - 1]
+        path[:, k - 1] = nxt
+        if tau != 0.0:
+            lse[:, k - 1] = logsumexp(ell / tau, axis=1)
+            logp[:, k - 1] = ell[np.arange(R), nxt] / tau - lse[:, k - 1]
+        if keep_logits:
+            logits[:, k - 1, :] = ell
+        prev = nxt
+    out = dict(tokens=tokens, conf=conf, z=z_out, margin=margin, lse=lse, logp=logp,
+               path=path)
+    if keep_logits:
+        out["logits"] = logits
+    return out
+
+
+def draft_score_gap(base, h, anchor, W1, W2, tau, seed, chosen, requests=None):
+    """For each (r, k): max score minus the score of `chosen[r, k]` on the path `chosen`.
+
+    Zero where `chosen` is an argmax; used to check that a token picked by
+    another implementation near a tie is still a valid maximiser.
+    """
+    base = to_f64(base)
+    anchor = to_i64(anchor)
+    W1 = to_f64(W1)
+    W2 = to_f64(W2)
+    chosen = to_i64(chosen)
+    R, G, V = base.shape
+    req = np.arange(R) if requests is None else to_i64(requests)
+    vocab = np.arange(V, dtype=np.uint64)
+    gap = np.zeros((R, G))
+    prev = anchor.copy()
+    for k in range(1, G + 1):
+        ell = base[:, k - 1, :] + W1[prev] @ W2
+        if tau == 0.0:
+            score = ell
+        else:
+            score = ell / tau + philox.gumbel(seed, k, req[:, None], philox.STREAM_DRAFT,
+                                              vocab[None, :])
+        gap[:, k - 1] = score.max(axis=1) - score[np.arange(R), chosen[:, k - 1]]
+        prev = chosen[:, k - 1]
+    return gap
+
+
+# ---------------------------------------------------------------------------
+# a5-a7: survival products, global sort, Theta search   [DD §二 scheduler, §三]
+# ---------------------------------------------------------------------------
+
+def survival(conf) -> np.ndarray:
+    """a_{r,j} = prod_{i<=j} c_{r,i}, float32 products taken left to right."""
+    c = np.asarray(to_f64(conf), dtype=np.float32)
+    a = np.empty_like(c)
+    a[:, 0] = c[:, 0]
+    for j in range(1, c.shape[1]):
+        a[:, j] = a[:, j - 1] * c[:, j]
+    return a
+
+
+def global_order(a: np.ndarray) -> np.ndarray:
+    """Flat candidate ids r*gamma + (j-1), sorted by a descending, ties by id ascending."""
+    flat = a.reshape(-1)
+    return np.array(sorted(range(flat.size), key=lambda i: (-float(flat[i]), i)),
+                    dtype=np.int64)
+
+
+def theta_curve(a: np.ndarray, order: np.ndarray, sps) -> np.ndarray:
+    """Theta(K) = (R + S_K) * SPS(R + K), K = 0..R*gamma, S_K = sum of the top-K a."""
+    R = a.shape[0]
+    sps = to_f64(sps)
+    sorted_a = a.reshape(-1)[order].astype(np.float64)
+    S = np.concatenate([[0.0], np.cumsum(sorted_a)])
+    K = np.arange(S.size)
+    return (R + S) * sps[R + K - 1]
+
+
+def schedule(conf, sps, mode: int = UNCONSTRAINED, k_fixed: int = 0) -> Dict[str, np.ndarray]:
+    """Per-request verify lengths l_r from the confidences.
+
+    mode UNCONSTRAINED: K = argmax_K Theta(K) over all budgets (ties: smallest K)
+    mode BREAK:         admit in sorted order while Theta strictly increases
+    mode FIXED_K:       admit the top min(k_fixed, R*gamma) candidates
+    """
+    a = survival(conf)
+    R, G = a.shape
+    sps = to_f64(sps)
+    if sps.size < R * (G + 1):
+        raise ValueError("SPS table shorter than R * (gamma + 1)")
+    order = global_order(a)
+    th = theta_curve(a, order, sps)
+    n = R * G
+    if mode == UNCONSTRAINED:
+        K = int(np.argmax(th))
+    elif mode == BREAK:
+        K = 0
+        while K < n and th[K + 1] > th[K]:
+            K += 1
+    elif mode == FIXED_K:
+        K = min(max(int(k_fixed), 0), n)
+    else:
+        raise ValueError(mode)
+    lens = np.bincount(order[:K] // G, minlength=R).astype(np.int64)
+    return dict(len=lens, K=K, theta=float(th[K]), thetas=th, a=a, order=order)
+
+
+def theta_of_lengths(a: np.ndarray, lens, sps) -> float:
+    """Theta for an explicit allocation: B = sum(1 + l_r), tau = sum(1 + sum_{j<=l_r} a_{r,j})."""
+    sps = to_f64(sps)
+    lens = to_i64(lens)
+    a64 = a.astype(np.float64)
+    B = int(np.sum(1 + lens))
+    tau = float(sum(1.0 + a64[r, :lens[r]].sum() for r in range(a.shape[0])))
+    return tau * sps[B - 1]
+
+
+# ---------------------------------------------------------------------------
+# a8: verification   [AR Fig. 1; DD §二 losslessness; standard speculative sampling]
+# ---------------------------------------------------------------------------
+
+def confidence_label(p_d: np.ndarray, p_t: np.ndarray) -> np.ndarray:
+    """c* = 1 - 1/2 ||p_d - p_t||_1 over the last axis  [DD §二 confidence label]."""
+    return 1.0 - 0.5 * np.sum(np.abs(p_d - p_t), axis=-1)
+
+
+def verify(tokens, lens, draft_logits, target, tau: float, seed: int,
+           requests: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
+    """Verify each request's admitted prefix against the target.
+
+    tokens [R, gamma]; lens [R]; draft_logits [R, gamma, V] (final l_k, only
+    read in sampling mode); target [R, gamma + 1, V] target logits, row j-1 is
+    the target's distribution for draft position j.
+    Returns accepted [R], bonus [R], and diagnostics: accept_margin [R, gamma]
+    (log u + log p_d - log p_t at each tested position, nan elsewhere) and
+    final_margin [R] (top-2 gap of the score that picked the bonus).
+    """
+    tokens = to_i64(tokens)
+    lens = to_i64(lens)
+    target = to_f64(target)
+    R, G1, V = target.shape
+    G = G1 - 1
+    req = np.arange(R) if requests is None else to_i64(requests)
+    dl = None if tau == 0.0 else to_f64(draft_logits)
+    vocab = np.arange(V, dtype=np.uint64)
+    accepted = np.zeros(R, dtype=np.int64)
+    bonus = np.zeros(R, dtype=np.int64)
+    acc_margin = np.full((R, G), np.nan)
+    final_margin = np.zeros(R)
+    for i in range(R):
+        L = int(lens[i])
+        rq = int(req[i])
+        n = L
+        if tau == 0.0:
+            for j in range(1, L + 1):
+                y = int(np.argmax(target[i, j - 1]))
+                if tokens[i, j - 1] != y:
+                    n = j - 1
+                    break
+            bonus[i] = int(np.argmax(target[i, n]))
+            final_margin[i] = top2_margin(target[i, n])
+            accepted[i] = n
+            continue
+        rejected = False
+        for j in range(1, L + 1):
+            lt = target[i, j - 1] / tau
+            ld = dl[i, j - 1] / tau
+            lse_t = logsumexp(lt)
+            lse_d = logsumexp(ld)
+            x = int(tokens[i, j - 1])
+            u = float(philox.uniform(seed, j, rq, philox.STREAM_ACCEPT, 0))
+            m = np.log(u) + (ld[x] - lse_d) - (lt[x] - lse_t)
+            acc_margin[i, j - 1] = m
+            if m < 0.0:                                  # u * p_d(x) < p_t(x)
+                continue
+            n = j - 1
+            p_t = np.exp(lt - lse_t)
+            p_d = np.exp(ld - lse_d)
+            q = np.maximum(p_t - p_d, 0.0)
+            g = philox.gumbel(seed, j, rq, philox.STREAM_RESIDUAL, vocab)
+            if np.any(q > 0.0):
+                with np.errstate(divide="ignore"):
+                    score = np.where(q > 0.0, np.log(q) + g, -np.inf)
+            else:
+                score = lt + g
+            bonus[i] = int(np.argmax(score))
+            final_margin[i] = top2_margin(score)
+            rejected = True
+            break
+        if not rejected:
+            g = philox.gumbel(seed, L + 1, rq, philox.STREAM_BONUS, vocab)
+            score = target[i, L] / tau + g
+            bonus[i] = int(np.argmax(score))
+            final_margin[i] = top2_margin(score)
+        accepted[i] = n
+    return dict(accepted=accepted, bonus=bonus, accept_margin=acc_margin,
+                final_margin=final_margin)
+
+
+# ---------------------------------------------------------------------------
+# one round, composed
+# ---------------------------------------------------------------------------
+
+def draft_round(inp: Dict, tau: float, seed: int, keep_logits: bool = False,
+                forced=None) -> Dict[str, np.ndarray]:
+    """a1-a4 on a workload's inputs (dict from workloads.make_inputs)."""
+    base = base_logits(inp["h"], inp["W_lm"])
+    out = markov_draft(base, inp["h"], inp["anchor"], inp["W1"], inp["W2"], inp["w_conf"],
+                       inp["T"], tau, seed, forced=forced, keep_logits=keep_logits)
+    out["base"] = base
+    return out

@@ -1,0 +1,428 @@
+"""Pins for the CPU oracle: checks against things other than the oracle itself.
+
+Each test ties one oracle function to a closed form, a brute-force enumeration,
+published known-answer vectors or a statistical law, so that a plausible
+mistake (dropped term, wrong sign or index, transposed operand) fails here.
+"""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+from scipy import stats
+
+import oracle
+from oracle import philox
+from oracle.dspark import sigmoid
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ----------------------------------------------------------------- Philox ---
+
+def test_philox_known_answers():
+    rows = []
+    with open(os.path.join(GOLDEN, "philox4x32_10_kat.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                rows.append([int(x, 16) for x in line.split()])
+    assert len(rows) == 3
+    for row in rows:
+        ctr, key, want = row[:4], row[4:6], row[6:]
+        got = philox.philox4x32_10(*ctr, *key)
+        assert [int(x) for x in got] == want
+
+
+def test_uniform_is_exact_float32_in_open_interval():
+    v = np.arange(4096, dtype=np.uint64)
+    u = philox.uniform(12345, 3, 7, 0, v)
+    assert np.all(u > 0) and np.all(u < 1)
+    assert np.array_equal(u.astype(np.float32).astype(np.float64), u)
+    # extremes of the map: word 0 -> 2^-24, word 2^32-1 -> 1 - 2^-24
+    lo = ((0 >> 9) + 0.5) * 2.0 ** -23
+    hi = (((2 ** 32 - 1) >> 9) + 0.5) * 2.0 ** -23
+    assert lo == 2.0 ** -24 and hi == 1 - 2.0 ** -24
+    # counter layout: slot v uses word v & 3 of counter (v >> 2, pos, req, stream)
+    w = philox.philox4x32_10(5, 3, 7, 0, 12345 & 0xFFFFFFFF, 12345 >> 32)
+    assert int(philox.words(12345, 3, 7, 0, 22)) == int(w[2])
+
+
+def test_uniform_distribution():
+    v = np.arange(200000, dtype=np.uint64)
+    u = philox.uniform(99, 1, 2, 1, v)
+    assert stats.kstest(u, "uniform").pvalue > 1e-4
+
+
+# ------------------------------------------------------- a1: base logits ---
+
+def test_base_logits_brute_force():
+    rng = np.random.default_rng(1)
+    h = rng.standard_normal((3, 5))
+    W = rng.standard_normal((7, 5))
+    want = np.zeros((3, 7))
+    for m in range(3):
+        for v in range(7):
+            want[m, v] = sum(h[m, i] * W[v, i] for i in range(5))
+    got = oracle.base_logits(h, W, bf16_out=False)
+    np.testing.assert_allclose(got, want, rtol=1e-13, atol=1e-13)
+    # bf16 materialisation: representable, and within half a bf16 ulp (+fp32 step)
+    gb = oracle.base_logits(h, W, bf16_out=True)
+    assert np.array_equal(oracle.round_bf16(gb), gb)
+    assert np.all(np.abs(gb - want) <= np.abs(want) * 2.0 ** -8 + 1e-30)
+
+
+def test_round_bf16_known_values():
+    # 1 + 2^-8 is a tie between 1 and 1 + 2^-7: round to even -> 1
+    x = np.array([1.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -2.5, 3.0e38])
+    got = oracle.round_bf16(x)
+    assert got[0] == 1.0 and got[1] == 1.0 and got[2] == 1.0 + 2 ** -6 and got[3] == -2.5
+    assert np.isfinite(got[4])
+
+
+# ------------------------------------------- a2-a4: Markov head and conf ---
+
+def _tiny_draft_inputs(R=3, G=4, V=11, r=3, d=5, seed=0, w2_zero=False):
+    rng = np.random.default_rng(seed)
+    base = rng.standard_normal((R, G, V))
+    h = rng.standard_normal((R, G, d))
+    anchor = rng.integers(0, V, R)
+    W1 = rng.standard_normal((V, r))
+    W2 = np.zeros((r, V)) if w2_zero else rng.standard_normal((r, V))
+    w = rng.standard_normal(d + r)
+    T = 1.0 + rng.random(G)
+    return base, h, anchor, W1, W2, w, T
+
+
+def test_markov_bias_is_row_of_explicit_transition_matrix():
+    base, h, anchor, W1, W2, w, T = _tiny_draft_inputs()
+    R, G, V = base.shape
+    P = [[sum(W1[a, i] * W2[i, b] for i in range(W1.shape[1])) for b in range(V)]
+         for a in range(V)]
+    out = oracle.markov_draft(base, h, anchor, W1, W2, w, T, 0.0, 0, keep_logits=True)
+    P = np.array(P)
+    assert not np.allclose(P, P.T)
+    prev = anchor.copy()
+    for k in range(G):
+        for rq in range(R):
+            want = base[rq, k] + P[prev[rq]]          # row of x_{k-1}, not column
+            np.testing.assert_allclose(out["logits"][rq, k], want, rtol=1e-12, atol=1e-12)
+            assert out["tokens"][rq, k] == int(np.argmax(want))
+        prev = out["tokens"][:, k]
+
+
+def test_w2_zero_reduces_to_parallel_drafting():
+    base, h, anchor, W1, W2, w, T = _tiny_draft_inputs(w2_zero=True, V=40)
+    out = oracle.markov_draft(base, h, anchor, W1, W2, w, T, 0.0, 0)
+    assert np.array_equal(out["tokens"], np.argmax(base, axis=2))
+
+
+def test_greedy_ties_pick_lowest_id():
+    R, G, V = 2, 2, 9
+    base = np.zeros((R, G, V))
+    base[:, :, 3] = 1.0
+    base[:, :, 6] = 1.0
+    out = oracle.markov_draft(base, np.zeros((R, G, 2)), np.zeros(R, int),
+                              np.zeros((V, 2)), np.zeros((2, V)), np.zeros(4), np.ones(G),
+                              0.0, 0)
+    assert np.all(out["tokens"] == 3)
+
+
+def test_confidence_head_brute_force():
+    base, h, anchor, W1, W2, w, T = _tiny_draft_inputs()
+    R, G, V = base.shape
+    d = h.shape[2]
+    out = oracle.markov_draft(base, h, anchor, W1, W2, w, T, 0.0, 0)
+    prev = anchor.copy()
+    for k in range(G):
+        for rq in range(R):
+            cat = list(h[rq, k]) + list(W1[prev[rq]])   # [h_k; W1[x_{k-1}]]
+            z = sum(wi * xi for wi, xi in zip(w, cat))
+            c = 1.0 / (1.0 + math.exp(-z / T[k]))
+            assert abs(out["conf"][rq, k] - c) < 1e-12
+            assert abs(out["z"][rq, k] - z) < 1e-12
+        prev = out["tokens"][:, k]
+    # T = 1 is the plain sigmoid; a hotter temperature pulls c toward 1/2
+    o1 = oracle.markov_draft(base, h, anchor, W1, W2, w, np.ones(G), 0.0, 0)
+    np.testing.assert_allclose(o1["conf"], sigmoid(o1["z"]), rtol=0, atol=0)
+    o3 = oracle.markov_draft(base, h, anchor, W1, W2, w, 3 * np.ones(G), 0.0, 0)
+    assert np.all(np.abs(o3["conf"] - 0.5) <= np.abs(o1["conf"] - 0.5) + 1e-15)
+    assert d == 5
+
+
+@pytest.mark.parametrize("tau", [0.7, 1.0, 1.6])
+def test_gumbel_max_follows_softmax(tau):
+    """Sampled draft tokens follow softmax(l / tau) (Gumbel-max law)."""
+    V, N = 6, 60000
+    logits = np.array([0.3, -1.0, 1.2, 0.0, 2.0, -0.4])
+    base = np.broadcast_to(logits, (N, 1, V)).copy()
+    out = oracle.markov_draft(base, np.zeros((N, 1, 1)), np.zeros(N, int),
+                              np.zeros((V, 1)), np.zeros((1, V)), np.zeros(2), np.ones(1),
+                              tau, seed=2024)
+    counts = np.bincount(out["tokens"][:, 0], minlength=V)
+    p = np.exp(logits / tau)
+    p /= p.sum()
+    assert stats.chisquare(counts, N * p).pvalue > 1e-4
+    # log p_d of the sampled token is reported
+    np.testing.assert_allclose(out["logp"][:, 0], np.log(p[out["tokens"][:, 0]]), atol=1e-12)
+
+
+# ---------------------------------------- a5-a7: survival, sort, Theta ---
+
+def test_survival_products_left_to_right_float32():
+    rng = np.random.default_rng(3)
+    c = rng.random((5, 6)).astype(np.float32)
+    c[2, 3] = 1.0
+    a = oracle.survival(c)
+    for rq in range(5):
+        acc = np.float32(1.0)
+        for j in range(6):
+            acc = np.float32(acc * c[rq, j]) if j else np.float32(c[rq, 0])
+            assert a[rq, j] == acc
+        assert np.all(np.diff(a[rq]) <= 0)
+
+
+def test_global_order_matches_lexsort():
+    rng = np.random.default_rng(4)
+    c = rng.random((9, 4)).astype(np.float32)
+    c[::3, 1:] = 1.0                     # equal survival products inside a request
+    c[4] = c[1]                          # equal products across requests
+    a = oracle.survival(c)
+    flat = a.reshape(-1)
+    idx = np.arange(flat.size)
+    want = np.lexsort((idx, -flat.astype(np.float64)))
+    assert np.array_equal(oracle.global_order(a), want)
+
+
+def _sps_tables(n):
+    B = np.arange(1, n + 1, dtype=np.float64)
+    rng = np.random.default_rng(n)
+    return {
+        "linear": 1000 * (1 - (B - 1) / (2 * n)),
+        "concave": 1000 * (1 - 0.75 * ((B - 1) / (n - 1)) ** 2),
+        "stair": 1000 / (1 + 0.15 * np.floor((B - 1) / 3)),
+        "noisy": np.sort(rng.uniform(100, 1000, n))[::-1] * (1 + 0.05 * rng.random(n)),
+        "flat": np.full(n, 500.0),
+    }
+
+
+@pytest.mark.parametrize("R,G", [(1, 4), (2, 3), (3, 3), (4, 2), (3, 4)])
+def test_unconstrained_theta_is_bruteforce_optimum(R, G):
+    rng = np.random.default_rng(10 * R + G)
+    for trial in range(4):
+        c = (0.05 + 0.95 * rng.random((R, G))).astype(np.float32)
+        if trial == 3:
+            c[0, :] = 1.0
+        for name, sps in _sps_tables(R * (G + 1)).items():
+            sps32 = sps.astype(np.float32)
+            s = oracle.schedule(c, sps32, oracle.UNCONSTRAINED)
+            a = s["a"]
+            best = max(oracle.theta_of_lengths(a, lens, sps32)
+                       for lens in itertools.product(range(G + 1), repeat=R))
+            assert s["theta"] == pytest.approx(best, rel=1e-12), name
+            assert oracle.theta_of_lengths(a, s["len"], sps32) == pytest.approx(best, rel=1e-12)
+            assert s["len"].sum() == s["K"]
+
+
+def test_admitted_set_is_prefix_closed_and_top_k():
+    rng = np.random.default_rng(7)
+    c = (0.05 + 0.95 * rng.random((20, 5))).astype(np.float32)
+    c[3, 1:4] = 1.0
+    sps = _sps_tables(120)["stair"].astype(np.float32)
+    for mode, kf in [(oracle.UNCONSTRAINED, 0), (oracle.BREAK, 0), (oracle.FIXED_K, 37)]:
+        s = oracle.schedule(c, sps, mode, kf)
+        a = s["a"]
+        admitted = {(i // 5, i % 5) for i in s["order"][:s["K"]]}
+        for (rq, j) in admitted:
+            assert j == 0 or (rq, j - 1) in admitted
+        assert sorted(admitted) == sorted((rq, j) for rq in range(20) for j in range(s["len"][rq]))
+        # admitted products dominate the rejected ones
+        if 0 < s["K"] < 100:
+            amin = min(a[rq, j] for rq, j in admitted)
+            amax = max(a[rq, j] for rq in range(20) for j in range(5) if (rq, j) not in admitted)
+            assert amin >= amax
+    assert oracle.schedule(c, sps, oracle.FIXED_K, 37)["K"] == 37
+    assert oracle.schedule(c, sps, oracle.FIXED_K, 1000)["K"] == 100
+
+
+def test_break_mode_first_local_maximum():
+    rng = np.random.default_rng(8)
+    for trial in range(20):
+        R, G = 6, 4
+        c = (0.05 + 0.95 * rng.random((R, G))).astype(np.float32)
+        sps = _sps_tables(R * (G + 1))
+        s = oracle.schedule(c, sps["stair"].astype(np.float32), oracle.BREAK)
+        th = s["thetas"]
+        K = s["K"]
+        assert all(th[i + 1] > th[i] for i in range(K))
+        assert K == R * G or th[K + 1] <= th[K]
+        # with a linear SPS table Theta(K) is concave, so break = global search
+        lin = sps["linear"].astype(np.float32)
+        assert (oracle.schedule(c, lin, oracle.BREAK)["K"]
+                == oracle.schedule(c, lin, oracle.UNCONSTRAINED)["K"])
+
+
+def test_theta_closed_form_on_hand_example():
+    # two requests, gamma 2: c = [[.5, .5], [.9, .1]]  -> a = [[.5,.25],[.9,.09]]
+    c = np.array([[0.5, 0.5], [0.9, 0.1]], dtype=np.float32)
+    sps = np.array([100, 100, 100, 90, 80, 10], dtype=np.float32)
+    s = oracle.schedule(c, sps, oracle.UNCONSTRAINED)
+    # sorted a: .9 (1,1), .5 (0,1), .25 (0,2), .09 (1,2)
+    th = [2 * 100, 2.9 * 100, 3.4 * 90, 3.65 * 80, 3.74 * 10]
+    np.testing.assert_allclose(s["thetas"], th, rtol=1e-7)
+    assert s["K"] == 2 and list(s["len"]) == [1, 1]
+    assert oracle.schedule(c, sps, oracle.BREAK)["K"] == 3 - 1
+
+
+# ------------------------------------------------------------ a8: verify ---
+
+def test_confidence_label_identity():
+    rng = np.random.default_rng(11)
+    for _ in range(50):
+        V = rng.integers(2, 40)
+        p = rng.dirichlet(np.ones(V) * rng.uniform(0.1, 3))
+        q = rng.dirichlet(np.ones(V) * rng.uniform(0.1, 3))
+        lab = oracle.confidence_label(p, q)
+        assert lab == pytest.approx(np.minimum(p, q).sum(), abs=1e-12)
+        assert 0.0 <= lab <= 1.0
+    assert oracle.confidence_label(p, p) == pytest.approx(1.0)
+
+
+def test_acceptance_rate_equals_confidence_label():
+    """P(accept position 1) = sum_v min(p_d, p_t) = 1 - TV(p_d, p_t)."""
+    V, N, tau = 7, 40000, 1.0
+    rng = np.random.default_rng(12)
+    ld = rng.standard_normal(V) * 1.3
+    lt = rng.standard_normal(V) * 1.3
+    base = np.broadcast_to(ld, (N, 1, V)).copy()
+    dr = oracle.markov_draft(base, np.zeros((N, 1, 1)), np.zeros(N, int), np.zeros((V, 1)),
+                             np.zeros((1, V)), np.zeros(2), np.ones(1), tau, seed=5)
+    target = np.broadcast_to(np.stack([lt, lt]), (N, 2, V)).copy()
+    res = oracle.verify(dr["tokens"], np.ones(N, int), base, target, tau, seed=6)
+    pd = np.exp(ld - oracle.dspark.logsumexp(ld))
+    pt = np.exp(lt - oracle.dspark.logsumexp(lt))
+    label = oracle.confidence_label(pd, pt)
+    rate = res["accepted"].mean()
+    assert abs(rate - label) < 4 * math.sqrt(label * (1 - label) / N)
+    # reversing the ratio (a plausible slip) would give a different rate here
+    wrong = np.sum(pd * np.minimum(1, pd / pt))
+    assert abs(wrong - label) > 8 * math.sqrt(label * (1 - label) / N)
+
+
+def test_greedy_verify_accepts_own_argmax():
+    rng = np.random.default_rng(13)
+    R, G, V = 6, 4, 50
+    target = rng.standard_normal((R, G + 1, V))
+    tokens = np.argmax(target[:, :G], axis=2)
+    lens = np.array([0, 1, 2, 3, 4, 4])
+    res = oracle.verify(tokens, lens, None, target, 0.0, 0)
+    assert list(res["accepted"]) == list(lens)
+    for i in range(R):
+        assert res["bonus"][i] == np.argmax(target[i, lens[i]])
+    # corrupt one draft: rejected there, the correction is that row's argmax
+    tokens2 = tokens.copy()
+    tokens2[5, 1] = (tokens2[5, 1] + 1) % V
+    res2 = oracle.verify(tokens2, lens, None, target, 0.0, 0)
+    assert res2["accepted"][5] == 1 and res2["bonus"][5] == np.argmax(target[5, 1])
+
+
+def test_sampling_verify_identical_distributions_always_accepts():
+    rng = np.random.default_rng(14)
+    R, G, V = 50, 3, 20
+    logits = rng.standard_normal((R, G + 1, V))
+    tokens = rng.integers(0, V, (R, G))
+    lens = np.full(R, G)
+    res = oracle.verify(tokens, lens, logits[:, :G], logits, 1.0, 9)
+    assert np.all(res["accepted"] == G)
+
+
+def _markov_target_rounds(mode, V=6, G=3, N=30000, L=3, seed=0):
+    """Decode L tokens per trial by draft -> schedule -> verify rounds (oracle only).
+
+    Target: a first-order Markov chain P_t(next | prev).  Draft: base logits per
+    position plus a low-rank Markov bias; confidences from the confidence head.
+    Returns the first L emitted tokens of each trial and the exact target joint.
+    """
+    rng = np.random.default_rng(seed)
+    logPt = rng.standard_normal((V, V)) * 1.2
+    Pt = np.exp(logPt - oracle.dspark.logsumexp(logPt, axis=1)[:, None])
+    base0 = rng.standard_normal((G, V)) * 0.8
+    r = 2
+    W1 = rng.standard_normal((V, r))
+    W2 = rng.standard_normal((r, V)) * 0.8
+    d = 3
+    h = rng.standard_normal((N, G, d))
+    w = rng.standard_normal(d + r) * 1.5
+    T = np.array([1.0, 1.3, 1.7])[:G]
+    sps = 1000 * (1 - np.arange(N * (G + 1)) / (N * (G + 1) * 1.1))
+    start = 2
+    anchor = np.full(N, start)
+    emitted = [[] for _ in range(N)]
+    rnd = 0
+    while min(len(e) for e in emitted) < L:
+        base = np.broadcast_to(base0, (N, G, V)).copy()
+        dr = oracle.markov_draft(base, h, anchor, W1, W2, w, T, 1.0, seed=1000 + rnd,
+                                 keep_logits=True)
+        x = dr["tokens"]
+        prev = np.concatenate([anchor[:, None], x], axis=1)        # x_0..x_G
+        target = logPt[prev]                                       # row j-1 | x_{j-1}
+        if mode == "full":
+            lens = np.full(N, G)
+        elif mode == "random":
+            lens = rng.integers(0, G + 1, N)
+        elif mode == "break":
+            lens = oracle.schedule(dr["conf"].astype(np.float32), sps, oracle.BREAK)["len"]
+        elif mode == "fixed_k":
+            lens = oracle.schedule(dr["conf"].astype(np.float32), sps, oracle.FIXED_K,
+                                   N * G // 2)["len"]
+        res = oracle.verify(x, lens, dr["logits"], target, 1.0, seed=5000 + rnd)
+        for i in range(N):
+            n = res["accepted"][i]
+            emitted[i].extend(list(x[i, :n]) + [res["bonus"][i]])
+            anchor[i] = emitted[i][-1]
+        rnd += 1
+    first = np.array([e[:L] for e in emitted])
+    joint = np.ones([V] * L)
+    for idx in itertools.product(range(V), repeat=L):
+        p, prv = 1.0, start
+        for t in idx:
+            p *= Pt[prv, t]
+            prv = t
+        joint[idx] = p
+    return first, joint
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("mode", ["full", "random", "break", "fixed_k"])
+def test_draft_schedule_verify_is_lossless(mode):
+    """Chi-square: emitted tokens follow the target chain in non-anticipating modes."""
+    V, L = 6, 3
+    first, joint = _markov_target_rounds(mode, V=V, L=L, N=24000, seed=hash(mode) % 1000)
+    cells = np.ravel_multi_index(first.T, [V] * L)
+    counts = np.bincount(cells, minlength=V ** L)
+    exp = joint.reshape(-1) * first.shape[0]
+    keep = exp >= 5
+    obs = np.append(counts[keep], counts[~keep].sum())
+    ex = np.append(exp[keep], exp[~keep].sum())
+    assert stats.chisquare(obs, ex).pvalue > 1e-4
+    # and marginally per position
+    for t in range(L):
+        m = np.bincount(first[:, t], minlength=V)
+        pm = joint.sum(axis=tuple(i for i in range(L) if i != t))
+        assert stats.chisquare(m, pm * first.shape[0]).pvalue > 1e-4
+
+
+def test_zero_length_and_bonus_row():
+    rng = np.random.default_rng(15)
+    R, G, V = 30, 2, 12
+    target = rng.standard_normal((R, G + 1, V))
+    res = oracle.verify(np.zeros((R, G), int), np.zeros(R, int), None, target, 0.0, 0)
+    assert np.all(res["accepted"] == 0)
+    assert np.array_equal(res["bonus"], np.argmax(target[:, 0], axis=1))
+    # sampling mode with nothing admitted: bonus is a plain sample from target row 1
+    res = oracle.verify(np.zeros((R, G), int), np.zeros(R, int), np.zeros((R, G, V)),
+                        target, 1.0, 3)
+    assert np.all(res["accepted"] == 0)
+    g = philox.gumbel(3, 1, np.arange(R)[:, None], philox.STREAM_BONUS,
+                      np.arange(V, dtype=np.uint64)[None, :])
+    assert np.array_equal(res["bonus"], np.argmax(target[:, 0] + g, axis=1))
