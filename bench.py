@@ -1,0 +1,423 @@
+"""Benchmark of one DSpark draft-head round (draft -> schedule -> verify) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl dspark|reference]
+
+A step is one whole round over one batch: base logits (LM head), the gamma-step
+Markov/confidence loop, the prefix scheduler and verification.  Inputs are
+synthetic, seeded, and resident in HBM before the timed region; the LM head
+weight (1.85 GB at the default workload) is larger than L2, so successive steps
+do not run from cache.  With N > 1 (launched by torchrun) every rank runs an
+independent replica on its own GPU: there is no collective on the data path.
+
+Prints one JSON line (rank 0).  `value` is drafted tokens/s over all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "drafted tokens/s"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "v4_dspark5"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    p.add_argument("--impl", default="dspark", choices=["dspark", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--cpu-sample", type=int, default=0,
+                   help="requests in the CPU-oracle sample (0 = sized automatically)")
+    return p.parse_args()
+
+
+# --------------------------------------------------------------- helpers ----
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            j = json.load(f)
+        return dict(hbm_gbs=j["hbm_gbs"], bf16=j["bf16_tflops"],
+                    bf16_sustained=j.get("bf16_tflops_sustained"), source="measured")
+    return dict(hbm_gbs=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def kernel_source_hash(names):
+    h = hashlib.sha256()
+    for n in names:
+        p = os.path.join(ROOT, "speculative_decoding_draft_02_gb300", "csrc", n)
+        if os.path.exists(p):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, src_hash: str, units: float):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current source of that kernel (else None).  The summary states the bytes
+    of its captured launch and the units it processed; scaled by `units`."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}.txt")
+    if not os.path.exists(path):
+        return None
+    kv = {}
+    for line in open(path):
+        if ":" in line and not line.startswith(" "):
+            k, v = line.split(":", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("source_hash") != src_hash:
+        return None
+    try:
+        b = float(kv["dram_bytes_per_launch"])
+        u = float(kv.get("units_per_launch", units))
+    except (KeyError, ValueError):
+        return None
+    return b * units / u
+
+
+# ----------------------------------------------------------- workload -----
+
+def build_inputs(w, rank: int, device="cuda"):
+    inp = workloads.make_inputs(w, device=device, seed=w.seed + 1000 * rank)
+    # Synthetic target model: target logits = draft base logits + N(0, sigma_r)
+    # for positions 1..gamma, and a fresh hidden state through the shared head
+    # for position gamma + 1.  Built with cuBLAS (torch.matmul) once, untimed.
+    R, G, V, d = w.R, w.gamma, w.V, w.d
+    Wl = inp["W_lm"].to(torch.bfloat16)
+    base = torch.matmul(inp["h"].to(torch.bfloat16).reshape(R * G, d), Wl.t()).view(R, G, V)
+    nxt = torch.matmul(inp["h_next"].to(torch.bfloat16), Wl.t()).view(R, 1, V)
+    target = torch.cat([base, nxt], dim=1).float().add_(inp.pop("noise").float())
+    inp["target"] = target.to(torch.bfloat16).contiguous()
+    del base, nxt, target
+    torch.cuda.empty_cache()
+    return inp
+
+
+# ------------------------------------------------------- CPU baseline -----
+
+def cpu_oracle_round(w, inp_cpu, S: int):
+    """Run the oracle's full round on the first S requests; returns seconds."""
+    import oracle
+    R, G, V, d = w.R, w.gamma, w.V, w.d
+    t0 = time.perf_counter()
+    h = inp_cpu["h"][:S]
+    base = oracle.base_logits(h.reshape(S * G, d), inp_cpu["W_lm"], vocab_chunk=8192).reshape(
+        S, G, V)
+    dr = oracle.markov_draft(base, h, inp_cpu["anchor"][:S], inp_cpu["W1"], inp_cpu["W2"],
+                             inp_cpu["w_conf"], inp_cpu["T"], w.tau, inp_cpu["draft_seed"],
+                             keep_logits=w.tau > 0)
+    sps = inp_cpu["sps"]
+    sch = oracle.schedule(dr["conf"].astype(np.float32), sps, oracle.UNCONSTRAINED)
+    oracle.verify(dr["tokens"], sch["len"], dr.get("logits"), inp_cpu["target"][:S], w.tau,
+                  inp_cpu["verify_seed"])
+    return time.perf_counter() - t0
+
+
+def cpu_inputs(w, inp_gpu):
+    keys = ["h", "anchor", "W_lm", "W1", "W2", "w_conf", "T", "sps"]
+    out = {k: inp_gpu[k].cpu() for k in keys}
+    out["draft_seed"] = inp_gpu["draft_seed"]
+    out["verify_seed"] = inp_gpu["verify_seed"]
+    return out
+
+
+def cpu_baseline(w, inp_gpu, S: int, target_s: float = 15.0):
+    cpu = cpu_inputs(w, inp_gpu)
+    cores = torch.get_num_threads()
+    # first a one-request probe to size the sample to about `target_s` seconds
+    cpu["target"] = inp_gpu["target"][:max(S, 1) if S else 1].cpu()
+    if not S:
+        t1 = cpu_oracle_round(w, cpu, 1)
+        S = int(max(1, min(w.R, math.floor(target_s / max(t1, 1e-3)))))
+        cpu["target"] = inp_gpu["target"][:S].cpu()
+    t = cpu_oracle_round(w, cpu, S)
+    return {"value": S * w.gamma / t, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"one full round (LM head, {w.gamma}-step Markov loop, schedule, verify) "
+                      f"for the first {S} of {w.R} requests of {w.name}, float64 numpy, "
+                      f"{t:.1f} s on {os.cpu_count()} host cores"}
+
+
+# ------------------------------------------------------------ arms --------
+
+def run_reference(args, w, ws, rank):
+    """The CPU oracle as the reference arm (rank 0 only)."""
+    if rank != 0:
+        return
+    torch.manual_seed(0)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    if dev == "cuda":
+        inp = build_inputs(w, 0)
+    else:
+        small = w.with_(R=min(w.R, 4))
+        inp = workloads.make_inputs(small, device="cpu")
+        inp["target"] = torch.zeros((small.R, w.gamma + 1, w.V), dtype=torch.bfloat16)
+    cpu = cpu_inputs(w, inp)
+    # size one step so that warmup + steps fit in about three minutes
+    S = args.cpu_sample or 1
+    cpu["target"] = inp["target"][:S].cpu()
+    if not args.cpu_sample:
+        t1 = cpu_oracle_round(w, cpu, 1)
+        S = int(max(1, min(w.R, math.floor(180.0 / (args.steps + args.warmup) / max(t1, 1e-3)))))
+        cpu["target"] = inp["target"][:S].cpu()
+    for _ in range(args.warmup):
+        cpu_oracle_round(w, cpu, S)
+    times = [cpu_oracle_round(w, cpu, S) for _ in range(args.steps)]
+    sec = sum(times) / len(times)
+    value = S * w.gamma / sec
+    cores = torch.get_num_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "R": w.R, "gamma": w.gamma, "V": w.V, "r": w.r, "d": w.d,
+                   "tau": w.tau, "sample_requests": S},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"each step: one oracle round for {S} of {w.R} requests"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_dspark(args, w, ws, rank, local):
+    import speculative_decoding_draft_02_gb300 as dsp
+    from speculative_decoding_draft_02_gb300 import build as dsp_build
+    if rank == 0:
+        dsp_build.build()
+    barrier(ws)
+    dsp.load_library()
+    inp = build_inputs(w, rank)
+    R, G, V, r, d = w.R, w.gamma, w.V, w.r, w.d
+    head = dsp.DraftHead.from_weights(R, G, inp["W_lm"], inp["W1"], inp["W2"], inp["w_conf"],
+                                      inp["T"])
+    rnd = dsp.Round(head)
+    h = inp["h"].to(torch.bfloat16).reshape(R * G, d).contiguous()
+    anchor = inp["anchor"].contiguous()
+    target = inp["target"]
+    sps = inp["sps"].contiguous()
+    tau, ds, vs = w.tau, inp["draft_seed"], inp["verify_seed"]
+    stream = torch.cuda.current_stream()
+    dims = head.dims
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        dsp.dspark_lm_head(dims, h, head.W_lm, rnd.base)
+        if ev is not None:
+            ev[1].record(stream)
+        dsp.dspark_markov_draft(dims, rnd.base, h, anchor, head.W1, head.W2t, head.w_conf,
+                                head.T, tau, ds, rnd.tokens, rnd.conf, rnd.logp_d, rnd.lse_d,
+                                rnd.ws_draft)
+        if ev is not None:
+            ev[2].record(stream)
+        rnd.schedule(sps)
+        if ev is not None:
+            ev[3].record(stream)
+        rnd.verify(anchor, target, tau, vs)
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    dsp.check_device_status()
+
+    # timed region: K whole rounds, events around each stage on the launching stream
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    clocks = ClockSampler(local) if rank == 0 else None
+    n0 = dsp.dspark_launch_count()
+    barrier(ws)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    launches = dsp.dspark_launch_count() - n0
+    clk = clocks.stop() if clocks else None
+    ms = start.elapsed_time(end) / args.steps
+    ms = max_over_ranks(ms, ws)
+    stage = {k: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
+             for i, k in enumerate(["lm_head", "markov_loop", "schedule", "verify"])}
+    dsp.check_device_status()
+    K_adm = int(rnd.K.item())
+    acc = rnd.accepted.float().mean().item()
+
+    # roofline of the dominant kernel (the LM-head GEMM, tensor-bound)
+    peaks = measured_peaks()
+    flops = 2.0 * R * G * V * d
+    ach_tf = flops / (stage["lm_head"] * 1e-3) / 1e12
+    src = kernel_source_hash(["lm_head.cu", "lm_head_tc.cu", "tcgen05.cuh"])
+    traffic = profiled_traffic("lm_head", src, R * G)
+    # the Markov loop against HBM: algorithmic bytes of one draft loop
+    markov_bytes = G * (V * r * 2 + R * V * 2 + R * r * 2)
+    markov_gbs = markov_bytes / (stage["markov_loop"] * 1e-3) / 1e9
+
+    line = {
+        "metric": METRIC, "value": ws * R * G / (ms * 1e-3), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "R": R, "gamma": G, "V": V, "r": r, "d": d, "tau": w.tau,
+                   "l2": "inputs larger than L2 (LM head 1.85 GB streamed every step)"
+                   if V * d * 2 > 129e6 else "L2 not flushed",
+                   "parallelism": f"replicas x{ws}"},
+        "rounds_per_s": ws / (ms * 1e-3),
+        "stages_ms": stage,
+        "admitted_K": K_adm, "mean_accepted": acc,
+        "roofline": {"bound": "tensor", "achieved": ach_tf, "peak": peaks["bf16"],
+                     "unit": "TFLOP/s", "frac": ach_tf / peaks["bf16"], "traffic": traffic,
+                     "kernel": "lm_head", "peak_source": peaks["source"] + " burst bf16"},
+        "markov_loop_hbm": {"achieved": markov_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                            "frac": markov_gbs / peaks["hbm_gbs"]},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+
+    if not args.no_e2e:
+        # end to end through the public API from pinned host buffers
+        h_host = h.cpu().pin_memory()
+        a_host = anchor.cpu().pin_memory()
+        t_host = target.cpu().pin_memory()
+        dev_in = {"h": torch.empty_like(h), "anchor": torch.empty_like(anchor),
+                  "target": torch.empty_like(target)}
+        out_host = {k: torch.empty(getattr(rnd, k).shape, dtype=getattr(rnd, k).dtype,
+                                   pin_memory=True)
+                    for k in ("tokens", "len", "accepted", "bonus")}
+        for _ in range(2):
+            rnd.run_host(h_host, a_host, t_host, sps, tau, ds, vs, dev_in, out_host)
+        torch.cuda.synchronize()
+        barrier(ws)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            rnd.run_host(h_host, a_host, t_host, sps, tau, ds, vs, dev_in, out_host)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws)
+        bi = h.numel() * 2 + anchor.numel() * 4 + target.numel() * 2
+        bo = sum(t.numel() * t.element_size() for t in out_host.values())
+        line["e2e"] = {"value": ws * R * G / (ems * 1e-3), "unit": UNIT,
+                       "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_sample)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_setup()
+    w = workloads.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w, ws, rank)
+    else:
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py: the DSpark CUDA path needs a GPU")
+        run_dspark(args, w, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

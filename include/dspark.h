@@ -1,0 +1,192 @@
+/*
+ * dspark.h — C ABI of the DSpark draft-head round on one GB300 (sm_103a).
+ *
+ * One round of DSpark semi-autoregressive speculative decoding after the
+ * parallel backbone, for R requests and gamma draft positions:
+ *   a1  base logits through the shared, frozen LM head     (dspark_lm_head)
+ *   a2  Markov-head bias B(x_{k-1}, .) = W1[x_{k-1}] W2 added to the logits
+ *   a3  sampling of x_k (greedy argmax or Gumbel-max)
+ *   a4  confidence head c_k = sigmoid(w^T [h_k; W1[x_{k-1}]] / T_k)
+ *                                                         (dspark_markov_draft)
+ *   a5  prefix survival products a_{r,j} = prod_{i<=j} c_{r,i}
+ *   a6  global descending sort of all R*gamma candidates
+ *   a7  Theta = tau * SPS(B) search -> per-request verify lengths
+ *                                                         (dspark_schedule)
+ *   a8  verification of the admitted prefixes against target logits
+ *                                                         (dspark_verify)
+ *
+ * Sources (page title, section):
+ *   "DSpark 深度解读" (zhichai.net) §二 设计一 (Markov head, W1: V x r, W2: r x V),
+ *   §二 设计二 (confidence head, Sequential Temperature Scaling, hardware-aware
+ *   prefix scheduler with Theta = tau * SPS(B)), §三 挑战1/挑战2 (asynchronous
+ *   top-K admission, unconstrained search over stepped SPS curves);
+ *   "DSpark整体架构" (10100.com) Fig. 1 (anchor -> draft -> schedule -> verify,
+ *   corrected token G*) and the two-stage semi-autoregressive description
+ *   (anchor is the first prediction position);
+ *   DeepSeek-V4-Pro-0813 DSpark article (demingchina.com) config table
+ *   (block size 5, Markov rank 512, fp32 confidence).
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers unless stated otherwise, owned by
+ *     the caller, row-major and densely packed.  The library allocates nothing
+ *     and keeps no state between calls except the sticky device status word.
+ *   - "bf16" = IEEE bfloat16 stored as uint16; "f32" = float; tokens are int32.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  Inputs are never modified.
+ *   - Return value: DSPARK_OK, or a host-detected error (bad argument, short
+ *     table, short workspace, CUDA launch failure) in which case nothing was
+ *     launched.  Problems found on the device (a token id >= V, a length >
+ *     gamma, a bounded wait that ran out) set the sticky device status word,
+ *     read with dspark_device_status().
+ *   - Random draws use Philox4x32-10 keyed by (seed) with counter
+ *     (v >> 2, position, request, stream), word v & 3, u = ((w >> 9) + 0.5) 2^-23;
+ *     streams: 0 draft Gumbel, 1 accept uniform, 2 residual Gumbel, 3 bonus Gumbel.
+ */
+#ifndef DSPARK_H
+#define DSPARK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *dspark_stream_t; /* identical to cudaStream_t */
+
+typedef struct dspark_dims {
+  int32_t R;     /* requests in the batch, >= 1                                   */
+  int32_t gamma; /* draft positions per request, 1..32                             */
+  int32_t V;     /* vocabulary size, multiple of 8                                 */
+  int32_t r;     /* Markov rank, multiple of 64                                    */
+  int32_t d;     /* backbone hidden size, multiple of 64                           */
+} dspark_dims;
+
+enum {
+  DSPARK_OK = 0,
+  DSPARK_ERR_ARG = 1,        /* null pointer, bad shape or mode                     */
+  DSPARK_ERR_SPS_SHORT = 2,  /* SPS table shorter than R * (gamma + 1)              */
+  DSPARK_ERR_CUDA = 3,       /* a CUDA call or launch failed                        */
+  DSPARK_ERR_WORKSPACE = 4,  /* workspace missing or smaller than required         */
+  DSPARK_ERR_TOKEN = 5,      /* device status: token id outside [0, V)              */
+  DSPARK_ERR_LENGTH = 6,     /* device status: verify length outside [0, gamma]     */
+  DSPARK_ERR_TIMEOUT = 7     /* device status: a bounded device-side wait ran out   */
+};
+
+enum {
+  DSPARK_SCHED_UNCONSTRAINED = 0, /* K = argmax_K Theta(K) over every budget        */
+  DSPARK_SCHED_BREAK = 1,         /* admit in sorted order while Theta increases    */
+  DSPARK_SCHED_FIXED_K = 2        /* admit the top min(k_fixed, R*gamma) candidates */
+};
+
+/* a1 — base draft logits, "DSpark 深度解读" §二 (parallel backbone -> base logits
+ * through the LM head shared with, and frozen from, the target).
+ *   h           bf16 [R*gamma, d]   backbone hidden states, row m = r*gamma + k-1
+ *   W_lm        bf16 [V, d]         LM head (each vocabulary row d-contiguous)
+ *   base_logits bf16 [R*gamma, V]   out: l0[m, v] = sum_i h[m, i] W_lm[v, i],
+ *                                   fp32 accumulation, rounded to bf16
+ * h, W_lm and base_logits must be 16-byte aligned. */
+int dspark_lm_head(const dspark_dims *dims, const void *h, const void *W_lm,
+                   void *base_logits, dspark_stream_t stream);
+
+/* Layout preparation for the Markov factor W2 (done once per weight load).
+ *   W2   bf16 [r, V]   as the pages define it (B = W1[x] W2)
+ *   W2t  bf16 [V, r]   out: W2t[v, i] = W2[i, v]  (rank-contiguous rows)
+ * Every later call takes W2t. */
+int dspark_pack_w2(const dspark_dims *dims, const void *W2, void *W2t, dspark_stream_t stream);
+
+/* Workspace bytes dspark_markov_draft / dspark_draft need for `dims`. */
+size_t dspark_markov_workspace_bytes(const dspark_dims *dims);
+
+/* a2-a4 — the gamma-step sequential (Markov) head with the confidence head,
+ * "DSpark 深度解读" §二 设计一 and 设计二; "DSpark整体架构" stage two.
+ * For k = 1..gamma, with x_0 = anchor:
+ *   l_k     = l0_k + W1[x_{k-1}] W2                   (f32, never written out)
+ *   x_k     = argmax_v l_k[v]                          tau == 0 (ties: lowest v)
+ *           = argmax_v l_k[v] / tau + Gumbel(seed; r, k, v, stream 0)   tau > 0
+ *   c_k     = sigmoid((w_h . h_k + w_e . W1[x_{k-1}]) / T_k),  w_conf = [w_h; w_e]
+ *   lse_k   = logsumexp_v(l_k[v] / tau)      (tau > 0 only; 0 when greedy)
+ *   logp_k  = l_k[x_k] / tau - lse_k          (tau > 0 only; 0 when greedy)
+ *   base_logits bf16 [R*gamma, V]   from dspark_lm_head
+ *   h           bf16 [R*gamma, d]
+ *   anchor      int32 [R]           anchor token per request (in [0, V))
+ *   W1          bf16 [V, r]         Markov embedding table
+ *   W2t         bf16 [V, r]         from dspark_pack_w2
+ *   w_conf      bf16 [d + r]        confidence head weight
+ *   T           f32  [gamma]        per-position STS temperatures (> 0)
+ *   tokens      int32 [R, gamma]    out
+ *   conf        f32  [R, gamma]     out
+ *   logp_d, lse_d f32 [R, gamma]    out, may be NULL (needed by sampling verify)
+ *   workspace   device buffer of dspark_markov_workspace_bytes(dims) bytes,
+ *               256-byte aligned; contents on entry are ignored. */
+int dspark_markov_draft(const dspark_dims *dims, const void *base_logits, const void *h,
+                        const int32_t *anchor, const void *W1, const void *W2t,
+                        const void *w_conf, const float *T, float tau, uint64_t seed,
+                        int32_t *tokens, float *conf, float *logp_d, float *lse_d,
+                        void *workspace, size_t workspace_bytes, dspark_stream_t stream);
+
+/* a1-a4 in one call: dspark_lm_head into `base_logits`, then dspark_markov_draft. */
+int dspark_draft(const dspark_dims *dims, const void *h, const int32_t *anchor,
+                 const void *W_lm, const void *W1, const void *W2t, const void *w_conf,
+                 const float *T, float tau, uint64_t seed, void *base_logits,
+                 int32_t *tokens, float *conf, float *logp_d, float *lse_d,
+                 void *workspace, size_t workspace_bytes, dspark_stream_t stream);
+
+/* a5-a7 — hardware-aware prefix scheduler, "DSpark 深度解读" §二 设计二 and §三.
+ *   conf   f32 [R, gamma]    confidences c_{r,j}
+ *   sps    f32 [n_sps]       profiled steps/s, sps[B-1] = SPS(B); n_sps >= R*(gamma+1)
+ *   mode   DSPARK_SCHED_*;   k_fixed used by FIXED_K only
+ *   len    int32 [R]         out: admitted draft length l_r per request
+ *   K_out  int32 [1]         out: total admitted candidates K = sum l_r
+ *   theta_out f64 [1]        out: Theta(K) = (R + S_K) * SPS(R + K)
+ *   a_out  f32 [R, gamma]    out, may be NULL: survival products (f32, left to right)
+ *   order_out int32 [R*gamma] out, may be NULL: candidate ids r*gamma + j-1 sorted by
+ *                            a descending, ties by id ascending
+ * S_K and Theta are evaluated in f64.  R*gamma <= 16384. */
+int dspark_schedule(const float *conf, int32_t R, int32_t gamma, const float *sps,
+                    int32_t n_sps, int32_t mode, int32_t k_fixed, int32_t *len,
+                    int32_t *K_out, double *theta_out, float *a_out, int32_t *order_out,
+                    dspark_stream_t stream);
+
+/* Workspace bytes dspark_verify needs for `dims`. */
+size_t dspark_verify_workspace_bytes(const dspark_dims *dims);
+
+/* a8 — verification, "DSpark整体架构" Fig. 1 (accept a run, emit a corrected
+ * token G*) with the standard speculative-sampling rule:
+ *   tau == 0: accept x_j iff x_j == argmax_v t_j[v]; the first mismatch row's
+ *             argmax (or row l_r + 1 when all match) is the bonus token.
+ *   tau > 0:  accept x_j iff u * p_d(x_j) < p_t(x_j), u = U(seed; r, j, stream 1);
+ *             on the first rejection sample norm(max(0, p_t - p_d)) at that row
+ *             (Gumbel stream 2); when all l_r are accepted sample target row
+ *             l_r + 1 (Gumbel stream 3).  p = softmax(logits / tau).
+ *   anchor   int32 [R];  tokens int32 [R, gamma];  len int32 [R] (0..gamma)
+ *   base_logits bf16 [R*gamma, V], W1 bf16 [V, r], W2t bf16 [V, r]: the draft's
+ *            operands, used to rebuild p_d on the rejected row (tau > 0 only)
+ *   lse_d, logp_d f32 [R, gamma] from dspark_markov_draft (tau > 0 only)
+ *   target   bf16 [R, gamma + 1, V]  target logits; row j-1 scores position j
+ *   accepted int32 [R] out: accepted draft tokens n_r (0..l_r)
+ *   bonus    int32 [R] out: corrected / bonus token emitted after them
+ *   workspace device buffer of dspark_verify_workspace_bytes(dims) bytes.
+ * Pointers only read when tau > 0 may be NULL when tau == 0. */
+int dspark_verify(const dspark_dims *dims, const int32_t *anchor, const int32_t *tokens,
+                  const int32_t *len, const void *base_logits, const void *W1,
+                  const void *W2t, const float *lse_d, const float *logp_d,
+                  const void *target, float tau, uint64_t seed, int32_t *accepted,
+                  int32_t *bonus, void *workspace, size_t workspace_bytes,
+                  dspark_stream_t stream);
+
+/* Synchronises `stream`, returns the sticky device status word (DSPARK_OK or a
+ * DSPARK_ERR_* code) and clears it when clear != 0. */
+int dspark_device_status(dspark_stream_t stream, int clear);
+
+/* Human-readable name of a return / status code (static string). */
+const char *dspark_error_string(int code);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t dspark_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSPARK_H */

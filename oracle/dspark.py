@@ -125,16 +125,17 @@ def base_logits(h, W_lm, bf16_out: bool = True, vocab_chunk: int = 0) -> np.ndar
 # ---------------------------------------------------------------------------
 
 def markov_draft(base, h, anchor, W1, W2, w_conf, T, tau: float, seed: int,
-                 forced=None, keep_logits: bool = False,
+                 forced=None, keep_logits: bool = False, keep_scores: bool = False,
                  requests: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
     """Run the sequential head for k = 1..gamma.
 
     base [R, gamma, V] base logits; h [R, gamma, d]; anchor [R]; W1 [V, r];
     W2 [r, V]; w_conf [d + r]; T [gamma]; tau sampling temperature (0 = greedy).
     `forced` [R, gamma]: when given, step k conditions on forced[:, k-1] instead
-    of the oracle's own x_k (teacher forcing), so each step can be checked on
-    the path another implementation took.  `requests` gives the request ids used
-    for the random streams (default 0..R-1).
+    of the oracle's own x_k (used to evaluate the draft distribution along a
+    given token path, e.g. for verification).  `requests` gives the request ids
+    used for the random streams (default 0..R-1).  `keep_scores` returns the
+    decision score of every vocabulary entry at every step.
 
     Returns tokens (the oracle's own choice at each step), conf, z, margin (top-2
     gap of the decision score), and in sampling mode lse = logsumexp(l_k / tau)
@@ -161,6 +162,7 @@ def markov_draft(base, h, anchor, W1, W2, w_conf, T, tau: float, seed: int,
     logp = np.zeros((R, G))
     path = np.zeros((R, G), dtype=np.int64)
     logits = np.zeros((R, G, V)) if keep_logits else None
+    scores = np.zeros((R, G, V)) if keep_scores else None
     forced = None if forced is None else to_i64(forced)
 
     prev = anchor.copy()
@@ -185,40 +187,16 @@ def markov_draft(base, h, anchor, W1, W2, w_conf, T, tau: float, seed: int,
             logp[:, k - 1] = ell[np.arange(R), nxt] / tau - lse[:, k - 1]
         if keep_logits:
             logits[:, k - 1, :] = ell
+        if keep_scores:
+            scores[:, k - 1, :] = score
         prev = nxt
     out = dict(tokens=tokens, conf=conf, z=z_out, margin=margin, lse=lse, logp=logp,
                path=path)
     if keep_logits:
         out["logits"] = logits
+    if keep_scores:
+        out["scores"] = scores
     return out
-
-
-def draft_score_gap(base, h, anchor, W1, W2, tau, seed, chosen, requests=None):
-    """For each (r, k): max score minus the score of `chosen[r, k]` on the path `chosen`.
-
-    Zero where `chosen` is an argmax; used to check that a token picked by
-    another implementation near a tie is still a valid maximiser.
-    """
-    base = to_f64(base)
-    anchor = to_i64(anchor)
-    W1 = to_f64(W1)
-    W2 = to_f64(W2)
-    chosen = to_i64(chosen)
-    R, G, V = base.shape
-    req = np.arange(R) if requests is None else to_i64(requests)
-    vocab = np.arange(V, dtype=np.uint64)
-    gap = np.zeros((R, G))
-    prev = anchor.copy()
-    for k in range(1, G + 1):
-        ell = base[:, k - 1, :] + W1[prev] @ W2
-        if tau == 0.0:
-            score = ell
-        else:
-            score = ell / tau + philox.gumbel(seed, k, req[:, None], philox.STREAM_DRAFT,
-                                              vocab[None, :])
-        gap[:, k - 1] = score.max(axis=1) - score[np.arange(R), chosen[:, k - 1]]
-        prev = chosen[:, k - 1]
-    return gap
 
 
 # ---------------------------------------------------------------------------

@@ -1,0 +1,141 @@
+// common.cuh — shared device helpers of the DSpark CUDA library (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dspark.h"
+
+typedef __nv_bfloat16 bf16;
+
+// ---------------------------------------------------------------------------
+// host-side plumbing shared by every translation unit (defined in abi.cu)
+// ---------------------------------------------------------------------------
+void dspark_count_launches(uint64_t n);
+
+#define DSPARK_CHECK_LAUNCH()                                   \
+  do {                                                          \
+    cudaError_t _e = cudaGetLastError();                        \
+    if (_e != cudaSuccess) return DSPARK_ERR_CUDA;              \
+  } while (0)
+
+static inline int dspark_dims_ok(const dspark_dims *d) {
+  return d && d->R >= 1 && d->gamma >= 1 && d->gamma <= 32 && d->V >= 8 && d->V % 8 == 0 &&
+         d->r >= 64 && d->r % 64 == 0 && d->d >= 64 && d->d % 64 == 0;
+}
+
+static inline size_t dspark_align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---------------------------------------------------------------------------
+// device status word: one per translation unit, read by dspark_device_status
+// ---------------------------------------------------------------------------
+#define DSPARK_DECLARE_STATUS(name)                                        \
+  static __device__ int name;                                              \
+  __device__ __forceinline__ void dspark_set_status(int code) {            \
+    atomicCAS(&name, 0, code);                                             \
+  }
+
+// ---------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): 10 rounds of
+//   (c0,c1,c2,c3) <- (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1, lo(M0 c0))
+// with the key bumped by the Weyl constants between rounds.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+    const uint32_t lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+
+// Random streams of the library's draw layout.
+enum { RNG_DRAFT = 0, RNG_ACCEPT = 1, RNG_RESIDUAL = 2, RNG_BONUS = 3 };
+
+// The four words for vocabulary slots 4*q .. 4*q+3 at (position, request, stream).
+__device__ __forceinline__ uint4 rng_words4(uint64_t seed, uint32_t q, uint32_t pos,
+                                            uint32_t req, uint32_t stream) {
+  return philox4x32_10(make_uint4(q, pos, req, stream), (uint32_t)seed,
+                       (uint32_t)(seed >> 32));
+}
+
+// u = ((w >> 9) + 1/2) * 2^-23: exact in float, strictly inside (0, 1).
+__device__ __forceinline__ float rng_uniform(uint32_t w) {
+  return fmaf((float)(w >> 9), 0x1p-23f, 0x1p-24f);
+}
+
+// Gumbel(0,1) from one word: -log(-log u).  The inner log needs full relative
+// accuracy near u = 1 (the largest Gumbel values), the outer one does not.
+__device__ __forceinline__ float rng_gumbel(uint32_t w) {
+  const float e = -logf(rng_uniform(w));
+  return -__logf(e);
+}
+
+__device__ __forceinline__ uint32_t uint4_get(const uint4 &v, int i) {
+  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+// ---------------------------------------------------------------------------
+// argmax / log-sum-exp partial state (one per row and vocabulary tile)
+// ---------------------------------------------------------------------------
+struct __align__(16) RowPartial {
+  float m;       // max of the scaled logits s = l / tau       (sampling)
+  float sum;     // sum exp(s - m)                               (sampling)
+  float best;    // best decision score (logit, or s + Gumbel, or residual score)
+  int32_t idx;   // vocabulary id of `best` (lowest on ties)
+  float best_s;  // scaled logit s at idx                        (sampling)
+  float pad0, pad1, pad2;
+};
+
+// Is (a, ia) a better decision than (b, ib)?  Larger score, ties to lower id.
+__device__ __forceinline__ bool better(float a, int ia, float b, int ib) {
+  return a > b || (a == b && ia < ib);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Combine an online (m, sum) log-sum-exp pair with another.
+__device__ __forceinline__ void lse_merge(float &m, float &s, float m2, float s2) {
+  if (m2 == -INFINITY) return;
+  if (m == -INFINITY) { m = m2; s = s2; return; }
+  if (m2 > m) { s = s * __expf(m - m2) + s2; m = m2; }
+  else        { s = s + s2 * __expf(m2 - m); }
+}
+
+// Warp-wide merge of (m, sum, best, idx, best_s); every lane gets the result.
+__device__ __forceinline__ void warp_merge(float &m, float &s, float &best, int &idx,
+                                           float &bs) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    const float b2 = __shfl_xor_sync(0xffffffffu, best, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
+    const float bs2 = __shfl_xor_sync(0xffffffffu, bs, o);
+    lse_merge(m, s, m2, s2);
+    if (better(b2, i2, best, idx)) { best = b2; idx = i2; bs = bs2; }
+  }
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }

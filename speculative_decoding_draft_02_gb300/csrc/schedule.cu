@@ -1,0 +1,235 @@
+// schedule.cu — a5-a7: the hardware-aware prefix scheduler.
+//
+// "DSpark 深度解读" §二 设计二 (Hardware-Aware Prefix Scheduler): prefix survival
+// a_{r,j} = prod_{i<=j} c_{r,i}; all candidate extensions sorted globally by a
+// descending; admitting K of them gives verify batch B = R + K and expected
+// accepted tokens tau = R + S_K (S_K = sum of the admitted a), and the system
+// throughput Theta = tau * SPS(B).  The theoretical greedy admission stops at
+// the first K where Theta stops increasing (non-anticipating); §三 挑战2 drops
+// that break and searches every budget because measured SPS(B) curves are
+// stair-stepped; §三 挑战1 admits a capacity K fixed ahead of time (top-K).
+//
+// One CTA of 1024 threads: f32 survival products, a bitonic sort of composite
+// keys (~bits(a) << 32 | id) so that ties go to the lower (request, position),
+// a f64 block scan of the sorted products and the Theta search.
+#include "common.cuh"
+
+DSPARK_DECLARE_STATUS(s_status_sched)
+
+namespace {
+
+constexpr int SCHED_THREADS = 1024;
+constexpr int SCHED_MAX = 16384;
+
+__device__ __forceinline__ double theta_at(long K, double S, int R, const float *sps) {
+  return ((double)R + S) * (double)sps[R + K - 1];
+}
+
+__global__ void __launch_bounds__(SCHED_THREADS) schedule_kernel(
+    const float *__restrict__ conf, int R, int gamma, const float *__restrict__ sps, int mode,
+    int k_fixed, int n_pad, int32_t *__restrict__ len, int32_t *__restrict__ K_out,
+    double *__restrict__ theta_out, float *__restrict__ a_out, int32_t *__restrict__ order_out) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  unsigned long long *keys = reinterpret_cast<unsigned long long *>(smem_raw);
+  int32_t *cnt = reinterpret_cast<int32_t *>(keys + n_pad);  // [R]
+  __shared__ double warp_tot[32];
+  __shared__ double red_val[32];
+  __shared__ long red_k[32];
+  __shared__ long s_K;
+  __shared__ double s_theta;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = R * gamma;
+
+  // a5: survival products, f32 left to right; keys for the global order
+  for (int i = tid; i < R; i += SCHED_THREADS) {
+    float a = 1.f;
+    for (int j = 0; j < gamma; ++j) {
+      float c = conf[(size_t)i * gamma + j];
+      if (!(c >= 0.f && c <= 1.f)) {  // NaN or outside [0, 1]
+        dspark_set_status(DSPARK_ERR_ARG);
+        c = c > 1.f ? 1.f : 0.f;
+      }
+      a = (j == 0) ? c : __fmul_rn(a, c);
+      const int id = i * gamma + j;
+      if (a_out) a_out[id] = a;
+      keys[id] = ((unsigned long long)(~__float_as_uint(a)) << 32) | (unsigned)id;
+    }
+    cnt[i] = 0;
+  }
+  for (int i = n + tid; i < n_pad; i += SCHED_THREADS) keys[i] = ~0ull;
+  __syncthreads();
+
+  // a6: bitonic sort, ascending keys = descending a, ties by ascending id
+  for (int size = 2; size <= n_pad; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int t = tid; t < n_pad / 2; t += SCHED_THREADS) {
+        const int lo = 2 * t - (t & (stride - 1));
+        const int hi = lo + stride;
+        const bool up = ((lo & size) == 0);
+        const unsigned long long x = keys[lo], y = keys[hi];
+        if ((x > y) == up) { keys[lo] = y; keys[hi] = x; }
+      }
+      __syncthreads();
+    }
+  }
+
+  // a7: S_K by a block scan in f64; thread t owns sorted slots [t*per, (t+1)*per)
+  const int per = (n_pad + SCHED_THREADS - 1) / SCHED_THREADS;
+  const int beg = tid * per;
+  double local = 0.0;
+  for (int p = beg; p < beg + per && p < n; ++p)
+    local += (double)__uint_as_float(~(unsigned)(keys[p] >> 32));
+  // exclusive scan of `local` over the block
+  double incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    double w = warp_tot[lane];
+    double wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    warp_tot[lane] = wi - w;  // exclusive prefix of warp totals
+  }
+  __syncthreads();
+  double excl = __shfl_up_sync(0xffffffffu, incl, 1);
+  if (lane == 0) excl = 0.0;
+  const double S_beg = warp_tot[warp] + excl;  // S_{beg}
+  double S = S_beg;
+
+  // Theta over K = beg .. beg+per (K = 0 handled by thread 0)
+  double best = -INFINITY;  // threads past the end never win the argmax
+  long bestK = 0x7fffffffffffffffL;
+  long firstDrop = 0x7fffffffffffffffL;  // smallest K with Theta(K+1) <= Theta(K)
+  double prevTheta = 0.0;
+  if (beg <= n) {  // sps[R + K - 1] exists for K <= n only
+    prevTheta = theta_at(beg, S, R, sps);
+    best = prevTheta;
+    bestK = beg;
+  }
+  for (int p = beg; p < beg + per && p < n; ++p) {
+    S += (double)__uint_as_float(~(unsigned)(keys[p] >> 32));
+    const long K = p + 1;
+    const double th = theta_at(K, S, R, sps);
+    if (th > best) { best = th; bestK = K; }
+    if (th <= prevTheta && firstDrop > K - 1) firstDrop = K - 1;
+    prevTheta = th;
+  }
+
+  long K = 0;
+  if (mode == DSPARK_SCHED_UNCONSTRAINED) {
+    // argmax Theta, ties to the smallest K
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const double b2 = __shfl_xor_sync(0xffffffffu, best, o);
+      const long k2 = __shfl_xor_sync(0xffffffffu, bestK, o);
+      if (b2 > best || (b2 == best && k2 < bestK)) { best = b2; bestK = k2; }
+    }
+    if (lane == 0) { red_val[warp] = best; red_k[warp] = bestK; }
+    __syncthreads();
+    if (warp == 0) {
+      best = red_val[lane];
+      bestK = red_k[lane];
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const double b2 = __shfl_xor_sync(0xffffffffu, best, o);
+        const long k2 = __shfl_xor_sync(0xffffffffu, bestK, o);
+        if (b2 > best || (b2 == best && k2 < bestK)) { best = b2; bestK = k2; }
+      }
+      if (lane == 0) s_K = bestK;
+    }
+  } else if (mode == DSPARK_SCHED_BREAK) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const long k2 = __shfl_xor_sync(0xffffffffu, firstDrop, o);
+      firstDrop = k2 < firstDrop ? k2 : firstDrop;
+    }
+    if (lane == 0) red_k[warp] = firstDrop;
+    __syncthreads();
+    if (warp == 0) {
+      long f = red_k[lane];
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const long k2 = __shfl_xor_sync(0xffffffffu, f, o);
+        f = k2 < f ? k2 : f;
+      }
+      if (lane == 0) s_K = f < n ? f : n;
+    }
+  } else {
+    if (tid == 0) s_K = k_fixed < 0 ? 0 : (k_fixed > n ? n : k_fixed);
+  }
+  __syncthreads();
+  K = s_K;
+  if (K < 0 || K > n) K = 0;  // unreachable for finite tables; keeps every index in range
+
+  // per-request lengths: count admitted candidates of each request
+  for (int p = tid; p < K; p += SCHED_THREADS) {
+    const int id = (int)(keys[p] & 0xffffffffu);
+    atomicAdd(&cnt[id / gamma], 1);
+  }
+  if (order_out)
+    for (int p = tid; p < n; p += SCHED_THREADS) order_out[p] = (int)(keys[p] & 0xffffffffu);
+  // Theta(K): the owner of slot K recomputes it from its scan segment
+  if (tid == 0 && K == 0) s_theta = theta_at(0, 0.0, R, sps);
+  {
+    double S2 = S_beg;
+    for (int p = beg; p < beg + per && p < n; ++p) {
+      S2 += (double)__uint_as_float(~(unsigned)(keys[p] >> 32));
+      if (p + 1 == K) s_theta = theta_at(K, S2, R, sps);
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < R; i += SCHED_THREADS) len[i] = cnt[i];
+  if (tid == 0) {
+    *K_out = (int32_t)K;
+    *theta_out = s_theta;
+  }
+}
+
+}  // namespace
+
+extern "C" int dspark_schedule(const float *conf, int32_t R, int32_t gamma, const float *sps,
+                               int32_t n_sps, int32_t mode, int32_t k_fixed, int32_t *len,
+                               int32_t *K_out, double *theta_out, float *a_out,
+                               int32_t *order_out, dspark_stream_t stream) {
+  if (!conf || !sps || !len || !K_out || !theta_out || R < 1 || gamma < 1 || gamma > 32)
+    return DSPARK_ERR_ARG;
+  if (mode < DSPARK_SCHED_UNCONSTRAINED || mode > DSPARK_SCHED_FIXED_K) return DSPARK_ERR_ARG;
+  const long n = (long)R * gamma;
+  if (n > SCHED_MAX) return DSPARK_ERR_ARG;
+  if ((long)n_sps < (long)R * (gamma + 1)) return DSPARK_ERR_SPS_SHORT;
+  int n_pad = 2;
+  while (n_pad < n) n_pad <<= 1;
+  const size_t smem = sizeof(unsigned long long) * n_pad + sizeof(int32_t) * R;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             sizeof(unsigned long long) * SCHED_MAX + sizeof(int32_t) * SCHED_MAX) !=
+        cudaSuccess)
+      return DSPARK_ERR_CUDA;
+    attr_set = true;
+  }
+  schedule_kernel<<<1, SCHED_THREADS, smem, stream>>>(conf, R, gamma, sps, mode, k_fixed, n_pad,
+                                                      len, K_out, theta_out, a_out, order_out);
+  DSPARK_CHECK_LAUNCH();
+  dspark_count_launches(1);
+  return DSPARK_OK;
+}
+
+int dspark_status_sched(int clear) {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, s_status_sched, sizeof(int)) != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (clear) {
+    const int z = 0;
+    cudaMemcpyToSymbol(s_status_sched, &z, sizeof(int));
+  }
+  return v;
+}

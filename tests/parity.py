@@ -1,0 +1,144 @@
+"""Comparison rules shared by the GPU parity tests (CUDA path vs CPU oracle).
+
+Expected values always come from the oracle's own run on the same seeded
+inputs; CUDA outputs are only compared, never fed to the oracle.
+
+Rules:
+* integers decided by exact comparisons on identical inputs (greedy verify,
+  schedule order/lengths) must match bit for bit;
+* a token decided by a floating-point argmax must match wherever the oracle's
+  top-2 margin exceeds `tol`; inside the margin the CUDA token must still be a
+  maximiser within `tol` of the oracle's score, and the rest of that request's
+  chain (which conditions on the token) is excused;
+* confidences, log-sum-exps and log-probabilities within `rtol`.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+import oracle
+
+
+def host(x):
+    if isinstance(x, torch.Tensor):
+        x = x.detach().cpu()
+        if x.dtype == torch.bfloat16:
+            x = x.float()
+        return x.numpy()
+    return np.asarray(x)
+
+
+@dataclass
+class DraftReport:
+    compared: int = 0
+    flagged: int = 0
+    excused: int = 0
+    max_conf_err: float = 0.0
+    max_lse_err: float = 0.0
+    notes: list = field(default_factory=list)
+
+
+def compare_draft(gpu_tokens, gpu_conf, gpu_lse, gpu_logp, orc, tau, tol_rel=1e-3,
+                  conf_rtol=1e-2, requests=None) -> DraftReport:
+    """Walk each request's chain; see module docstring.  `orc` from oracle.markov_draft(keep_scores)."""
+    gt = host(gpu_tokens).astype(np.int64)
+    gc = host(gpu_conf).astype(np.float64)
+    gl = None if gpu_lse is None else host(gpu_lse).astype(np.float64)
+    gp = None if gpu_logp is None else host(gpu_logp).astype(np.float64)
+    R, G = orc["tokens"].shape
+    rows = range(R) if requests is None else requests
+    rep = DraftReport()
+    for oi, i in enumerate(rows):
+        for k in range(G):
+            c_o = orc["conf"][oi, k]
+            err = abs(gc[i, k] - c_o)
+            rep.max_conf_err = max(rep.max_conf_err, err / max(abs(c_o), 1e-30))
+            assert err <= conf_rtol * abs(c_o) + 1e-6, (i, k, gc[i, k], c_o)
+            s = orc["scores"][oi, k]
+            smax = float(s.max())
+            tol = tol_rel * max(1.0, abs(smax))
+            g = int(gt[i, k])
+            assert 0 <= g < s.size
+            rep.compared += 1
+            if orc["margin"][oi, k] > tol:
+                assert g == orc["tokens"][oi, k], (i, k, g, orc["tokens"][oi, k],
+                                                   orc["margin"][oi, k])
+            else:
+                rep.flagged += 1
+                assert smax - s[g] <= tol, (i, k, smax - s[g], tol)
+            if tau > 0 and gl is not None:
+                e = abs(gl[i, k] - orc["lse"][oi, k])
+                rep.max_lse_err = max(rep.max_lse_err, e)
+                assert e <= conf_rtol * max(1.0, abs(orc["lse"][oi, k])), (i, k, e)
+                if g == orc["tokens"][oi, k] and gp is not None:
+                    assert abs(gp[i, k] - orc["logp"][oi, k]) <= conf_rtol * max(
+                        1.0, abs(orc["logp"][oi, k])), (i, k, gp[i, k], orc["logp"][oi, k])
+            if g != orc["tokens"][oi, k]:
+                rep.excused += G - k - 1
+                break
+    return rep
+
+
+def compare_verify(gpu_acc, gpu_bonus, orc, tau, tol=1e-3):
+    """Accepted counts and bonus tokens; sampling decisions inside `tol` are flagged."""
+    ga = host(gpu_acc).astype(np.int64)
+    gb = host(gpu_bonus).astype(np.int64)
+    flagged = 0
+    R = orc["accepted"].size
+    for i in range(R):
+        if tau == 0.0:
+            assert ga[i] == orc["accepted"][i], (i, ga[i], orc["accepted"][i])
+            assert gb[i] == orc["bonus"][i], (i, gb[i], orc["bonus"][i])
+            continue
+        m = orc["accept_margin"][i]
+        n_o = orc["accepted"][i]
+        tested = m[:min(n_o + 1, m.size)]
+        tested = tested[~np.isnan(tested)]
+        if np.any(np.abs(tested) < tol):
+            flagged += 1
+            continue
+        assert ga[i] == n_o, (i, ga[i], n_o)
+        if orc["final_margin"][i] <= tol:
+            flagged += 1
+            continue
+        assert gb[i] == orc["bonus"][i], (i, gb[i], orc["bonus"][i])
+    return flagged
+
+
+def sorted_order_ok(order, a):
+    """order lists every id once, a non-increasing along it, ties by ascending id."""
+    order = np.asarray(order)
+    flat = a.reshape(-1)
+    assert sorted(order.tolist()) == list(range(flat.size))
+    for p in range(flat.size - 1):
+        x, y = flat[order[p]], flat[order[p + 1]]
+        assert x > y or (x == y and order[p] < order[p + 1])
+    return True
+
+
+def oracle_draft_inputs(inp):
+    """Convert a workloads.make_inputs dict to the oracle's float64 view."""
+    return {k: (oracle.dspark.to_f64(v) if isinstance(v, torch.Tensor) and v.is_floating_point()
+                else v) for k, v in inp.items()}
+
+
+def schedule_is_robust(o_s, rel=1e-4) -> bool:
+    """True when perturbing the confidences by `rel` cannot change the oracle's
+    schedule: distinct survival products are `rel` apart and the chosen Theta
+    beats every other budget by `rel` (unconstrained) or every step is `rel`
+    away from a tie (break)."""
+    a = np.sort(o_s["a"].reshape(-1).astype(np.float64))
+    d = np.diff(a)
+    d = d[d > 0]
+    if d.size and np.min(d / a[1:][np.diff(a) > 0]) < rel:
+        return False
+    th = o_s["thetas"]
+    K = o_s["K"]
+    others = np.delete(th, K)
+    if others.size and np.max(others) > th[K] * (1 - rel):
+        step = np.abs(np.diff(th)) / th[1:]
+        return bool(np.min(step) > rel)
+    return True

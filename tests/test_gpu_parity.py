@@ -1,0 +1,313 @@
+"""GPU parity: every stage of the CUDA path against the CPU oracle, through the C-ABI.
+
+Sizes span several tiles with a ragged tail and finish in seconds on the oracle;
+full-size checks at the benchmark's workload are in test_gpu_fullsize.py.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from parity import (compare_draft, compare_verify, host, schedule_is_robust,
+                    sorted_order_ok)
+
+pytestmark = pytest.mark.gpu
+
+dsp = pytest.importorskip("speculative_decoding_draft_02_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from speculative_decoding_draft_02_gb300 import build
+    build.build()
+    dsp.load_library()
+    yield
+    assert dsp.dspark_device_status() == 0
+
+
+def dev(t, dtype=None):
+    t = t.to("cuda")
+    return t.to(dtype) if dtype is not None else t
+
+
+SHAPES = [  # (R, gamma, V, r, d)
+    (4, 5, 1024, 64, 256),       # the tiny workload
+    (37, 4, 1000, 128, 320),     # ragged in rows and vocabulary
+    (3, 3, 4104, 256, 512),      # vocabulary tail of 8
+    (130, 2, 2056, 64, 192),     # rows past one 128-row tile
+    (1, 1, 520, 64, 64),         # degenerate: one request, one position
+]
+
+
+def _weights(R, G, V, r, d, seed):
+    w = workloads.WORKLOADS["tiny"].with_(R=R, gamma=G, V=V, r=r, d=d, anchor_hi=V)
+    return workloads.make_inputs(w, seed=seed, with_target_noise=False)
+
+
+# ------------------------------------------------------------------ a1 ----
+
+@pytest.mark.parametrize("shape", SHAPES)
+def test_lm_head_matches_oracle(shape):
+    R, G, V, r, d = shape
+    inp = _weights(R, G, V, r, d, seed=100 + V)
+    h = inp["h"].reshape(R * G, d)
+    want = oracle.base_logits(h, inp["W_lm"])                       # bf16-rounded
+    dims = dsp.dims_of(R, G, V, r, d)
+    out = torch.empty((R * G, V), dtype=torch.bfloat16, device="cuda")
+    dsp.dspark_lm_head(dims, dev(h, torch.bfloat16), dev(inp["W_lm"], torch.bfloat16), out)
+    got = host(out).astype(np.float64)
+    exact = oracle.base_logits(h, inp["W_lm"], bf16_out=False)
+    # within one bf16 rounding step of the exact value (1e-2 relative is the bar)
+    err = np.abs(got - exact)
+    assert np.all(err <= 2.0 ** -8 * np.abs(exact) + 1e-6), err.max()
+    assert np.mean(got == want) > 0.999
+
+
+def test_pack_w2_is_transpose():
+    inp = _weights(2, 2, 1000, 128, 64, seed=7)
+    dims = dsp.dims_of(2, 2, 1000, 128, 64)
+    W2 = dev(inp["W2"], torch.bfloat16)
+    W2t = torch.empty((1000, 128), dtype=torch.bfloat16, device="cuda")
+    dsp.dspark_pack_w2(dims, W2, W2t)
+    assert torch.equal(W2t, W2.t().contiguous())
+
+
+# --------------------------------------------------------------- a2-a4 ----
+
+def _draft_case(shape, tau, seed):
+    R, G, V, r, d = shape
+    inp = _weights(R, G, V, r, d, seed=seed)
+    base = workloads.random_normal((R, G, V), 1.0, seed + 1)
+    orc = oracle.markov_draft(base, inp["h"], inp["anchor"], inp["W1"], inp["W2"],
+                              inp["w_conf"], inp["T"], tau, seed=12345 + seed, keep_scores=True)
+    head = dsp.DraftHead.from_weights(R, G, inp["W_lm"], inp["W1"], inp["W2"], inp["w_conf"],
+                                      inp["T"])
+    rnd = dsp.Round(head)
+    rnd.base.copy_(dev(base.reshape(R * G, V)))
+    dsp.dspark_markov_draft(head.dims, rnd.base, dev(inp["h"], torch.bfloat16).contiguous(),
+                            dev(inp["anchor"]), head.W1, head.W2t, head.w_conf, head.T, tau,
+                            12345 + seed, rnd.tokens, rnd.conf, rnd.logp_d, rnd.lse_d,
+                            rnd.ws_draft)
+    return rnd, orc
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("tau", [0.0, 1.0, 0.6])
+def test_markov_draft_matches_oracle(shape, tau):
+    rnd, orc = _draft_case(shape, tau, seed=200 + shape[2])
+    rep = compare_draft(rnd.tokens, rnd.conf, rnd.lse_d if tau > 0 else None,
+                        rnd.logp_d if tau > 0 else None, orc, tau)
+    assert rep.compared >= shape[0]
+    assert rep.flagged <= max(2, rep.compared // 50)
+    assert dsp.dspark_device_status() == 0
+
+
+def test_markov_zero_bias_is_parallel_argmax():
+    """W2 = 0 gives plain parallel drafting: x_k = argmax of the base logits."""
+    R, G, V, r, d = 9, 3, 1000, 64, 128
+    inp = _weights(R, G, V, r, d, seed=31)
+    inp["W2"] = torch.zeros_like(inp["W2"])
+    base = workloads.random_normal((R, G, V), 1.0, 32)
+    head = dsp.DraftHead.from_weights(R, G, inp["W_lm"], inp["W1"], inp["W2"], inp["w_conf"],
+                                      inp["T"])
+    rnd = dsp.Round(head)
+    rnd.base.copy_(dev(base.reshape(R * G, V)))
+    dsp.dspark_markov_draft(head.dims, rnd.base, dev(inp["h"], torch.bfloat16).contiguous(),
+                            dev(inp["anchor"]), head.W1, head.W2t, head.w_conf, head.T, 0.0, 0,
+                            rnd.tokens, rnd.conf, None, None, rnd.ws_draft)
+    want = torch.argmax(base.float(), dim=2)  # first maximum on ties
+    assert torch.equal(rnd.tokens.cpu().long(), want)
+
+
+# --------------------------------------------------------------- a5-a7 ----
+
+SPS_KINDS = ["linear", "concave", "stair"]
+
+
+def sps_for(kind, n):
+    """Positive SPS tables of n entries (the workloads' linear table is 64 long)."""
+    if kind == "linear":
+        B = torch.arange(1, n + 1, dtype=torch.float64)
+        return (1000.0 * (1.0 - (B - 1.0) / (2.0 * n))).to(torch.float32)
+    return workloads.sps_table(kind, n)
+
+
+@pytest.mark.parametrize("R,G", [(4, 5), (1, 8), (64, 8), (256, 5), (1024, 7), (3, 1),
+                                 (2047, 8)])
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_schedule_matches_oracle(R, G, mode):
+    for kind in SPS_KINDS:
+        c = workloads.random_confidences(R, G, seed=R * 31 + G, ones_frac=0.05)
+        n = R * (G + 1)
+        sps = sps_for(kind, n)
+        kf = (R * G) // 3
+        o = oracle.schedule(c, sps, mode, kf)
+        length = torch.empty(R, dtype=torch.int32, device="cuda")
+        K = torch.empty(1, dtype=torch.int32, device="cuda")
+        th = torch.empty(1, dtype=torch.float64, device="cuda")
+        a = torch.empty((R, G), dtype=torch.float32, device="cuda")
+        order = torch.empty(R * G, dtype=torch.int32, device="cuda")
+        dsp.dspark_schedule(dev(c), R, G, dev(sps), mode, kf, length, K, th, a, order)
+        assert np.array_equal(host(a), o["a"])                         # bit-exact f32 products
+        assert np.array_equal(host(order), o["order"])                 # same total order
+        k_gpu = int(K.item())
+        if k_gpu != o["K"]:  # only a floating tie of Theta may separate them
+            assert abs(o["thetas"][k_gpu] - o["theta"]) <= 1e-12 * o["theta"], (kind, k_gpu)
+        else:
+            assert np.array_equal(host(length), o["len"])
+        assert float(th.item()) == pytest.approx(o["thetas"][k_gpu], rel=1e-12)
+
+
+def test_schedule_extremes():
+    R, G = 50, 4
+    c = workloads.random_confidences(R, G, seed=5)
+    dec = torch.tensor(np.geomspace(1000, 1e-3, R * (G + 1)), dtype=torch.float32)
+    flat = torch.full((R * (G + 1),), 500.0)
+    neg = -torch.arange(1, R * (G + 1) + 1, dtype=torch.float32)  # meaningless but must be safe
+    for sps, want_k in [(dec, 0), (flat, R * G), (neg, oracle.schedule(c, neg)["K"])]:
+        length = torch.empty(R, dtype=torch.int32, device="cuda")
+        K = torch.empty(1, dtype=torch.int32, device="cuda")
+        th = torch.empty(1, dtype=torch.float64, device="cuda")
+        dsp.dspark_schedule(dev(c), R, G, dev(sps), 0, 0, length, K, th)
+        assert int(K.item()) == want_k
+        assert int(length.sum().item()) == want_k
+        assert sorted_order_ok(oracle.schedule(c, sps)["order"], oracle.survival(c))
+
+
+# ------------------------------------------------------------------ a8 ----
+
+def _verify_case(shape, tau, seed, accept_bias=0.7):
+    R, G, V, r, d = shape
+    inp = _weights(R, G, V, r, d, seed=seed)
+    base = workloads.random_normal((R, G, V), 1.0, seed + 1)
+    tokens = workloads.random_tokens(R, G, V, seed + 2)
+    lens = workloads.random_lengths(R, G, seed + 3)
+    noise = workloads.random_normal((R, G + 1, V), 0.3, seed + 4, dtype=torch.float32)
+    if tau == 0.0:
+        target = workloads.random_normal((R, G + 1, V), 1.0, seed + 5)
+        # make runs of accepted tokens likely: drafts equal the target argmax mostly
+        am = torch.argmax(target[:, :G].float(), dim=2).to(torch.int32)
+        pick = workloads.random_normal((R, G), 1.0, seed + 6, dtype=torch.float32) < accept_bias
+        tokens = torch.where(pick, am, tokens)
+        dl = None
+        lse_d = logp_d = torch.zeros((R, G))
+    else:
+        orc_d = oracle.markov_draft(base, inp["h"], inp["anchor"], inp["W1"], inp["W2"],
+                                    inp["w_conf"], inp["T"], tau, 0, forced=tokens,
+                                    keep_logits=True)
+        dl = orc_d["logits"]
+        lse_d = torch.tensor(orc_d["lse"], dtype=torch.float32)
+        logp_d = torch.tensor(orc_d["logp"], dtype=torch.float32)
+        # target near the draft so that acceptance and rejection both happen
+        t = np.concatenate([dl, dl[:, -1:]], axis=1) + noise.numpy()
+        target = torch.tensor(t, dtype=torch.float32).to(torch.bfloat16)
+    orc = oracle.verify(tokens, lens, dl, target, tau, seed=777 + seed)
+    head = dsp.DraftHead.from_weights(R, G, inp["W_lm"], inp["W1"], inp["W2"], inp["w_conf"],
+                                      inp["T"])
+    rnd = dsp.Round(head)
+    rnd.base.copy_(dev(base.reshape(R * G, V)))
+    rnd.tokens.copy_(dev(tokens))
+    rnd.len.copy_(dev(lens))
+    rnd.lse_d.copy_(dev(lse_d))
+    rnd.logp_d.copy_(dev(logp_d))
+    rnd.verify(dev(inp["anchor"]), dev(target).contiguous(), tau, 777 + seed)
+    return rnd, orc, lens
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("tau", [0.0, 1.0, 0.8])
+def test_verify_matches_oracle(shape, tau):
+    rnd, orc, lens = _verify_case(shape, tau, seed=300 + shape[2])
+    flagged = compare_verify(rnd.accepted, rnd.bonus, orc, tau)
+    assert flagged <= max(1, shape[0] // 20)
+    acc = host(rnd.accepted)
+    assert np.all(acc >= 0) and np.all(acc <= host(lens))
+    assert dsp.dspark_device_status() == 0
+
+
+def test_verify_zero_lengths_take_bonus_from_row_one():
+    shape = (16, 3, 1000, 64, 64)
+    R, G, V = shape[:3]
+    for tau in (0.0, 1.0):
+        inp = _weights(*shape, seed=41)
+        target = workloads.random_normal((R, G + 1, V), 1.0, 42)
+        head = dsp.DraftHead.from_weights(R, G, inp["W_lm"], inp["W1"], inp["W2"],
+                                          inp["w_conf"], inp["T"])
+        rnd = dsp.Round(head)
+        rnd.tokens.zero_()
+        rnd.len.zero_()
+        rnd.lse_d.zero_()
+        rnd.logp_d.zero_()
+        rnd.base.zero_()
+        rnd.verify(dev(inp["anchor"]), dev(target), tau, 9)
+        orc = oracle.verify(np.zeros((R, G), int), np.zeros(R, int), np.zeros((R, G, V)),
+                            target, tau, 9)
+        assert np.all(host(rnd.accepted) == 0)
+        compare_verify(rnd.accepted, rnd.bonus, orc, tau)
+
+
+def test_device_status_reports_bad_tokens_and_lengths():
+    shape = (4, 3, 1000, 64, 64)
+    R, G, V = shape[:3]
+    inp = _weights(*shape, seed=51)
+    head = dsp.DraftHead.from_weights(R, G, inp["W_lm"], inp["W1"], inp["W2"], inp["w_conf"],
+                                      inp["T"])
+    rnd = dsp.Round(head)
+    assert dsp.dspark_device_status() == 0
+    bad_anchor = torch.tensor([0, 1, V + 5, 2], dtype=torch.int32, device="cuda")
+    h = dev(inp["h"], torch.bfloat16).contiguous()
+    rnd.base.zero_()
+    dsp.dspark_markov_draft(head.dims, rnd.base, h, bad_anchor, head.W1, head.W2t, head.w_conf,
+                            head.T, 0.0, 0, rnd.tokens, rnd.conf, None, None, rnd.ws_draft)
+    assert dsp.dspark_device_status() == 5          # DSPARK_ERR_TOKEN, then cleared
+    assert dsp.dspark_device_status() == 0
+    rnd.len.copy_(torch.tensor([0, 1, G + 2, 1], dtype=torch.int32))
+    target = torch.zeros((R, G + 1, V), dtype=torch.bfloat16, device="cuda")
+    rnd.verify(dev(inp["anchor"]), target, 0.0, 1)
+    assert dsp.dspark_device_status() == 6          # DSPARK_ERR_LENGTH
+    with pytest.raises(dsp.DSparkError):
+        dsp.dspark_verify(head.dims, None, rnd.tokens, rnd.len, None, None, None, None, None,
+                          target, 1.0, 0, rnd.accepted, rnd.bonus, rnd.ws_verify)
+
+
+# ------------------------------------------------------------ the round ---
+
+@pytest.mark.parametrize("name,tau,mode", [("tiny", 0.0, 0), ("tiny", 1.0, 1),
+                                           ("tiny", 0.7, 2)])
+def test_round_matches_oracle_end_to_end(name, tau, mode):
+    w = workloads.WORKLOADS[name]
+    inp = workloads.make_inputs(w)
+    R, G, V, d = w.R, w.gamma, w.V, w.d
+    orc_base = oracle.base_logits(inp["h"], inp["W_lm"])
+    nxt = oracle.base_logits(inp["h_next"], inp["W_lm"])
+    target_np = np.concatenate([orc_base, nxt[:, None, :]], axis=1) + host(inp["noise"])
+    target = torch.tensor(target_np, dtype=torch.float32).to(torch.bfloat16)
+    ds, vs = inp["draft_seed"], inp["verify_seed"]
+    orc = oracle.markov_draft(orc_base, inp["h"], inp["anchor"], inp["W1"], inp["W2"],
+                              inp["w_conf"], inp["T"], tau, ds, keep_scores=True,
+                              keep_logits=True)
+    head = dsp.DraftHead.from_weights(R, G, inp["W_lm"], inp["W1"], inp["W2"], inp["w_conf"],
+                                      inp["T"])
+    rnd = dsp.Round(head)
+    h = dev(inp["h"], torch.bfloat16).contiguous()
+    anchor = dev(inp["anchor"])
+    sps = dev(inp["sps"])
+    rnd.run(h, anchor, dev(target).contiguous(), sps, tau, ds, vs, mode=mode, k_fixed=R * G // 2)
+    torch.cuda.synchronize()
+    rep = compare_draft(rnd.tokens, rnd.conf, rnd.lse_d if tau > 0 else None,
+                        rnd.logp_d if tau > 0 else None, orc, tau, tol_rel=1e-2)
+    same_tokens = np.array_equal(host(rnd.tokens), orc["tokens"])
+    if same_tokens:
+        # the GPU schedules its own confidences (equal to the oracle's within
+        # rounding); compare with the oracle's schedule where that is robust
+        o_s = oracle.schedule(orc["conf"].astype(np.float32), inp["sps"], mode, R * G // 2)
+        if schedule_is_robust(o_s, rel=1e-4):
+            assert np.array_equal(host(rnd.len), o_s["len"])
+            ov = oracle.verify(orc["tokens"], o_s["len"], orc["logits"], target, tau, vs)
+            compare_verify(rnd.accepted, rnd.bonus, ov, tau)
+    assert dsp.dspark_device_status() == 0

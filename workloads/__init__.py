@@ -186,3 +186,12 @@ def random_lengths(R: int, gamma: int, seed: int, device: str = "cpu") -> torch.
     g.manual_seed(seed)
     return torch.randint(0, gamma + 1, (R,), generator=g, device=device,
                          dtype=torch.int64).to(torch.int32)
+
+
+def random_normal(shape, std: float, seed: int, device: str = "cpu",
+                  dtype=torch.bfloat16) -> torch.Tensor:
+    """N(0, std) samples rounded to `dtype` (e.g. stand-alone logits for stage tests)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    t = torch.randn(tuple(shape), generator=g, device=device, dtype=torch.float32)
+    return t.mul_(std).to(dtype)
