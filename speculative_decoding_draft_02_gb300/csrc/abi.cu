@@ -8,8 +8,9 @@ static std::atomic<uint64_t> g_launches{0};
 
 void dspark_count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
-int dspark_lm_head_simple(const dspark_dims *, const void *, const void *, void *, cudaStream_t);
+int dspark_lm_head_tc(const dspark_dims *, const void *, const void *, void *, cudaStream_t);
 int dspark_status_lmhead(int clear);
+int dspark_status_lmhead_tc(int clear);
 int dspark_status_markov(int clear);
 int dspark_status_verify(int clear);
 int dspark_status_sched(int clear);
@@ -33,8 +34,9 @@ extern "C" const char *dspark_error_string(int code) {
 extern "C" int dspark_device_status(dspark_stream_t stream, int clear) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return DSPARK_ERR_CUDA;
   int first = DSPARK_OK;
-  const int vals[4] = {dspark_status_lmhead(clear), dspark_status_markov(clear),
-                       dspark_status_verify(clear), dspark_status_sched(clear)};
+  const int vals[5] = {dspark_status_lmhead(clear), dspark_status_lmhead_tc(clear),
+                       dspark_status_markov(clear), dspark_status_verify(clear),
+                       dspark_status_sched(clear)};
   for (int v : vals)
     if (first == DSPARK_OK && v != DSPARK_OK) first = v;
   return first;
@@ -44,7 +46,7 @@ extern "C" int dspark_lm_head(const dspark_dims *dims, const void *h, const void
                               void *base_logits, dspark_stream_t stream) {
   if (!dspark_dims_ok(dims) || !h || !W_lm || !base_logits) return DSPARK_ERR_ARG;
   if (((uintptr_t)h | (uintptr_t)W_lm | (uintptr_t)base_logits) & 15) return DSPARK_ERR_ARG;
-  return dspark_lm_head_simple(dims, h, W_lm, base_logits, stream);
+  return dspark_lm_head_tc(dims, h, W_lm, base_logits, stream);
 }
 
 extern "C" int dspark_draft(const dspark_dims *dims, const void *h, const int32_t *anchor,

@@ -1,0 +1,203 @@
+// umma_gemm.cuh — persistent tcgen05 GEMM  D[M, N] = A[M, K] . B[N, K]^T with a
+// pluggable epilogue that reads the f32 accumulator straight from TMEM.
+//
+// One CTA per SM, 192 threads:
+//   warp 0      one thread issues TMA loads of A (128 x 64) and B (256 x 64)
+//               tiles into a STAGES-deep shared-memory ring;
+//   warp 1      allocates TMEM (2 x 256 columns: a double-buffered 128 x 256 f32
+//               accumulator) and one thread issues tcgen05.mma (M=128, N=256,
+//               K=16 per instruction, 4 per 64-wide stage), committing each
+//               stage back to the producer and each finished tile to the
+//               epilogue;
+//   warps 2..5  the epilogue: thread t owns accumulator row t (TMEM lane), so a
+//               row-wise reduction over the tile needs no shuffles.
+// Tiles are visited m-fastest, so the CTAs working at the same time share one
+// B tile (one read from HBM, the rest from L2).  Every wait is bounded; on
+// timeout the CTA raises DSPARK_ERR_TIMEOUT, drains its own copies and MMAs,
+// frees TMEM and exits.
+#pragma once
+#include "tcgen05.cuh"
+
+namespace gemm {
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NUM_THREADS = 192;
+constexpr int EPI_THREADS = 128;
+constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
+
+struct SharedCtl {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// Epi must provide: __device__ void operator()(int m0, int n0, int row, uint32_t taddr) const
+// (all 128 epilogue threads call it for each tile; it must tcgen05.ld every
+// 32-column chunk of the 256 columns warp-uniformly) and
+// __device__ void on_timeout() const.
+template <class Epi>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
+                     const __grid_constant__ CUtensorMap tma_b, int M, int N, int K, Epi epi) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *base = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *sA = base;
+  uint8_t *sB = base + STAGES * A_BYTES;
+  SharedCtl *ctl = reinterpret_cast<SharedCtl *>(base + STAGES * STAGE_BYTES);
+  volatile int *abort = &ctl->abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_m = (M + BM - 1) / BM, num_n = (N + BN - 1) / BN;
+  const int num_tiles = num_m * num_n;
+  const int k_iters = K / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(&ctl->full[s], 1);
+      tc::mbar_init(&ctl->empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&ctl->tfull[b], 1);
+      tc::mbar_init(&ctl->tempty[b], EPI_THREADS);
+    }
+    tc::mbar_init(&ctl->drain, 1);
+    ctl->abort = 0;
+    tc::fence_barrier_init();
+    tc::tma_prefetch_desc(&tma_a);
+    tc::tma_prefetch_desc(&tma_b);
+  }
+  if (warp == 1) tc::tmem_alloc(&ctl->tmem_base, TMEM_COLS);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem_base = ctl->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer ----
+      const uint64_t pol_a = tc::policy_evict_last();   // A tiles are re-read
+      const uint64_t pol_b = tc::policy_evict_first();  // B streams through
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued[STAGES];
+      for (int s = 0; s < STAGES; ++s) issued[s] = -1;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        const int m_blk = tile % num_m, n_blk = tile / num_m;
+        for (int kb = 0; kb < k_iters; ++kb) {
+          if (!tc::mbar_wait(&ctl->empty[stage], phase ^ 1, abort)) { ok = false; break; }
+          tc::mbar_expect_tx(&ctl->full[stage], STAGE_BYTES);
+          tc::tma_load_2d(sA + stage * A_BYTES, &tma_a, kb * BK, m_blk * BM, &ctl->full[stage],
+                          pol_a);
+          tc::tma_load_2d(sB + stage * B_BYTES, &tma_b, kb * BK, n_blk * BN, &ctl->full[stage],
+                          pol_b);
+          issued[stage] = (int)phase;
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+      // drain: every copy this thread issued has landed before the CTA exits
+      volatile int never = 0;
+      for (int s = 0; s < STAGES; ++s)
+        if (issued[s] >= 0) tc::mbar_wait(&ctl->full[s], (uint32_t)issued[s], &never);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------- MMA issuer -----
+      const uint32_t idesc = tc::idesc_bf16(BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        if (!tc::mbar_wait(&ctl->tempty[acc], acc_phase ^ 1, abort)) break;
+        tc::fence_after_sync();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < k_iters; ++kb) {
+          if (!tc::mbar_wait(&ctl->full[stage], phase, abort)) { ok = false; break; }
+          tc::fence_after_sync();
+          const uint64_t a_desc = tc::smem_desc_sw128(sA + stage * A_BYTES);
+          const uint64_t b_desc = tc::smem_desc_sw128(sB + stage * B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)  // +32 B per 16-element K step
+            tc::umma_bf16(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc,
+                          (kb | k) != 0 ? 1u : 0u);
+          tc::umma_commit(&ctl->empty[stage]);
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        tc::umma_commit(&ctl->tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      // drain: all MMAs issued by this thread have finished
+      tc::umma_commit(&ctl->drain);
+      volatile int never = 0;
+      tc::mbar_wait(&ctl->drain, 0, &never);
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------- epilogue --------
+    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      const int m_blk = tile % num_m, n_blk = tile / num_m;
+      // one lane polls, then the warp proceeds together (tcgen05.ld is warp-wide)
+      int ok = 1;
+      if (lane == 0) ok = tc::mbar_wait(&ctl->tfull[acc], acc_phase, abort) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc::fence_after_sync();
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+      epi(m_blk * BM, n_blk * BN, row, taddr);
+      tc::fence_before_sync();
+      tc::mbar_arrive(&ctl->tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (ctl->abort && threadIdx.x == 0) epi.on_timeout();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+template <class Epi>
+int launch(const void *A, const void *B, int M, int N, int K, const Epi &epi,
+           cudaStream_t stream) {
+  CUtensorMap ta, tb;
+  if (dspark_make_tmap_bf16(&ta, A, (uint64_t)M, (uint64_t)K, BM) != 0) return DSPARK_ERR_CUDA;
+  if (dspark_make_tmap_bf16(&tb, B, (uint64_t)N, (uint64_t)K, BN) != 0) return DSPARK_ERR_CUDA;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(umma_gemm_kernel<Epi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SMEM_BYTES) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
+    attr = true;
+  }
+  const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const int grid = tiles < dspark_sm_count() ? tiles : dspark_sm_count();
+  umma_gemm_kernel<Epi><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ta, tb, M, N, K, epi);
+  if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+  dspark_count_launches(1);
+  return DSPARK_OK;
+}
+
+}  // namespace gemm
