@@ -10,7 +10,6 @@ void dspark_count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_ord
 
 int dspark_lm_head_tc(const dspark_dims *, const void *, const void *, void *, cudaStream_t);
 int dspark_status_lmhead(int clear);
-int dspark_status_lmhead_tc(int clear);
 int dspark_status_markov(int clear);
 int dspark_status_verify(int clear);
 int dspark_status_sched(int clear);
@@ -34,9 +33,8 @@ extern "C" const char *dspark_error_string(int code) {
 extern "C" int dspark_device_status(dspark_stream_t stream, int clear) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return DSPARK_ERR_CUDA;
   int first = DSPARK_OK;
-  const int vals[5] = {dspark_status_lmhead(clear), dspark_status_lmhead_tc(clear),
-                       dspark_status_markov(clear), dspark_status_verify(clear),
-                       dspark_status_sched(clear)};
+  const int vals[4] = {dspark_status_lmhead(clear), dspark_status_markov(clear),
+                       dspark_status_verify(clear), dspark_status_sched(clear)};
   for (int v : vals)
     if (first == DSPARK_OK && v != DSPARK_OK) first = v;
   return first;

@@ -30,11 +30,14 @@ static inline size_t dspark_align_up(size_t x, size_t a) { return (x + a - 1) / 
 // ---------------------------------------------------------------------------
 // device status word: one per translation unit, read by dspark_device_status
 // ---------------------------------------------------------------------------
+// Each translation unit that launches kernels defines its own word with
+// DSPARK_DECLARE_STATUS and exports a host reader; device code records the
+// first problem it finds with dspark_set_status().
+static __device__ void dspark_set_status(int code);
+
 #define DSPARK_DECLARE_STATUS(name)                                        \
   static __device__ int name;                                              \
-  __device__ __forceinline__ void dspark_set_status(int code) {            \
-    atomicCAS(&name, 0, code);                                             \
-  }
+  static __device__ void dspark_set_status(int code) { atomicCAS(&name, 0, code); }
 
 // ---------------------------------------------------------------------------
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): 10 rounds of
@@ -44,16 +47,41 @@ static inline size_t dspark_align_up(size_t x, size_t a) { return (x + a - 1) / 
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
 #pragma unroll
   for (int i = 0; i < 10; ++i) {
-    const uint32_t lo0 = 0xD2511F53u * c.x;
-    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x);
-    const uint32_t lo1 = 0xCD9E8D57u * c.z;
-    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z);
-    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    const uint64_t p0 = (uint64_t)0xD2511F53u * c.x;  // one wide multiply: hi and lo
+    const uint64_t p1 = (uint64_t)0xCD9E8D57u * c.z;
+    c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k0, (uint32_t)p1,
+                   (uint32_t)(p0 >> 32) ^ c.w ^ k1, (uint32_t)p0);
     k0 += 0x9E3779B9u;
     k1 += 0xBB67AE85u;
   }
   return c;
 }
+
+// Philox with the ten round keys computed once (the key is the seed, fixed for
+// a whole pass over the vocabulary).
+struct PhiloxKeys {
+  uint32_t k0[10], k1[10];
+  __device__ __forceinline__ explicit PhiloxKeys(uint64_t seed) {
+    uint32_t a = (uint32_t)seed, b = (uint32_t)(seed >> 32);
+#pragma unroll
+    for (int i = 0; i < 10; ++i) {
+      k0[i] = a;
+      k1[i] = b;
+      a += 0x9E3779B9u;
+      b += 0xBB67AE85u;
+    }
+  }
+  __device__ __forceinline__ uint4 operator()(uint4 c) const {
+#pragma unroll
+    for (int i = 0; i < 10; ++i) {
+      const uint64_t p0 = (uint64_t)0xD2511F53u * c.x;
+      const uint64_t p1 = (uint64_t)0xCD9E8D57u * c.z;
+      c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k0[i], (uint32_t)p1,
+                     (uint32_t)(p0 >> 32) ^ c.w ^ k1[i], (uint32_t)p0);
+    }
+    return c;
+  }
+};
 
 // Random streams of the library's draw layout.
 enum { RNG_DRAFT = 0, RNG_ACCEPT = 1, RNG_RESIDUAL = 2, RNG_BONUS = 3 };
@@ -135,6 +163,21 @@ __device__ __forceinline__ void warp_merge(float &m, float &s, float &best, int 
     lse_merge(m, s, m2, s2);
     if (better(b2, i2, best, idx)) { best = b2; idx = i2; bs = bs2; }
   }
+}
+
+// 2^x with the hardware approximation (flushes subnormal results to zero).
+__device__ __forceinline__ float ex2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// atomic max on a float in global memory (handles both signs)
+__device__ __forceinline__ void atomic_max_float(float *addr, float v) {
+  if (v >= 0.f)
+    atomicMax(reinterpret_cast<int *>(addr), __float_as_int(v));
+  else
+    atomicMin(reinterpret_cast<unsigned int *>(addr), __float_as_uint(v));
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }

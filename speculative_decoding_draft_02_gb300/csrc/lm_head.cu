@@ -1,67 +1,56 @@
-// lm_head.cu — a1: base draft logits through the shared LM head, and the W2
-// layout preparation.
+// lm_head.cu — a1: base draft logits through the shared LM head, on the tensor
+// cores, and the one-time W2 layout preparation.
 //
 // "DSpark 深度解读" §二 (architecture): the parallel backbone emits gamma hidden
-// states; base logits come from the LM head shared with, and frozen from, the
-// target.  l0[m, v] = sum_i h[m, i] W_lm[v, i], m = r*gamma + k - 1.
-#include "common.cuh"
+// states and the base logits of all positions come from one pass through the
+// LM head shared with, and frozen from, the target:
+//   l0[m, v] = sum_i h[m, i] W_lm[v, i],  m = r*gamma + k - 1.
+// The contraction runs on the persistent tcgen05 GEMM (TMA-fed, f32
+// accumulation in TMEM); the epilogue rounds each accumulator row to bf16.
+#include "umma_gemm.cuh"
 
 DSPARK_DECLARE_STATUS(s_status_lmhead)
 
-int dspark_lm_head_tc(const dspark_dims *dims, const void *h, const void *W_lm,
-                      void *base_logits, cudaStream_t stream);  // lm_head_tc.cu
-
 namespace {
 
-// Plain smem-tiled FMA GEMM C[M, N] = A[M, K] B[N, K]^T (both K-contiguous),
-// f32 accumulation, bf16 output.  64x64 tile, 256 threads, 4x4 per thread.
-constexpr int SBM = 64, SBN = 64, SBK = 32;
-
-__global__ void __launch_bounds__(256) gemm_nt_simple(const bf16 *__restrict__ A,
-                                                      const bf16 *__restrict__ B,
-                                                      bf16 *__restrict__ C, int M, int N,
-                                                      int K) {
-  __shared__ float As[SBK][SBM + 1];
-  __shared__ float Bs[SBK][SBN + 1];
-  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
-  const int m0 = blockIdx.y * SBM, n0 = blockIdx.x * SBN;
-  float acc[4][4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-  for (int k0 = 0; k0 < K; k0 += SBK) {
-    for (int e = threadIdx.x; e < SBM * SBK; e += 256) {
-      const int mm = e / SBK, kk = e % SBK;
-      As[kk][mm] = (m0 + mm < M) ? __bfloat162float(A[(size_t)(m0 + mm) * K + k0 + kk]) : 0.f;
-      Bs[kk][mm] = (n0 + mm < N) ? __bfloat162float(B[(size_t)(n0 + mm) * K + k0 + kk]) : 0.f;
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int kk = 0; kk < SBK; ++kk) {
-      float a[4], b[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int m = m0 + ty * 4 + i;
-    if (m >= M) continue;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int n = n0 + tx * 4 + j;
-      if (n < N) C[(size_t)m * N + n] = __float2bfloat16_rn(acc[i][j]);
-    }
-  }
+__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));
+  return *reinterpret_cast<const uint32_t *>(&v);
 }
+
+struct EpiStoreBF16 {
+  bf16 *C;
+  int M, N;
+  struct State {};
+  static constexpr bool kRowAffine = false;
+  __device__ void prefetch(int, int, int, int, int, State &) const {}
+  __device__ void operator()(int m0, int n0, int row, uint32_t taddr, int c0, int c1,
+                             State &) const {
+    const int m = m0 + row;
+    bf16 *dst_row = C + (size_t)m * N;
+#pragma unroll 1
+    for (int c = c0; c < c1; c += 32) {
+      uint32_t r[32];
+      tc::tmem_ld32(taddr + (uint32_t)c, r);
+      tc::tmem_wait_ld();
+      if (m < M) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int n = n0 + c + q * 8;
+          if (n + 8 <= N) {
+            uint4 v;
+            v.x = pack_bf16x2(r[q * 8 + 0], r[q * 8 + 1]);
+            v.y = pack_bf16x2(r[q * 8 + 2], r[q * 8 + 3]);
+            v.z = pack_bf16x2(r[q * 8 + 4], r[q * 8 + 5]);
+            v.w = pack_bf16x2(r[q * 8 + 6], r[q * 8 + 7]);
+            *reinterpret_cast<uint4 *>(dst_row + n) = v;
+          }
+        }
+      }
+    }
+  }
+  __device__ void on_timeout() const { dspark_set_status(DSPARK_ERR_TIMEOUT); }
+};
 
 // W2t[v, i] = W2[i, v] through 32x32 shared tiles.
 __global__ void transpose_bf16(const bf16 *__restrict__ in, bf16 *__restrict__ out, int rows,
@@ -79,17 +68,54 @@ __global__ void transpose_bf16(const bf16 *__restrict__ in, bf16 *__restrict__ o
   }
 }
 
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
 }  // namespace
 
-int dspark_lm_head_simple(const dspark_dims *dims, const void *h, const void *W_lm,
-                          void *base_logits, cudaStream_t stream) {
-  const int M = dims->R * dims->gamma, N = dims->V, K = dims->d;
-  dim3 grid((N + SBN - 1) / SBN, (M + SBM - 1) / SBM);
-  gemm_nt_simple<<<grid, 256, 0, stream>>>((const bf16 *)h, (const bf16 *)W_lm,
-                                           (bf16 *)base_logits, M, N, K);
-  DSPARK_CHECK_LAUNCH();
-  dspark_count_launches(1);
-  return DSPARK_OK;
+int dspark_make_tmap_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                          uint32_t box_rows) {
+  static EncodeTiledFn encode = nullptr;
+  if (!encode) {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return -1;
+    encode = (EncodeTiledFn)fn;
+  }
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base),
+                            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : -1;
+}
+
+int dspark_sm_count() {
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 1;
+  }
+  return sms;
+}
+
+int dspark_lm_head_tc(const dspark_dims *dims, const void *h, const void *W_lm,
+                      void *base_logits, cudaStream_t stream) {
+  EpiStoreBF16 epi;
+  epi.C = (bf16 *)base_logits;
+  epi.M = dims->R * dims->gamma;
+  epi.N = dims->V;
+  return gemm::launch<4>(h, W_lm, epi.M, epi.N, dims->d, epi, stream);
 }
 
 extern "C" int dspark_pack_w2(const dspark_dims *dims, const void *W2, void *W2t,
@@ -105,7 +131,8 @@ extern "C" int dspark_pack_w2(const dspark_dims *dims, const void *W2, void *W2t
 
 int dspark_status_lmhead(int clear) {
   int v = 0;
-  if (cudaMemcpyFromSymbol(&v, s_status_lmhead, sizeof(int)) != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(&v, s_status_lmhead, sizeof(int)) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
   if (clear) {
     const int z = 0;
     cudaMemcpyToSymbol(s_status_lmhead, &z, sizeof(int));

@@ -1,161 +1,313 @@
-// logits_tile.cuh — one pass over the vocabulary for a batch of rows:
-//   l[i, v] = l0[row_i, v] + E[i, :] . W2t[v, :]        (Markov bias, rank r)
-// fused with a per-row decision over v (argmax, Gumbel-max, or the residual
-// max(0, p_t - p_d) Gumbel-max of verification) and the log-sum-exp of l / tau.
-// Logits stay on chip: each tile leaves only a RowPartial per row.
+// logits_tile.cuh — the fused vocabulary pass behind the Markov head and the
+// verification resample, as an epilogue of the tcgen05 GEMM:
 //
-// "DSpark 深度解读" §二 设计一: B(x_{k-1}, .) = W1[x_{k-1}] W2 added to the base
-// logits; "DSpark整体架构" stage two (sample left to right).
+//   bias[i, v] = E[i, :] . W2t[v, :]          (tensor cores, f32 in TMEM;
+//                                              E[i] = W1[x_{k-1}] of row i)
+//   l[i, v]    = l0[row_i, v] + bias[i, v]     (never written to memory)
+//
+// followed, per row and per PART_N-wide vocabulary slice, by the decision the
+// mode asks for and the online log-sum-exp of l / tau.  Each slice leaves one
+// RowPartial per row; a small reduction combines the slices.
+//
+// "DSpark 深度解读" §二 设计一: B(x_{k-1}, .) = W1[x_{k-1}] W2 is added to the base
+// logits and x_k is sampled from the result, left to right.
 #pragma once
-#include "common.cuh"
+#include "umma_gemm.cuh"
 
 enum TileMode { MODE_GREEDY = 0, MODE_SAMPLE = 1, MODE_RESIDUAL = 2 };
-enum RowKind { KIND_NONE = 0, KIND_RESIDUAL = 1, KIND_BONUS = 2 };
+enum RowKind { KIND_NONE = 0, KIND_RESIDUAL = 1, KIND_BONUS = 2, KIND_FALLBACK = 3 };
+// KIND_FALLBACK: the residual max(0, p_t - p_d) of the rejected row was empty in
+// floating point; the row is then sampled from p_t itself (residual stream).
 
-// Per-row context of a verification resample (one per request).
+// Per-request context of a verification resample.
 struct __align__(16) ResampleRow {
   int32_t kind;     // RowKind
-  int32_t pos;      // 1-based draft position j* of the rejected (or bonus) row
+  int32_t pos;      // 1-based position j* of the rejected (or bonus) row
   int32_t prev;     // token x_{j*-1} whose W1 row conditions the Markov bias
   float lse_t;      // logsumexp(t_{j*} / tau)
   float lse_d;      // logsumexp(l_{j*} / tau)
   int32_t pad[3];
 };
 
-struct TileArgs {
-  const bf16 *base;      // [R*gamma, V]
-  const bf16 *E;         // [M, r]  gathered W1 rows, one per row i
-  const bf16 *W2t;       // [V, r]
-  const bf16 *target;    // [R, gamma+1, V]            (residual)
-  const ResampleRow *rows;  //                          (residual)
-  RowPartial *part;      // [M, n_tiles]
-  int M, V, r, gamma, k; // k: 1-based draft step (draft modes)
-  int n_tiles;
-  float inv_tau;
-  uint64_t seed;
-};
+constexpr int LOGITS_EPI_WARPS = 8;                         // two warps per TMEM lane quarter
+constexpr int PART_N = gemm::BN / (LOGITS_EPI_WARPS / 4);   // vocabulary entries per partial
 
-// Decision score of one vocabulary entry; also returns the scaled logit.
-template <int MODE>
-__device__ __forceinline__ float tile_score(const TileArgs &a, float logit, int v, int req,
-                                            int pos, float lse_t, float lse_d, float tv,
-                                            float &s, uint4 &rw, int &rw_q) {
-  if (MODE == MODE_GREEDY) {
-    s = logit;
-    return logit;
-  }
-  const int q = v >> 2;
-  if (q != rw_q) {
-    rw = rng_words4(a.seed, (uint32_t)q, (uint32_t)pos, (uint32_t)req,
-                    MODE == MODE_SAMPLE ? RNG_DRAFT : RNG_RESIDUAL);
-    rw_q = q;
-  }
-  const float g = rng_gumbel(uint4_get(rw, v & 3));
-  s = logit * a.inv_tau;
-  if (MODE == MODE_SAMPLE) return s + g;
-  // residual: p_t - p_d over the row
-  const float pt = __expf(tv * a.inv_tau - lse_t);
-  const float pd = __expf(s - lse_d);
-  const float qv = pt - pd;
-  return qv > 0.f ? __logf(qv) + g : -INFINITY;
+static inline size_t logits_parts(int V) { return (size_t)(V + PART_N - 1) / PART_N; }
+
+// 32 bf16 starting at src[n] as four 16-byte words; groups past V read nothing.
+__device__ __forceinline__ void load_raw32(const bf16 *src, int n, int V, uint4 (&w)[4]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    w[q] = (n + q * 8 + 8 <= V) ? __ldg(reinterpret_cast<const uint4 *>(src + n + q * 8))
+                                : make_uint4(0, 0, 0, 0);
 }
-
-// v0 tile: 32 rows x 128 vocabulary entries per CTA, rank streamed in chunks of
-// 32 through shared memory, 4x4 outputs per thread, then one warp per row.
-constexpr int TM = 32, TN = 128, TK = 32;
-
-template <int MODE>
-__global__ void __launch_bounds__(256) logits_tile_simple(TileArgs a) {
-  __shared__ float Es[TK][TM + 1];
-  __shared__ float Ws[TK][TN + 1];
-  __shared__ float Ls[TM][TN + 1];
-  const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;
-  const int m0 = blockIdx.y * TM, n0 = blockIdx.x * TN;
-  float acc[4][4];
+// Unpack to floats; entries past V become -inf.
+__device__ __forceinline__ void unpack32(const uint4 (&w)[4], int n, int V, float (&out)[32]) {
+  if (n + 32 <= V) {  // whole chunk inside the vocabulary (warp-uniform)
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t ws[4] = {w[q].x, w[q].y, w[q].z, w[q].w};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-  for (int k0 = 0; k0 < a.r; k0 += TK) {
-    for (int e = threadIdx.x; e < TM * TK; e += 256) {
-      const int mm = e / TK, kk = e % TK;
-      Es[kk][mm] = (m0 + mm < a.M) ? __bfloat162float(a.E[(size_t)(m0 + mm) * a.r + k0 + kk]) : 0.f;
-    }
-    for (int e = threadIdx.x; e < TN * TK; e += 256) {
-      const int nn = e / TK, kk = e % TK;
-      Ws[kk][nn] = (n0 + nn < a.V) ? __bfloat162float(a.W2t[(size_t)(n0 + nn) * a.r + k0 + kk]) : 0.f;
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int kk = 0; kk < TK; ++kk) {
-      float e4[4], w4[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) e4[i] = Es[kk][ty * 4 + i];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) w4[j] = Ws[kk][tx + 32 * j];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(e4[i], w4[j], acc[i][j]);
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) Ls[ty * 4 + i][tx + 32 * j] = acc[i][j];
-  __syncthreads();
-
-  // one warp per row: add base logits, score, reduce
-  for (int rr = ty; rr < TM; rr += 8) {
-    const int i = m0 + rr;
-    if (i >= a.M) break;
-    int base_row, pos = a.k, req = i;
-    float lse_t = 0.f, lse_d = 0.f;
-    const bf16 *trow = nullptr;
-    if (MODE == MODE_RESIDUAL) {
-      const ResampleRow rw = a.rows[i];
-      if (rw.kind != KIND_RESIDUAL) continue;
-      pos = rw.pos;
-      lse_t = rw.lse_t;
-      lse_d = rw.lse_d;
-      base_row = i * a.gamma + pos - 1;
-      trow = a.target + ((size_t)i * (a.gamma + 1) + pos - 1) * a.V;
-    } else {
-      base_row = i * a.gamma + a.k - 1;
-    }
-    const bf16 *brow = a.base + (size_t)base_row * a.V;
-    float m = -INFINITY, s = 0.f, best = -INFINITY, bs = 0.f;
-    int idx = 0x7fffffff;
-    float fb = -INFINITY;
-    int fidx = 0x7fffffff;  // residual fallback: plain target sample
-    uint4 rw4 = make_uint4(0, 0, 0, 0);
-    int rw_q = -1;
-    for (int c = tx; c < TN; c += 32) {
-      const int v = n0 + c;
-      if (v >= a.V) break;
-      const float logit = __bfloat162float(brow[v]) + Ls[rr][c];
-      const float tv = (MODE == MODE_RESIDUAL) ? __bfloat162float(trow[v]) : 0.f;
-      float sc;
-      const float score = tile_score<MODE>(a, logit, v, req, pos, lse_t, lse_d, tv, sc, rw4, rw_q);
-      if (better(score, v, best, idx)) { best = score; idx = v; bs = sc; }
-      if (MODE == MODE_SAMPLE) lse_merge(m, s, sc, 1.f);
-      if (MODE == MODE_RESIDUAL) {
-        const float g = rng_gumbel(uint4_get(rw4, v & 3));
-        const float f = tv * a.inv_tau + g;
-        if (better(f, v, fb, fidx)) { fb = f; fidx = v; }
+      for (int t = 0; t < 4; ++t) {
+        out[q * 8 + 2 * t] = bf16_lo(ws[t]);
+        out[q * 8 + 2 * t + 1] = bf16_hi(ws[t]);
       }
     }
-    warp_merge(m, s, best, idx, bs);
-    if (MODE == MODE_RESIDUAL) {
-      float d0 = 0.f, d1 = 0.f, d2 = 0.f;
-      warp_merge(d0, d1, fb, fidx, d2);
-    }
-    if (tx == 0) {
-      RowPartial p;
-      p.m = m; p.sum = s; p.best = best; p.idx = idx; p.best_s = bs;
-      p.pad0 = fb; p.pad1 = __int_as_float(fidx); p.pad2 = 0.f;
-      a.part[(size_t)i * a.n_tiles + blockIdx.x] = p;
+    return;
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const bool ok = n + q * 8 + 8 <= V;
+    const uint32_t ws[4] = {w[q].x, w[q].y, w[q].z, w[q].w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      out[q * 8 + 2 * t] = ok ? bf16_lo(ws[t]) : -INFINITY;
+      out[q * 8 + 2 * t + 1] = ok ? bf16_hi(ws[t]) : -INFINITY;
     }
   }
 }
+
+template <int MODE>
+struct EpiLogits {
+  const bf16 *base;          // [R*gamma, V]
+  const bf16 *target;        // [R, gamma+1, V]       (residual)
+  const ResampleRow *rows;   // [R]                    (residual)
+  RowPartial *part;          // [R, n_parts]
+  float *gfloor;             // [R] best Gumbel score found so far on each row, shared by
+                             // every CTA of the pass (set to -inf before the pass)
+  int M, V, gamma, k, n_parts;
+  float inv_tau;
+  uint64_t seed;
+
+  static constexpr bool kRowAffine = true;
+  static constexpr int CHUNKS = PART_N / 32;
+
+  // Kept by each epilogue thread across the tiles it processes.
+  struct State {
+    int m0 = -1;               // row block the floor belongs to
+    float floor = -INFINITY;   // best score known on this row (own tiles + shared floor)
+    float seen = -INFINITY;    // shared floor read at the start of the current tile
+    uint4 buf[4 * CHUNKS];     // base logits prefetched before the accumulator is ready
+  };
+
+  __device__ __forceinline__ bool draft_row(int m0, int row, const bf16 *&brow) const {
+    const int i = m0 + row;
+    brow = base + (size_t)(i * gamma + k - 1) * V;
+    return i < M;
+  }
+
+  __device__ void prefetch(int m0, int n0, int row, int c0, int, State &st) const {
+    const int i = m0 + row;
+    if (MODE != MODE_GREEDY && i < M)
+      st.seen = *reinterpret_cast<volatile const float *>(gfloor + i);
+    if (MODE == MODE_RESIDUAL) return;
+    const bf16 *brow;
+    if (!draft_row(m0, row, brow)) return;
+    const int n = n0 + c0;
+    if (MODE == MODE_GREEDY) {  // the whole slice: the epilogue then never waits on HBM
+#pragma unroll
+      for (int q = 0; q < 4 * CHUNKS; ++q)
+        st.buf[q] = (n + q * 8 + 8 <= V) ? __ldg(reinterpret_cast<const uint4 *>(brow + n + q * 8))
+                                         : make_uint4(0, 0, 0, 0);
+    } else {  // the first chunk; later chunks are loaded one ahead
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        st.buf[q] = (n + q * 8 + 8 <= V) ? __ldg(reinterpret_cast<const uint4 *>(brow + n + q * 8))
+                                         : make_uint4(0, 0, 0, 0);
+    }
+  }
+
+  __device__ void operator()(int m0, int n0, int row, uint32_t taddr, int c0, int c1,
+                             State &st) const {
+    constexpr float LOG2E = 1.4426950408889634f, LN2 = 0.6931471805599453f;
+    const int i = m0 + row;
+    bool active = i < M;
+    int pos = k;
+    float lse_t = 0.f, lse_d = 0.f;
+    const bf16 *trow = nullptr;
+    const bf16 *brow = base;
+    if (MODE == MODE_RESIDUAL) {
+      if (active) {
+        const ResampleRow rr = rows[i];
+        active = rr.kind == KIND_RESIDUAL;
+        pos = rr.pos;
+        lse_t = rr.lse_t;
+        lse_d = rr.lse_d;
+        brow = base + (size_t)(i * gamma + pos - 1) * V;
+        trow = target + ((size_t)i * (gamma + 1) + pos - 1) * V;
+      }
+    } else {
+      draft_row(m0, row, brow);
+    }
+    if (st.m0 != m0) { st.m0 = m0; st.floor = -INFINITY; }
+    st.floor = fmaxf(st.floor, st.seen);
+    const uint32_t stream = MODE == MODE_SAMPLE ? RNG_DRAFT : RNG_RESIDUAL;
+
+    float m2 = -INFINITY, s = 0.f, best = -INFINITY, bs = 0.f;
+    int idx = 0x7fffffff;
+
+    if (MODE == MODE_GREEDY) {
+#pragma unroll
+      for (int cc = 0; cc < CHUNKS; ++cc) {
+        const int c = c0 + cc * 32;
+        uint32_t acc[32];
+        tc::tmem_ld32(taddr + (uint32_t)c, acc);
+        tc::tmem_wait_ld();
+        const int n = n0 + c;
+        if (active && n < V) {
+          const uint4 w4[4] = {st.buf[cc * 4], st.buf[cc * 4 + 1], st.buf[cc * 4 + 2],
+                               st.buf[cc * 4 + 3]};
+          float sv[32];
+          unpack32(w4, n, V, sv);
+          // four interleaved argmax chains (entries j = 4 q + p), merged with
+          // ties to the lower id
+          float pb[4] = {best, -INFINITY, -INFINITY, -INFINITY};
+          int pi[4] = {idx, 0x7fffffff, 0x7fffffff, 0x7fffffff};
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float l = sv[j] + __uint_as_float(acc[j]);
+            const bool b = l > pb[j & 3];  // strict: within a chain ids increase
+            pb[j & 3] = b ? l : pb[j & 3];
+            pi[j & 3] = b ? n + j : pi[j & 3];
+          }
+#pragma unroll
+          for (int p = 1; p < 4; ++p)
+            if (better(pb[p], pi[p], pb[0], pi[0])) { pb[0] = pb[p]; pi[0] = pi[p]; }
+          best = pb[0];
+          idx = pi[0];
+        }
+      }
+    } else {
+      const PhiloxKeys keys(seed);
+      const float c2 = inv_tau * LOG2E;  // scaled logits in log2 units
+      uint4 nxt[4] = {st.buf[0], st.buf[1], st.buf[2], st.buf[3]};
+      if (MODE == MODE_RESIDUAL && active) load_raw32(brow, n0 + c0, V, nxt);
+#pragma unroll 1
+      for (int c = c0; c < c1; c += 32) {
+        uint32_t acc[32];
+        tc::tmem_ld32(taddr + (uint32_t)c, acc);
+        tc::tmem_wait_ld();
+        const int n = n0 + c;
+        if (active && n < V) {
+          uint4 cur[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) cur[q] = nxt[q];
+          if (c + 32 < c1) load_raw32(brow, n + 32, V, nxt);  // prefetch the next chunk
+          float sv[32];
+          unpack32(cur, n, V, sv);
+          const float F = fmaxf(best, st.floor);  // a score some entry of the row reaches
+
+          if (MODE == MODE_SAMPLE) {
+            float x2[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x2[j] = (sv[j] + __uint_as_float(acc[j])) * c2;
+            float mx[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) mx[j] = fmaxf(x2[j], x2[j + 16]);
+#pragma unroll
+            for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+              for (int j = 0; j < w; ++j) mx[j] = fmaxf(mx[j], mx[j + w]);
+            const float cmax2 = mx[0];
+            // online log-sum-exp in base 2 (four partial sums)
+            if (cmax2 > m2) {
+              s *= ex2_fast(m2 - cmax2);
+              m2 = cmax2;
+            }
+            float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int j = 0; j < 32; ++j) ps[j & 3] += ex2_fast(x2[j] - m2);
+            s += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+
+            // Gumbel-max without the logarithms of entries that cannot win.
+            // Entry j beats F only if g_j > F - s_j.  Since -log u >= 1 - u,
+            // 1 - u_j >= e^{s_j - F + 0.01} implies g_j < F - s_j - 0.01.
+            // Chunk test first (s_j <= cmax, an integer threshold on w >> 9,
+            // u = ((w >> 9) + 1/2) 2^-23), then the same test per entry with
+            // e^{s_j - F} = 2^{x2_j - m2} e^{m - F}.
+            int w_thr = -1;
+            if (F > -INFINITY) {
+              const float t = fminf(F - cmax2 * LN2, 15.f);
+              const float X = __expf(-(t - 0.01f)) * 8388608.f;
+              w_thr = X >= 8388607.f ? -1 : 8388607 - (int)ceilf(X);
+            }
+            const float K = F > -INFINITY ? __expf(m2 * LN2 - F + 0.01f) : INFINITY;
+            const bool per_entry = K < 1e30f;
+            // Philox words in two halves of 16 entries (one call per 4 entries)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              uint32_t ws[16];
+              uint32_t wmax = 0;
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const uint4 w = keys(make_uint4((uint32_t)((n >> 2) + 4 * h + q), (uint32_t)pos,
+                                                (uint32_t)i, stream));
+                ws[q * 4 + 0] = w.x; ws[q * 4 + 1] = w.y; ws[q * 4 + 2] = w.z; ws[q * 4 + 3] = w.w;
+                wmax = max(max(wmax, max(w.x, w.y)), max(w.z, w.w));
+              }
+              if ((int)(wmax >> 9) > w_thr) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                  const int j = 16 * h + e;
+                  const bool cand =
+                      !per_entry || (1.f - rng_uniform(ws[e])) < ex2_fast(x2[j] - m2) * K;
+                  if (cand) {
+                    const float sn = x2[j] * LN2;
+                    const float sc = sn + rng_gumbel(ws[e]);
+                    if (sc > best) { best = sc; idx = n + j; bs = sn; }
+                  }
+                }
+              }
+            }
+          } else {
+            // residual max(0, p_t - p_d) at the rejected position.  The score
+            // log q_j + g_j <= log p_t(j) + g_j, so with the same argument an
+            // entry is skipped when 1 - u_j >= p_t(j) e^{-F + 0.01}.
+            uint4 tw[4];
+            load_raw32(trow, n, V, tw);
+            float tv[32];
+            unpack32(tw, n, V, tv);
+            const float K = F > -INFINITY ? __expf(0.01f - F) : INFINITY;
+            const bool per_entry = K < 1e30f;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const uint4 w = keys(make_uint4((uint32_t)((n >> 2) + q), (uint32_t)pos,
+                                              (uint32_t)i, stream));
+              const uint32_t wq[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+              for (int l = 0; l < 4; ++l) {
+                const int j = q * 4 + l;
+                const float pt = __expf(tv[j] * inv_tau - lse_t);
+                const bool cand = (n + j < V) &&
+                                  (!per_entry || (1.f - rng_uniform(wq[l])) < pt * K);
+                if (cand) {
+                  const float sl = (sv[j] + __uint_as_float(acc[j])) * inv_tau;
+                  const float qv = pt - __expf(sl - lse_d);
+                  if (qv > 0.f) {
+                    const float sc = __logf(qv) + rng_gumbel(wq[l]);
+                    if (sc > best) { best = sc; idx = n + j; }
+                  }
+                }
+              }
+            }
+          }
+        }
+      }
+    }
+    if (MODE != MODE_GREEDY && active) {
+      st.floor = fmaxf(st.floor, best);
+      if (st.floor > st.seen) atomic_max_float(gfloor + i, st.floor);
+    }
+    if (active && n0 + c0 < V) {
+      RowPartial p;
+      p.m = MODE == MODE_SAMPLE ? m2 * LN2 : -INFINITY;
+      p.sum = s;
+      p.best = best;
+      p.idx = idx;
+      p.best_s = bs;
+      p.pad0 = p.pad1 = p.pad2 = 0.f;
+      part[(size_t)i * n_parts + (n0 + c0) / PART_N] = p;
+    }
+  }
+  __device__ void on_timeout() const { dspark_set_status(DSPARK_ERR_TIMEOUT); }
+};

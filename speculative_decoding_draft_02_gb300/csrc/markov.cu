@@ -6,9 +6,11 @@
 // calibrated per position by a temperature T_k.  "DSpark整体架构": the anchor is
 // the first prediction position, so x_0 = anchor.
 //
-// Per step k the library runs: step_prep (gather E = W1[x_{k-1}], confidence
-// c_k), one vocabulary pass (bias + base logits + decision, logits stay on
-// chip), and row_reduce (combine the per-tile partials into x_k, lse_k, logp_k).
+// Before the loop: zh = w_h . h for every row, and step 1's gather E = W1[x_0]
+// with the confidence c_1.  Per step k: one vocabulary pass (bias + base logits
+// + decision on the tensor cores, logits stay on chip), then reduce_prep
+// (combine the per-slice partials into x_k, lse_k, logp_k, and gather
+// E = W1[x_k] with c_{k+1} for the next step).
 #include "logits_tile.cuh"
 
 DSPARK_DECLARE_STATUS(s_status_markov)
@@ -40,10 +42,11 @@ __global__ void conf_hidden(const bf16 *__restrict__ h, const bf16 *__restrict__
 __global__ void step_prep(const int32_t *__restrict__ anchor, const int32_t *__restrict__ tokens,
                           const bf16 *__restrict__ W1, const bf16 *__restrict__ w_e,
                           const float *__restrict__ zh, const float *__restrict__ T,
-                          bf16 *__restrict__ E, float *__restrict__ conf, int R, int gamma,
-                          int V, int r, int k) {
+                          bf16 *__restrict__ E, float *__restrict__ conf,
+                          float *__restrict__ gfloor, int R, int gamma, int V, int r, int k) {
   const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (i >= R) return;
+  if (lane == 0) gfloor[i] = -INFINITY;
   int prev = (k == 1) ? anchor[i] : tokens[(size_t)i * gamma + k - 2];
   if (prev < 0 || prev >= V) {
     if (lane == 0) dspark_set_status(DSPARK_ERR_TOKEN);
@@ -71,36 +74,94 @@ __global__ void step_prep(const int32_t *__restrict__ anchor, const int32_t *__r
   }
 }
 
-// Combine the vocabulary-tile partials of each row into x_k, lse_k, logp_k.
+// Combine the vocabulary-slice partials of request i into x_k, lse_k, logp_k,
+// then (k < gamma) prepare step k+1: E[i] = W1[x_k] and the confidence c_{k+1}.
+// One CTA of 128 threads per request.
 template <int MODE>
-__global__ void row_reduce(const RowPartial *__restrict__ part, int n_tiles, int R, int gamma,
-                           int k, int32_t *__restrict__ tokens, float *__restrict__ lse_out,
-                           float *__restrict__ logp_out) {
-  const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  if (i >= R) return;
+__global__ void __launch_bounds__(128) reduce_prep(
+    const RowPartial *__restrict__ part, int n_parts, int gamma, int V, int r, int k,
+    int32_t *__restrict__ tokens, float *__restrict__ lse_out, float *__restrict__ logp_out,
+    const bf16 *__restrict__ W1, const bf16 *__restrict__ w_e, const float *__restrict__ zh,
+    const float *__restrict__ T, bf16 *__restrict__ E, float *__restrict__ conf,
+    float *__restrict__ gfloor) {
+  const int i = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   float m = -INFINITY, s = 0.f, best = -INFINITY, bs = 0.f;
   int idx = 0x7fffffff;
-  for (int t = lane; t < n_tiles; t += 32) {
-    const RowPartial p = part[(size_t)i * n_tiles + t];
-    lse_merge(m, s, p.m, p.sum);
-    if (better(p.best, p.idx, best, idx)) { best = p.best; idx = p.idx; bs = p.best_s; }
+  const RowPartial *pr = part + (size_t)i * n_parts;
+  for (int t0 = 0; t0 < n_parts; t0 += 4 * 128) {  // four independent loads in flight
+    RowPartial p[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int t = t0 + u * 128 + tid;
+      if (t < n_parts) p[u] = pr[t];
+      else { p[u].m = -INFINITY; p[u].sum = 0.f; p[u].best = -INFINITY; p[u].idx = 0x7fffffff; p[u].best_s = 0.f; }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      lse_merge(m, s, p[u].m, p[u].sum);
+      if (better(p[u].best, p[u].idx, best, idx)) { best = p[u].best; idx = p[u].idx; bs = p[u].best_s; }
+    }
   }
   warp_merge(m, s, best, idx, bs);
-  if (lane == 0) {
-    const size_t o = (size_t)i * gamma + k - 1;
-    tokens[o] = idx;
-    float lse = 0.f, logp = 0.f;
-    if (MODE == MODE_SAMPLE) {
-      lse = m + logf(s);
-      logp = bs - lse;
+  __shared__ float sm[4], ss[4], sb[4], sbs[4], sdot[4];
+  __shared__ int si[4], s_tok;
+  if (lane == 0) { sm[warp] = m; ss[warp] = s; sb[warp] = best; si[warp] = idx; sbs[warp] = bs; }
+  __syncthreads();
+  if (warp == 0) {
+    m = lane < 4 ? sm[lane] : -INFINITY;
+    s = lane < 4 ? ss[lane] : 0.f;
+    best = lane < 4 ? sb[lane] : -INFINITY;
+    idx = lane < 4 ? si[lane] : 0x7fffffff;
+    bs = lane < 4 ? sbs[lane] : 0.f;
+    warp_merge(m, s, best, idx, bs);
+    if (lane == 0) {
+      const size_t o = (size_t)i * gamma + k - 1;
+      tokens[o] = idx;
+      float lse = 0.f, logp = 0.f;
+      if (MODE == MODE_SAMPLE) {
+        lse = m + logf(s);
+        logp = bs - lse;
+      }
+      if (lse_out) lse_out[o] = lse;
+      if (logp_out) logp_out[o] = logp;
+      s_tok = idx;
     }
-    if (lse_out) lse_out[o] = lse;
-    if (logp_out) logp_out[o] = logp;
+  }
+  __syncthreads();
+  if (k >= gamma) return;
+  if (tid == 0) gfloor[i] = -INFINITY;  // fresh shared floor for step k + 1
+  int prev = s_tok;
+  if (prev < 0 || prev >= V) {
+    if (tid == 0) dspark_set_status(DSPARK_ERR_TOKEN);
+    prev = 0;
+  }
+  const uint4 *src = reinterpret_cast<const uint4 *>(W1 + (size_t)prev * r);
+  uint4 *dst = reinterpret_cast<uint4 *>(E + (size_t)i * r);
+  const uint4 *wr = reinterpret_cast<const uint4 *>(w_e);
+  float acc = 0.f;
+  for (int c = tid; c < r / 8; c += 128) {
+    const uint4 a = src[c], b = wr[c];
+    dst[c] = a;
+    const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      acc = fmaf(bf16_lo(av[t]), bf16_lo(bv[t]), acc);
+      acc = fmaf(bf16_hi(av[t]), bf16_hi(bv[t]), acc);
+    }
+  }
+  acc = warp_sum(acc);
+  if (lane == 0) sdot[warp] = acc;
+  __syncthreads();
+  if (tid == 0) {
+    const size_t o = (size_t)i * gamma + k;  // position k + 1
+    const float z = zh[o] + sdot[0] + sdot[1] + sdot[2] + sdot[3];
+    conf[o] = 1.f / (1.f + expf(-z / T[k]));
   }
 }
 
 struct MarkovWs {
   float *zh;
+  float *gfloor;
   bf16 *E;
   RowPartial *part;
   size_t bytes;
@@ -111,11 +172,12 @@ MarkovWs markov_layout(const dspark_dims *d, char *base) {
   size_t off = 0;
   w.zh = (float *)(base + off);
   off = dspark_align_up(off + sizeof(float) * (size_t)d->R * d->gamma, 256);
+  w.gfloor = (float *)(base + off);
+  off = dspark_align_up(off + sizeof(float) * (size_t)d->R, 256);
   w.E = (bf16 *)(base + off);
   off = dspark_align_up(off + sizeof(bf16) * (size_t)d->R * d->r, 256);
   w.part = (RowPartial *)(base + off);
-  const size_t n_tiles = (d->V + TN - 1) / TN;
-  off = dspark_align_up(off + sizeof(RowPartial) * (size_t)d->R * n_tiles, 256);
+  off = dspark_align_up(off + sizeof(RowPartial) * (size_t)d->R * logits_parts(d->V), 256);
   w.bytes = off;
   return w;
 }
@@ -136,6 +198,8 @@ extern "C" int dspark_markov_draft(const dspark_dims *dims, const void *base_log
   if (!dspark_dims_ok(dims) || !base_logits || !h || !anchor || !W1 || !W2t || !w_conf || !T ||
       !tokens || !conf || !(tau >= 0.f))
     return DSPARK_ERR_ARG;
+  if (((uintptr_t)W2t | (uintptr_t)W1 | (uintptr_t)h | (uintptr_t)base_logits) & 15)
+    return DSPARK_ERR_ARG;  // TMA and 16-byte vector loads
   MarkovWs ws = markov_layout(dims, (char *)workspace);
   if (!workspace || workspace_bytes < ws.bytes || ((uintptr_t)workspace & 255))
     return DSPARK_ERR_WORKSPACE;
@@ -144,41 +208,35 @@ extern "C" int dspark_markov_draft(const dspark_dims *dims, const void *base_log
   conf_hidden<<<(rows * 32 + 255) / 256, 256, 0, stream>>>((const bf16 *)h, (const bf16 *)w_conf,
                                                           ws.zh, rows, d);
   DSPARK_CHECK_LAUNCH();
-  TileArgs ta;
-  ta.base = (const bf16 *)base_logits;
-  ta.E = ws.E;
-  ta.W2t = (const bf16 *)W2t;
-  ta.target = nullptr;
-  ta.rows = nullptr;
-  ta.part = ws.part;
-  ta.M = R;
-  ta.V = V;
-  ta.r = r;
-  ta.gamma = G;
-  ta.n_tiles = (V + TN - 1) / TN;
-  ta.inv_tau = tau > 0.f ? 1.f / tau : 1.f;
-  ta.seed = seed;
-  const dim3 tgrid(ta.n_tiles, (R + TM - 1) / TM);
+  const int n_tiles = (int)logits_parts(V);
+  const float inv_tau = tau > 0.f ? 1.f / tau : 1.f;
+  step_prep<<<(R * 32 + 255) / 256, 256, 0, stream>>>(anchor, tokens, (const bf16 *)W1,
+                                                     (const bf16 *)w_conf + d, ws.zh, T, ws.E,
+                                                     conf, ws.gfloor, R, G, V, r, 1);
+  DSPARK_CHECK_LAUNCH();
+  const bf16 *w_e = (const bf16 *)w_conf + d;
   for (int k = 1; k <= G; ++k) {
-    step_prep<<<(R * 32 + 255) / 256, 256, 0, stream>>>(
-        anchor, tokens, (const bf16 *)W1, (const bf16 *)w_conf + d, ws.zh, T, ws.E, conf, R, G,
-        V, r, k);
-    DSPARK_CHECK_LAUNCH();
-    ta.k = k;
+    int rc;
     if (tau > 0.f) {
-      logits_tile_simple<MODE_SAMPLE><<<tgrid, 256, 0, stream>>>(ta);
-      DSPARK_CHECK_LAUNCH();
-      row_reduce<MODE_SAMPLE><<<(R * 32 + 255) / 256, 256, 0, stream>>>(
-          ws.part, ta.n_tiles, R, G, k, tokens, lse_d, logp_d);
+      EpiLogits<MODE_SAMPLE> epi{(const bf16 *)base_logits, nullptr, nullptr, ws.part, ws.gfloor,
+                                 R, V, G, k, n_tiles, inv_tau, seed};
+      rc = gemm::launch<LOGITS_EPI_WARPS>(ws.E, W2t, R, V, r, epi, stream);
+      if (rc != DSPARK_OK) return rc;
+      reduce_prep<MODE_SAMPLE><<<R, 128, 0, stream>>>(ws.part, n_tiles, G, V, r, k, tokens, lse_d,
+                                                      logp_d, (const bf16 *)W1, w_e, ws.zh, T,
+                                                      ws.E, conf, ws.gfloor);
     } else {
-      logits_tile_simple<MODE_GREEDY><<<tgrid, 256, 0, stream>>>(ta);
-      DSPARK_CHECK_LAUNCH();
-      row_reduce<MODE_GREEDY><<<(R * 32 + 255) / 256, 256, 0, stream>>>(
-          ws.part, ta.n_tiles, R, G, k, tokens, lse_d, logp_d);
+      EpiLogits<MODE_GREEDY> epi{(const bf16 *)base_logits, nullptr, nullptr, ws.part, ws.gfloor,
+                                 R, V, G, k, n_tiles, 1.f, seed};
+      rc = gemm::launch<LOGITS_EPI_WARPS>(ws.E, W2t, R, V, r, epi, stream);
+      if (rc != DSPARK_OK) return rc;
+      reduce_prep<MODE_GREEDY><<<R, 128, 0, stream>>>(ws.part, n_tiles, G, V, r, k, tokens, lse_d,
+                                                      logp_d, (const bf16 *)W1, w_e, ws.zh, T,
+                                                      ws.E, conf, ws.gfloor);
     }
     DSPARK_CHECK_LAUNCH();
   }
-  dspark_count_launches(1 + 3 * (uint64_t)G);
+  dspark_count_launches(2 + (uint64_t)G);  // + one GEMM per step, counted by launch()
   return DSPARK_OK;
 }
 

@@ -115,6 +115,7 @@ __device__ __forceinline__ void fence_after_sync() {
 // 32 lanes x 32 columns of 32-bit accumulators: thread t of the warp gets row
 // (quarter*32 + t), columns [col, col + 32).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  __syncwarp();  // the load is warp-wide (.sync.aligned): reconverge first
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
       "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "

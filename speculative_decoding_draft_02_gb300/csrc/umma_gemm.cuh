@@ -1,7 +1,7 @@
 // umma_gemm.cuh — persistent tcgen05 GEMM  D[M, N] = A[M, K] . B[N, K]^T with a
 // pluggable epilogue that reads the f32 accumulator straight from TMEM.
 //
-// One CTA per SM, 192 threads:
+// One CTA per SM, 64 + 32 * EPI_WARPS threads:
 //   warp 0      one thread issues TMA loads of A (128 x 64) and B (256 x 64)
 //               tiles into a STAGES-deep shared-memory ring;
 //   warp 1      allocates TMEM (2 x 256 columns: a double-buffered 128 x 256 f32
@@ -9,8 +9,10 @@
 //               K=16 per instruction, 4 per 64-wide stage), committing each
 //               stage back to the producer and each finished tile to the
 //               epilogue;
-//   warps 2..5  the epilogue: thread t owns accumulator row t (TMEM lane), so a
-//               row-wise reduction over the tile needs no shuffles.
+//   warps 2..   the epilogue (EPI_WARPS = 4 or 8): a thread owns one accumulator
+//               row (its TMEM lane) and a contiguous slice of its columns
+//               (all 256, or one half with 8 warps), so a row-wise reduction
+//               over the slice needs no shuffles.
 // Tiles are visited m-fastest, so the CTAs working at the same time share one
 // B tile (one read from HBM, the rest from L2).  Every wait is bounded; on
 // timeout the CTA raises DSPARK_ERR_TIMEOUT, drains its own copies and MMAs,
@@ -25,8 +27,6 @@ constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int NUM_THREADS = 192;
-constexpr int EPI_THREADS = 128;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
 
@@ -40,12 +40,18 @@ struct SharedCtl {
   int abort;
 };
 
-// Epi must provide: __device__ void operator()(int m0, int n0, int row, uint32_t taddr) const
-// (all 128 epilogue threads call it for each tile; it must tcgen05.ld every
-// 32-column chunk of the 256 columns warp-uniformly) and
-// __device__ void on_timeout() const.
-template <class Epi>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+// Epi must provide
+//   struct State;                         per-thread state kept across tiles
+//   static constexpr bool kRowAffine;     keep each thread on one row when possible
+//   __device__ void prefetch(int m0, int n0, int row, int c0, int c1, State &) const
+//       (called before the tile's accumulator is ready: start global loads)
+//   __device__ void operator()(int m0, int n0, int row, uint32_t taddr, int c0, int c1,
+//                              State &) const
+//       (every epilogue thread, once per tile, for its row and column slice
+//        [c0, c1); tcgen05.ld of each 32-column chunk must be warp-uniform)
+//   __device__ void on_timeout() const.
+template <class Epi, int EPI_WARPS>
+__global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
                      const __grid_constant__ CUtensorMap tma_b, int M, int N, int K, Epi epi) {
   extern __shared__ uint8_t smem_raw[];
@@ -68,7 +74,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&ctl->tfull[b], 1);
-      tc::mbar_init(&ctl->tempty[b], EPI_THREADS);
+      tc::mbar_init(&ctl->tempty[b], 32 * EPI_WARPS);
     }
     tc::mbar_init(&ctl->drain, 1);
     ctl->abort = 0;
@@ -151,10 +157,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // -------------------------------------------------- epilogue --------
     const int quarter = warp & 3;  // TMEM lane quarter this warp may access
     const int row = quarter * 32 + lane;
+    constexpr int SLICE = BN / (EPI_WARPS / 4);
+    const int c0 = ((warp - 2) >> 2) * SLICE;
     int acc = 0;
     uint32_t acc_phase = 0;
+    typename Epi::State st;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const int m_blk = tile % num_m, n_blk = tile / num_m;
+      epi.prefetch(m_blk * BM, n_blk * BN, row, c0, c0 + SLICE, st);
       // one lane polls, then the warp proceeds together (tcgen05.ld is warp-wide)
       int ok = 1;
       if (lane == 0) ok = tc::mbar_wait(&ctl->tfull[acc], acc_phase, abort) ? 1 : 0;
@@ -162,7 +172,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!ok) break;
       tc::fence_after_sync();
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
-      epi(m_blk * BM, n_blk * BN, row, taddr);
+      epi(m_blk * BM, n_blk * BN, row, taddr, c0, c0 + SLICE, st);
       tc::fence_before_sync();
       tc::mbar_arrive(&ctl->tempty[acc]);
       acc ^= 1;
@@ -179,22 +189,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-template <class Epi>
+template <int EPI_WARPS, class Epi>
 int launch(const void *A, const void *B, int M, int N, int K, const Epi &epi,
            cudaStream_t stream) {
+  static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "4 or 8 epilogue warps");
   CUtensorMap ta, tb;
   if (dspark_make_tmap_bf16(&ta, A, (uint64_t)M, (uint64_t)K, BM) != 0) return DSPARK_ERR_CUDA;
   if (dspark_make_tmap_bf16(&tb, B, (uint64_t)N, (uint64_t)K, BN) != 0) return DSPARK_ERR_CUDA;
   static bool attr = false;
   if (!attr) {
-    if (cudaFuncSetAttribute(umma_gemm_kernel<Epi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(umma_gemm_kernel<Epi, EPI_WARPS>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SMEM_BYTES) != cudaSuccess)
       return DSPARK_ERR_CUDA;
     attr = true;
   }
-  const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-  const int grid = tiles < dspark_sm_count() ? tiles : dspark_sm_count();
-  umma_gemm_kernel<Epi><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ta, tb, M, N, K, epi);
+  const int num_m = (M + BM - 1) / BM;
+  const int tiles = num_m * ((N + BN - 1) / BN);
+  int grid = tiles < dspark_sm_count() ? tiles : dspark_sm_count();
+  // a multiple of the M-block count keeps every CTA (and epilogue thread) on one row block
+  if (Epi::kRowAffine && grid > num_m) grid = grid / num_m * num_m;
+  umma_gemm_kernel<Epi, EPI_WARPS><<<grid, 64 + 32 * EPI_WARPS, SMEM_BYTES, stream>>>(
+      ta, tb, M, N, K, epi);
   if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
   dspark_count_launches(1);
   return DSPARK_OK;

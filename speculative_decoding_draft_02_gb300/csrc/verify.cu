@@ -50,8 +50,7 @@ __global__ void __launch_bounds__(256) verify_rows(const bf16 *__restrict__ targ
   const uint4 *row4 = reinterpret_cast<const uint4 *>(row);
   float m = -INFINITY, s = 0.f, best = -INFINITY, bs = 0.f;
   int idx = 0x7fffffff;
-  for (int c = threadIdx.x; c < V / 8; c += blockDim.x) {
-    const uint4 q = row4[c];
+  auto consume = [&](const uint4 q, int c) {
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
     float vals[8];
 #pragma unroll
@@ -72,7 +71,19 @@ __global__ void __launch_bounds__(256) verify_rows(const bf16 *__restrict__ targ
       for (int t = 0; t < 8; ++t) cs += __expf(vals[t] * inv_tau - cm);
       lse_merge(m, s, cm, cs);
     }
+  };
+  // four independent 16-byte loads in flight per thread
+  const int n8 = V / 8, step = blockDim.x;
+  int c = threadIdx.x;
+  for (; c + 3 * step < n8; c += 4 * step) {
+    const uint4 q0 = __ldg(row4 + c), q1 = __ldg(row4 + c + step);
+    const uint4 q2 = __ldg(row4 + c + 2 * step), q3 = __ldg(row4 + c + 3 * step);
+    consume(q0, c);
+    consume(q1, c + step);
+    consume(q2, c + 2 * step);
+    consume(q3, c + 3 * step);
   }
+  for (; c < n8; c += step) consume(__ldg(row4 + c), c);
   warp_merge(m, s, best, idx, bs);
   __shared__ float sm[8], ss[8], sb[8];
   __shared__ int si[8];
@@ -151,9 +162,10 @@ __global__ void verify_decide(const RowStat *__restrict__ stat, const int32_t *_
 
 // E[i] = W1[x_{j*-1}] for residual rows, zero elsewhere; one warp per request.
 __global__ void resample_gather(const ResampleRow *__restrict__ rows, const bf16 *__restrict__ W1,
-                                bf16 *__restrict__ E, int R, int r) {
+                                bf16 *__restrict__ E, float *__restrict__ gfloor, int R, int r) {
   const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (i >= R) return;
+  if (lane == 0) gfloor[i] = -INFINITY;
   const ResampleRow rr = rows[i];
   uint4 *dst = reinterpret_cast<uint4 *>(E + (size_t)i * r);
   const uint4 *src = reinterpret_cast<const uint4 *>(W1 + (size_t)rr.prev * r);
@@ -161,67 +173,104 @@ __global__ void resample_gather(const ResampleRow *__restrict__ rows, const bf16
     dst[c] = rr.kind == KIND_RESIDUAL ? src[c] : make_uint4(0, 0, 0, 0);
 }
 
-// Bonus rows: Gumbel-max over target row pos (stream 3), 128 entries per tile;
-// one warp per request, 8 requests per CTA.
-__global__ void __launch_bounds__(256) bonus_tile(const ResampleRow *__restrict__ rows,
-                                                  const bf16 *__restrict__ target,
-                                                  RowPartial *__restrict__ part, int R,
-                                                  int gamma, int V, int n_tiles, float inv_tau,
-                                                  uint64_t seed) {
-  const int i = blockIdx.y * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (i >= R) return;
+// Plain target samples: the bonus row l_r + 1 when every draft passed (stream
+// 3), or the rejected row when its residual was empty (stream 2).  Gumbel-max
+// over t / tau; one CTA of 512 threads per request, 4 entries (one Philox call)
+// per thread and step.  Entries that cannot beat the best score the warp has
+// seen skip their logarithms (1 - u >= e^{s - F + 0.01} implies s + g < F).
+__global__ void __launch_bounds__(512) bonus_row(const ResampleRow *__restrict__ rows,
+                                                 const bf16 *__restrict__ target,
+                                                 int32_t *__restrict__ bonus, int gamma, int V,
+                                                 float inv_tau, uint64_t seed) {
+  const int i = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const ResampleRow rr = rows[i];
-  if (rr.kind != KIND_BONUS) return;
+  if (rr.kind != KIND_BONUS && rr.kind != KIND_FALLBACK) return;
+  const uint32_t stream = rr.kind == KIND_BONUS ? RNG_BONUS : RNG_RESIDUAL;
   const bf16 *trow = target + ((size_t)i * (gamma + 1) + rr.pos - 1) * V;
-  const int n0 = blockIdx.x * TN;
+  const PhiloxKeys keys(seed);
   float best = -INFINITY, bs = 0.f, m = -INFINITY, s = 0.f;
   int idx = 0x7fffffff;
-  // each lane owns 4 consecutive entries: one Philox call per lane
-  const int v0 = n0 + lane * 4;
-  if (v0 < V) {
-    const uint4 w = rng_words4(seed, (uint32_t)(v0 >> 2), (uint32_t)rr.pos, (uint32_t)i, RNG_BONUS);
+  // warp-uniform trip count: every lane reaches every shuffle; lanes past V are
+  // masked.  Each lane takes 8 entries (16 bytes, two Philox calls) per step
+  // and the next step's 16 bytes are in flight while the current ones are used.
+  constexpr int STEP = 16 * 256;  // 16 warps x 32 lanes x 8 entries
+  int base = warp * 256;
+  uint4 nq = make_uint4(0, 0, 0, 0);
+  if (base + lane * 8 < V) nq = __ldg(reinterpret_cast<const uint4 *>(trow + base + lane * 8));
+  for (; base < V; base += STEP) {
+    const int v0 = base + lane * 8;
+    const bool valid = v0 < V;  // V % 8 == 0: a valid group has all 8 entries
+    const uint4 q = nq;
+    if (base + STEP + lane * 8 < V)
+      nq = __ldg(reinterpret_cast<const uint4 *>(trow + base + STEP + lane * 8));
+    float tv[8];
+    uint32_t ws[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    {
+      const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const int v = v0 + t;
-      if (v < V) {
-        const float sc = __bfloat162float(trow[v]) * inv_tau + rng_gumbel(uint4_get(w, t));
-        if (better(sc, v, best, idx)) { best = sc; idx = v; }
+      for (int t = 0; t < 4; ++t) {
+        tv[2 * t] = valid ? bf16_lo(qw[t]) * inv_tau : -INFINITY;
+        tv[2 * t + 1] = valid ? bf16_hi(qw[t]) * inv_tau : -INFINITY;
+      }
+    }
+    if (valid) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint4 w = keys(make_uint4((uint32_t)((v0 >> 2) + h), (uint32_t)rr.pos, (uint32_t)i,
+                                        stream));
+        ws[4 * h] = w.x; ws[4 * h + 1] = w.y; ws[4 * h + 2] = w.z; ws[4 * h + 3] = w.w;
+      }
+    }
+    const float F = warp_max(best);
+    if (valid) {
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const bool cand = !(F > -INFINITY) ||
+                          (1.f - rng_uniform(ws[t])) < __expf(tv[t] - F + 0.01f);
+        if (cand) {
+          const float sc = tv[t] + rng_gumbel(ws[t]);
+          if (better(sc, v0 + t, best, idx)) { best = sc; idx = v0 + t; }
+        }
       }
     }
   }
   warp_merge(m, s, best, idx, bs);
-  if (lane == 0) {
-    RowPartial p;
-    p.m = -INFINITY; p.sum = 0.f; p.best = best; p.idx = idx; p.best_s = 0.f;
-    p.pad0 = -INFINITY; p.pad1 = __int_as_float(0x7fffffff); p.pad2 = 0.f;
-    part[(size_t)i * n_tiles + blockIdx.x] = p;
+  __shared__ float sb[16];
+  __shared__ int si[16];
+  if (lane == 0) { sb[warp] = best; si[warp] = idx; }
+  __syncthreads();
+  if (warp == 0) {
+    best = lane < 16 ? sb[lane] : -INFINITY;
+    idx = lane < 16 ? si[lane] : 0x7fffffff;
+    warp_merge(m, s, best, idx, bs);
+    if (lane == 0) bonus[i] = idx;
   }
 }
 
-// Final residual / bonus token per request.
-__global__ void resample_reduce(const ResampleRow *__restrict__ rows,
-                                const RowPartial *__restrict__ part, int n_tiles, int R,
-                                int32_t *__restrict__ bonus) {
+// Residual rows: combine the slice partials into the corrected token; a row
+// whose residual came out empty is handed to the plain target sample.
+__global__ void resample_reduce(ResampleRow *__restrict__ rows, const RowPartial *__restrict__ part,
+                                int n_parts, int R, int32_t *__restrict__ bonus) {
   const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (i >= R) return;
-  if (rows[i].kind == KIND_NONE) return;
-  float best = -INFINITY, fb = -INFINITY, d0 = 0.f, d1 = 0.f, d2 = 0.f, e0 = 0.f, e1 = 0.f,
-        e2 = 0.f;
-  int idx = 0x7fffffff, fidx = 0x7fffffff;
-  for (int t = lane; t < n_tiles; t += 32) {
-    const RowPartial p = part[(size_t)i * n_tiles + t];
+  if (rows[i].kind != KIND_RESIDUAL) return;
+  float best = -INFINITY, d0 = 0.f, d1 = 0.f, d2 = 0.f;
+  int idx = 0x7fffffff;
+  for (int t = lane; t < n_parts; t += 32) {
+    const RowPartial p = part[(size_t)i * n_parts + t];
     if (better(p.best, p.idx, best, idx)) { best = p.best; idx = p.idx; }
-    const int pi = __float_as_int(p.pad1);
-    if (better(p.pad0, pi, fb, fidx)) { fb = p.pad0; fidx = pi; }
   }
   warp_merge(d0, d1, best, idx, d2);
-  warp_merge(e0, e1, fb, fidx, e2);
-  if (lane == 0) bonus[i] = (best > -INFINITY) ? idx : fidx;
+  if (lane == 0) {
+    if (best > -INFINITY) bonus[i] = idx;
+    else rows[i].kind = KIND_FALLBACK;
+  }
 }
 
 struct VerifyWs {
   RowStat *stat;
   ResampleRow *rows;
+  float *gfloor;
   bf16 *E;
   RowPartial *part;
   size_t bytes;
@@ -234,11 +283,12 @@ VerifyWs verify_layout(const dspark_dims *d, char *base) {
   off = dspark_align_up(off + sizeof(RowStat) * (size_t)d->R * (d->gamma + 1), 256);
   w.rows = (ResampleRow *)(base + off);
   off = dspark_align_up(off + sizeof(ResampleRow) * (size_t)d->R, 256);
+  w.gfloor = (float *)(base + off);
+  off = dspark_align_up(off + sizeof(float) * (size_t)d->R, 256);
   w.E = (bf16 *)(base + off);
   off = dspark_align_up(off + sizeof(bf16) * (size_t)d->R * d->r, 256);
   w.part = (RowPartial *)(base + off);
-  const size_t n_tiles = (d->V + TN - 1) / TN;
-  off = dspark_align_up(off + sizeof(RowPartial) * (size_t)d->R * n_tiles, 256);
+  off = dspark_align_up(off + sizeof(RowPartial) * (size_t)d->R * logits_parts(d->V), 256);
   w.bytes = off;
   return w;
 }
@@ -260,6 +310,9 @@ extern "C" int dspark_verify(const dspark_dims *dims, const int32_t *anchor, con
     return DSPARK_ERR_ARG;
   const bool sample = tau > 0.f;
   if (sample && (!anchor || !base_logits || !W1 || !W2t || !lse_d || !logp_d)) return DSPARK_ERR_ARG;
+  if (((uintptr_t)target | (sample ? ((uintptr_t)W2t | (uintptr_t)W1 | (uintptr_t)base_logits)
+                                   : (uintptr_t)0)) & 15)
+    return DSPARK_ERR_ARG;  // TMA and 16-byte vector loads
   VerifyWs ws = verify_layout(dims, (char *)workspace);
   if (!workspace || workspace_bytes < ws.bytes || ((uintptr_t)workspace & 255))
     return DSPARK_ERR_WORKSPACE;
@@ -282,32 +335,19 @@ extern "C" int dspark_verify(const dspark_dims *dims, const int32_t *anchor, con
   verify_decide<MODE_SAMPLE><<<(R + 127) / 128, 128, 0, stream>>>(
       ws.stat, anchor, tokens, len, lse_d, logp_d, ws.rows, accepted, bonus, R, G, V, seed);
   DSPARK_CHECK_LAUNCH();
-  resample_gather<<<(R * 32 + 255) / 256, 256, 0, stream>>>(ws.rows, (const bf16 *)W1, ws.E, R, r);
+  resample_gather<<<(R * 32 + 255) / 256, 256, 0, stream>>>(ws.rows, (const bf16 *)W1, ws.E,
+                                                          ws.gfloor, R, r);
   DSPARK_CHECK_LAUNCH();
-  TileArgs ta;
-  ta.base = (const bf16 *)base_logits;
-  ta.E = ws.E;
-  ta.W2t = (const bf16 *)W2t;
-  ta.target = (const bf16 *)target;
-  ta.rows = ws.rows;
-  ta.part = ws.part;
-  ta.M = R;
-  ta.V = V;
-  ta.r = r;
-  ta.gamma = G;
-  ta.k = 0;
-  ta.n_tiles = (V + TN - 1) / TN;
-  ta.inv_tau = inv_tau;
-  ta.seed = seed;
-  logits_tile_simple<MODE_RESIDUAL><<<dim3(ta.n_tiles, (R + TM - 1) / TM), 256, 0, stream>>>(ta);
+  const int n_tiles = (int)logits_parts(V);
+  EpiLogits<MODE_RESIDUAL> epi{(const bf16 *)base_logits, (const bf16 *)target, ws.rows, ws.part,
+                               ws.gfloor, R, V, G, 0, n_tiles, inv_tau, seed};
+  const int rc = gemm::launch<LOGITS_EPI_WARPS>(ws.E, W2t, R, V, r, epi, stream);
+  if (rc != DSPARK_OK) return rc;
+  resample_reduce<<<(R * 32 + 255) / 256, 256, 0, stream>>>(ws.rows, ws.part, n_tiles, R, bonus);
   DSPARK_CHECK_LAUNCH();
-  bonus_tile<<<dim3(ta.n_tiles, (R + 7) / 8), 256, 0, stream>>>(ws.rows, (const bf16 *)target,
-                                                              ws.part, R, G, V, ta.n_tiles,
-                                                              inv_tau, seed);
+  bonus_row<<<R, 512, 0, stream>>>(ws.rows, (const bf16 *)target, bonus, G, V, inv_tau, seed);
   DSPARK_CHECK_LAUNCH();
-  resample_reduce<<<(R * 32 + 255) / 256, 256, 0, stream>>>(ws.rows, ws.part, ta.n_tiles, R, bonus);
-  DSPARK_CHECK_LAUNCH();
-  dspark_count_launches(6);
+  dspark_count_launches(5);  // + the GEMM, counted by launch()
   return DSPARK_OK;
 }
 
