@@ -70,7 +70,8 @@ enum {
   DSPARK_ERR_WORKSPACE = 4,  /* workspace missing or smaller than required         */
   DSPARK_ERR_TOKEN = 5,      /* device status: token id outside [0, V)              */
   DSPARK_ERR_LENGTH = 6,     /* device status: verify length outside [0, gamma]     */
-  DSPARK_ERR_TIMEOUT = 7     /* device status: a bounded device-side wait ran out   */
+  DSPARK_ERR_TIMEOUT = 7,    /* device status: a bounded device-side wait ran out   */
+  DSPARK_ERR_TOO_LARGE = 8   /* problem needs more than the library's static scratch */
 };
 
 enum {
@@ -174,6 +175,33 @@ int dspark_verify(const dspark_dims *dims, const int32_t *anchor, const int32_t 
                   const void *target, float tau, uint64_t seed, int32_t *accepted,
                   int32_t *bonus, void *workspace, size_t workspace_bytes,
                   dspark_stream_t stream);
+
+/* Bytes of scratch the library keeps inside itself for dspark_markov_draft_static. */
+#define DSPARK_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/* dspark_markov_draft without a caller-provided workspace.  No counterpart on
+ * the method's pages: it exists for callers that cannot allocate device
+ * memory, such as a plugin interface that hands the library only its input
+ * and output tensors with no allocator, or a serving loop whose memory planner
+ * forbids allocations once it has started.  The scratch lives in one
+ * file-scope device array of DSPARK_STATIC_SCRATCH_BYTES (16 MiB) that every
+ * GPU loading the library holds until the process exits; this call itself
+ * allocates nothing.
+ *   Arguments, outputs and results are those of dspark_markov_draft.
+ *   Returns DSPARK_ERR_TOO_LARGE (nothing launched) when
+ *   dspark_markov_workspace_bytes(dims) > DSPARK_STATIC_SCRATCH_BYTES; the V4
+ *   shape (R=256, gamma=5, V=129280, r=512) needs about 8.6 MB.
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ *   Every call shares the one array: calls whose work overlaps on the GPU
+ *   (other streams, other host threads) race and must be serialised by the
+ *   caller.  Nothing in the array needs to start at zero. */
+int dspark_markov_draft_static(const dspark_dims *dims, const void *base_logits, const void *h,
+                               const int32_t *anchor, const void *W1, const void *W2t,
+                               const void *w_conf, const float *T, float tau, uint64_t seed,
+                               int32_t *tokens, float *conf, float *logp_d, float *lse_d,
+                               dspark_stream_t stream);
 
 /* Synchronises `stream`, returns the sticky device status word (DSPARK_OK or a
  * DSPARK_ERR_* code) and clears it when clear != 0. */

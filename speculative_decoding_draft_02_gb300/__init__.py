@@ -28,7 +28,9 @@ EXPORTS = [
     "dspark_lm_head", "dspark_pack_w2", "dspark_markov_workspace_bytes", "dspark_markov_draft",
     "dspark_draft", "dspark_schedule", "dspark_verify_workspace_bytes", "dspark_verify",
     "dspark_device_status", "dspark_error_string", "dspark_launch_count",
+    "dspark_markov_draft_static",
 ]
+STATIC_SCRATCH_BYTES = 16 << 20
 
 
 class DSparkError(RuntimeError):
@@ -67,6 +69,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "dspark_verify_workspace_bytes": (SZ, [DP]),
         "dspark_verify": (ctypes.c_int, [DP, P, P, P, P, P, P, P, P, P, F32, U64, P, P, P, SZ,
                                          P]),
+        "dspark_markov_draft_static": (ctypes.c_int, [DP, P, P, P, P, P, P, P, F32, U64, P, P, P,
+                                                      P, P]),
         "dspark_device_status": (ctypes.c_int, [P, ctypes.c_int]),
         "dspark_error_string": (ctypes.c_char_p, [ctypes.c_int]),
         "dspark_launch_count": (U64, []),
@@ -138,6 +142,15 @@ def dspark_markov_draft(dims, base_logits, h, anchor, W1, W2t, w_conf, T, tau, s
         ctypes.byref(dims), _ptr(base_logits), _ptr(h), _ptr(anchor), _ptr(W1), _ptr(W2t),
         _ptr(w_conf), _ptr(T), float(tau), _u64(seed), _ptr(tokens), _ptr(conf), _ptr(logp_d),
         _ptr(lse_d), _ptr(workspace), workspace.numel(), _stream(stream)), "dspark_markov_draft")
+
+
+def dspark_markov_draft_static(dims, base_logits, h, anchor, W1, W2t, w_conf, T, tau, seed,
+                               tokens, conf, logp_d, lse_d, stream=None):
+    """dspark_markov_draft with the scratch kept inside the library (no workspace)."""
+    _check(load_library().dspark_markov_draft_static(
+        ctypes.byref(dims), _ptr(base_logits), _ptr(h), _ptr(anchor), _ptr(W1), _ptr(W2t),
+        _ptr(w_conf), _ptr(T), float(tau), _u64(seed), _ptr(tokens), _ptr(conf), _ptr(logp_d),
+        _ptr(lse_d), _stream(stream)), "dspark_markov_draft_static")
 
 
 def dspark_draft(dims, h, anchor, W_lm, W1, W2t, w_conf, T, tau, seed, base_logits, tokens, conf,

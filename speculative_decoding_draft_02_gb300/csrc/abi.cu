@@ -26,6 +26,7 @@ extern "C" const char *dspark_error_string(int code) {
     case DSPARK_ERR_TOKEN: return "token id outside [0, V)";
     case DSPARK_ERR_LENGTH: return "verify length outside [0, gamma]";
     case DSPARK_ERR_TIMEOUT: return "device-side wait timed out";
+    case DSPARK_ERR_TOO_LARGE: return "problem exceeds the library's static scratch";
     default: return "unknown error";
   }
 }

@@ -11,6 +11,8 @@
 // + decision on the tensor cores, logits stay on chip), then reduce_prep
 // (combine the per-slice partials into x_k, lse_k, logp_k, and gather
 // E = W1[x_k] with c_{k+1} for the next step).
+#include <mutex>
+
 #include "logits_tile.cuh"
 
 DSPARK_DECLARE_STATUS(s_status_markov)
@@ -248,4 +250,45 @@ int dspark_status_markov(int clear) {
     cudaMemcpyToSymbol(s_status_markov, &z, sizeof(int));
   }
   return v;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant: the same draft loop with its scratch in one static
+// device array.  For callers that have no way to allocate device memory (a
+// plugin interface that passes only tensors, a serving loop that forbids
+// allocations after start-up).  The array is shared by every call: overlapping
+// calls race.  No field of the scratch needs to start at zero: the draft loop
+// writes every word it reads (the shared floor is reset before each step).
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_markov_scratch[DSPARK_STATIC_SCRATCH_BYTES];
+
+namespace {
+constexpr int MAX_DEVICES = 64;
+std::mutex g_scratch_mu;
+void *g_scratch_ptr[MAX_DEVICES] = {};
+}  // namespace
+
+extern "C" int dspark_markov_draft_static(const dspark_dims *dims, const void *base_logits,
+                                          const void *h, const int32_t *anchor, const void *W1,
+                                          const void *W2t, const void *w_conf, const float *T,
+                                          float tau, uint64_t seed, int32_t *tokens, float *conf,
+                                          float *logp_d, float *lse_d, dspark_stream_t stream) {
+  if (!dspark_dims_ok(dims)) return DSPARK_ERR_ARG;
+  if (dspark_markov_workspace_bytes(dims) > DSPARK_STATIC_SCRATCH_BYTES) return DSPARK_ERR_TOO_LARGE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return DSPARK_ERR_CUDA;
+  void *ptr;
+  {
+    // set-up once per device, with that device current: the host-side symbol is
+    // only a stand-in, the kernels need the array's device address
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+      void *p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_markov_scratch) != cudaSuccess || !p) return DSPARK_ERR_CUDA;
+      g_scratch_ptr[dev] = p;
+    }
+    ptr = g_scratch_ptr[dev];
+  }
+  return dspark_markov_draft(dims, base_logits, h, anchor, W1, W2t, w_conf, T, tau, seed, tokens,
+                             conf, logp_d, lse_d, ptr, DSPARK_STATIC_SCRATCH_BYTES, stream);
 }
