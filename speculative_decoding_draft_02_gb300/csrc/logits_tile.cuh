@@ -72,6 +72,8 @@ struct EpiLogits {
   const bf16 *base;          // [R*gamma, V]
   const bf16 *target;        // [R, gamma+1, V]       (residual)
   const ResampleRow *rows;   // [R]                    (residual)
+  const int *list;           // [R] request of each compacted row (residual)
+  const int *count;          // number of compacted rows           (residual)
   RowPartial *part;          // [R, n_parts]
   float *gfloor;             // [R] best Gumbel score found so far on each row, shared by
                              // every CTA of the pass (set to -inf before the pass)
@@ -126,15 +128,17 @@ struct EpiLogits {
     float lse_t = 0.f, lse_d = 0.f;
     const bf16 *trow = nullptr;
     const bf16 *brow = base;
+    int req = i;  // request id: keys the random stream and the logit rows
     if (MODE == MODE_RESIDUAL) {
+      active = i < *count;
       if (active) {
-        const ResampleRow rr = rows[i];
-        active = rr.kind == KIND_RESIDUAL;
+        req = list[i];
+        const ResampleRow rr = rows[req];
         pos = rr.pos;
         lse_t = rr.lse_t;
         lse_d = rr.lse_d;
-        brow = base + (size_t)(i * gamma + pos - 1) * V;
-        trow = target + ((size_t)i * (gamma + 1) + pos - 1) * V;
+        brow = base + (size_t)(req * gamma + pos - 1) * V;
+        trow = target + ((size_t)req * (gamma + 1) + pos - 1) * V;
       }
     } else {
       draft_row(m0, row, brow);
@@ -241,7 +245,7 @@ struct EpiLogits {
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
                 const uint4 w = keys(make_uint4((uint32_t)((n >> 2) + 4 * h + q), (uint32_t)pos,
-                                                (uint32_t)i, stream));
+                                                (uint32_t)req, stream));
                 ws[q * 4 + 0] = w.x; ws[q * 4 + 1] = w.y; ws[q * 4 + 2] = w.z; ws[q * 4 + 3] = w.w;
                 wmax = max(max(wmax, max(w.x, w.y)), max(w.z, w.w));
               }
@@ -261,31 +265,52 @@ struct EpiLogits {
             }
           } else {
             // residual max(0, p_t - p_d) at the rejected position.  The score
-            // log q_j + g_j <= log p_t(j) + g_j, so with the same argument an
-            // entry is skipped when 1 - u_j >= p_t(j) e^{-F + 0.01}.
+            // log q_j + g_j <= log p_t(j) + g_j, so by the same argument an
+            // entry is skipped when 1 - u_j >= p_t(j) e^{-F + 0.01}; the chunk
+            // test uses the chunk's largest p_t.
             uint4 tw[4];
             load_raw32(trow, n, V, tw);
             float tv[32];
             unpack32(tw, n, V, tv);
+            float mx[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) mx[j] = fmaxf(tv[j], tv[j + 16]);
+#pragma unroll
+            for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+              for (int j = 0; j < w; ++j) mx[j] = fmaxf(mx[j], mx[j + w]);
+            int w_thr = -1;
+            if (F > -INFINITY) {
+              const float X = __expf(fminf(mx[0] * inv_tau - lse_t - F + 0.01f, 0.f)) * 8388608.f;
+              w_thr = X >= 8388607.f ? -1 : 8388607 - (int)ceilf(X);
+            }
             const float K = F > -INFINITY ? __expf(0.01f - F) : INFINITY;
             const bool per_entry = K < 1e30f;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const uint4 w = keys(make_uint4((uint32_t)((n >> 2) + q), (uint32_t)pos,
-                                              (uint32_t)i, stream));
-              const uint32_t wq[4] = {w.x, w.y, w.z, w.w};
+            for (int h = 0; h < 2; ++h) {
+              uint32_t ws[16];
+              uint32_t wmax = 0;
 #pragma unroll
-              for (int l = 0; l < 4; ++l) {
-                const int j = q * 4 + l;
-                const float pt = __expf(tv[j] * inv_tau - lse_t);
-                const bool cand = (n + j < V) &&
-                                  (!per_entry || (1.f - rng_uniform(wq[l])) < pt * K);
-                if (cand) {
-                  const float sl = (sv[j] + __uint_as_float(acc[j])) * inv_tau;
-                  const float qv = pt - __expf(sl - lse_d);
-                  if (qv > 0.f) {
-                    const float sc = __logf(qv) + rng_gumbel(wq[l]);
-                    if (sc > best) { best = sc; idx = n + j; }
+              for (int q = 0; q < 4; ++q) {
+                const uint4 w = keys(make_uint4((uint32_t)((n >> 2) + 4 * h + q), (uint32_t)pos,
+                                                (uint32_t)req, stream));
+                ws[q * 4 + 0] = w.x; ws[q * 4 + 1] = w.y; ws[q * 4 + 2] = w.z; ws[q * 4 + 3] = w.w;
+                wmax = max(max(wmax, max(w.x, w.y)), max(w.z, w.w));
+              }
+              if ((int)(wmax >> 9) > w_thr) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                  const int j = 16 * h + e;
+                  const float pt = __expf(tv[j] * inv_tau - lse_t);
+                  const bool cand = (n + j < V) &&
+                                    (!per_entry || (1.f - rng_uniform(ws[e])) < pt * K);
+                  if (cand) {
+                    const float sl = (sv[j] + __uint_as_float(acc[j])) * inv_tau;
+                    const float qv = pt - __expf(sl - lse_d);
+                    if (qv > 0.f) {
+                      const float sc = __logf(qv) + rng_gumbel(ws[e]);
+                      if (sc > best) { best = sc; idx = n + j; }
+                    }
                   }
                 }
               }

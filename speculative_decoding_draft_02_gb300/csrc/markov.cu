@@ -220,7 +220,8 @@ extern "C" int dspark_markov_draft(const dspark_dims *dims, const void *base_log
   for (int k = 1; k <= G; ++k) {
     int rc;
     if (tau > 0.f) {
-      EpiLogits<MODE_SAMPLE> epi{(const bf16 *)base_logits, nullptr, nullptr, ws.part, ws.gfloor,
+      EpiLogits<MODE_SAMPLE> epi{(const bf16 *)base_logits, nullptr, nullptr, nullptr, nullptr,
+                                 ws.part, ws.gfloor,
                                  R, V, G, k, n_tiles, inv_tau, seed};
       rc = gemm::launch<LOGITS_EPI_WARPS>(ws.E, W2t, R, V, r, epi, stream);
       if (rc != DSPARK_OK) return rc;
@@ -228,7 +229,8 @@ extern "C" int dspark_markov_draft(const dspark_dims *dims, const void *base_log
                                                       logp_d, (const bf16 *)W1, w_e, ws.zh, T,
                                                       ws.E, conf, ws.gfloor);
     } else {
-      EpiLogits<MODE_GREEDY> epi{(const bf16 *)base_logits, nullptr, nullptr, ws.part, ws.gfloor,
+      EpiLogits<MODE_GREEDY> epi{(const bf16 *)base_logits, nullptr, nullptr, nullptr, nullptr,
+                                 ws.part, ws.gfloor,
                                  R, V, G, k, n_tiles, 1.f, seed};
       rc = gemm::launch<LOGITS_EPI_WARPS>(ws.E, W2t, R, V, r, epi, stream);
       if (rc != DSPARK_OK) return rc;

@@ -53,7 +53,8 @@ struct SharedCtl {
 template <class Epi, int EPI_WARPS>
 __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
-                     const __grid_constant__ CUtensorMap tma_b, int M, int N, int K, Epi epi) {
+                     const __grid_constant__ CUtensorMap tma_b, int M, int N, int K,
+                     const int *m_dev, Epi epi) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -63,6 +64,10 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
   volatile int *abort = &ctl->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (m_dev) {  // rows counted on the device by an earlier kernel (at most M)
+    const int md = *m_dev;
+    M = md < M ? (md > 0 ? md : 0) : M;
+  }
   const int num_m = (M + BM - 1) / BM, num_n = (N + BN - 1) / BN;
   const int num_tiles = num_m * num_n;
   const int k_iters = K / BK;
@@ -189,9 +194,12 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
   }
 }
 
+// M rows of A are described to TMA; when m_dev is given the kernel processes
+// only the first *m_dev of them (read on the device, so the count can come from
+// an earlier kernel in the stream).
 template <int EPI_WARPS, class Epi>
 int launch(const void *A, const void *B, int M, int N, int K, const Epi &epi,
-           cudaStream_t stream) {
+           cudaStream_t stream, const int *m_dev = nullptr) {
   static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "4 or 8 epilogue warps");
   CUtensorMap ta, tb;
   if (dspark_make_tmap_bf16(&ta, A, (uint64_t)M, (uint64_t)K, BM) != 0) return DSPARK_ERR_CUDA;
@@ -210,7 +218,7 @@ int launch(const void *A, const void *B, int M, int N, int K, const Epi &epi,
   // a multiple of the M-block count keeps every CTA (and epilogue thread) on one row block
   if (Epi::kRowAffine && grid > num_m) grid = grid / num_m * num_m;
   umma_gemm_kernel<Epi, EPI_WARPS><<<grid, 64 + 32 * EPI_WARPS, SMEM_BYTES, stream>>>(
-      ta, tb, M, N, K, epi);
+      ta, tb, M, N, K, m_dev, epi);
   if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
   dspark_count_launches(1);
   return DSPARK_OK;

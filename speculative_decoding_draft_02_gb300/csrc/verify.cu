@@ -20,11 +20,14 @@ DSPARK_DECLARE_STATUS(s_status_verify)
 
 namespace {
 
-struct __align__(16) RowStat {
-  int32_t argmax;  // argmax_v t[v]          (greedy)
-  float lse_t;     // logsumexp(t / tau)     (sampling)
-  float tx;        // t[x_j] / tau           (sampling, rows with a draft token)
-  int32_t pad;
+constexpr int NSEG = 4;  // CTAs per target row in the first pass
+
+// Per (request, row, segment): online log-sum-exp of t / tau (sampling) or the
+// argmax (greedy) over one quarter of the vocabulary.
+struct __align__(16) SegStat {
+  float m, s;      // sampling
+  float best;      // greedy
+  int32_t idx;     // greedy
 };
 
 __device__ __forceinline__ int clamp_len(const int32_t *len, int i, int gamma) {
@@ -36,20 +39,28 @@ __device__ __forceinline__ int clamp_len(const int32_t *len, int i, int gamma) {
   return L;
 }
 
-// One CTA per (row j, request i) with j <= l_i: argmax or log-sum-exp over V.
+__device__ __forceinline__ int seg_len(int V) { return ((V + NSEG - 1) / NSEG + 7) / 8 * 8; }
+
+// Pass 1: grid (NSEG * (gamma+1), R).  Greedy scans rows 1..l_r+1 (their
+// argmaxes decide acceptance and give the correction or bonus token); sampling
+// scans rows 1..l_r (their normalisers enter the acceptance test; the bonus
+// row needs none).  Block (0, 0) also clears the residual-row counter.
 template <int MODE>
 __global__ void __launch_bounds__(256) verify_rows(const bf16 *__restrict__ target,
-                                                   const int32_t *__restrict__ tokens,
                                                    const int32_t *__restrict__ len,
-                                                   RowStat *__restrict__ stat, int gamma,
-                                                   int V, float inv_tau) {
-  const int j = blockIdx.x, i = blockIdx.y;  // j: 0-based row (position j + 1)
+                                                   SegStat *__restrict__ stat,
+                                                   int *__restrict__ count, int gamma, int V,
+                                                   float inv_tau) {
+  const int j = blockIdx.x / NSEG, seg = blockIdx.x % NSEG, i = blockIdx.y;
+  if (blockIdx.x == 0 && i == 0 && threadIdx.x == 0) *count = 0;
   const int L = clamp_len(len, i, gamma);
-  if (j > L) return;
+  if (MODE == MODE_GREEDY ? j > L : j >= L) return;
+  const int sl = seg_len(V), v_beg = seg * sl, v_end = min(V, v_beg + sl);
   const bf16 *row = target + ((size_t)i * (gamma + 1) + j) * V;
   const uint4 *row4 = reinterpret_cast<const uint4 *>(row);
   float m = -INFINITY, s = 0.f, best = -INFINITY, bs = 0.f;
   int idx = 0x7fffffff;
+  const float c2 = inv_tau * 1.4426950408889634f;
   auto consume = [&](const uint4 q, int c) {
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
     float vals[8];
@@ -61,21 +72,21 @@ __global__ void __launch_bounds__(256) verify_rows(const bf16 *__restrict__ targ
     if (MODE == MODE_GREEDY) {
 #pragma unroll
       for (int t = 0; t < 8; ++t)
-        if (better(vals[t], c * 8 + t, best, idx)) { best = vals[t]; idx = c * 8 + t; }
+        if (vals[t] > best) { best = vals[t]; idx = c * 8 + t; }  // ids increase per thread
     } else {
-      float cm = vals[0] * inv_tau;
+      float cm = vals[0];
 #pragma unroll
-      for (int t = 1; t < 8; ++t) cm = fmaxf(cm, vals[t] * inv_tau);
-      float cs = 0.f;
+      for (int t = 1; t < 8; ++t) cm = fmaxf(cm, vals[t]);
+      cm *= c2;  // log2 units
+      if (cm > m) { s *= ex2_fast(m - cm); m = cm; }
 #pragma unroll
-      for (int t = 0; t < 8; ++t) cs += __expf(vals[t] * inv_tau - cm);
-      lse_merge(m, s, cm, cs);
+      for (int t = 0; t < 8; ++t) s += ex2_fast(vals[t] * c2 - m);
     }
   };
   // four independent 16-byte loads in flight per thread
-  const int n8 = V / 8, step = blockDim.x;
-  int c = threadIdx.x;
-  for (; c + 3 * step < n8; c += 4 * step) {
+  const int c_end = v_end / 8, step = blockDim.x;
+  int c = v_beg / 8 + threadIdx.x;
+  for (; c + 3 * step < c_end; c += 4 * step) {
     const uint4 q0 = __ldg(row4 + c), q1 = __ldg(row4 + c + step);
     const uint4 q2 = __ldg(row4 + c + 2 * step), q3 = __ldg(row4 + c + 3 * step);
     consume(q0, c);
@@ -83,7 +94,9 @@ __global__ void __launch_bounds__(256) verify_rows(const bf16 *__restrict__ targ
     consume(q2, c + 2 * step);
     consume(q3, c + 3 * step);
   }
-  for (; c < n8; c += step) consume(__ldg(row4 + c), c);
+  for (; c < c_end; c += step) consume(__ldg(row4 + c), c);
+  constexpr float LN2 = 0.6931471805599453f;
+  m = m > -INFINITY ? m * LN2 : m;  // back to natural units
   warp_merge(m, s, best, idx, bs);
   __shared__ float sm[8], ss[8], sb[8];
   __shared__ int si[8];
@@ -98,86 +111,119 @@ __global__ void __launch_bounds__(256) verify_rows(const bf16 *__restrict__ targ
     idx = lane < nw ? si[lane] : 0x7fffffff;
     warp_merge(m, s, best, idx, bs);
     if (lane == 0) {
-      RowStat st;
-      st.argmax = idx;
-      st.lse_t = m + logf(s);
-      st.tx = 0.f;
-      st.pad = 0;
-      if (MODE != MODE_GREEDY && j < L) {
-        int x = tokens[(size_t)i * gamma + j];
-        if (x < 0 || x >= V) { dspark_set_status(DSPARK_ERR_TOKEN); x = 0; }
-        st.tx = __bfloat162float(row[x]) * inv_tau;
-      }
-      stat[(size_t)i * (gamma + 1) + j] = st;
+      SegStat st;
+      st.m = m; st.s = s; st.best = best; st.idx = idx;
+      stat[((size_t)i * (gamma + 1) + j) * NSEG + seg] = st;
     }
   }
 }
 
-// Walk each request's admitted prefix; one thread per request.
+// Pass 2: walk each request's admitted prefix; one thread per request.
 template <int MODE>
-__global__ void verify_decide(const RowStat *__restrict__ stat, const int32_t *__restrict__ anchor,
+__global__ void verify_decide(const SegStat *__restrict__ stat, const bf16 *__restrict__ target,
+                              const int32_t *__restrict__ anchor,
                               const int32_t *__restrict__ tokens, const int32_t *__restrict__ len,
                               const float *__restrict__ lse_d, const float *__restrict__ logp_d,
-                              ResampleRow *__restrict__ rows, int32_t *__restrict__ accepted,
-                              int32_t *__restrict__ bonus, int R, int gamma, int V, uint64_t seed) {
+                              ResampleRow *__restrict__ rows, int *__restrict__ list,
+                              int *__restrict__ count, int32_t *__restrict__ accepted,
+                              int32_t *__restrict__ bonus, int R, int gamma, int V, float inv_tau,
+                              uint64_t seed) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= R) return;
   const int L = clamp_len(len, i, gamma);
-  const RowStat *st = stat + (size_t)i * (gamma + 1);
+  const SegStat *st = stat + (size_t)i * (gamma + 1) * NSEG;
   const int32_t *x = tokens + (size_t)i * gamma;
   int n = L;
   if (MODE == MODE_GREEDY) {
+    auto row_argmax = [&](int j) {  // 0-based row
+      float b = -INFINITY;
+      int id = 0x7fffffff;
+      for (int g = 0; g < NSEG; ++g)
+        if (better(st[j * NSEG + g].best, st[j * NSEG + g].idx, b, id)) {
+          b = st[j * NSEG + g].best;
+          id = st[j * NSEG + g].idx;
+        }
+      return id;
+    };
     for (int j = 1; j <= L; ++j)
-      if (x[j - 1] != st[j - 1].argmax) { n = j - 1; break; }
+      if (x[j - 1] != row_argmax(j - 1)) { n = j - 1; break; }
     accepted[i] = n;
-    bonus[i] = st[n].argmax;
+    bonus[i] = row_argmax(n);
     return;
   }
   ResampleRow rr;
   rr.kind = KIND_BONUS;
   rr.pos = L + 1;
   rr.prev = 0;
-  rr.lse_t = st[L].lse_t;
+  rr.lse_t = 0.f;
   rr.lse_d = 0.f;
   rr.pad[0] = rr.pad[1] = rr.pad[2] = 0;
   for (int j = 1; j <= L; ++j) {
+    float m = -INFINITY, s = 0.f;
+    for (int g = 0; g < NSEG; ++g) lse_merge(m, s, st[(j - 1) * NSEG + g].m, st[(j - 1) * NSEG + g].s);
+    const float lse_t = m + logf(s);
+    int xj = x[j - 1];
+    if (xj < 0 || xj >= V) { dspark_set_status(DSPARK_ERR_TOKEN); xj = 0; }
+    const float tx = __bfloat162float(target[((size_t)i * (gamma + 1) + j - 1) * V + xj]) * inv_tau;
     const uint4 w = rng_words4(seed, 0u, (uint32_t)j, (uint32_t)i, RNG_ACCEPT);
     const float u = rng_uniform(w.x);
     const size_t o = (size_t)i * gamma + j - 1;
-    const float margin = logf(u) + logp_d[o] - (st[j - 1].tx - st[j - 1].lse_t);
-    if (margin < 0.f) continue;  // u * p_d(x_j) < p_t(x_j): accepted
+    if (logf(u) + logp_d[o] < tx - lse_t) continue;  // u * p_d(x_j) < p_t(x_j): accepted
     n = j - 1;
     rr.kind = KIND_RESIDUAL;
     rr.pos = j;
     int prev = (j == 1) ? anchor[i] : x[j - 2];
     if (prev < 0 || prev >= V) { dspark_set_status(DSPARK_ERR_TOKEN); prev = 0; }
     rr.prev = prev;
-    rr.lse_t = st[j - 1].lse_t;
+    rr.lse_t = lse_t;
     rr.lse_d = lse_d[o];
+    list[atomicAdd(count, 1)] = i;  // compacted residual rows (order irrelevant)
     break;
   }
   accepted[i] = n;
   rows[i] = rr;
 }
 
-// E[i] = W1[x_{j*-1}] for residual rows, zero elsewhere; one warp per request.
-__global__ void resample_gather(const ResampleRow *__restrict__ rows, const bf16 *__restrict__ W1,
-                                bf16 *__restrict__ E, float *__restrict__ gfloor, int R, int r) {
-  const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  if (i >= R) return;
-  if (lane == 0) gfloor[i] = -INFINITY;
-  const ResampleRow rr = rows[i];
-  uint4 *dst = reinterpret_cast<uint4 *>(E + (size_t)i * r);
+// E[slot] = W1[x_{j*-1}] of the slot's request; fresh shared floor per slot.
+__global__ void resample_gather(const ResampleRow *__restrict__ rows, const int *__restrict__ list,
+                                const int *__restrict__ count, const bf16 *__restrict__ W1,
+                                bf16 *__restrict__ E, float *__restrict__ gfloor, int r) {
+  const int slot = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (slot >= *count) return;
+  if (lane == 0) gfloor[slot] = -INFINITY;
+  const ResampleRow rr = rows[list[slot]];
+  uint4 *dst = reinterpret_cast<uint4 *>(E + (size_t)slot * r);
   const uint4 *src = reinterpret_cast<const uint4 *>(W1 + (size_t)rr.prev * r);
-  for (int c = lane; c < r / 8; c += 32)
-    dst[c] = rr.kind == KIND_RESIDUAL ? src[c] : make_uint4(0, 0, 0, 0);
+  for (int c = lane; c < r / 8; c += 32) dst[c] = src[c];
+}
+
+// Residual rows: combine the slice partials into the corrected token; a row
+// whose residual came out empty is handed to the plain target sample.
+__global__ void resample_reduce(ResampleRow *__restrict__ rows, const int *__restrict__ list,
+                                const int *__restrict__ count,
+                                const RowPartial *__restrict__ part, int n_parts,
+                                int32_t *__restrict__ bonus) {
+  const int slot = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (slot >= *count) return;
+  const int req = list[slot];
+  float best = -INFINITY, d0 = 0.f, d1 = 0.f, d2 = 0.f;
+  int idx = 0x7fffffff;
+  for (int t = lane; t < n_parts; t += 32) {
+    const RowPartial p = part[(size_t)slot * n_parts + t];
+    if (better(p.best, p.idx, best, idx)) { best = p.best; idx = p.idx; }
+  }
+  warp_merge(d0, d1, best, idx, d2);
+  if (lane == 0) {
+    if (best > -INFINITY) bonus[req] = idx;
+    else rows[req].kind = KIND_FALLBACK;
+  }
 }
 
 // Plain target samples: the bonus row l_r + 1 when every draft passed (stream
 // 3), or the rejected row when its residual was empty (stream 2).  Gumbel-max
-// over t / tau; one CTA of 512 threads per request, 4 entries (one Philox call)
-// per thread and step.  Entries that cannot beat the best score the warp has
-// seen skip their logarithms (1 - u >= e^{s - F + 0.01} implies s + g < F).
+// over t / tau; one CTA of 512 threads per request.  Entries that cannot beat
+// the best score the warp has seen skip their logarithms
+// (1 - u >= e^{s - F + 0.01} implies s + g < F).
 __global__ void __launch_bounds__(512) bonus_row(const ResampleRow *__restrict__ rows,
                                                  const bf16 *__restrict__ target,
                                                  int32_t *__restrict__ bonus, int gamma, int V,
@@ -247,29 +293,11 @@ __global__ void __launch_bounds__(512) bonus_row(const ResampleRow *__restrict__
   }
 }
 
-// Residual rows: combine the slice partials into the corrected token; a row
-// whose residual came out empty is handed to the plain target sample.
-__global__ void resample_reduce(ResampleRow *__restrict__ rows, const RowPartial *__restrict__ part,
-                                int n_parts, int R, int32_t *__restrict__ bonus) {
-  const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  if (i >= R) return;
-  if (rows[i].kind != KIND_RESIDUAL) return;
-  float best = -INFINITY, d0 = 0.f, d1 = 0.f, d2 = 0.f;
-  int idx = 0x7fffffff;
-  for (int t = lane; t < n_parts; t += 32) {
-    const RowPartial p = part[(size_t)i * n_parts + t];
-    if (better(p.best, p.idx, best, idx)) { best = p.best; idx = p.idx; }
-  }
-  warp_merge(d0, d1, best, idx, d2);
-  if (lane == 0) {
-    if (best > -INFINITY) bonus[i] = idx;
-    else rows[i].kind = KIND_FALLBACK;
-  }
-}
-
 struct VerifyWs {
-  RowStat *stat;
+  SegStat *stat;
   ResampleRow *rows;
+  int *list;
+  int *count;
   float *gfloor;
   bf16 *E;
   RowPartial *part;
@@ -279,10 +307,14 @@ struct VerifyWs {
 VerifyWs verify_layout(const dspark_dims *d, char *base) {
   VerifyWs w;
   size_t off = 0;
-  w.stat = (RowStat *)(base + off);
-  off = dspark_align_up(off + sizeof(RowStat) * (size_t)d->R * (d->gamma + 1), 256);
+  w.stat = (SegStat *)(base + off);
+  off = dspark_align_up(off + sizeof(SegStat) * (size_t)d->R * (d->gamma + 1) * NSEG, 256);
   w.rows = (ResampleRow *)(base + off);
   off = dspark_align_up(off + sizeof(ResampleRow) * (size_t)d->R, 256);
+  w.list = (int *)(base + off);
+  off = dspark_align_up(off + sizeof(int) * (size_t)d->R, 256);
+  w.count = (int *)(base + off);
+  off = dspark_align_up(off + sizeof(int), 256);
   w.gfloor = (float *)(base + off);
   off = dspark_align_up(off + sizeof(float) * (size_t)d->R, 256);
   w.E = (bf16 *)(base + off);
@@ -318,34 +350,36 @@ extern "C" int dspark_verify(const dspark_dims *dims, const int32_t *anchor, con
     return DSPARK_ERR_WORKSPACE;
   const int R = dims->R, G = dims->gamma, V = dims->V, r = dims->r;
   const float inv_tau = sample ? 1.f / tau : 1.f;
-  const dim3 rgrid(G + 1, R);
+  const dim3 rgrid(NSEG * (G + 1), R);
+  const bf16 *tgt = (const bf16 *)target;
   if (!sample) {
-    verify_rows<MODE_GREEDY><<<rgrid, 256, 0, stream>>>((const bf16 *)target, tokens, len,
-                                                        ws.stat, G, V, inv_tau);
+    verify_rows<MODE_GREEDY><<<rgrid, 256, 0, stream>>>(tgt, len, ws.stat, ws.count, G, V, inv_tau);
     DSPARK_CHECK_LAUNCH();
     verify_decide<MODE_GREEDY><<<(R + 127) / 128, 128, 0, stream>>>(
-        ws.stat, anchor, tokens, len, lse_d, logp_d, ws.rows, accepted, bonus, R, G, V, seed);
+        ws.stat, tgt, anchor, tokens, len, lse_d, logp_d, ws.rows, ws.list, ws.count, accepted,
+        bonus, R, G, V, inv_tau, seed);
     DSPARK_CHECK_LAUNCH();
     dspark_count_launches(2);
     return DSPARK_OK;
   }
-  verify_rows<MODE_SAMPLE><<<rgrid, 256, 0, stream>>>((const bf16 *)target, tokens, len, ws.stat,
-                                                      G, V, inv_tau);
+  verify_rows<MODE_SAMPLE><<<rgrid, 256, 0, stream>>>(tgt, len, ws.stat, ws.count, G, V, inv_tau);
   DSPARK_CHECK_LAUNCH();
   verify_decide<MODE_SAMPLE><<<(R + 127) / 128, 128, 0, stream>>>(
-      ws.stat, anchor, tokens, len, lse_d, logp_d, ws.rows, accepted, bonus, R, G, V, seed);
+      ws.stat, tgt, anchor, tokens, len, lse_d, logp_d, ws.rows, ws.list, ws.count, accepted,
+      bonus, R, G, V, inv_tau, seed);
   DSPARK_CHECK_LAUNCH();
-  resample_gather<<<(R * 32 + 255) / 256, 256, 0, stream>>>(ws.rows, (const bf16 *)W1, ws.E,
-                                                          ws.gfloor, R, r);
+  resample_gather<<<(R * 32 + 255) / 256, 256, 0, stream>>>(ws.rows, ws.list, ws.count,
+                                                          (const bf16 *)W1, ws.E, ws.gfloor, r);
   DSPARK_CHECK_LAUNCH();
-  const int n_tiles = (int)logits_parts(V);
-  EpiLogits<MODE_RESIDUAL> epi{(const bf16 *)base_logits, (const bf16 *)target, ws.rows, ws.part,
-                               ws.gfloor, R, V, G, 0, n_tiles, inv_tau, seed};
-  const int rc = gemm::launch<LOGITS_EPI_WARPS>(ws.E, W2t, R, V, r, epi, stream);
+  const int n_parts = (int)logits_parts(V);
+  EpiLogits<MODE_RESIDUAL> epi{(const bf16 *)base_logits, tgt, ws.rows, ws.list, ws.count, ws.part,
+                               ws.gfloor, R, V, G, 0, n_parts, inv_tau, seed};
+  const int rc = gemm::launch<LOGITS_EPI_WARPS>(ws.E, W2t, R, V, r, epi, stream, ws.count);
   if (rc != DSPARK_OK) return rc;
-  resample_reduce<<<(R * 32 + 255) / 256, 256, 0, stream>>>(ws.rows, ws.part, n_tiles, R, bonus);
+  resample_reduce<<<(R * 32 + 255) / 256, 256, 0, stream>>>(ws.rows, ws.list, ws.count, ws.part,
+                                                          n_parts, bonus);
   DSPARK_CHECK_LAUNCH();
-  bonus_row<<<R, 512, 0, stream>>>(ws.rows, (const bf16 *)target, bonus, G, V, inv_tau, seed);
+  bonus_row<<<R, 512, 0, stream>>>(ws.rows, tgt, bonus, G, V, inv_tau, seed);
   DSPARK_CHECK_LAUNCH();
   dspark_count_launches(5);  // + the GEMM, counted by launch()
   return DSPARK_OK;
