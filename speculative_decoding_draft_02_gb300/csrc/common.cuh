@@ -117,8 +117,6 @@ struct __align__(16) RowPartial {
   float sum;     // sum exp(s - m)                               (sampling)
   float best;    // best decision score (logit, or s + Gumbel, or residual score)
   int32_t idx;   // vocabulary id of `best` (lowest on ties)
-  float best_s;  // scaled logit s at idx                        (sampling)
-  float pad0, pad1, pad2;
 };
 
 // Is (a, ia) a better decision than (b, ib)?  Larger score, ties to lower id.

@@ -29,23 +29,44 @@ struct __align__(16) ResampleRow {
   int32_t pad[3];
 };
 
-constexpr int LOGITS_EPI_WARPS = 8;                         // two warps per TMEM lane quarter
-constexpr int PART_N = gemm::BN / (LOGITS_EPI_WARPS / 4);   // vocabulary entries per partial
+// Epilogue geometry of each mode: BN columns per tile, EPI_WARPS epilogue warps
+// (each TMEM lane quarter is shared by EPI_WARPS / 4 warps), SLICE columns per
+// thread and tile (= vocabulary entries per partial), CH columns per TMEM
+// load.  Sampling runs the most warps per column: its per-entry work (Philox
+// words, log-sum-exp) needs the latency hiding.
+template <int MODE>
+struct LogitsCfg {
+  static constexpr int BN = 256;                                     // N-tile
+  static constexpr int EPI_WARPS = MODE == MODE_GREEDY ? 8 : 16;
+  static constexpr int SLICE = BN / (EPI_WARPS / 4);
+  static constexpr int CH = MODE == MODE_GREEDY ? 32 : 16;
+};
+constexpr int MIN_PART_N = 64;  // the narrowest slice of any mode
 
-static inline size_t logits_parts(int V) { return (size_t)(V + PART_N - 1) / PART_N; }
+template <int MODE>
+static inline int logits_parts(int V) {
+  return (V + LogitsCfg<MODE>::SLICE - 1) / LogitsCfg<MODE>::SLICE;
+}
+// Partials per row to size a workspace for every mode.
+static inline size_t logits_parts_max(int V) { return (size_t)(V + MIN_PART_N - 1) / MIN_PART_N; }
 
-// 32 bf16 starting at src[n] as four 16-byte words; groups past V read nothing.
-__device__ __forceinline__ void load_raw32(const bf16 *src, int n, int V, uint4 (&w)[4]) {
+// CH bf16 starting at src[n] as 16-byte words; groups past V read nothing.
+template <int CH>
+__device__ __forceinline__ void load_raw(const bf16 *src, int n, int V, uint4 (&w)[CH / 8]) {
 #pragma unroll
-  for (int q = 0; q < 4; ++q)
+  for (int q = 0; q < CH / 8; ++q)
     w[q] = (n + q * 8 + 8 <= V) ? __ldg(reinterpret_cast<const uint4 *>(src + n + q * 8))
                                 : make_uint4(0, 0, 0, 0);
 }
+__device__ __forceinline__ void load_raw32(const bf16 *src, int n, int V, uint4 (&w)[4]) {
+  load_raw<32>(src, n, V, w);
+}
 // Unpack to floats; entries past V become -inf.
-__device__ __forceinline__ void unpack32(const uint4 (&w)[4], int n, int V, float (&out)[32]) {
-  if (n + 32 <= V) {  // whole chunk inside the vocabulary (warp-uniform)
+template <int CH>
+__device__ __forceinline__ void unpack(const uint4 (&w)[CH / 8], int n, int V, float (&out)[CH]) {
+  if (n + CH <= V) {  // whole chunk inside the vocabulary (warp-uniform)
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < CH / 8; ++q) {
       const uint32_t ws[4] = {w[q].x, w[q].y, w[q].z, w[q].w};
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
@@ -56,7 +77,7 @@ __device__ __forceinline__ void unpack32(const uint4 (&w)[4], int n, int V, floa
     return;
   }
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < CH / 8; ++q) {
     const bool ok = n + q * 8 + 8 <= V;
     const uint32_t ws[4] = {w[q].x, w[q].y, w[q].z, w[q].w};
 #pragma unroll
@@ -65,6 +86,9 @@ __device__ __forceinline__ void unpack32(const uint4 (&w)[4], int n, int V, floa
       out[q * 8 + 2 * t + 1] = ok ? bf16_hi(ws[t]) : -INFINITY;
     }
   }
+}
+__device__ __forceinline__ void unpack32(const uint4 (&w)[4], int n, int V, float (&out)[32]) {
+  unpack<32>(w, n, V, out);
 }
 
 template <int MODE>
@@ -82,14 +106,18 @@ struct EpiLogits {
   uint64_t seed;
 
   static constexpr bool kRowAffine = true;
-  static constexpr int CHUNKS = PART_N / 32;
+  static constexpr bool kStreamB = false;  // W2t is re-read by the other M blocks and steps
+  static constexpr int SLICE = LogitsCfg<MODE>::SLICE;
+  static constexpr int CH = LogitsCfg<MODE>::CH;
+  static constexpr int CHUNKS = SLICE / 32;                       // greedy: 32-column loads
+  static constexpr int BUF = MODE == MODE_GREEDY ? SLICE / 8 : CH / 8;
 
   // Kept by each epilogue thread across the tiles it processes.
   struct State {
     int m0 = -1;               // row block the floor belongs to
     float floor = -INFINITY;   // best score known on this row (own tiles + shared floor)
     float seen = -INFINITY;    // shared floor read at the start of the current tile
-    uint4 buf[4 * CHUNKS];     // base logits prefetched before the accumulator is ready
+    uint4 buf[BUF];            // base logits prefetched before the accumulator is ready
   };
 
   __device__ __forceinline__ bool draft_row(int m0, int row, const bf16 *&brow) const {
@@ -106,17 +134,12 @@ struct EpiLogits {
     const bf16 *brow;
     if (!draft_row(m0, row, brow)) return;
     const int n = n0 + c0;
-    if (MODE == MODE_GREEDY) {  // the whole slice: the epilogue then never waits on HBM
+    // greedy: the whole slice, so the epilogue never waits on HBM; sampling:
+    // the first chunk, later chunks are loaded one ahead
 #pragma unroll
-      for (int q = 0; q < 4 * CHUNKS; ++q)
-        st.buf[q] = (n + q * 8 + 8 <= V) ? __ldg(reinterpret_cast<const uint4 *>(brow + n + q * 8))
-                                         : make_uint4(0, 0, 0, 0);
-    } else {  // the first chunk; later chunks are loaded one ahead
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        st.buf[q] = (n + q * 8 + 8 <= V) ? __ldg(reinterpret_cast<const uint4 *>(brow + n + q * 8))
-                                         : make_uint4(0, 0, 0, 0);
-    }
+    for (int q = 0; q < BUF; ++q)
+      st.buf[q] = (n + q * 8 + 8 <= V) ? __ldg(reinterpret_cast<const uint4 *>(brow + n + q * 8))
+                                       : make_uint4(0, 0, 0, 0);
   }
 
   __device__ void operator()(int m0, int n0, int row, uint32_t taddr, int c0, int c1,
@@ -184,51 +207,57 @@ struct EpiLogits {
     } else {
       const PhiloxKeys keys(seed);
       const float c2 = inv_tau * LOG2E;  // scaled logits in log2 units
-      uint4 nxt[4] = {st.buf[0], st.buf[1], st.buf[2], st.buf[3]};
-      if (MODE == MODE_RESIDUAL && active) load_raw32(brow, n0 + c0, V, nxt);
+      constexpr int NQ = CH / 8;         // 16-byte words per chunk
+      constexpr int NH = CH / 16;        // halves of 16 entries (4 Philox calls each)
+      uint4 nxt[NQ];
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) nxt[q] = st.buf[q];
+      if (MODE == MODE_RESIDUAL && active) load_raw<CH>(brow, n0 + c0, V, nxt);
 #pragma unroll 1
-      for (int c = c0; c < c1; c += 32) {
-        uint32_t acc[32];
-        tc::tmem_ld32(taddr + (uint32_t)c, acc);
+      for (int c = c0; c < c1; c += CH) {
+        uint32_t acc[CH];
+        tc::tmem_ld<CH>(taddr + (uint32_t)c, acc);
         tc::tmem_wait_ld();
         const int n = n0 + c;
         if (active && n < V) {
-          uint4 cur[4];
+          uint4 cur[NQ];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) cur[q] = nxt[q];
-          if (c + 32 < c1) load_raw32(brow, n + 32, V, nxt);  // prefetch the next chunk
-          float sv[32];
-          unpack32(cur, n, V, sv);
+          for (int q = 0; q < NQ; ++q) cur[q] = nxt[q];
+          if (c + CH < c1) load_raw<CH>(brow, n + CH, V, nxt);  // prefetch the next chunk
+          float sv[CH];
+          unpack<CH>(cur, n, V, sv);
           const float F = fmaxf(best, st.floor);  // a score some entry of the row reaches
 
           if (MODE == MODE_SAMPLE) {
-            float x2[32];
+            // y = base + bias (unscaled); the draft distribution is softmax(y / tau)
+            float y[CH];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) x2[j] = (sv[j] + __uint_as_float(acc[j])) * c2;
-            float mx[16];
+            for (int j = 0; j < CH; ++j) y[j] = sv[j] + __uint_as_float(acc[j]);
+            float mx[CH / 2];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) mx[j] = fmaxf(x2[j], x2[j + 16]);
+            for (int j = 0; j < CH / 2; ++j) mx[j] = fmaxf(y[j], y[j + CH / 2]);
 #pragma unroll
-            for (int w = 8; w >= 1; w >>= 1)
+            for (int w = CH / 4; w >= 1; w >>= 1)
 #pragma unroll
               for (int j = 0; j < w; ++j) mx[j] = fmaxf(mx[j], mx[j + w]);
-            const float cmax2 = mx[0];
+            const float cmax2 = mx[0] * c2;  // c2 = log2(e) / tau > 0
             // online log-sum-exp in base 2 (four partial sums)
             if (cmax2 > m2) {
               s *= ex2_fast(m2 - cmax2);
               m2 = cmax2;
             }
+            const float nm2 = -m2;
             float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int j = 0; j < 32; ++j) ps[j & 3] += ex2_fast(x2[j] - m2);
+            for (int j = 0; j < CH; ++j) ps[j & 3] += ex2_fast(fmaf(y[j], c2, nm2));
             s += (ps[0] + ps[1]) + (ps[2] + ps[3]);
 
             // Gumbel-max without the logarithms of entries that cannot win.
-            // Entry j beats F only if g_j > F - s_j.  Since -log u >= 1 - u,
-            // 1 - u_j >= e^{s_j - F + 0.01} implies g_j < F - s_j - 0.01.
-            // Chunk test first (s_j <= cmax, an integer threshold on w >> 9,
-            // u = ((w >> 9) + 1/2) 2^-23), then the same test per entry with
-            // e^{s_j - F} = 2^{x2_j - m2} e^{m - F}.
+            // Entry j beats F only if g_j > F - s_j (s_j = y_j / tau).  Since
+            // -log u >= 1 - u, 1 - u_j >= e^{s_j - F + 0.01} implies
+            // g_j < F - s_j - 0.01.  Chunk test first (s_j <= cmax, an integer
+            // threshold on w >> 9, u = ((w >> 9) + 1/2) 2^-23), then the same
+            // test per entry with e^{s_j - F} = 2^{y_j c2 - m2} e^{m - F}.
             int w_thr = -1;
             if (F > -INFINITY) {
               const float t = fminf(F - cmax2 * LN2, 15.f);
@@ -237,28 +266,34 @@ struct EpiLogits {
             }
             const float K = F > -INFINITY ? __expf(m2 * LN2 - F + 0.01f) : INFINITY;
             const bool per_entry = K < 1e30f;
-            // Philox words in two halves of 16 entries (one call per 4 entries)
+            // Philox words in halves of 16 entries (one call per 4 entries).
+            // The common path needs only their maximum; the per-entry test,
+            // needed only when the chunk test fails, draws them again.
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              uint32_t ws[16];
+            for (int h = 0; h < NH; ++h) {
               uint32_t wmax = 0;
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
                 const uint4 w = keys(make_uint4((uint32_t)((n >> 2) + 4 * h + q), (uint32_t)pos,
                                                 (uint32_t)req, stream));
-                ws[q * 4 + 0] = w.x; ws[q * 4 + 1] = w.y; ws[q * 4 + 2] = w.z; ws[q * 4 + 3] = w.w;
                 wmax = max(max(wmax, max(w.x, w.y)), max(w.z, w.w));
               }
               if ((int)(wmax >> 9) > w_thr) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                  const int j = 16 * h + e;
-                  const bool cand =
-                      !per_entry || (1.f - rng_uniform(ws[e])) < ex2_fast(x2[j] - m2) * K;
-                  if (cand) {
-                    const float sn = x2[j] * LN2;
-                    const float sc = sn + rng_gumbel(ws[e]);
-                    if (sc > best) { best = sc; idx = n + j; bs = sn; }
+                for (int q = 0; q < 4; ++q) {
+                  const uint4 w = keys(make_uint4((uint32_t)((n >> 2) + 4 * h + q),
+                                                  (uint32_t)pos, (uint32_t)req, stream));
+                  const uint32_t wq[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                  for (int l = 0; l < 4; ++l) {
+                    const int j = 16 * h + 4 * q + l;
+                    const bool cand = !per_entry || (1.f - rng_uniform(wq[l])) <
+                                                        ex2_fast(fmaf(y[j], c2, nm2)) * K;
+                    if (cand) {
+                      const float sn = y[j] * inv_tau;
+                      const float sc = sn + rng_gumbel(wq[l]);
+                      if (sc > best) { best = sc; idx = n + j; bs = sn; }
+                    }
                   }
                 }
               }
@@ -268,15 +303,15 @@ struct EpiLogits {
             // log q_j + g_j <= log p_t(j) + g_j, so by the same argument an
             // entry is skipped when 1 - u_j >= p_t(j) e^{-F + 0.01}; the chunk
             // test uses the chunk's largest p_t.
-            uint4 tw[4];
-            load_raw32(trow, n, V, tw);
-            float tv[32];
-            unpack32(tw, n, V, tv);
-            float mx[16];
+            uint4 tw[NQ];
+            load_raw<CH>(trow, n, V, tw);
+            float tv[CH];
+            unpack<CH>(tw, n, V, tv);
+            float mx[CH / 2];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) mx[j] = fmaxf(tv[j], tv[j + 16]);
+            for (int j = 0; j < CH / 2; ++j) mx[j] = fmaxf(tv[j], tv[j + CH / 2]);
 #pragma unroll
-            for (int w = 8; w >= 1; w >>= 1)
+            for (int w = CH / 4; w >= 1; w >>= 1)
 #pragma unroll
               for (int j = 0; j < w; ++j) mx[j] = fmaxf(mx[j], mx[j + w]);
             int w_thr = -1;
@@ -287,7 +322,7 @@ struct EpiLogits {
             const float K = F > -INFINITY ? __expf(0.01f - F) : INFINITY;
             const bool per_entry = K < 1e30f;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int h = 0; h < NH; ++h) {
               uint32_t ws[16];
               uint32_t wmax = 0;
 #pragma unroll
@@ -329,9 +364,7 @@ struct EpiLogits {
       p.sum = s;
       p.best = best;
       p.idx = idx;
-      p.best_s = bs;
-      p.pad0 = p.pad1 = p.pad2 = 0.f;
-      part[(size_t)i * n_parts + (n0 + c0) / PART_N] = p;
+      part[(size_t)i * n_parts + (n0 + c0) / SLICE] = p;
     }
   }
   __device__ void on_timeout() const { dspark_set_status(DSPARK_ERR_TIMEOUT); }

@@ -78,14 +78,17 @@ __global__ void step_prep(const int32_t *__restrict__ anchor, const int32_t *__r
 
 // Combine the vocabulary-slice partials of request i into x_k, lse_k, logp_k,
 // then (k < gamma) prepare step k+1: E[i] = W1[x_k] and the confidence c_{k+1}.
-// One CTA of 128 threads per request.
+// One CTA of 128 threads per request.  log p_d(x_k) = l_k[x_k] / tau - lse_k
+// needs the winner's logit: the base logit plus W1[x_{k-1}] . W2t[x_k] (E still
+// holds W1[x_{k-1}] here).
 template <int MODE>
 __global__ void __launch_bounds__(128) reduce_prep(
     const RowPartial *__restrict__ part, int n_parts, int gamma, int V, int r, int k,
     int32_t *__restrict__ tokens, float *__restrict__ lse_out, float *__restrict__ logp_out,
     const bf16 *__restrict__ W1, const bf16 *__restrict__ w_e, const float *__restrict__ zh,
     const float *__restrict__ T, bf16 *__restrict__ E, float *__restrict__ conf,
-    float *__restrict__ gfloor) {
+    float *__restrict__ gfloor, const bf16 *__restrict__ base, const bf16 *__restrict__ W2t,
+    float inv_tau) {
   const int i = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   float m = -INFINITY, s = 0.f, best = -INFINITY, bs = 0.f;
   int idx = 0x7fffffff;
@@ -96,40 +99,64 @@ __global__ void __launch_bounds__(128) reduce_prep(
     for (int u = 0; u < 4; ++u) {
       const int t = t0 + u * 128 + tid;
       if (t < n_parts) p[u] = pr[t];
-      else { p[u].m = -INFINITY; p[u].sum = 0.f; p[u].best = -INFINITY; p[u].idx = 0x7fffffff; p[u].best_s = 0.f; }
+      else { p[u].m = -INFINITY; p[u].sum = 0.f; p[u].best = -INFINITY; p[u].idx = 0x7fffffff; }
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       lse_merge(m, s, p[u].m, p[u].sum);
-      if (better(p[u].best, p[u].idx, best, idx)) { best = p[u].best; idx = p[u].idx; bs = p[u].best_s; }
+      if (better(p[u].best, p[u].idx, best, idx)) { best = p[u].best; idx = p[u].idx; }
     }
   }
   warp_merge(m, s, best, idx, bs);
-  __shared__ float sm[4], ss[4], sb[4], sbs[4], sdot[4];
+  __shared__ float sm[4], ss[4], sb[4], sdot[4], s_lse;
   __shared__ int si[4], s_tok;
-  if (lane == 0) { sm[warp] = m; ss[warp] = s; sb[warp] = best; si[warp] = idx; sbs[warp] = bs; }
+  if (lane == 0) { sm[warp] = m; ss[warp] = s; sb[warp] = best; si[warp] = idx; }
   __syncthreads();
   if (warp == 0) {
     m = lane < 4 ? sm[lane] : -INFINITY;
     s = lane < 4 ? ss[lane] : 0.f;
     best = lane < 4 ? sb[lane] : -INFINITY;
     idx = lane < 4 ? si[lane] : 0x7fffffff;
-    bs = lane < 4 ? sbs[lane] : 0.f;
     warp_merge(m, s, best, idx, bs);
     if (lane == 0) {
       const size_t o = (size_t)i * gamma + k - 1;
       tokens[o] = idx;
-      float lse = 0.f, logp = 0.f;
-      if (MODE == MODE_SAMPLE) {
-        lse = m + logf(s);
-        logp = bs - lse;
-      }
-      if (lse_out) lse_out[o] = lse;
-      if (logp_out) logp_out[o] = logp;
+      s_lse = MODE == MODE_SAMPLE ? m + logf(s) : 0.f;
+      if (lse_out) lse_out[o] = s_lse;
       s_tok = idx;
     }
   }
   __syncthreads();
+  const int tok = s_tok;
+  if (MODE == MODE_SAMPLE) {
+    // winner's logit: base + W1[x_{k-1}] . W2t[x_k]
+    float d = 0.f;
+    if (tok >= 0 && tok < V) {
+      const uint4 *er = reinterpret_cast<const uint4 *>(E + (size_t)i * r);
+      const uint4 *wr2 = reinterpret_cast<const uint4 *>(W2t + (size_t)tok * r);
+      for (int c = tid; c < r / 8; c += 128) {
+        const uint4 a = er[c], b = wr2[c];
+        const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          d = fmaf(bf16_lo(av[t]), bf16_lo(bv[t]), d);
+          d = fmaf(bf16_hi(av[t]), bf16_hi(bv[t]), d);
+        }
+      }
+    }
+    d = warp_sum(d);
+    if (lane == 0) sdot[warp] = d;
+    __syncthreads();
+    if (tid == 0) {
+      const size_t o = (size_t)i * gamma + k - 1;
+      const float bl = (tok >= 0 && tok < V) ? __bfloat162float(base[o * V + tok]) : 0.f;
+      const float logit = bl + (sdot[0] + sdot[1]) + (sdot[2] + sdot[3]);
+      if (logp_out) logp_out[o] = logit * inv_tau - s_lse;
+    }
+    __syncthreads();  // E is rewritten below
+  } else if (tid == 0 && logp_out) {
+    logp_out[(size_t)i * gamma + k - 1] = 0.f;
+  }
   if (k >= gamma) return;
   if (tid == 0) gfloor[i] = -INFINITY;  // fresh shared floor for step k + 1
   int prev = s_tok;
@@ -179,7 +206,7 @@ MarkovWs markov_layout(const dspark_dims *d, char *base) {
   w.E = (bf16 *)(base + off);
   off = dspark_align_up(off + sizeof(bf16) * (size_t)d->R * d->r, 256);
   w.part = (RowPartial *)(base + off);
-  off = dspark_align_up(off + sizeof(RowPartial) * (size_t)d->R * logits_parts(d->V), 256);
+  off = dspark_align_up(off + sizeof(RowPartial) * (size_t)d->R * logits_parts_max(d->V), 256);
   w.bytes = off;
   return w;
 }
@@ -210,7 +237,6 @@ extern "C" int dspark_markov_draft(const dspark_dims *dims, const void *base_log
   conf_hidden<<<(rows * 32 + 255) / 256, 256, 0, stream>>>((const bf16 *)h, (const bf16 *)w_conf,
                                                           ws.zh, rows, d);
   DSPARK_CHECK_LAUNCH();
-  const int n_tiles = (int)logits_parts(V);
   const float inv_tau = tau > 0.f ? 1.f / tau : 1.f;
   step_prep<<<(R * 32 + 255) / 256, 256, 0, stream>>>(anchor, tokens, (const bf16 *)W1,
                                                      (const bf16 *)w_conf + d, ws.zh, T, ws.E,
@@ -220,23 +246,29 @@ extern "C" int dspark_markov_draft(const dspark_dims *dims, const void *base_log
   for (int k = 1; k <= G; ++k) {
     int rc;
     if (tau > 0.f) {
+      const int n_tiles = logits_parts<MODE_SAMPLE>(V);
       EpiLogits<MODE_SAMPLE> epi{(const bf16 *)base_logits, nullptr, nullptr, nullptr, nullptr,
                                  ws.part, ws.gfloor,
                                  R, V, G, k, n_tiles, inv_tau, seed};
-      rc = gemm::launch<LOGITS_EPI_WARPS>(ws.E, W2t, R, V, r, epi, stream);
+      rc = gemm::launch<LogitsCfg<MODE_SAMPLE>::EPI_WARPS, LogitsCfg<MODE_SAMPLE>::BN>(ws.E, W2t, R, V, r, epi, stream);
       if (rc != DSPARK_OK) return rc;
       reduce_prep<MODE_SAMPLE><<<R, 128, 0, stream>>>(ws.part, n_tiles, G, V, r, k, tokens, lse_d,
                                                       logp_d, (const bf16 *)W1, w_e, ws.zh, T,
-                                                      ws.E, conf, ws.gfloor);
+                                                      ws.E, conf, ws.gfloor,
+                                                      (const bf16 *)base_logits,
+                                                      (const bf16 *)W2t, inv_tau);
     } else {
+      const int n_tiles = logits_parts<MODE_GREEDY>(V);
       EpiLogits<MODE_GREEDY> epi{(const bf16 *)base_logits, nullptr, nullptr, nullptr, nullptr,
                                  ws.part, ws.gfloor,
                                  R, V, G, k, n_tiles, 1.f, seed};
-      rc = gemm::launch<LOGITS_EPI_WARPS>(ws.E, W2t, R, V, r, epi, stream);
+      rc = gemm::launch<LogitsCfg<MODE_GREEDY>::EPI_WARPS, LogitsCfg<MODE_GREEDY>::BN>(ws.E, W2t, R, V, r, epi, stream);
       if (rc != DSPARK_OK) return rc;
       reduce_prep<MODE_GREEDY><<<R, 128, 0, stream>>>(ws.part, n_tiles, G, V, r, k, tokens, lse_d,
                                                       logp_d, (const bf16 *)W1, w_e, ws.zh, T,
-                                                      ws.E, conf, ws.gfloor);
+                                                      ws.E, conf, ws.gfloor,
+                                                      (const bf16 *)base_logits,
+                                                      (const bf16 *)W2t, inv_tau);
     }
     DSPARK_CHECK_LAUNCH();
   }

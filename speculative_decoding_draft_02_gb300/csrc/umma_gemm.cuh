@@ -9,10 +9,10 @@
 //               K=16 per instruction, 4 per 64-wide stage), committing each
 //               stage back to the producer and each finished tile to the
 //               epilogue;
-//   warps 2..   the epilogue (EPI_WARPS = 4 or 8): a thread owns one accumulator
-//               row (its TMEM lane) and a contiguous slice of its columns
-//               (all 256, or one half with 8 warps), so a row-wise reduction
-//               over the slice needs no shuffles.
+//   warps 2..   the epilogue (EPI_WARPS = 4, 8 or 16): a thread owns one
+//               accumulator row (its TMEM lane) and a contiguous slice of its
+//               columns (256, 128 or 64), so a row-wise reduction over the
+//               slice needs no shuffles.
 // Tiles are visited m-fastest, so the CTAs working at the same time share one
 // B tile (one read from HBM, the rest from L2).  Every wait is bounded; on
 // timeout the CTA raises DSPARK_ERR_TIMEOUT, drains its own copies and MMAs,
@@ -22,14 +22,28 @@
 
 namespace gemm {
 
-constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int STAGES = 4;
+constexpr int BM = 128, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr uint32_t TMEM_COLS = 2 * BN;
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
+constexpr size_t SMEM_LIMIT = 232448;  // opt-in dynamic shared memory per CTA
 
+// Tile geometry for an N-tile of BN columns (BN = 256 or 192): the ring holds
+// as many 64-deep stages of A and B as fit, the double-buffered accumulator
+// takes 2*BN TMEM columns (allocated as the next power of two).
+template <int BN_>
+struct Geo {
+  static constexpr int BN = BN_;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (int)((SMEM_LIMIT - 1024 - 512) / STAGE_BYTES) > 6
+                                    ? 6
+                                    : (int)((SMEM_LIMIT - 1024 - 512) / STAGE_BYTES);
+  static constexpr uint32_t TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
+  static constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 512;
+  static_assert(BN % 16 == 0 && BN >= 64 && BN <= 256, "UMMA N for M = 128");
+};
+constexpr int BN = 256;  // the default N-tile (LM head, greedy and residual passes)
+
+template <int STAGES>
 struct SharedCtl {
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
@@ -43,6 +57,7 @@ struct SharedCtl {
 // Epi must provide
 //   struct State;                         per-thread state kept across tiles
 //   static constexpr bool kRowAffine;     keep each thread on one row when possible
+//   static constexpr bool kStreamB;       B is read once: evict its tiles from L2 first
 //   __device__ void prefetch(int m0, int n0, int row, int c0, int c1, State &) const
 //       (called before the tile's accumulator is ready: start global loads)
 //   __device__ void operator()(int m0, int n0, int row, uint32_t taddr, int c0, int c1,
@@ -50,17 +65,21 @@ struct SharedCtl {
 //       (every epilogue thread, once per tile, for its row and column slice
 //        [c0, c1); tcgen05.ld of each 32-column chunk must be warp-uniform)
 //   __device__ void on_timeout() const.
-template <class Epi, int EPI_WARPS>
+template <class Epi, int EPI_WARPS, int BN_>
 __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
                      const __grid_constant__ CUtensorMap tma_b, int M, int N, int K,
                      const int *m_dev, Epi epi) {
+  using G = Geo<BN_>;
+  constexpr int BN = G::BN, STAGES = G::STAGES, B_BYTES = G::B_BYTES;
+  constexpr int STAGE_BYTES = G::STAGE_BYTES;
+  constexpr uint32_t TMEM_COLS = G::TMEM_COLS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *sA = base;
   uint8_t *sB = base + STAGES * A_BYTES;
-  SharedCtl *ctl = reinterpret_cast<SharedCtl *>(base + STAGES * STAGE_BYTES);
+  SharedCtl<STAGES> *ctl = reinterpret_cast<SharedCtl<STAGES> *>(base + STAGES * STAGE_BYTES);
   volatile int *abort = &ctl->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -97,7 +116,8 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
     if (lane == 0) {
       // ------------------------------------------------ TMA producer ----
       const uint64_t pol_a = tc::policy_evict_last();   // A tiles are re-read
-      const uint64_t pol_b = tc::policy_evict_first();  // B streams through
+      // B: streamed once (LM head) or re-read by other M blocks and later steps
+      const uint64_t pol_b = Epi::kStreamB ? tc::policy_evict_first() : tc::policy_evict_normal();
       int stage = 0;
       uint32_t phase = 0;
       int issued[STAGES];
@@ -197,18 +217,22 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
 // M rows of A are described to TMA; when m_dev is given the kernel processes
 // only the first *m_dev of them (read on the device, so the count can come from
 // an earlier kernel in the stream).
-template <int EPI_WARPS, class Epi>
+template <int EPI_WARPS, int BN_ = 256, class Epi>
 int launch(const void *A, const void *B, int M, int N, int K, const Epi &epi,
            cudaStream_t stream, const int *m_dev = nullptr) {
-  static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "4 or 8 epilogue warps");
+  using G = Geo<BN_>;
+  constexpr int BN = G::BN;
+  static_assert(EPI_WARPS % 4 == 0 && EPI_WARPS >= 4 && EPI_WARPS <= 16 &&
+                    BN % (EPI_WARPS / 4) == 0 && (BN / (EPI_WARPS / 4)) % 32 == 0,
+                "epilogue warps: 4 per TMEM lane quarter group, slices of whole 32-column loads");
   CUtensorMap ta, tb;
   if (dspark_make_tmap_bf16(&ta, A, (uint64_t)M, (uint64_t)K, BM) != 0) return DSPARK_ERR_CUDA;
   if (dspark_make_tmap_bf16(&tb, B, (uint64_t)N, (uint64_t)K, BN) != 0) return DSPARK_ERR_CUDA;
   static bool attr = false;
   if (!attr) {
-    if (cudaFuncSetAttribute(umma_gemm_kernel<Epi, EPI_WARPS>,
+    if (cudaFuncSetAttribute(umma_gemm_kernel<Epi, EPI_WARPS, BN_>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)SMEM_BYTES) != cudaSuccess)
+                             (int)G::SMEM_BYTES) != cudaSuccess)
       return DSPARK_ERR_CUDA;
     attr = true;
   }
@@ -217,7 +241,7 @@ int launch(const void *A, const void *B, int M, int N, int K, const Epi &epi,
   int grid = tiles < dspark_sm_count() ? tiles : dspark_sm_count();
   // a multiple of the M-block count keeps every CTA (and epilogue thread) on one row block
   if (Epi::kRowAffine && grid > num_m) grid = grid / num_m * num_m;
-  umma_gemm_kernel<Epi, EPI_WARPS><<<grid, 64 + 32 * EPI_WARPS, SMEM_BYTES, stream>>>(
+  umma_gemm_kernel<Epi, EPI_WARPS, BN_><<<grid, 64 + 32 * EPI_WARPS, G::SMEM_BYTES, stream>>>(
       ta, tb, M, N, K, m_dev, epi);
   if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
   dspark_count_launches(1);

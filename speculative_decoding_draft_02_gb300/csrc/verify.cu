@@ -269,13 +269,28 @@ __global__ void __launch_bounds__(512) bonus_row(const ResampleRow *__restrict__
     }
     const float F = warp_max(best);
     if (valid) {
+      // group test first: with tmax the largest of the 8 scaled logits, every
+      // entry needs g > F - tmax; as an integer bound on the words (see the
+      // draft epilogue), then per entry
+      float tmax = fmaxf(fmaxf(fmaxf(tv[0], tv[1]), fmaxf(tv[2], tv[3])),
+                         fmaxf(fmaxf(tv[4], tv[5]), fmaxf(tv[6], tv[7])));
+      int w_thr = -1;
+      if (F > -INFINITY) {
+        const float X = __expf(fminf(tmax - F + 0.01f, 0.f)) * 8388608.f;
+        w_thr = X >= 8388607.f ? -1 : 8388607 - (int)ceilf(X);
+      }
+      uint32_t wmax = 0;
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const bool cand = !(F > -INFINITY) ||
-                          (1.f - rng_uniform(ws[t])) < __expf(tv[t] - F + 0.01f);
-        if (cand) {
-          const float sc = tv[t] + rng_gumbel(ws[t]);
-          if (better(sc, v0 + t, best, idx)) { best = sc; idx = v0 + t; }
+      for (int t = 0; t < 8; ++t) wmax = max(wmax, ws[t]);
+      if ((int)(wmax >> 9) > w_thr) {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const bool cand = !(F > -INFINITY) ||
+                            (1.f - rng_uniform(ws[t])) < __expf(tv[t] - F + 0.01f);
+          if (cand) {
+            const float sc = tv[t] + rng_gumbel(ws[t]);
+            if (better(sc, v0 + t, best, idx)) { best = sc; idx = v0 + t; }
+          }
         }
       }
     }
@@ -320,7 +335,7 @@ VerifyWs verify_layout(const dspark_dims *d, char *base) {
   w.E = (bf16 *)(base + off);
   off = dspark_align_up(off + sizeof(bf16) * (size_t)d->R * d->r, 256);
   w.part = (RowPartial *)(base + off);
-  off = dspark_align_up(off + sizeof(RowPartial) * (size_t)d->R * logits_parts(d->V), 256);
+  off = dspark_align_up(off + sizeof(RowPartial) * (size_t)d->R * logits_parts_max(d->V), 256);
   w.bytes = off;
   return w;
 }
@@ -371,10 +386,11 @@ extern "C" int dspark_verify(const dspark_dims *dims, const int32_t *anchor, con
   resample_gather<<<(R * 32 + 255) / 256, 256, 0, stream>>>(ws.rows, ws.list, ws.count,
                                                           (const bf16 *)W1, ws.E, ws.gfloor, r);
   DSPARK_CHECK_LAUNCH();
-  const int n_parts = (int)logits_parts(V);
+  const int n_parts = logits_parts<MODE_RESIDUAL>(V);
   EpiLogits<MODE_RESIDUAL> epi{(const bf16 *)base_logits, tgt, ws.rows, ws.list, ws.count, ws.part,
                                ws.gfloor, R, V, G, 0, n_parts, inv_tau, seed};
-  const int rc = gemm::launch<LOGITS_EPI_WARPS>(ws.E, W2t, R, V, r, epi, stream, ws.count);
+  const int rc = gemm::launch<LogitsCfg<MODE_RESIDUAL>::EPI_WARPS, LogitsCfg<MODE_RESIDUAL>::BN>(ws.E, W2t, R, V, r, epi, stream,
+                                                                  ws.count);
   if (rc != DSPARK_OK) return rc;
   resample_reduce<<<(R * 32 + 255) / 256, 256, 0, stream>>>(ws.rows, ws.list, ws.count, ws.part,
                                                           n_parts, bonus);
