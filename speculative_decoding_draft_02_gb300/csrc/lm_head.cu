@@ -116,7 +116,13 @@ int dspark_lm_head_tc(const dspark_dims *dims, const void *h, const void *W_lm,
   epi.C = (bf16 *)base_logits;
   epi.M = dims->R * dims->gamma;
   epi.N = dims->V;
-  return gemm::launch<4>(h, W_lm, epi.M, epi.N, dims->d, epi, stream);
+  // Many M blocks (large R * gamma): CTA pairs share each W_lm tile by multicast,
+  // halving the operand bytes each SM pulls from L2.  With few M blocks the
+  // single-CTA kernel reuses W_lm tiles through L2 well enough and wins.
+  const int num_m = (epi.M + gemm::BM - 1) / gemm::BM;
+  if (num_m >= 16)
+    return gemm::launch<4, 256, true>(h, W_lm, epi.M, epi.N, dims->d, epi, stream);
+  return gemm::launch<4, 256, false>(h, W_lm, epi.M, epi.N, dims->d, epi, stream);
 }
 
 extern "C" int dspark_pack_w2(const dspark_dims *dims, const void *W2, void *W2t,

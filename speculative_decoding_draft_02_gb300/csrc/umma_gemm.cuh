@@ -65,7 +65,11 @@ struct SharedCtl {
 //       (every epilogue thread, once per tile, for its row and column slice
 //        [c0, c1); tcgen05.ld of each 32-column chunk must be warp-uniform)
 //   __device__ void on_timeout() const.
-template <class Epi, int EPI_WARPS, int BN_>
+// PAIR: CTAs run as clusters of two over two M blocks of the same N tile; each
+// loads its own A tile and half of the B tile, multicast to both, so the B
+// bytes brought from L2 per SM are halved.  A stage is reused only after both
+// CTAs' MMAs released it (their commits are multicast to both empty barriers).
+template <class Epi, int EPI_WARPS, int BN_, bool PAIR>
 __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
                      const __grid_constant__ CUtensorMap tma_b, int M, int N, int K,
@@ -88,13 +92,23 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
     M = md < M ? (md > 0 ? md : 0) : M;
   }
   const int num_m = (M + BM - 1) / BM, num_n = (N + BN - 1) / BN;
-  const int num_tiles = num_m * num_n;
   const int k_iters = K / BK;
+  // tile sequence: t -> (m block, n block), m fastest; a pair walks pairs of M blocks
+  const uint32_t rank = PAIR ? tc::cluster_ctarank() : 0u;
+  const int num_mp = PAIR ? (num_m + 1) / 2 : num_m;
+  const int num_tiles = num_mp * num_n;
+  const int first = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int stride = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  auto coords = [&](int t, int &m_blk, int &n_blk) {
+    const int mp = t % num_mp;
+    n_blk = t / num_mp;
+    m_blk = PAIR ? 2 * mp + (int)rank : mp;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       tc::mbar_init(&ctl->full[s], 1);
-      tc::mbar_init(&ctl->empty[s], 1);
+      tc::mbar_init(&ctl->empty[s], PAIR ? 2 : 1);
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&ctl->tfull[b], 1);
@@ -109,6 +123,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
   if (warp == 1) tc::tmem_alloc(&ctl->tmem_base, TMEM_COLS);
   tc::fence_before_sync();
   __syncthreads();
+  if (PAIR) tc::cluster_sync();  // the peer's barriers exist before any multicast
   tc::fence_after_sync();
   const uint32_t tmem_base = ctl->tmem_base;
 
@@ -117,21 +132,30 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
       // ------------------------------------------------ TMA producer ----
       const uint64_t pol_a = tc::policy_evict_last();   // A tiles are re-read
       // B: streamed once (LM head) or re-read by other M blocks and later steps
-      const uint64_t pol_b = Epi::kStreamB ? tc::policy_evict_first() : tc::policy_evict_normal();
+      // (a pair fetches each B line once per cluster; with several clusters on one
+      // N tile the lines must survive until the last of them reads them)
+      const uint64_t pol_b =
+          (Epi::kStreamB && !PAIR) ? tc::policy_evict_first() : tc::policy_evict_normal();
       int stage = 0;
       uint32_t phase = 0;
       int issued[STAGES];
       for (int s = 0; s < STAGES; ++s) issued[s] = -1;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        const int m_blk = tile % num_m, n_blk = tile / num_m;
+      for (int tile = first; ok && tile < num_tiles; tile += stride) {
+        int m_blk, n_blk;
+        coords(tile, m_blk, n_blk);
         for (int kb = 0; kb < k_iters; ++kb) {
           if (!tc::mbar_wait(&ctl->empty[stage], phase ^ 1, abort)) { ok = false; break; }
-          tc::mbar_expect_tx(&ctl->full[stage], STAGE_BYTES);
+          tc::mbar_expect_tx(&ctl->full[stage], STAGE_BYTES);  // A + both halves of B
           tc::tma_load_2d(sA + stage * A_BYTES, &tma_a, kb * BK, m_blk * BM, &ctl->full[stage],
                           pol_a);
-          tc::tma_load_2d(sB + stage * B_BYTES, &tma_b, kb * BK, n_blk * BN, &ctl->full[stage],
-                          pol_b);
+          if (PAIR)
+            tc::tma_load_2d_mcast(sB + stage * B_BYTES + rank * (B_BYTES / 2), &tma_b, kb * BK,
+                                  n_blk * BN + (int)rank * (BN / 2), &ctl->full[stage],
+                                  (uint16_t)0x3, pol_b);
+          else
+            tc::tma_load_2d(sB + stage * B_BYTES, &tma_b, kb * BK, n_blk * BN, &ctl->full[stage],
+                            pol_b);
           issued[stage] = (int)phase;
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
@@ -151,7 +175,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+      for (int tile = first; ok && tile < num_tiles; tile += stride) {
         if (!tc::mbar_wait(&ctl->tempty[acc], acc_phase ^ 1, abort)) break;
         tc::fence_after_sync();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
@@ -164,7 +188,10 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
           for (int k = 0; k < BK / 16; ++k)  // +32 B per 16-element K step
             tc::umma_bf16(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc,
                           (kb | k) != 0 ? 1u : 0u);
-          tc::umma_commit(&ctl->empty[stage]);
+          if (PAIR)
+            tc::umma_commit_mcast(&ctl->empty[stage], (uint16_t)0x3);  // both CTAs' slots
+          else
+            tc::umma_commit(&ctl->empty[stage]);
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
@@ -187,8 +214,9 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     typename Epi::State st;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      const int m_blk = tile % num_m, n_blk = tile / num_m;
+    for (int tile = first; tile < num_tiles; tile += stride) {
+      int m_blk, n_blk;
+      coords(tile, m_blk, n_blk);
       epi.prefetch(m_blk * BM, n_blk * BN, row, c0, c0 + SLICE, st);
       // one lane polls, then the warp proceeds together (tcgen05.ld is warp-wide)
       int ok = 1;
@@ -207,6 +235,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
 
   tc::fence_before_sync();
   __syncthreads();
+  if (PAIR) tc::cluster_sync();  // no peer multicast or commit still targets this CTA
   if (ctl->abort && threadIdx.x == 0) epi.on_timeout();
   if (warp == 1) {
     tc::fence_after_sync();
@@ -216,8 +245,9 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
 
 // M rows of A are described to TMA; when m_dev is given the kernel processes
 // only the first *m_dev of them (read on the device, so the count can come from
-// an earlier kernel in the stream).
-template <int EPI_WARPS, int BN_ = 256, class Epi>
+// an earlier kernel in the stream).  PAIR launches clusters of two CTAs that
+// share B tiles by multicast (see umma_gemm_kernel).
+template <int EPI_WARPS, int BN_ = 256, bool PAIR = false, class Epi>
 int launch(const void *A, const void *B, int M, int N, int K, const Epi &epi,
            cudaStream_t stream, const int *m_dev = nullptr) {
   using G = Geo<BN_>;
@@ -225,24 +255,53 @@ int launch(const void *A, const void *B, int M, int N, int K, const Epi &epi,
   static_assert(EPI_WARPS % 4 == 0 && EPI_WARPS >= 4 && EPI_WARPS <= 16 &&
                     BN % (EPI_WARPS / 4) == 0 && (BN / (EPI_WARPS / 4)) % 32 == 0,
                 "epilogue warps: 4 per TMEM lane quarter group, slices of whole 32-column loads");
+  auto kernel = umma_gemm_kernel<Epi, EPI_WARPS, BN_, PAIR>;
   CUtensorMap ta, tb;
   if (dspark_make_tmap_bf16(&ta, A, (uint64_t)M, (uint64_t)K, BM) != 0) return DSPARK_ERR_CUDA;
-  if (dspark_make_tmap_bf16(&tb, B, (uint64_t)N, (uint64_t)K, BN) != 0) return DSPARK_ERR_CUDA;
+  if (dspark_make_tmap_bf16(&tb, B, (uint64_t)N, (uint64_t)K, PAIR ? BN / 2 : BN) != 0)
+    return DSPARK_ERR_CUDA;
   static bool attr = false;
+  static int max_clusters = 0;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute cluster_attr;
+  cluster_attr.id = cudaLaunchAttributeClusterDimension;
+  cluster_attr.val.clusterDim.x = 2;
+  cluster_attr.val.clusterDim.y = 1;
+  cluster_attr.val.clusterDim.z = 1;
+  cfg.blockDim = dim3(64 + 32 * EPI_WARPS);
+  cfg.dynamicSmemBytes = G::SMEM_BYTES;
+  cfg.stream = stream;
+  if (PAIR) {
+    cfg.attrs = &cluster_attr;
+    cfg.numAttrs = 1;
+  }
   if (!attr) {
-    if (cudaFuncSetAttribute(umma_gemm_kernel<Epi, EPI_WARPS, BN_>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)G::SMEM_BYTES) != cudaSuccess)
       return DSPARK_ERR_CUDA;
+    if (PAIR) {
+      cfg.gridDim = dim3(2 * (dspark_sm_count() / 2));
+      if (cudaOccupancyMaxActiveClusters(&max_clusters, kernel, &cfg) != cudaSuccess ||
+          max_clusters < 1)
+        return DSPARK_ERR_CUDA;
+    }
     attr = true;
   }
   const int num_m = (M + BM - 1) / BM;
-  const int tiles = num_m * ((N + BN - 1) / BN);
-  int grid = tiles < dspark_sm_count() ? tiles : dspark_sm_count();
-  // a multiple of the M-block count keeps every CTA (and epilogue thread) on one row block
-  if (Epi::kRowAffine && grid > num_m) grid = grid / num_m * num_m;
-  umma_gemm_kernel<Epi, EPI_WARPS, BN_><<<grid, 64 + 32 * EPI_WARPS, G::SMEM_BYTES, stream>>>(
-      ta, tb, M, N, K, m_dev, epi);
+  const int num_n = (N + BN - 1) / BN;
+  int grid;
+  if (PAIR) {
+    const int pairs = ((num_m + 1) / 2) * num_n;
+    grid = 2 * (pairs < max_clusters ? pairs : max_clusters);
+  } else {
+    const int tiles = num_m * num_n;
+    grid = tiles < dspark_sm_count() ? tiles : dspark_sm_count();
+    // a multiple of the M-block count keeps every CTA (and epilogue thread) on one row block
+    if (Epi::kRowAffine && grid > num_m) grid = grid / num_m * num_m;
+  }
+  cfg.gridDim = dim3(grid);
+  if (cudaLaunchKernelEx(&cfg, kernel, ta, tb, M, N, K, m_dev, epi) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
   dspark_count_launches(1);
   return DSPARK_OK;
