@@ -19,25 +19,38 @@ DSPARK_DECLARE_STATUS(s_status_markov)
 
 namespace {
 
-// zh[m] = w_h . h[m] for every (request, position) row m; one warp per row.
-__global__ void conf_hidden(const bf16 *__restrict__ h, const bf16 *__restrict__ w_conf,
-                            float *__restrict__ zh, int rows, int d) {
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  if (warp >= rows) return;
-  const uint4 *hr = reinterpret_cast<const uint4 *>(h + (size_t)warp * d);
-  const uint4 *wr = reinterpret_cast<const uint4 *>(w_conf);
-  float acc = 0.f;
-  for (int c = lane; c < d / 8; c += 32) {
-    const uint4 a = hr[c], b = wr[c];
-    const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+__device__ __forceinline__ float dot8_bf16(const uint4 a, const uint4 b, float acc) {
+  const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      acc = fmaf(bf16_lo(av[t]), bf16_lo(bv[t]), acc);
-      acc = fmaf(bf16_hi(av[t]), bf16_hi(bv[t]), acc);
-    }
+  for (int t = 0; t < 4; ++t) {
+    acc = fmaf(bf16_lo(av[t]), bf16_lo(bv[t]), acc);
+    acc = fmaf(bf16_hi(av[t]), bf16_hi(bv[t]), acc);
   }
-  acc = warp_sum(acc);
-  if (lane == 0) zh[warp] = acc;
+  return acc;
+}
+
+// zh[m] = w_h . h[m] for every (request, position) row m; one CTA of 128
+// threads per row, each thread a strided quarter of the row's 16-byte words.
+__global__ void __launch_bounds__(128) conf_hidden(const bf16 *__restrict__ h,
+                                                   const bf16 *__restrict__ w_conf,
+                                                   float *__restrict__ zh, int d) {
+  const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint4 *hr = reinterpret_cast<const uint4 *>(h + (size_t)row * d);
+  const uint4 *wr = reinterpret_cast<const uint4 *>(w_conf);
+  const int n8 = d / 8;
+  float acc[2] = {0.f, 0.f};
+  int c = tid;
+  for (; c + 128 < n8; c += 256) {
+    const uint4 a0 = __ldg(hr + c), a1 = __ldg(hr + c + 128);
+    acc[0] = dot8_bf16(a0, __ldg(wr + c), acc[0]);
+    acc[1] = dot8_bf16(a1, __ldg(wr + c + 128), acc[1]);
+  }
+  for (; c < n8; c += 128) acc[0] = dot8_bf16(__ldg(hr + c), __ldg(wr + c), acc[0]);
+  const float t = warp_sum(acc[0] + acc[1]);
+  __shared__ float part[4];
+  if (lane == 0) part[warp] = t;
+  __syncthreads();
+  if (tid == 0) zh[row] = (part[0] + part[1]) + (part[2] + part[3]);
 }
 
 // Step k: E[i] = W1[x_{k-1}], c_k = sigmoid((zh + w_e . E[i]) / T_k); one warp per request.
@@ -78,11 +91,13 @@ __global__ void step_prep(const int32_t *__restrict__ anchor, const int32_t *__r
 
 // Combine the vocabulary-slice partials of request i into x_k, lse_k, logp_k,
 // then (k < gamma) prepare step k+1: E[i] = W1[x_k] and the confidence c_{k+1}.
-// One CTA of 128 threads per request.  log p_d(x_k) = l_k[x_k] / tau - lse_k
+// One CTA of RP_THREADS threads per request.  log p_d(x_k) = l_k[x_k] / tau - lse_k
 // needs the winner's logit: the base logit plus W1[x_{k-1}] . W2t[x_k] (E still
 // holds W1[x_{k-1}] here).
+constexpr int RP_THREADS = 256;
+
 template <int MODE>
-__global__ void __launch_bounds__(128) reduce_prep(
+__global__ void __launch_bounds__(RP_THREADS) reduce_prep(
     const RowPartial *__restrict__ part, int n_parts, int gamma, int V, int r, int k,
     int32_t *__restrict__ tokens, float *__restrict__ lse_out, float *__restrict__ logp_out,
     const bf16 *__restrict__ W1, const bf16 *__restrict__ w_e, const float *__restrict__ zh,
@@ -93,30 +108,31 @@ __global__ void __launch_bounds__(128) reduce_prep(
   float m = -INFINITY, s = 0.f, best = -INFINITY, bs = 0.f;
   int idx = 0x7fffffff;
   const RowPartial *pr = part + (size_t)i * n_parts;
-  for (int t0 = 0; t0 < n_parts; t0 += 4 * 128) {  // four independent loads in flight
-    RowPartial p[4];
+  for (int t0 = 0; t0 < n_parts; t0 += 8 * RP_THREADS) {  // eight loads in flight
+    RowPartial p[8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int t = t0 + u * 128 + tid;
+    for (int u = 0; u < 8; ++u) {
+      const int t = t0 + u * RP_THREADS + tid;
       if (t < n_parts) p[u] = pr[t];
       else { p[u].m = -INFINITY; p[u].sum = 0.f; p[u].best = -INFINITY; p[u].idx = 0x7fffffff; }
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < 8; ++u) {
       lse_merge(m, s, p[u].m, p[u].sum);
       if (better(p[u].best, p[u].idx, best, idx)) { best = p[u].best; idx = p[u].idx; }
     }
   }
   warp_merge(m, s, best, idx, bs);
-  __shared__ float sm[4], ss[4], sb[4], sdot[4], s_lse;
-  __shared__ int si[4], s_tok;
+  constexpr int NW = RP_THREADS / 32;
+  __shared__ float sm[NW], ss[NW], sb[NW], sdot[NW], s_lse;
+  __shared__ int si[NW], s_tok;
   if (lane == 0) { sm[warp] = m; ss[warp] = s; sb[warp] = best; si[warp] = idx; }
   __syncthreads();
   if (warp == 0) {
-    m = lane < 4 ? sm[lane] : -INFINITY;
-    s = lane < 4 ? ss[lane] : 0.f;
-    best = lane < 4 ? sb[lane] : -INFINITY;
-    idx = lane < 4 ? si[lane] : 0x7fffffff;
+    m = lane < NW ? sm[lane] : -INFINITY;
+    s = lane < NW ? ss[lane] : 0.f;
+    best = lane < NW ? sb[lane] : -INFINITY;
+    idx = lane < NW ? si[lane] : 0x7fffffff;
     warp_merge(m, s, best, idx, bs);
     if (lane == 0) {
       const size_t o = (size_t)i * gamma + k - 1;
@@ -134,7 +150,7 @@ __global__ void __launch_bounds__(128) reduce_prep(
     if (tok >= 0 && tok < V) {
       const uint4 *er = reinterpret_cast<const uint4 *>(E + (size_t)i * r);
       const uint4 *wr2 = reinterpret_cast<const uint4 *>(W2t + (size_t)tok * r);
-      for (int c = tid; c < r / 8; c += 128) {
+      for (int c = tid; c < r / 8; c += RP_THREADS) {
         const uint4 a = er[c], b = wr2[c];
         const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
@@ -150,7 +166,9 @@ __global__ void __launch_bounds__(128) reduce_prep(
     if (tid == 0) {
       const size_t o = (size_t)i * gamma + k - 1;
       const float bl = (tok >= 0 && tok < V) ? __bfloat162float(base[o * V + tok]) : 0.f;
-      const float logit = bl + (sdot[0] + sdot[1]) + (sdot[2] + sdot[3]);
+      float dsum = 0.f;
+      for (int w = 0; w < NW; ++w) dsum += sdot[w];
+      const float logit = bl + dsum;
       if (logp_out) logp_out[o] = logit * inv_tau - s_lse;
     }
     __syncthreads();  // E is rewritten below
@@ -168,7 +186,7 @@ __global__ void __launch_bounds__(128) reduce_prep(
   uint4 *dst = reinterpret_cast<uint4 *>(E + (size_t)i * r);
   const uint4 *wr = reinterpret_cast<const uint4 *>(w_e);
   float acc = 0.f;
-  for (int c = tid; c < r / 8; c += 128) {
+  for (int c = tid; c < r / 8; c += RP_THREADS) {
     const uint4 a = src[c], b = wr[c];
     dst[c] = a;
     const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
@@ -183,7 +201,9 @@ __global__ void __launch_bounds__(128) reduce_prep(
   __syncthreads();
   if (tid == 0) {
     const size_t o = (size_t)i * gamma + k;  // position k + 1
-    const float z = zh[o] + sdot[0] + sdot[1] + sdot[2] + sdot[3];
+    float zs = zh[o];
+    for (int w = 0; w < NW; ++w) zs += sdot[w];
+    const float z = zs;
     conf[o] = 1.f / (1.f + expf(-z / T[k]));
   }
 }
@@ -234,8 +254,7 @@ extern "C" int dspark_markov_draft(const dspark_dims *dims, const void *base_log
     return DSPARK_ERR_WORKSPACE;
   const int R = dims->R, G = dims->gamma, V = dims->V, r = dims->r, d = dims->d;
   const int rows = R * G;
-  conf_hidden<<<(rows * 32 + 255) / 256, 256, 0, stream>>>((const bf16 *)h, (const bf16 *)w_conf,
-                                                          ws.zh, rows, d);
+  conf_hidden<<<rows, 128, 0, stream>>>((const bf16 *)h, (const bf16 *)w_conf, ws.zh, d);
   DSPARK_CHECK_LAUNCH();
   const float inv_tau = tau > 0.f ? 1.f / tau : 1.f;
   step_prep<<<(R * 32 + 255) / 256, 256, 0, stream>>>(anchor, tokens, (const bf16 *)W1,
@@ -252,7 +271,7 @@ extern "C" int dspark_markov_draft(const dspark_dims *dims, const void *base_log
                                  R, V, G, k, n_tiles, inv_tau, seed};
       rc = gemm::launch<LogitsCfg<MODE_SAMPLE>::EPI_WARPS, LogitsCfg<MODE_SAMPLE>::BN>(ws.E, W2t, R, V, r, epi, stream);
       if (rc != DSPARK_OK) return rc;
-      reduce_prep<MODE_SAMPLE><<<R, 128, 0, stream>>>(ws.part, n_tiles, G, V, r, k, tokens, lse_d,
+      reduce_prep<MODE_SAMPLE><<<R, RP_THREADS, 0, stream>>>(ws.part, n_tiles, G, V, r, k, tokens, lse_d,
                                                       logp_d, (const bf16 *)W1, w_e, ws.zh, T,
                                                       ws.E, conf, ws.gfloor,
                                                       (const bf16 *)base_logits,
@@ -264,7 +283,7 @@ extern "C" int dspark_markov_draft(const dspark_dims *dims, const void *base_log
                                  R, V, G, k, n_tiles, 1.f, seed};
       rc = gemm::launch<LogitsCfg<MODE_GREEDY>::EPI_WARPS, LogitsCfg<MODE_GREEDY>::BN>(ws.E, W2t, R, V, r, epi, stream);
       if (rc != DSPARK_OK) return rc;
-      reduce_prep<MODE_GREEDY><<<R, 128, 0, stream>>>(ws.part, n_tiles, G, V, r, k, tokens, lse_d,
+      reduce_prep<MODE_GREEDY><<<R, RP_THREADS, 0, stream>>>(ws.part, n_tiles, G, V, r, k, tokens, lse_d,
                                                       logp_d, (const bf16 *)W1, w_e, ws.zh, T,
                                                       ws.E, conf, ws.gfloor,
                                                       (const bf16 *)base_logits,

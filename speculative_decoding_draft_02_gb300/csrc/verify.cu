@@ -198,24 +198,50 @@ __global__ void resample_gather(const ResampleRow *__restrict__ rows, const int 
 }
 
 // Residual rows: combine the slice partials into the corrected token; a row
-// whose residual came out empty is handed to the plain target sample.
-__global__ void resample_reduce(ResampleRow *__restrict__ rows, const int *__restrict__ list,
-                                const int *__restrict__ count,
-                                const RowPartial *__restrict__ part, int n_parts,
-                                int32_t *__restrict__ bonus) {
-  const int slot = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+// whose residual came out empty is handed to the plain target sample.  One CTA
+// of 256 threads per compacted row, eight partial loads in flight per thread.
+__global__ void __launch_bounds__(256) resample_reduce(ResampleRow *__restrict__ rows,
+                                                       const int *__restrict__ list,
+                                                       const int *__restrict__ count,
+                                                       const RowPartial *__restrict__ part,
+                                                       int n_parts, int32_t *__restrict__ bonus) {
+  const int slot = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (slot >= *count) return;
-  const int req = list[slot];
   float best = -INFINITY, d0 = 0.f, d1 = 0.f, d2 = 0.f;
   int idx = 0x7fffffff;
-  for (int t = lane; t < n_parts; t += 32) {
-    const RowPartial p = part[(size_t)slot * n_parts + t];
-    if (better(p.best, p.idx, best, idx)) { best = p.best; idx = p.idx; }
+  const RowPartial *pr = part + (size_t)slot * n_parts;
+  for (int t0 = 0; t0 < n_parts; t0 += 8 * 256) {
+    float b[8];
+    int id[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int t = t0 + u * 256 + tid;
+      b[u] = -INFINITY;
+      id[u] = 0x7fffffff;
+      if (t < n_parts) {
+        const RowPartial p = pr[t];
+        b[u] = p.best;
+        id[u] = p.idx;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (better(b[u], id[u], best, idx)) { best = b[u]; idx = id[u]; }
   }
   warp_merge(d0, d1, best, idx, d2);
-  if (lane == 0) {
-    if (best > -INFINITY) bonus[req] = idx;
-    else rows[req].kind = KIND_FALLBACK;
+  __shared__ float sb[8];
+  __shared__ int si[8];
+  if (lane == 0) { sb[warp] = best; si[warp] = idx; }
+  __syncthreads();
+  if (warp == 0) {
+    best = lane < 8 ? sb[lane] : -INFINITY;
+    idx = lane < 8 ? si[lane] : 0x7fffffff;
+    warp_merge(d0, d1, best, idx, d2);
+    if (lane == 0) {
+      const int req = list[slot];
+      if (best > -INFINITY) bonus[req] = idx;
+      else rows[req].kind = KIND_FALLBACK;
+    }
   }
 }
 
@@ -392,8 +418,7 @@ extern "C" int dspark_verify(const dspark_dims *dims, const int32_t *anchor, con
   const int rc = gemm::launch<LogitsCfg<MODE_RESIDUAL>::EPI_WARPS, LogitsCfg<MODE_RESIDUAL>::BN>(ws.E, W2t, R, V, r, epi, stream,
                                                                   ws.count);
   if (rc != DSPARK_OK) return rc;
-  resample_reduce<<<(R * 32 + 255) / 256, 256, 0, stream>>>(ws.rows, ws.list, ws.count, ws.part,
-                                                          n_parts, bonus);
+  resample_reduce<<<R, 256, 0, stream>>>(ws.rows, ws.list, ws.count, ws.part, n_parts, bonus);
   DSPARK_CHECK_LAUNCH();
   bonus_row<<<R, 512, 0, stream>>>(ws.rows, tgt, bonus, G, V, inv_tau, seed);
   DSPARK_CHECK_LAUNCH();
