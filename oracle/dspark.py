@@ -24,7 +24,8 @@ Readings where the pages are silent (each listed in the design notes):
   * T_k divides the confidence logit: c_k = sigmoid(z_k / T_k).  No bias term.
   * Sampling temperature tau divides (base + bias); tau = 0 means greedy argmax
     (ties to the lowest vocabulary id); tau > 0 samples by Gumbel-max with the
-    Philox layout of oracle.philox.  The target uses the same tau.
+    Philox layout of oracle.philox, in two levels over blocks of 64 vocabulary
+    entries (gumbel_max below).  The target uses the same tau.
   * Base logits are materialised in bf16 (the LM head's output type); every
     later step accumulates in float64 here.
   * Confidences are float32; survival products a_{r,j} are float32 products
@@ -94,6 +95,80 @@ def top2_margin(score: np.ndarray) -> np.ndarray:
     return part[..., -1] - part[..., -2]
 
 
+def _block_logsumexp(x: np.ndarray) -> np.ndarray:
+    """logsumexp over the last axis; -inf for an all -inf row (an empty block)."""
+    m = np.max(x, axis=-1, keepdims=True)
+    finite = np.isfinite(m)
+    safe = np.where(finite, m, 0.0)
+    with np.errstate(divide="ignore"):
+        out = safe + np.log(np.sum(np.exp(x - safe), axis=-1, keepdims=True))
+    return np.where(finite, out, -np.inf).squeeze(-1)
+
+
+# ---------------------------------------------------------------------------
+# the sampler shared by every random draw of the round
+# ---------------------------------------------------------------------------
+
+GUMBEL_BLOCK = 64
+
+
+def gumbel_max(score, seed: int, position, request, stream: int,
+               block: int = GUMBEL_BLOCK) -> Dict[str, np.ndarray]:
+    """One draw from softmax(score) per row, by Gumbel-max in two levels.
+
+    score [N, V] float64 log-weights (-inf excludes an entry); position and
+    request broadcast to [N].  The pages name Gumbel-max keyed by
+    (seed, request, position) and fix nothing further; this is the reading:
+
+      1. cut the vocabulary into blocks of `block` consecutive ids (the last
+         one shorter when V is not a multiple);
+      2. block b scores G_b = log sum_{v in b} e^{score_v} + g_b, g_b the Gumbel
+         of block id b in stream `stream + 4`;
+      3. b* = argmax_b G_b (lowest b on ties; blocks of zero mass never win);
+      4. the token is argmax over v in b* of score_v + g_v, g_v the Gumbel of
+         vocabulary id v in stream `stream` (lowest v on ties).
+
+    Exactness (max-stability of the Gumbel law): max_{v in b}(score_v + g_v)
+    is Gumbel with location log Z_b, so step 3 picks b with probability
+    Z_b / Z and step 4 picks v in b with probability e^{score_v} / Z_b; the
+    product is softmax(score)_v (Maddison, Tarlow, Minka, "A* Sampling",
+    NIPS 2014, on the top-down construction of Gumbel processes).
+
+    Returns token [N] (-1 when every entry is -inf), margin [N] (the smaller
+    of the two levels' top-2 gaps; +inf where a level has one candidate),
+    block_scores [N, nb] and entry_scores [N, V] (score + g for every id).
+    """
+    score = np.atleast_2d(to_f64(score))
+    N, V = score.shape
+    nb = (V + block - 1) // block
+    pos = np.broadcast_to(np.asarray(position, dtype=np.uint64), (N,))
+    req = np.broadcast_to(np.asarray(request, dtype=np.uint64), (N,))
+    padded = np.full((N, nb * block), -np.inf)
+    padded[:, :V] = score
+    lse_b = _block_logsumexp(padded.reshape(N, nb, block))
+    g_b = philox.gumbel(seed, pos[:, None], req[:, None], stream + philox.BLOCK_STREAM_OFFSET,
+                        np.arange(nb, dtype=np.uint64)[None, :])
+    G = lse_b + g_b                                      # -inf for empty blocks
+    g_v = philox.gumbel(seed, pos[:, None], req[:, None], stream,
+                        np.arange(V, dtype=np.uint64)[None, :])
+    e = score + g_v
+    bstar = np.argmax(G, axis=1)
+    token = np.full(N, -1, dtype=np.int64)
+    margin = np.full(N, np.inf)
+    for n in range(N):
+        if not np.isfinite(G[n, bstar[n]]):
+            continue
+        lo, hi = bstar[n] * block, min(V, bstar[n] * block + block)
+        inner = e[n, lo:hi]
+        token[n] = lo + int(np.argmax(inner))
+        gb = G[n][np.isfinite(G[n])]
+        gi = inner[np.isfinite(inner)]
+        m_b = top2_margin(gb) if gb.size > 1 else np.inf
+        m_i = top2_margin(gi) if gi.size > 1 else np.inf
+        margin[n] = min(m_b, m_i)
+    return dict(token=token, margin=margin, block_scores=G, entry_scores=e)
+
+
 # ---------------------------------------------------------------------------
 # a1: base logits through the shared, frozen LM head   [DD §二 architecture; AR]
 # ---------------------------------------------------------------------------
@@ -126,7 +201,8 @@ def base_logits(h, W_lm, bf16_out: bool = True, vocab_chunk: int = 0) -> np.ndar
 
 def markov_draft(base, h, anchor, W1, W2, w_conf, T, tau: float, seed: int,
                  forced=None, keep_logits: bool = False, keep_scores: bool = False,
-                 requests: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
+                 requests: Optional[np.ndarray] = None,
+                 block: int = GUMBEL_BLOCK) -> Dict[str, np.ndarray]:
     """Run the sequential head for k = 1..gamma.
 
     base [R, gamma, V] base logits; h [R, gamma, d]; anchor [R]; W1 [V, r];
@@ -135,7 +211,8 @@ def markov_draft(base, h, anchor, W1, W2, w_conf, T, tau: float, seed: int,
     of the oracle's own x_k (used to evaluate the draft distribution along a
     given token path, e.g. for verification).  `requests` gives the request ids
     used for the random streams (default 0..R-1).  `keep_scores` returns the
-    decision score of every vocabulary entry at every step.
+    decision score of every vocabulary entry at every step (sampling: also the
+    block scores of gumbel_max).  `block` is the sampler's block width.
 
     Returns tokens (the oracle's own choice at each step), conf, z, margin (top-2
     gap of the decision score), and in sampling mode lse = logsumexp(l_k / tau)
@@ -152,7 +229,6 @@ def markov_draft(base, h, anchor, W1, W2, w_conf, T, tau: float, seed: int,
     d = h.shape[-1]
     w_h, w_e = w_conf[:d], w_conf[d:]
     req = np.arange(R) if requests is None else to_i64(requests)
-    vocab = np.arange(V, dtype=np.uint64)
 
     tokens = np.zeros((R, G), dtype=np.int64)
     conf = np.zeros((R, G))
@@ -163,6 +239,8 @@ def markov_draft(base, h, anchor, W1, W2, w_conf, T, tau: float, seed: int,
     path = np.zeros((R, G), dtype=np.int64)
     logits = np.zeros((R, G, V)) if keep_logits else None
     scores = np.zeros((R, G, V)) if keep_scores else None
+    nb = (V + block - 1) // block
+    bscores = np.zeros((R, G, nb)) if keep_scores and tau != 0.0 else None
     forced = None if forced is None else to_i64(forced)
 
     prev = anchor.copy()
@@ -174,12 +252,16 @@ def markov_draft(base, h, anchor, W1, W2, w_conf, T, tau: float, seed: int,
         z_out[:, k - 1] = z
         if tau == 0.0:
             score = ell
+            x = np.argmax(score, axis=1)               # first maximum: lowest id
+            margin[:, k - 1] = top2_margin(score)
         else:
-            g = philox.gumbel(seed, k, req[:, None], philox.STREAM_DRAFT, vocab[None, :])
-            score = ell / tau + g
-        x = np.argmax(score, axis=1)                   # first maximum: lowest id
+            smp = gumbel_max(ell / tau, seed, k, req, philox.STREAM_DRAFT, block)
+            score = smp["entry_scores"]
+            x = smp["token"]
+            margin[:, k - 1] = smp["margin"]
+            if bscores is not None:
+                bscores[:, k - 1, :] = smp["block_scores"]
         tokens[:, k - 1] = x
-        margin[:, k - 1] = top2_margin(score)
         nxt = x if forced is None else forced[:, k - 1]
         path[:, k - 1] = nxt
         if tau != 0.0:
@@ -196,6 +278,9 @@ def markov_draft(base, h, anchor, W1, W2, w_conf, T, tau: float, seed: int,
         out["logits"] = logits
     if keep_scores:
         out["scores"] = scores
+        if bscores is not None:
+            out["block_scores"] = bscores
+            out["block"] = block
     return out
 
 
@@ -279,7 +364,8 @@ def confidence_label(p_d: np.ndarray, p_t: np.ndarray) -> np.ndarray:
 
 
 def verify(tokens, lens, draft_logits, target, tau: float, seed: int,
-           requests: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
+           requests: Optional[np.ndarray] = None,
+           block: int = GUMBEL_BLOCK) -> Dict[str, np.ndarray]:
     """Verify each request's admitted prefix against the target.
 
     tokens [R, gamma]; lens [R]; draft_logits [R, gamma, V] (final l_k, only
@@ -287,7 +373,9 @@ def verify(tokens, lens, draft_logits, target, tau: float, seed: int,
     the target's distribution for draft position j.
     Returns accepted [R], bonus [R], and diagnostics: accept_margin [R, gamma]
     (log u + log p_d - log p_t at each tested position, nan elsewhere) and
-    final_margin [R] (top-2 gap of the score that picked the bonus).
+    final_margin [R] (top-2 gap of the score that picked the bonus; sampling:
+    the margin of gumbel_max), and final_kind [R] (0 greedy, 1 residual,
+    2 bonus row, 3 residual that was empty, drawn from p_t instead).
     """
     tokens = to_i64(tokens)
     lens = to_i64(lens)
@@ -296,11 +384,11 @@ def verify(tokens, lens, draft_logits, target, tau: float, seed: int,
     G = G1 - 1
     req = np.arange(R) if requests is None else to_i64(requests)
     dl = None if tau == 0.0 else to_f64(draft_logits)
-    vocab = np.arange(V, dtype=np.uint64)
     accepted = np.zeros(R, dtype=np.int64)
     bonus = np.zeros(R, dtype=np.int64)
     acc_margin = np.full((R, G), np.nan)
     final_margin = np.zeros(R)
+    final_kind = np.zeros(R, dtype=np.int64)
     for i in range(R):
         L = int(lens[i])
         rq = int(req[i])
@@ -331,24 +419,24 @@ def verify(tokens, lens, draft_logits, target, tau: float, seed: int,
             p_t = np.exp(lt - lse_t)
             p_d = np.exp(ld - lse_d)
             q = np.maximum(p_t - p_d, 0.0)
-            g = philox.gumbel(seed, j, rq, philox.STREAM_RESIDUAL, vocab)
-            if np.any(q > 0.0):
-                with np.errstate(divide="ignore"):
-                    score = np.where(q > 0.0, np.log(q) + g, -np.inf)
-            else:
-                score = lt + g
-            bonus[i] = int(np.argmax(score))
-            final_margin[i] = top2_margin(score)
+            with np.errstate(divide="ignore"):
+                smp = gumbel_max(np.log(q), seed, j, rq, philox.STREAM_RESIDUAL, block)
+            final_kind[i] = 1
+            if smp["token"][0] < 0:                      # empty residual: draw from p_t
+                smp = gumbel_max(lt, seed, j, rq, philox.STREAM_RESIDUAL, block)
+                final_kind[i] = 3
+            bonus[i] = int(smp["token"][0])
+            final_margin[i] = smp["margin"][0]
             rejected = True
             break
         if not rejected:
-            g = philox.gumbel(seed, L + 1, rq, philox.STREAM_BONUS, vocab)
-            score = target[i, L] / tau + g
-            bonus[i] = int(np.argmax(score))
-            final_margin[i] = top2_margin(score)
+            smp = gumbel_max(target[i, L] / tau, seed, L + 1, rq, philox.STREAM_BONUS, block)
+            bonus[i] = int(smp["token"][0])
+            final_margin[i] = smp["margin"][0]
+            final_kind[i] = 2
         accepted[i] = n
     return dict(accepted=accepted, bonus=bonus, accept_margin=acc_margin,
-                final_margin=final_margin)
+                final_margin=final_margin, final_kind=final_kind)
 
 
 # ---------------------------------------------------------------------------

@@ -17,7 +17,9 @@ written independently draws the same numbers:
     counter = (v >> 2, position, request, stream)    output word = v & 3
     u       = ((word >> 9) + 1/2) * 2^-23            exact in float32, in (0, 1)
     Gumbel  = -log(-log u)
-Streams: 0 draft Gumbel, 1 accept uniform (v = 0), 2 residual Gumbel, 3 bonus Gumbel.
+Streams: 0 draft Gumbel, 1 accept uniform (v = 0), 2 residual Gumbel, 3 bonus Gumbel;
+4, 5, 6 the block-level Gumbels of the draft, residual and bonus draws (v = the
+block index; see oracle.dspark.gumbel_max).
 """
 from __future__ import annotations
 
@@ -33,6 +35,7 @@ STREAM_DRAFT = 0
 STREAM_ACCEPT = 1
 STREAM_RESIDUAL = 2
 STREAM_BONUS = 3
+BLOCK_STREAM_OFFSET = 4   # block-level draws of stream s use stream s + 4
 
 
 def philox4x32_10(c0, c1, c2, c3, k0: int, k1: int):

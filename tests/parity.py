@@ -9,7 +9,10 @@ Rules:
 * a token decided by a floating-point argmax must match wherever the oracle's
   top-2 margin exceeds `tol`; inside the margin the CUDA token must still be a
   maximiser within `tol` of the oracle's score, and the rest of that request's
-  chain (which conditions on the token) is excused;
+  chain (which conditions on the token) is excused.  A sampled token is decided
+  in two levels (oracle.dspark.gumbel_max): its margin is the smaller of the
+  two, and a flagged token's block must be within `tol` of the best block
+  score and the token within `tol` of the best entry of that block;
 * confidences, log-sum-exps and log-probabilities within `rtol`.
 """
 from __future__ import annotations
@@ -59,13 +62,26 @@ def compare_draft(gpu_tokens, gpu_conf, gpu_lse, gpu_logp, orc, tau, tol_rel=1e-
             assert err <= conf_rtol * abs(c_o) + 1e-6, (i, k, gc[i, k], c_o)
             s = orc["scores"][oi, k]
             smax = float(s.max())
-            tol = tol_rel * max(1.0, abs(smax))
+            two_level = tau > 0 and "block_scores" in orc
+            if two_level:
+                bs = orc["block_scores"][oi, k]
+                bmax = float(bs.max())
+                tol = tol_rel * max(1.0, abs(smax), abs(bmax))
+            else:
+                tol = tol_rel * max(1.0, abs(smax))
             g = int(gt[i, k])
             assert 0 <= g < s.size
             rep.compared += 1
             if orc["margin"][oi, k] > tol:
                 assert g == orc["tokens"][oi, k], (i, k, g, orc["tokens"][oi, k],
                                                    orc["margin"][oi, k])
+            elif two_level:
+                rep.flagged += 1
+                blk = orc["block"]
+                b = g // blk
+                assert bmax - bs[b] <= tol, (i, k, bmax - bs[b], tol)
+                inner = s[b * blk:(b + 1) * blk]
+                assert float(inner.max()) - s[g] <= tol, (i, k, float(inner.max()) - s[g], tol)
             else:
                 rep.flagged += 1
                 assert smax - s[g] <= tol, (i, k, smax - s[g], tol)

@@ -150,21 +150,68 @@ def test_confidence_head_brute_force():
     assert d == 5
 
 
-@pytest.mark.parametrize("tau", [0.7, 1.0, 1.6])
-def test_gumbel_max_follows_softmax(tau):
-    """Sampled draft tokens follow softmax(l / tau) (Gumbel-max law)."""
+@pytest.mark.parametrize("tau,block", [(0.7, 64), (1.0, 64), (1.6, 64), (1.0, 2), (0.7, 4)])
+def test_gumbel_max_follows_softmax(tau, block):
+    """Sampled draft tokens follow softmax(l / tau) (Gumbel-max law), with the
+    vocabulary in one block (plain Gumbel-max) or cut into several."""
     V, N = 6, 60000
     logits = np.array([0.3, -1.0, 1.2, 0.0, 2.0, -0.4])
     base = np.broadcast_to(logits, (N, 1, V)).copy()
     out = oracle.markov_draft(base, np.zeros((N, 1, 1)), np.zeros(N, int),
                               np.zeros((V, 1)), np.zeros((1, V)), np.zeros(2), np.ones(1),
-                              tau, seed=2024)
+                              tau, seed=2024, block=block)
     counts = np.bincount(out["tokens"][:, 0], minlength=V)
     p = np.exp(logits / tau)
     p /= p.sum()
     assert stats.chisquare(counts, N * p).pvalue > 1e-4
     # log p_d of the sampled token is reported
     np.testing.assert_allclose(out["logp"][:, 0], np.log(p[out["tokens"][:, 0]]), atol=1e-12)
+
+
+def test_two_level_gumbel_law_with_excluded_entries_and_ragged_block():
+    """Blocks of 3 over V = 8 (last block of 2); one whole block and one more
+    entry at -inf.  Frequencies follow softmax over the finite entries, the
+    excluded ids never come up, and each token lies in its row's top block."""
+    N, block = 90000, 3
+    score = np.array([0.4, -0.7, 1.1, -np.inf, -np.inf, -np.inf, 0.9, -np.inf])
+    smp = oracle.dspark.gumbel_max(np.broadcast_to(score, (N, 8)), 77, 3, np.arange(N), 0, block)
+    tok = smp["token"]
+    counts = np.bincount(tok, minlength=8)
+    assert counts[3] == counts[4] == counts[5] == counts[7] == 0
+    fin = np.isfinite(score)
+    p = np.exp(score[fin] - score[fin].max())
+    p /= p.sum()
+    assert stats.chisquare(counts[fin], N * p).pvalue > 1e-4
+    assert np.array_equal(tok // block, np.argmax(smp["block_scores"], axis=1))
+    assert np.all(np.isneginf(smp["block_scores"][:, 1]))     # the empty block
+
+
+def test_two_level_gumbel_in_one_block_is_plain_gumbel_max():
+    """With one block the draw is the textbook argmax(score + g_v)."""
+    rng = np.random.default_rng(41)
+    N, V = 500, 50
+    score = rng.standard_normal((N, V)) * 2.0
+    req = np.arange(N) + 1000
+    smp = oracle.dspark.gumbel_max(score, 5, 2, req, philox.STREAM_BONUS)  # V <= 64
+    g = philox.gumbel(5, 2, req[:, None], philox.STREAM_BONUS, np.arange(V, dtype=np.uint64)[None, :])
+    assert np.array_equal(smp["token"], np.argmax(score + g, axis=1))
+    # an all -inf row has nothing to draw
+    empty = oracle.dspark.gumbel_max(np.full((1, V), -np.inf), 5, 2, 0, 0)
+    assert empty["token"][0] == -1
+
+
+def test_two_level_gumbel_block_choice_follows_block_mass():
+    """Block b* comes up with probability Z_b / Z (the first level alone)."""
+    N, block = 80000, 4
+    rng = np.random.default_rng(42)
+    score = rng.standard_normal(16) * 1.5
+    smp = oracle.dspark.gumbel_max(np.broadcast_to(score, (N, 16)), 9, 1, np.arange(N), 2, block)
+    counts = np.bincount(smp["token"] // block, minlength=4)
+    Z = np.exp(score).reshape(4, block).sum(axis=1)
+    assert stats.chisquare(counts, N * Z / Z.sum()).pvalue > 1e-4
+    # a max over the block instead of its mass (a plausible slip) is rejected here
+    M = np.exp(score.reshape(4, block).max(axis=1))
+    assert stats.chisquare(counts, N * M / M.sum()).pvalue < 1e-6
 
 
 # ---------------------------------------- a5-a7: survival, sort, Theta ---
@@ -336,11 +383,13 @@ def test_sampling_verify_identical_distributions_always_accepts():
     assert np.all(res["accepted"] == G)
 
 
-def _markov_target_rounds(mode, V=6, G=3, N=30000, L=3, seed=0):
+def _markov_target_rounds(mode, V=6, G=3, N=30000, L=3, seed=0, block=2):
     """Decode L tokens per trial by draft -> schedule -> verify rounds (oracle only).
 
     Target: a first-order Markov chain P_t(next | prev).  Draft: base logits per
     position plus a low-rank Markov bias; confidences from the confidence head.
+    Every draw cuts the vocabulary into sampler blocks of `block` ids (three
+    blocks over V = 6 by default), so both levels of the sampler take part.
     Returns the first L emitted tokens of each trial and the exact target joint.
     """
     rng = np.random.default_rng(seed)
@@ -362,7 +411,7 @@ def _markov_target_rounds(mode, V=6, G=3, N=30000, L=3, seed=0):
     while min(len(e) for e in emitted) < L:
         base = np.broadcast_to(base0, (N, G, V)).copy()
         dr = oracle.markov_draft(base, h, anchor, W1, W2, w, T, 1.0, seed=1000 + rnd,
-                                 keep_logits=True)
+                                 keep_logits=True, block=block)
         x = dr["tokens"]
         prev = np.concatenate([anchor[:, None], x], axis=1)        # x_0..x_G
         target = logPt[prev]                                       # row j-1 | x_{j-1}
@@ -375,7 +424,7 @@ def _markov_target_rounds(mode, V=6, G=3, N=30000, L=3, seed=0):
         elif mode == "fixed_k":
             lens = oracle.schedule(dr["conf"].astype(np.float32), sps, oracle.FIXED_K,
                                    N * G // 2)["len"]
-        res = oracle.verify(x, lens, dr["logits"], target, 1.0, seed=5000 + rnd)
+        res = oracle.verify(x, lens, dr["logits"], target, 1.0, seed=5000 + rnd, block=block)
         for i in range(N):
             n = res["accepted"][i]
             emitted[i].extend(list(x[i, :n]) + [res["bonus"][i]])
