@@ -71,7 +71,8 @@ enum {
   DSPARK_ERR_TOKEN = 5,      /* device status: token id outside [0, V)              */
   DSPARK_ERR_LENGTH = 6,     /* device status: verify length outside [0, gamma]     */
   DSPARK_ERR_TIMEOUT = 7,    /* device status: a bounded device-side wait ran out   */
-  DSPARK_ERR_TOO_LARGE = 8   /* problem needs more than the library's static scratch */
+  DSPARK_ERR_TOO_LARGE = 8   /* problem exceeds a fixed library limit (static scratch,
+                                sampling verify with V > 3604480)                  */
 };
 
 enum {
@@ -104,7 +105,12 @@ size_t dspark_markov_workspace_bytes(const dspark_dims *dims);
  * For k = 1..gamma, with x_0 = anchor:
  *   l_k     = l0_k + W1[x_{k-1}] W2                   (f32, never written out)
  *   x_k     = argmax_v l_k[v]                          tau == 0 (ties: lowest v)
- *           = argmax_v l_k[v] / tau + Gumbel(seed; r, k, v, stream 0)   tau > 0
+ *           = a draw from softmax(l_k / tau)                             tau > 0
+ *             by two-level Gumbel-max: the vocabulary is cut into blocks of 64
+ *             ids; block b* = argmax_b log sum_{v in b} e^{l_k[v]/tau}
+ *             + Gumbel(seed; r, k, b, stream 4), then x_k = argmax over v in b*
+ *             of l_k[v]/tau + Gumbel(seed; r, k, v, stream 0); ties to the
+ *             lowest id at both levels
  *   c_k     = sigmoid((w_h . h_k + w_e . W1[x_{k-1}]) / T_k),  w_conf = [w_h; w_e]
  *   lse_k   = logsumexp_v(l_k[v] / tau)      (tau > 0 only; 0 when greedy)
  *   logp_k  = l_k[x_k] / tau - lse_k          (tau > 0 only; 0 when greedy)
@@ -158,8 +164,12 @@ size_t dspark_verify_workspace_bytes(const dspark_dims *dims);
  *             argmax (or row l_r + 1 when all match) is the bonus token.
  *   tau > 0:  accept x_j iff u * p_d(x_j) < p_t(x_j), u = U(seed; r, j, stream 1);
  *             on the first rejection sample norm(max(0, p_t - p_d)) at that row
- *             (Gumbel stream 2); when all l_r are accepted sample target row
- *             l_r + 1 (Gumbel stream 3).  p = softmax(logits / tau).
+ *             (Gumbel streams 2 and 6); when all l_r are accepted sample target
+ *             row l_r + 1 (streams 3 and 7).  p = softmax(logits / tau).  Each
+ *             draw is the two-level Gumbel-max of dspark_markov_draft (entry
+ *             stream s, block stream s + 4); a residual that is empty in
+ *             floating point is replaced by p_t itself (streams 2 and 6).
+ *             Returns DSPARK_ERR_TOO_LARGE when tau > 0 and V > 3604480.
  *   anchor   int32 [R];  tokens int32 [R, gamma];  len int32 [R] (0..gamma)
  *   base_logits bf16 [R*gamma, V], W1 bf16 [V, r], W2t bf16 [V, r]: the draft's
  *            operands, used to rebuild p_d on the rejected row (tau > 0 only)

@@ -18,8 +18,8 @@ written independently draws the same numbers:
     u       = ((word >> 9) + 1/2) * 2^-23            exact in float32, in (0, 1)
     Gumbel  = -log(-log u)
 Streams: 0 draft Gumbel, 1 accept uniform (v = 0), 2 residual Gumbel, 3 bonus Gumbel;
-4, 5, 6 the block-level Gumbels of the draft, residual and bonus draws (v = the
-block index; see oracle.dspark.gumbel_max).
+the block-level Gumbels of a draw in stream s use stream s + 4 (4 draft,
+6 residual, 7 bonus; v = the block index; see oracle.dspark.gumbel_max).
 """
 from __future__ import annotations
 

@@ -83,8 +83,15 @@ struct PhiloxKeys {
   }
 };
 
-// Random streams of the library's draw layout.
-enum { RNG_DRAFT = 0, RNG_ACCEPT = 1, RNG_RESIDUAL = 2, RNG_BONUS = 3 };
+// Random streams of the library's draw layout.  Every draw from a softmax is a
+// two-level Gumbel-max over blocks of GUMBEL_BLOCK consecutive vocabulary ids:
+// block b scores log(sum of its weights) + the Gumbel of id b in stream
+// s + RNG_BLOCK_OFFSET, and inside the best block each id v scores its
+// log-weight + the Gumbel of id v in stream s.  Max-stability of the Gumbel
+// law makes this an exact sample (Maddison, Tarlow, Minka, "A* Sampling",
+// NIPS 2014, top-down Gumbel processes).
+enum { RNG_DRAFT = 0, RNG_ACCEPT = 1, RNG_RESIDUAL = 2, RNG_BONUS = 3, RNG_BLOCK_OFFSET = 4 };
+constexpr int GUMBEL_BLOCK = 64;
 
 // The four words for vocabulary slots 4*q .. 4*q+3 at (position, request, stream).
 __device__ __forceinline__ uint4 rng_words4(uint64_t seed, uint32_t q, uint32_t pos,
@@ -170,13 +177,16 @@ __device__ __forceinline__ float ex2_fast(float x) {
   return y;
 }
 
-// atomic max on a float in global memory (handles both signs)
-__device__ __forceinline__ void atomic_max_float(float *addr, float v) {
-  if (v >= 0.f)
-    atomicMax(reinterpret_cast<int *>(addr), __float_as_int(v));
-  else
-    atomicMin(reinterpret_cast<unsigned int *>(addr), __float_as_uint(v));
-}
-
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// acc + the dot product of eight bf16 pairs packed in two 16-byte words
+__device__ __forceinline__ float dot8_bf16(const uint4 a, const uint4 b, float acc) {
+  const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    acc = fmaf(bf16_lo(av[t]), bf16_lo(bv[t]), acc);
+    acc = fmaf(bf16_hi(av[t]), bf16_hi(bv[t]), acc);
+  }
+  return acc;
+}

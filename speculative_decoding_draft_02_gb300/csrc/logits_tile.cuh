@@ -5,9 +5,13 @@
 //                                              E[i] = W1[x_{k-1}] of row i)
 //   l[i, v]    = l0[row_i, v] + bias[i, v]     (never written to memory)
 //
-// followed, per row and per PART_N-wide vocabulary slice, by the decision the
-// mode asks for and the online log-sum-exp of l / tau.  Each slice leaves one
-// RowPartial per row; a small reduction combines the slices.
+// followed, per row and per SLICE-wide vocabulary slice, by what the mode asks
+// for: greedy the slice's argmax; sampling the slice's log-sum-exp of l / tau
+// and its block score (the first level of the two-level Gumbel-max draw, one
+// slice = one sampler block); residual the block score of max(0, p_t - p_d).
+// Each slice leaves one RowPartial per row; a small reduction combines the
+// slices and, when sampling, draws inside the winning block (block_logits and
+// block_pick below).
 //
 // "DSpark 深度解读" §二 设计一: B(x_{k-1}, .) = W1[x_{k-1}] W2 is added to the base
 // logits and x_k is sampled from the result, left to right.
@@ -91,6 +95,7 @@ __device__ __forceinline__ void unpack32(const uint4 (&w)[4], int n, int V, floa
   unpack<32>(w, n, V, out);
 }
 
+
 template <int MODE>
 struct EpiLogits {
   const bf16 *base;          // [R*gamma, V]
@@ -99,8 +104,6 @@ struct EpiLogits {
   const int *list;           // [R] request of each compacted row (residual)
   const int *count;          // number of compacted rows           (residual)
   RowPartial *part;          // [R, n_parts]
-  float *gfloor;             // [R] best Gumbel score found so far on each row, shared by
-                             // every CTA of the pass (set to -inf before the pass)
   int M, V, gamma, k, n_parts;
   float inv_tau;
   uint64_t seed;
@@ -111,13 +114,12 @@ struct EpiLogits {
   static constexpr int CH = LogitsCfg<MODE>::CH;
   static constexpr int CHUNKS = SLICE / 32;                       // greedy: 32-column loads
   static constexpr int BUF = MODE == MODE_GREEDY ? SLICE / 8 : CH / 8;
+  static_assert(MODE == MODE_GREEDY || SLICE == GUMBEL_BLOCK,
+                "a sampling slice is exactly one sampler block");
 
   // Kept by each epilogue thread across the tiles it processes.
   struct State {
-    int m0 = -1;               // row block the floor belongs to
-    float floor = -INFINITY;   // best score known on this row (own tiles + shared floor)
-    float seen = -INFINITY;    // shared floor read at the start of the current tile
-    uint4 buf[BUF];            // base logits prefetched before the accumulator is ready
+    uint4 buf[BUF];  // base logits prefetched before the accumulator is ready
   };
 
   __device__ __forceinline__ bool draft_row(int m0, int row, const bf16 *&brow) const {
@@ -127,9 +129,6 @@ struct EpiLogits {
   }
 
   __device__ void prefetch(int m0, int n0, int row, int c0, int, State &st) const {
-    const int i = m0 + row;
-    if (MODE != MODE_GREEDY && i < M)
-      st.seen = *reinterpret_cast<volatile const float *>(gfloor + i);
     if (MODE == MODE_RESIDUAL) return;
     const bf16 *brow;
     if (!draft_row(m0, row, brow)) return;
@@ -166,11 +165,8 @@ struct EpiLogits {
     } else {
       draft_row(m0, row, brow);
     }
-    if (st.m0 != m0) { st.m0 = m0; st.floor = -INFINITY; }
-    st.floor = fmaxf(st.floor, st.seen);
-    const uint32_t stream = MODE == MODE_SAMPLE ? RNG_DRAFT : RNG_RESIDUAL;
 
-    float m2 = -INFINITY, s = 0.f, best = -INFINITY, bs = 0.f;
+    float m2 = -INFINITY, s = 0.f, best = -INFINITY;
     int idx = 0x7fffffff;
 
     if (MODE == MODE_GREEDY) {
@@ -205,14 +201,13 @@ struct EpiLogits {
         }
       }
     } else {
-      const PhiloxKeys keys(seed);
       const float c2 = inv_tau * LOG2E;  // scaled logits in log2 units
       constexpr int NQ = CH / 8;         // 16-byte words per chunk
-      constexpr int NH = CH / 16;        // halves of 16 entries (4 Philox calls each)
       uint4 nxt[NQ];
 #pragma unroll
       for (int q = 0; q < NQ; ++q) nxt[q] = st.buf[q];
       if (MODE == MODE_RESIDUAL && active) load_raw<CH>(brow, n0 + c0, V, nxt);
+      float z[4] = {0.f, 0.f, 0.f, 0.f};  // residual mass of the block (four partial sums)
 #pragma unroll 1
       for (int c = c0; c < c1; c += CH) {
         uint32_t acc[CH];
@@ -226,10 +221,8 @@ struct EpiLogits {
           if (c + CH < c1) load_raw<CH>(brow, n + CH, V, nxt);  // prefetch the next chunk
           float sv[CH];
           unpack<CH>(cur, n, V, sv);
-          const float F = fmaxf(best, st.floor);  // a score some entry of the row reaches
-
           if (MODE == MODE_SAMPLE) {
-            // y = base + bias (unscaled); the draft distribution is softmax(y / tau)
+            // y = base + bias (unscaled); online log-sum-exp of y / tau in base 2
             float y[CH];
 #pragma unroll
             for (int j = 0; j < CH; ++j) y[j] = sv[j] + __uint_as_float(acc[j]);
@@ -241,7 +234,6 @@ struct EpiLogits {
 #pragma unroll
               for (int j = 0; j < w; ++j) mx[j] = fmaxf(mx[j], mx[j + w]);
             const float cmax2 = mx[0] * c2;  // c2 = log2(e) / tau > 0
-            // online log-sum-exp in base 2 (four partial sums)
             if (cmax2 > m2) {
               s *= ex2_fast(m2 - cmax2);
               m2 = cmax2;
@@ -251,112 +243,38 @@ struct EpiLogits {
 #pragma unroll
             for (int j = 0; j < CH; ++j) ps[j & 3] += ex2_fast(fmaf(y[j], c2, nm2));
             s += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-
-            // Gumbel-max without the logarithms of entries that cannot win.
-            // Entry j beats F only if g_j > F - s_j (s_j = y_j / tau).  Since
-            // -log u >= 1 - u, 1 - u_j >= e^{s_j - F + 0.01} implies
-            // g_j < F - s_j - 0.01.  Chunk test first (s_j <= cmax, an integer
-            // threshold on w >> 9, u = ((w >> 9) + 1/2) 2^-23), then the same
-            // test per entry with e^{s_j - F} = 2^{y_j c2 - m2} e^{m - F}.
-            int w_thr = -1;
-            if (F > -INFINITY) {
-              const float t = fminf(F - cmax2 * LN2, 15.f);
-              const float X = __expf(-(t - 0.01f)) * 8388608.f;
-              w_thr = X >= 8388607.f ? -1 : 8388607 - (int)ceilf(X);
-            }
-            const float K = F > -INFINITY ? __expf(m2 * LN2 - F + 0.01f) : INFINITY;
-            const bool per_entry = K < 1e30f;
-            // Philox words in halves of 16 entries (one call per 4 entries).
-            // The common path needs only their maximum; the per-entry test,
-            // needed only when the chunk test fails, draws them again.
-#pragma unroll
-            for (int h = 0; h < NH; ++h) {
-              uint32_t wmax = 0;
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const uint4 w = keys(make_uint4((uint32_t)((n >> 2) + 4 * h + q), (uint32_t)pos,
-                                                (uint32_t)req, stream));
-                wmax = max(max(wmax, max(w.x, w.y)), max(w.z, w.w));
-              }
-              if ((int)(wmax >> 9) > w_thr) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                  const uint4 w = keys(make_uint4((uint32_t)((n >> 2) + 4 * h + q),
-                                                  (uint32_t)pos, (uint32_t)req, stream));
-                  const uint32_t wq[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                  for (int l = 0; l < 4; ++l) {
-                    const int j = 16 * h + 4 * q + l;
-                    const bool cand = !per_entry || (1.f - rng_uniform(wq[l])) <
-                                                        ex2_fast(fmaf(y[j], c2, nm2)) * K;
-                    if (cand) {
-                      const float sn = y[j] * inv_tau;
-                      const float sc = sn + rng_gumbel(wq[l]);
-                      if (sc > best) { best = sc; idx = n + j; bs = sn; }
-                    }
-                  }
-                }
-              }
-            }
           } else {
-            // residual max(0, p_t - p_d) at the rejected position.  The score
-            // log q_j + g_j <= log p_t(j) + g_j, so by the same argument an
-            // entry is skipped when 1 - u_j >= p_t(j) e^{-F + 0.01}; the chunk
-            // test uses the chunk's largest p_t.
+            // residual mass sum_v max(0, p_t(v) - p_d(v)) at the rejected row;
+            // ids past V read -inf on both sides and add nothing
             uint4 tw[NQ];
             load_raw<CH>(trow, n, V, tw);
             float tv[CH];
             unpack<CH>(tw, n, V, tv);
-            float mx[CH / 2];
+            const float nt = -lse_t * LOG2E, nd = -lse_d * LOG2E;
 #pragma unroll
-            for (int j = 0; j < CH / 2; ++j) mx[j] = fmaxf(tv[j], tv[j + CH / 2]);
-#pragma unroll
-            for (int w = CH / 4; w >= 1; w >>= 1)
-#pragma unroll
-              for (int j = 0; j < w; ++j) mx[j] = fmaxf(mx[j], mx[j + w]);
-            int w_thr = -1;
-            if (F > -INFINITY) {
-              const float X = __expf(fminf(mx[0] * inv_tau - lse_t - F + 0.01f, 0.f)) * 8388608.f;
-              w_thr = X >= 8388607.f ? -1 : 8388607 - (int)ceilf(X);
-            }
-            const float K = F > -INFINITY ? __expf(0.01f - F) : INFINITY;
-            const bool per_entry = K < 1e30f;
-#pragma unroll
-            for (int h = 0; h < NH; ++h) {
-              uint32_t ws[16];
-              uint32_t wmax = 0;
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const uint4 w = keys(make_uint4((uint32_t)((n >> 2) + 4 * h + q), (uint32_t)pos,
-                                                (uint32_t)req, stream));
-                ws[q * 4 + 0] = w.x; ws[q * 4 + 1] = w.y; ws[q * 4 + 2] = w.z; ws[q * 4 + 3] = w.w;
-                wmax = max(max(wmax, max(w.x, w.y)), max(w.z, w.w));
-              }
-              if ((int)(wmax >> 9) > w_thr) {
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                  const int j = 16 * h + e;
-                  const float pt = __expf(tv[j] * inv_tau - lse_t);
-                  const bool cand = (n + j < V) &&
-                                    (!per_entry || (1.f - rng_uniform(ws[e])) < pt * K);
-                  if (cand) {
-                    const float sl = (sv[j] + __uint_as_float(acc[j])) * inv_tau;
-                    const float qv = pt - __expf(sl - lse_d);
-                    if (qv > 0.f) {
-                      const float sc = __logf(qv) + rng_gumbel(ws[e]);
-                      if (sc > best) { best = sc; idx = n + j; }
-                    }
-                  }
-                }
-              }
+            for (int j = 0; j < CH; ++j) {
+              const float pt = ex2_fast(fmaf(tv[j], c2, nt));
+              const float pd = ex2_fast(fmaf(sv[j] + __uint_as_float(acc[j]), c2, nd));
+              z[j & 3] += fmaxf(pt - pd, 0.f);
             }
           }
         }
       }
-    }
-    if (MODE != MODE_GREEDY && active) {
-      st.floor = fmaxf(st.floor, best);
-      if (st.floor > st.seen) atomic_max_float(gfloor + i, st.floor);
+      // first level of the draw: the block score of this slice
+      if (active && n0 + c0 < V) {
+        const int b = (n0 + c0) / GUMBEL_BLOCK;
+        const uint32_t stream = (MODE == MODE_SAMPLE ? RNG_DRAFT : RNG_RESIDUAL) + RNG_BLOCK_OFFSET;
+        const uint4 w = rng_words4(seed, (uint32_t)(b >> 2), (uint32_t)pos, (uint32_t)req, stream);
+        const float g = rng_gumbel(uint4_get(w, b & 3));
+        if (MODE == MODE_SAMPLE) {
+          best = m2 * LN2 + logf(s) + g;  // s >= 1: the block's first id is inside V
+        } else {
+          const float zb = (z[0] + z[1]) + (z[2] + z[3]);
+          best = zb > 0.f ? logf(zb) + g : -INFINITY;
+          s = zb;
+        }
+        idx = b;
+      }
     }
     if (active && n0 + c0 < V) {
       RowPartial p;
@@ -369,3 +287,71 @@ struct EpiLogits {
   }
   __device__ void on_timeout() const { dspark_set_status(DSPARK_ERR_TIMEOUT); }
 };
+
+// ---------------------------------------------------------------------------
+// Second level of a draw: the ids of the winning sampler block
+// ---------------------------------------------------------------------------
+
+// out[j] = base_row[v] + E . W2t[v] for v = b * GUMBEL_BLOCK + j, and -inf past
+// V: the block's logits rebuilt from the Markov bias (E = W1[x_{k-1}]).  Every
+// thread of a CTA of NT threads calls it; each warp takes GUMBEL_BLOCK / (NT/32)
+// ids and keeps all their W2t words of one pass in flight.  Ends with a
+// __syncthreads().
+template <int NT>
+__device__ void block_logits(const bf16 *__restrict__ base_row, const bf16 *__restrict__ E,
+                             const bf16 *__restrict__ W2t, int b, int V, int r,
+                             float *__restrict__ out) {
+  constexpr int NW = NT / 32, PER = GUMBEL_BLOCK / NW;
+  static_assert(PER * NW == GUMBEL_BLOCK, "warps must split the block evenly");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int v0 = b * GUMBEL_BLOCK + warp * PER;
+  const uint4 *e4 = reinterpret_cast<const uint4 *>(E);
+  const int r8 = r / 8;
+  float acc[PER];
+#pragma unroll
+  for (int u = 0; u < PER; ++u) acc[u] = 0.f;
+  for (int c = lane; c < r8; c += 32) {
+    const uint4 a = e4[c];
+    uint4 w[PER];
+#pragma unroll
+    for (int u = 0; u < PER; ++u)
+      w[u] = (v0 + u < V) ? __ldg(reinterpret_cast<const uint4 *>(W2t + (size_t)(v0 + u) * r) + c)
+                          : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < PER; ++u) acc[u] = dot8_bf16(a, w[u], acc[u]);
+  }
+#pragma unroll
+  for (int u = 0; u < PER; ++u) acc[u] = warp_sum(acc[u]);
+  if (lane == 0) {
+#pragma unroll
+    for (int u = 0; u < PER; ++u)
+      out[warp * PER + u] =
+          v0 + u < V ? __bfloat162float(base_row[v0 + u]) + acc[u] : -INFINITY;
+  }
+  __syncthreads();
+}
+
+// Inside block b: the id with the largest score[j] + Gumbel(id, stream) (lowest
+// id on ties) among the ids with a finite score.  Called by one whole warp;
+// every lane gets the id (-1 when no id qualifies).  score is in shared memory.
+__device__ __forceinline__ int block_pick(const float *score, int b, int V, uint64_t seed,
+                                          uint32_t pos, uint32_t req, uint32_t stream) {
+  const int lane = threadIdx.x & 31;
+  float best = -INFINITY, d0 = 0.f, d1 = 0.f, d2 = 0.f;
+  int idx = 0x7fffffff;
+  if (lane < GUMBEL_BLOCK / 4) {
+    const int v0 = b * GUMBEL_BLOCK + 4 * lane;
+    const uint4 w = rng_words4(seed, (uint32_t)(v0 >> 2), pos, req, stream);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const float sc = score[4 * lane + t];
+      if (v0 + t < V && sc > -INFINITY) {
+        const float e = sc + rng_gumbel(ws[t]);
+        if (better(e, v0 + t, best, idx)) { best = e; idx = v0 + t; }
+      }
+    }
+  }
+  warp_merge(d0, d1, best, idx, d2);
+  return best > -INFINITY ? idx : -1;
+}

@@ -8,9 +8,10 @@
 //
 // Before the loop: zh = w_h . h for every row, and step 1's gather E = W1[x_0]
 // with the confidence c_1.  Per step k: one vocabulary pass (bias + base logits
-// + decision on the tensor cores, logits stay on chip), then reduce_prep
-// (combine the per-slice partials into x_k, lse_k, logp_k, and gather
-// E = W1[x_k] with c_{k+1} for the next step).
+// on the tensor cores, logits stay on chip; per 64-id block its log-sum-exp and
+// block score), then reduce_prep (combine the blocks into lse_k and the winning
+// block, draw x_k inside it, logp_k, and gather E = W1[x_k] with c_{k+1} for
+// the next step).
 #include <mutex>
 
 #include "logits_tile.cuh"
@@ -18,16 +19,6 @@
 DSPARK_DECLARE_STATUS(s_status_markov)
 
 namespace {
-
-__device__ __forceinline__ float dot8_bf16(const uint4 a, const uint4 b, float acc) {
-  const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    acc = fmaf(bf16_lo(av[t]), bf16_lo(bv[t]), acc);
-    acc = fmaf(bf16_hi(av[t]), bf16_hi(bv[t]), acc);
-  }
-  return acc;
-}
 
 // zh[m] = w_h . h[m] for every (request, position) row m; one CTA of 128
 // threads per row, each thread a strided quarter of the row's 16-byte words.
@@ -57,11 +48,10 @@ __global__ void __launch_bounds__(128) conf_hidden(const bf16 *__restrict__ h,
 __global__ void step_prep(const int32_t *__restrict__ anchor, const int32_t *__restrict__ tokens,
                           const bf16 *__restrict__ W1, const bf16 *__restrict__ w_e,
                           const float *__restrict__ zh, const float *__restrict__ T,
-                          bf16 *__restrict__ E, float *__restrict__ conf,
-                          float *__restrict__ gfloor, int R, int gamma, int V, int r, int k) {
+                          bf16 *__restrict__ E, float *__restrict__ conf, int R, int gamma,
+                          int V, int r, int k) {
   const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (i >= R) return;
-  if (lane == 0) gfloor[i] = -INFINITY;
   int prev = (k == 1) ? anchor[i] : tokens[(size_t)i * gamma + k - 2];
   if (prev < 0 || prev >= V) {
     if (lane == 0) dspark_set_status(DSPARK_ERR_TOKEN);
@@ -91,9 +81,10 @@ __global__ void step_prep(const int32_t *__restrict__ anchor, const int32_t *__r
 
 // Combine the vocabulary-slice partials of request i into x_k, lse_k, logp_k,
 // then (k < gamma) prepare step k+1: E[i] = W1[x_k] and the confidence c_{k+1}.
-// One CTA of RP_THREADS threads per request.  log p_d(x_k) = l_k[x_k] / tau - lse_k
-// needs the winner's logit: the base logit plus W1[x_{k-1}] . W2t[x_k] (E still
-// holds W1[x_{k-1}] here).
+// One CTA of RP_THREADS threads per request.  Greedy: the partials carry the
+// argmax.  Sampling: they carry block scores; the best block's 64 logits are
+// rebuilt (base logit + W1[x_{k-1}] . W2t[v], E still holds W1[x_{k-1}] here),
+// x_k is drawn among them and log p_d(x_k) = l_k[x_k] / tau - lse_k.
 constexpr int RP_THREADS = 256;
 
 template <int MODE>
@@ -102,8 +93,7 @@ __global__ void __launch_bounds__(RP_THREADS) reduce_prep(
     int32_t *__restrict__ tokens, float *__restrict__ lse_out, float *__restrict__ logp_out,
     const bf16 *__restrict__ W1, const bf16 *__restrict__ w_e, const float *__restrict__ zh,
     const float *__restrict__ T, bf16 *__restrict__ E, float *__restrict__ conf,
-    float *__restrict__ gfloor, const bf16 *__restrict__ base, const bf16 *__restrict__ W2t,
-    float inv_tau) {
+    const bf16 *__restrict__ base, const bf16 *__restrict__ W2t, float inv_tau, uint64_t seed) {
   const int i = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   float m = -INFINITY, s = 0.f, best = -INFINITY, bs = 0.f;
   int idx = 0x7fffffff;
@@ -125,6 +115,7 @@ __global__ void __launch_bounds__(RP_THREADS) reduce_prep(
   warp_merge(m, s, best, idx, bs);
   constexpr int NW = RP_THREADS / 32;
   __shared__ float sm[NW], ss[NW], sb[NW], sdot[NW], s_lse;
+  __shared__ float s_logit[GUMBEL_BLOCK], s_score[GUMBEL_BLOCK];
   __shared__ int si[NW], s_tok;
   if (lane == 0) { sm[warp] = m; ss[warp] = s; sb[warp] = best; si[warp] = idx; }
   __syncthreads();
@@ -135,48 +126,41 @@ __global__ void __launch_bounds__(RP_THREADS) reduce_prep(
     idx = lane < NW ? si[lane] : 0x7fffffff;
     warp_merge(m, s, best, idx, bs);
     if (lane == 0) {
-      const size_t o = (size_t)i * gamma + k - 1;
-      tokens[o] = idx;
       s_lse = MODE == MODE_SAMPLE ? m + logf(s) : 0.f;
-      if (lse_out) lse_out[o] = s_lse;
-      s_tok = idx;
+      s_tok = idx;  // greedy: the token; sampling: the winning block
     }
   }
   __syncthreads();
-  const int tok = s_tok;
+  const size_t o = (size_t)i * gamma + k - 1;
   if (MODE == MODE_SAMPLE) {
-    // winner's logit: base + W1[x_{k-1}] . W2t[x_k]
-    float d = 0.f;
-    if (tok >= 0 && tok < V) {
-      const uint4 *er = reinterpret_cast<const uint4 *>(E + (size_t)i * r);
-      const uint4 *wr2 = reinterpret_cast<const uint4 *>(W2t + (size_t)tok * r);
-      for (int c = tid; c < r / 8; c += RP_THREADS) {
-        const uint4 a = er[c], b = wr2[c];
-        const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          d = fmaf(bf16_lo(av[t]), bf16_lo(bv[t]), d);
-          d = fmaf(bf16_hi(av[t]), bf16_hi(bv[t]), d);
-        }
+    int b = s_tok;
+    if (b < 0 || b * GUMBEL_BLOCK >= V) {  // no finite block score (non-finite logits)
+      if (tid == 0) dspark_set_status(DSPARK_ERR_TOKEN);
+      b = 0;
+    }
+    block_logits<RP_THREADS>(base + o * V, E + (size_t)i * r, W2t, b, V, r, s_logit);
+    if (warp == 0) {
+      for (int j = lane; j < GUMBEL_BLOCK; j += 32) s_score[j] = s_logit[j] * inv_tau;
+      __syncwarp();
+      int tok = block_pick(s_score, b, V, seed, (uint32_t)k, (uint32_t)i, RNG_DRAFT);
+      if (tok < 0) {
+        if (lane == 0) dspark_set_status(DSPARK_ERR_TOKEN);
+        tok = b * GUMBEL_BLOCK;
+      }
+      if (lane == 0) {
+        tokens[o] = tok;
+        if (lse_out) lse_out[o] = s_lse;
+        if (logp_out) logp_out[o] = s_logit[tok - b * GUMBEL_BLOCK] * inv_tau - s_lse;
+        s_tok = tok;
       }
     }
-    d = warp_sum(d);
-    if (lane == 0) sdot[warp] = d;
-    __syncthreads();
-    if (tid == 0) {
-      const size_t o = (size_t)i * gamma + k - 1;
-      const float bl = (tok >= 0 && tok < V) ? __bfloat162float(base[o * V + tok]) : 0.f;
-      float dsum = 0.f;
-      for (int w = 0; w < NW; ++w) dsum += sdot[w];
-      const float logit = bl + dsum;
-      if (logp_out) logp_out[o] = logit * inv_tau - s_lse;
-    }
-    __syncthreads();  // E is rewritten below
-  } else if (tid == 0 && logp_out) {
-    logp_out[(size_t)i * gamma + k - 1] = 0.f;
+    __syncthreads();  // s_tok is read and E is rewritten below
+  } else if (tid == 0) {
+    tokens[o] = s_tok;
+    if (lse_out) lse_out[o] = 0.f;
+    if (logp_out) logp_out[o] = 0.f;
   }
   if (k >= gamma) return;
-  if (tid == 0) gfloor[i] = -INFINITY;  // fresh shared floor for step k + 1
   int prev = s_tok;
   if (prev < 0 || prev >= V) {
     if (tid == 0) dspark_set_status(DSPARK_ERR_TOKEN);
@@ -210,7 +194,6 @@ __global__ void __launch_bounds__(RP_THREADS) reduce_prep(
 
 struct MarkovWs {
   float *zh;
-  float *gfloor;
   bf16 *E;
   RowPartial *part;
   size_t bytes;
@@ -221,8 +204,6 @@ MarkovWs markov_layout(const dspark_dims *d, char *base) {
   size_t off = 0;
   w.zh = (float *)(base + off);
   off = dspark_align_up(off + sizeof(float) * (size_t)d->R * d->gamma, 256);
-  w.gfloor = (float *)(base + off);
-  off = dspark_align_up(off + sizeof(float) * (size_t)d->R, 256);
   w.E = (bf16 *)(base + off);
   off = dspark_align_up(off + sizeof(bf16) * (size_t)d->R * d->r, 256);
   w.part = (RowPartial *)(base + off);
@@ -259,35 +240,31 @@ extern "C" int dspark_markov_draft(const dspark_dims *dims, const void *base_log
   const float inv_tau = tau > 0.f ? 1.f / tau : 1.f;
   step_prep<<<(R * 32 + 255) / 256, 256, 0, stream>>>(anchor, tokens, (const bf16 *)W1,
                                                      (const bf16 *)w_conf + d, ws.zh, T, ws.E,
-                                                     conf, ws.gfloor, R, G, V, r, 1);
+                                                     conf, R, G, V, r, 1);
   DSPARK_CHECK_LAUNCH();
   const bf16 *w_e = (const bf16 *)w_conf + d;
   for (int k = 1; k <= G; ++k) {
     int rc;
     if (tau > 0.f) {
-      const int n_tiles = logits_parts<MODE_SAMPLE>(V);
+      const int n_parts = logits_parts<MODE_SAMPLE>(V);
       EpiLogits<MODE_SAMPLE> epi{(const bf16 *)base_logits, nullptr, nullptr, nullptr, nullptr,
-                                 ws.part, ws.gfloor,
-                                 R, V, G, k, n_tiles, inv_tau, seed};
-      rc = gemm::launch<LogitsCfg<MODE_SAMPLE>::EPI_WARPS, LogitsCfg<MODE_SAMPLE>::BN>(ws.E, W2t, R, V, r, epi, stream);
+                                 ws.part, R, V, G, k, n_parts, inv_tau, seed};
+      rc = gemm::launch<LogitsCfg<MODE_SAMPLE>::EPI_WARPS, LogitsCfg<MODE_SAMPLE>::BN>(
+          ws.E, W2t, R, V, r, epi, stream);
       if (rc != DSPARK_OK) return rc;
-      reduce_prep<MODE_SAMPLE><<<R, RP_THREADS, 0, stream>>>(ws.part, n_tiles, G, V, r, k, tokens, lse_d,
-                                                      logp_d, (const bf16 *)W1, w_e, ws.zh, T,
-                                                      ws.E, conf, ws.gfloor,
-                                                      (const bf16 *)base_logits,
-                                                      (const bf16 *)W2t, inv_tau);
+      reduce_prep<MODE_SAMPLE><<<R, RP_THREADS, 0, stream>>>(
+          ws.part, n_parts, G, V, r, k, tokens, lse_d, logp_d, (const bf16 *)W1, w_e, ws.zh, T,
+          ws.E, conf, (const bf16 *)base_logits, (const bf16 *)W2t, inv_tau, seed);
     } else {
-      const int n_tiles = logits_parts<MODE_GREEDY>(V);
+      const int n_parts = logits_parts<MODE_GREEDY>(V);
       EpiLogits<MODE_GREEDY> epi{(const bf16 *)base_logits, nullptr, nullptr, nullptr, nullptr,
-                                 ws.part, ws.gfloor,
-                                 R, V, G, k, n_tiles, 1.f, seed};
-      rc = gemm::launch<LogitsCfg<MODE_GREEDY>::EPI_WARPS, LogitsCfg<MODE_GREEDY>::BN>(ws.E, W2t, R, V, r, epi, stream);
+                                 ws.part, R, V, G, k, n_parts, 1.f, seed};
+      rc = gemm::launch<LogitsCfg<MODE_GREEDY>::EPI_WARPS, LogitsCfg<MODE_GREEDY>::BN>(
+          ws.E, W2t, R, V, r, epi, stream);
       if (rc != DSPARK_OK) return rc;
-      reduce_prep<MODE_GREEDY><<<R, RP_THREADS, 0, stream>>>(ws.part, n_tiles, G, V, r, k, tokens, lse_d,
-                                                      logp_d, (const bf16 *)W1, w_e, ws.zh, T,
-                                                      ws.E, conf, ws.gfloor,
-                                                      (const bf16 *)base_logits,
-                                                      (const bf16 *)W2t, inv_tau);
+      reduce_prep<MODE_GREEDY><<<R, RP_THREADS, 0, stream>>>(
+          ws.part, n_parts, G, V, r, k, tokens, lse_d, logp_d, (const bf16 *)W1, w_e, ws.zh, T,
+          ws.E, conf, (const bf16 *)base_logits, (const bf16 *)W2t, inv_tau, seed);
     }
     DSPARK_CHECK_LAUNCH();
   }
@@ -311,7 +288,7 @@ int dspark_status_markov(int clear) {
 // plugin interface that passes only tensors, a serving loop that forbids
 // allocations after start-up).  The array is shared by every call: overlapping
 // calls race.  No field of the scratch needs to start at zero: the draft loop
-// writes every word it reads (the shared floor is reset before each step).
+// writes every word it reads.
 // ---------------------------------------------------------------------------
 static __device__ __align__(256) unsigned char g_markov_scratch[DSPARK_STATIC_SCRATCH_BYTES];
 

@@ -184,27 +184,29 @@ __global__ void verify_decide(const SegStat *__restrict__ stat, const bf16 *__re
   rows[i] = rr;
 }
 
-// E[slot] = W1[x_{j*-1}] of the slot's request; fresh shared floor per slot.
+// E[slot] = W1[x_{j*-1}] of the slot's request.
 __global__ void resample_gather(const ResampleRow *__restrict__ rows, const int *__restrict__ list,
                                 const int *__restrict__ count, const bf16 *__restrict__ W1,
-                                bf16 *__restrict__ E, float *__restrict__ gfloor, int r) {
+                                bf16 *__restrict__ E, int r) {
   const int slot = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (slot >= *count) return;
-  if (lane == 0) gfloor[slot] = -INFINITY;
   const ResampleRow rr = rows[list[slot]];
   uint4 *dst = reinterpret_cast<uint4 *>(E + (size_t)slot * r);
   const uint4 *src = reinterpret_cast<const uint4 *>(W1 + (size_t)rr.prev * r);
   for (int c = lane; c < r / 8; c += 32) dst[c] = src[c];
 }
 
-// Residual rows: combine the slice partials into the corrected token; a row
-// whose residual came out empty is handed to the plain target sample.  One CTA
-// of 256 threads per compacted row, eight partial loads in flight per thread.
-__global__ void __launch_bounds__(256) resample_reduce(ResampleRow *__restrict__ rows,
-                                                       const int *__restrict__ list,
-                                                       const int *__restrict__ count,
-                                                       const RowPartial *__restrict__ part,
-                                                       int n_parts, int32_t *__restrict__ bonus) {
+// Residual rows: the block scores of the slices pick a block of 64 ids; inside
+// it the residual q = max(0, p_t - p_d) is rebuilt (target row, base logits and
+// the Markov bias W1[x_{j*-1}] . W2t[v]) and the corrected token is drawn from
+// log q + Gumbel.  A row whose residual came out empty is handed to the plain
+// target sample.  One CTA of 256 threads per compacted row, eight partial
+// loads in flight per thread.
+__global__ void __launch_bounds__(256) resample_reduce(
+    ResampleRow *__restrict__ rows, const int *__restrict__ list, const int *__restrict__ count,
+    const RowPartial *__restrict__ part, int n_parts, const bf16 *__restrict__ base,
+    const bf16 *__restrict__ target, const bf16 *__restrict__ E, const bf16 *__restrict__ W2t,
+    int gamma, int V, int r, float inv_tau, uint64_t seed, int32_t *__restrict__ bonus) {
   const int slot = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (slot >= *count) return;
   float best = -INFINITY, d0 = 0.f, d1 = 0.f, d2 = 0.f;
@@ -229,108 +231,144 @@ __global__ void __launch_bounds__(256) resample_reduce(ResampleRow *__restrict__
       if (better(b[u], id[u], best, idx)) { best = b[u]; idx = id[u]; }
   }
   warp_merge(d0, d1, best, idx, d2);
-  __shared__ float sb[8];
-  __shared__ int si[8];
+  __shared__ float sb[8], s_logit[GUMBEL_BLOCK], s_score[GUMBEL_BLOCK];
+  __shared__ int si[8], s_blk;
   if (lane == 0) { sb[warp] = best; si[warp] = idx; }
   __syncthreads();
   if (warp == 0) {
     best = lane < 8 ? sb[lane] : -INFINITY;
     idx = lane < 8 ? si[lane] : 0x7fffffff;
     warp_merge(d0, d1, best, idx, d2);
+    if (lane == 0) s_blk = best > -INFINITY ? idx : -1;
+  }
+  __syncthreads();
+  const int req = list[slot];
+  const int b = s_blk;
+  if (b < 0 || b * GUMBEL_BLOCK >= V) {  // every block empty
+    if (tid == 0) rows[req].kind = KIND_FALLBACK;
+    return;
+  }
+  const ResampleRow rr = rows[req];
+  block_logits<256>(base + ((size_t)req * gamma + rr.pos - 1) * V, E + (size_t)slot * r, W2t, b,
+                    V, r, s_logit);
+  if (warp == 0) {
+    const bf16 *trow = target + ((size_t)req * (gamma + 1) + rr.pos - 1) * V;
+    for (int j = lane; j < GUMBEL_BLOCK; j += 32) {
+      const int v = b * GUMBEL_BLOCK + j;
+      float sc = -INFINITY;
+      if (v < V) {
+        const float pt = __expf(__bfloat162float(trow[v]) * inv_tau - rr.lse_t);
+        const float pd = __expf(s_logit[j] * inv_tau - rr.lse_d);
+        if (pt > pd) sc = __logf(pt - pd);
+      }
+      s_score[j] = sc;
+    }
+    __syncwarp();
+    const int tok = block_pick(s_score, b, V, seed, (uint32_t)rr.pos, (uint32_t)req, RNG_RESIDUAL);
     if (lane == 0) {
-      const int req = list[slot];
-      if (best > -INFINITY) bonus[req] = idx;
-      else rows[req].kind = KIND_FALLBACK;
+      if (tok >= 0) bonus[req] = tok;
+      else rows[req].kind = KIND_FALLBACK;  // the block's mass was rounding only
     }
   }
 }
 
 // Plain target samples: the bonus row l_r + 1 when every draft passed (stream
-// 3), or the rejected row when its residual was empty (stream 2).  Gumbel-max
-// over t / tau; one CTA of 512 threads per request.  Entries that cannot beat
-// the best score the warp has seen skip their logarithms
-// (1 - u >= e^{s - F + 0.01} implies s + g < F).
-__global__ void __launch_bounds__(512) bonus_row(const ResampleRow *__restrict__ rows,
-                                                 const bf16 *__restrict__ target,
-                                                 int32_t *__restrict__ bonus, int gamma, int V,
-                                                 float inv_tau, uint64_t seed) {
+// 3), or the rejected row when its residual was empty (stream 2), drawn from
+// softmax(t / tau) in two levels.  One CTA of 512 threads per request: pass 1
+// leaves log Z_b of every 64-id block in shared memory (eight lanes per block,
+// one 16-byte word each, four words in flight), pass 2 scores the blocks (one
+// Philox call per four blocks), pass 3 draws inside the best block.
+constexpr int BONUS_THREADS = 512;
+constexpr size_t BONUS_MAX_SMEM = 220 * 1024;  // log Z_b of up to 56320 blocks: V <= 3604480
+
+__global__ void __launch_bounds__(BONUS_THREADS) bonus_row(const ResampleRow *__restrict__ rows,
+                                                           const bf16 *__restrict__ target,
+                                                           int32_t *__restrict__ bonus, int gamma,
+                                                           int V, float inv_tau, uint64_t seed) {
+  extern __shared__ float s_lz[];  // [n_blocks]: log Z_b
+  constexpr float LOG2E = 1.4426950408889634f, LN2 = 0.6931471805599453f;
+  constexpr int GROUPS = BONUS_THREADS / 8, U = 4;
   const int i = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const ResampleRow rr = rows[i];
   if (rr.kind != KIND_BONUS && rr.kind != KIND_FALLBACK) return;
   const uint32_t stream = rr.kind == KIND_BONUS ? RNG_BONUS : RNG_RESIDUAL;
   const bf16 *trow = target + ((size_t)i * (gamma + 1) + rr.pos - 1) * V;
-  const PhiloxKeys keys(seed);
-  float best = -INFINITY, bs = 0.f, m = -INFINITY, s = 0.f;
-  int idx = 0x7fffffff;
-  // warp-uniform trip count: every lane reaches every shuffle; lanes past V are
-  // masked.  Each lane takes 8 entries (16 bytes, two Philox calls) per step
-  // and the next step's 16 bytes are in flight while the current ones are used.
-  constexpr int STEP = 16 * 256;  // 16 warps x 32 lanes x 8 entries
-  int base = warp * 256;
-  uint4 nq = make_uint4(0, 0, 0, 0);
-  if (base + lane * 8 < V) nq = __ldg(reinterpret_cast<const uint4 *>(trow + base + lane * 8));
-  for (; base < V; base += STEP) {
-    const int v0 = base + lane * 8;
-    const bool valid = v0 < V;  // V % 8 == 0: a valid group has all 8 entries
-    const uint4 q = nq;
-    if (base + STEP + lane * 8 < V)
-      nq = __ldg(reinterpret_cast<const uint4 *>(trow + base + STEP + lane * 8));
-    float tv[8];
-    uint32_t ws[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    {
-      const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+  const int nb = (V + GUMBEL_BLOCK - 1) / GUMBEL_BLOCK;
+  const int grp = tid >> 3, sub = tid & 7;
+  const float c2 = inv_tau * LOG2E;
+  // pass 1: the trip count depends on nb only, so every lane reaches every shuffle
+  for (int b0 = 0; b0 < nb; b0 += GROUPS * U) {
+    uint4 q[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int b = b0 + u * GROUPS + grp, v = b * GUMBEL_BLOCK + sub * 8;
+      q[u] = (b < nb && v < V) ? __ldg(reinterpret_cast<const uint4 *>(trow + v))
+                               : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int b = b0 + u * GROUPS + grp, v = b * GUMBEL_BLOCK + sub * 8;
+      const bool ok = b < nb && v < V;  // V % 8 == 0: a word is all inside or all past V
+      const uint32_t w[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+      float x[8];
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
-        tv[2 * t] = valid ? bf16_lo(qw[t]) * inv_tau : -INFINITY;
-        tv[2 * t + 1] = valid ? bf16_hi(qw[t]) * inv_tau : -INFINITY;
+        x[2 * t] = ok ? bf16_lo(w[t]) * c2 : -INFINITY;
+        x[2 * t + 1] = ok ? bf16_hi(w[t]) * c2 : -INFINITY;
       }
+      float mx = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])),
+                       fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      float sm = 0.f;
+      if (mx > -INFINITY) {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) sm += ex2_fast(x[t] - mx);
+      }
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
+      if (sub == 0 && b < nb) s_lz[b] = mx > -INFINITY ? (mx + __log2f(sm)) * LN2 : -INFINITY;
     }
-    if (valid) {
+  }
+  __syncthreads();
+  // pass 2: G_b = log Z_b + Gumbel(block id b, block stream)
+  float best = -INFINITY, d0 = 0.f, d1 = 0.f, d2 = 0.f;
+  int idx = 0x7fffffff;
+  for (int q4 = tid; q4 * 4 < nb; q4 += BONUS_THREADS) {
+    const uint4 w = rng_words4(seed, (uint32_t)q4, (uint32_t)rr.pos, (uint32_t)i,
+                               stream + RNG_BLOCK_OFFSET);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint4 w = keys(make_uint4((uint32_t)((v0 >> 2) + h), (uint32_t)rr.pos, (uint32_t)i,
-                                        stream));
-        ws[4 * h] = w.x; ws[4 * h + 1] = w.y; ws[4 * h + 2] = w.z; ws[4 * h + 3] = w.w;
-      }
-    }
-    const float F = warp_max(best);
-    if (valid) {
-      // group test first: with tmax the largest of the 8 scaled logits, every
-      // entry needs g > F - tmax; as an integer bound on the words (see the
-      // draft epilogue), then per entry
-      float tmax = fmaxf(fmaxf(fmaxf(tv[0], tv[1]), fmaxf(tv[2], tv[3])),
-                         fmaxf(fmaxf(tv[4], tv[5]), fmaxf(tv[6], tv[7])));
-      int w_thr = -1;
-      if (F > -INFINITY) {
-        const float X = __expf(fminf(tmax - F + 0.01f, 0.f)) * 8388608.f;
-        w_thr = X >= 8388607.f ? -1 : 8388607 - (int)ceilf(X);
-      }
-      uint32_t wmax = 0;
-#pragma unroll
-      for (int t = 0; t < 8; ++t) wmax = max(wmax, ws[t]);
-      if ((int)(wmax >> 9) > w_thr) {
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const bool cand = !(F > -INFINITY) ||
-                            (1.f - rng_uniform(ws[t])) < __expf(tv[t] - F + 0.01f);
-          if (cand) {
-            const float sc = tv[t] + rng_gumbel(ws[t]);
-            if (better(sc, v0 + t, best, idx)) { best = sc; idx = v0 + t; }
-          }
-        }
+    for (int t = 0; t < 4; ++t) {
+      const int b = 4 * q4 + t;
+      if (b < nb && s_lz[b] > -INFINITY) {
+        const float G = s_lz[b] + rng_gumbel(ws[t]);
+        if (better(G, b, best, idx)) { best = G; idx = b; }
       }
     }
   }
-  warp_merge(m, s, best, idx, bs);
-  __shared__ float sb[16];
-  __shared__ int si[16];
+  warp_merge(d0, d1, best, idx, d2);
+  __shared__ float sb[BONUS_THREADS / 32], s_score[GUMBEL_BLOCK];
+  __shared__ int si[BONUS_THREADS / 32];
   if (lane == 0) { sb[warp] = best; si[warp] = idx; }
   __syncthreads();
   if (warp == 0) {
-    best = lane < 16 ? sb[lane] : -INFINITY;
-    idx = lane < 16 ? si[lane] : 0x7fffffff;
-    warp_merge(m, s, best, idx, bs);
-    if (lane == 0) bonus[i] = idx;
+    best = lane < BONUS_THREADS / 32 ? sb[lane] : -INFINITY;
+    idx = lane < BONUS_THREADS / 32 ? si[lane] : 0x7fffffff;
+    warp_merge(d0, d1, best, idx, d2);
+    int b = idx;
+    if (!(best > -INFINITY) || b >= nb) {  // non-finite target row
+      if (lane == 0) dspark_set_status(DSPARK_ERR_TOKEN);
+      b = 0;
+    }
+    // pass 3: inside block b, t / tau + Gumbel(id, entry stream)
+    for (int j = lane; j < GUMBEL_BLOCK; j += 32) {
+      const int v = b * GUMBEL_BLOCK + j;
+      s_score[j] = v < V ? __bfloat162float(trow[v]) * inv_tau : -INFINITY;
+    }
+    __syncwarp();
+    const int tok = block_pick(s_score, b, V, seed, (uint32_t)rr.pos, (uint32_t)i, stream);
+    if (lane == 0) bonus[i] = tok >= 0 ? tok : b * GUMBEL_BLOCK;
   }
 }
 
@@ -339,7 +377,6 @@ struct VerifyWs {
   ResampleRow *rows;
   int *list;
   int *count;
-  float *gfloor;
   bf16 *E;
   RowPartial *part;
   size_t bytes;
@@ -356,8 +393,6 @@ VerifyWs verify_layout(const dspark_dims *d, char *base) {
   off = dspark_align_up(off + sizeof(int) * (size_t)d->R, 256);
   w.count = (int *)(base + off);
   off = dspark_align_up(off + sizeof(int), 256);
-  w.gfloor = (float *)(base + off);
-  off = dspark_align_up(off + sizeof(float) * (size_t)d->R, 256);
   w.E = (bf16 *)(base + off);
   off = dspark_align_up(off + sizeof(bf16) * (size_t)d->R * d->r, 256);
   w.part = (RowPartial *)(base + off);
@@ -403,6 +438,13 @@ extern "C" int dspark_verify(const dspark_dims *dims, const int32_t *anchor, con
     dspark_count_launches(2);
     return DSPARK_OK;
   }
+  // bonus_row keeps log Z_b of every sampler block in shared memory
+  const size_t lz_bytes = sizeof(float) * (size_t)((V + GUMBEL_BLOCK - 1) / GUMBEL_BLOCK);
+  if (lz_bytes > BONUS_MAX_SMEM) return DSPARK_ERR_TOO_LARGE;
+  if (lz_bytes > 48 * 1024 &&
+      cudaFuncSetAttribute(bonus_row, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)lz_bytes) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
   verify_rows<MODE_SAMPLE><<<rgrid, 256, 0, stream>>>(tgt, len, ws.stat, ws.count, G, V, inv_tau);
   DSPARK_CHECK_LAUNCH();
   verify_decide<MODE_SAMPLE><<<(R + 127) / 128, 128, 0, stream>>>(
@@ -410,17 +452,19 @@ extern "C" int dspark_verify(const dspark_dims *dims, const int32_t *anchor, con
       bonus, R, G, V, inv_tau, seed);
   DSPARK_CHECK_LAUNCH();
   resample_gather<<<(R * 32 + 255) / 256, 256, 0, stream>>>(ws.rows, ws.list, ws.count,
-                                                          (const bf16 *)W1, ws.E, ws.gfloor, r);
+                                                          (const bf16 *)W1, ws.E, r);
   DSPARK_CHECK_LAUNCH();
   const int n_parts = logits_parts<MODE_RESIDUAL>(V);
-  EpiLogits<MODE_RESIDUAL> epi{(const bf16 *)base_logits, tgt, ws.rows, ws.list, ws.count, ws.part,
-                               ws.gfloor, R, V, G, 0, n_parts, inv_tau, seed};
-  const int rc = gemm::launch<LogitsCfg<MODE_RESIDUAL>::EPI_WARPS, LogitsCfg<MODE_RESIDUAL>::BN>(ws.E, W2t, R, V, r, epi, stream,
-                                                                  ws.count);
+  EpiLogits<MODE_RESIDUAL> epi{(const bf16 *)base_logits, tgt, ws.rows, ws.list, ws.count,
+                               ws.part, R, V, G, 0, n_parts, inv_tau, seed};
+  const int rc = gemm::launch<LogitsCfg<MODE_RESIDUAL>::EPI_WARPS, LogitsCfg<MODE_RESIDUAL>::BN>(
+      ws.E, W2t, R, V, r, epi, stream, ws.count);
   if (rc != DSPARK_OK) return rc;
-  resample_reduce<<<R, 256, 0, stream>>>(ws.rows, ws.list, ws.count, ws.part, n_parts, bonus);
+  resample_reduce<<<R, 256, 0, stream>>>(ws.rows, ws.list, ws.count, ws.part, n_parts,
+                                         (const bf16 *)base_logits, tgt, ws.E,
+                                         (const bf16 *)W2t, G, V, r, inv_tau, seed, bonus);
   DSPARK_CHECK_LAUNCH();
-  bonus_row<<<R, 512, 0, stream>>>(ws.rows, tgt, bonus, G, V, inv_tau, seed);
+  bonus_row<<<R, BONUS_THREADS, lz_bytes, stream>>>(ws.rows, tgt, bonus, G, V, inv_tau, seed);
   DSPARK_CHECK_LAUNCH();
   dspark_count_launches(5);  // + the GEMM, counted by launch()
   return DSPARK_OK;

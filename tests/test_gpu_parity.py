@@ -104,7 +104,8 @@ def test_markov_draft_matches_oracle(shape, tau):
     rep = compare_draft(rnd.tokens, rnd.conf, rnd.lse_d if tau > 0 else None,
                         rnd.logp_d if tau > 0 else None, orc, tau)
     assert rep.compared >= shape[0]
-    assert rep.flagged <= max(2, rep.compared // 50)
+    # a sampled token is two decisions (block, then id), each with its tie band
+    assert rep.flagged <= max(2, rep.compared // (50 if tau == 0 else 25))
     assert dsp.dspark_device_status() == 0
 
 
