@@ -27,6 +27,23 @@ static inline int dspark_dims_ok(const dspark_dims *d) {
 
 static inline size_t dspark_align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Launch with the programmatic stream-serialisation attribute (see pdl_wait).
+template <class... KArgs, class... Args>
+static inline cudaError_t dspark_launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                                            size_t smem, cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---------------------------------------------------------------------------
 // device status word: one per translation unit, read by dspark_device_status
 // ---------------------------------------------------------------------------
@@ -168,6 +185,18 @@ __device__ __forceinline__ void warp_merge(float &m, float &s, float &best, int 
     lse_merge(m, s, m2, s2);
     if (better(b2, i2, best, idx)) { best = b2; idx = i2; bs = bs2; }
   }
+}
+
+// Programmatic dependent launch.  A kernel launched with the programmatic
+// stream-serialisation attribute may start while its predecessor in the stream
+// still runs; pdl_wait() returns once that predecessor has completed and its
+// memory is visible (immediately when there is no such predecessor), and
+// pdl_trigger() lets the successor's launch begin.  Every kernel of the library
+// triggers only after it is resident and never waits on its successor, so a
+// chain of them cannot deadlock.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // 2^x with the hardware approximation (flushes subnormal results to zero).

@@ -25,7 +25,7 @@ struct EpiStoreBF16 {
   static constexpr bool kRowAffine = false;
   static constexpr bool kStreamB = true;  // W_lm streams through once per launch
   __device__ void prefetch(int, int, int, int, int, State &) const {}
-  __device__ void operator()(int m0, int n0, int row, uint32_t taddr, int c0, int c1,
+  __device__ void operator()(int m0, int n0, int row, uint32_t taddr, int c0, int c1, int, int,
                              State &) const {
     const int m = m0 + row;
     bf16 *dst_row = C + (size_t)m * N;

@@ -113,13 +113,15 @@ struct EpiLogits {
   static constexpr int SLICE = LogitsCfg<MODE>::SLICE;
   static constexpr int CH = LogitsCfg<MODE>::CH;
   static constexpr int CHUNKS = SLICE / 32;                       // greedy: 32-column loads
-  static constexpr int BUF = MODE == MODE_GREEDY ? SLICE / 8 : CH / 8;
+  // base-logit words prefetched per thread: the whole slice (greedy, sampling)
+  // or the first chunk (residual, whose rows are known only inside the tile)
+  static constexpr int BUF = MODE == MODE_RESIDUAL ? CH / 8 : SLICE / 8;
   static_assert(MODE == MODE_GREEDY || SLICE == GUMBEL_BLOCK,
                 "a sampling slice is exactly one sampler block");
 
   // Kept by each epilogue thread across the tiles it processes.
   struct State {
-    uint4 buf[BUF];  // base logits prefetched before the accumulator is ready
+    uint4 buf[BUF];  // base logits of the tile to process next, loaded ahead
   };
 
   __device__ __forceinline__ bool draft_row(int m0, int row, const bf16 *&brow) const {
@@ -128,21 +130,29 @@ struct EpiLogits {
     return i < M;
   }
 
+  // First tile: the whole slice, issued before the accumulator is ready.  Later
+  // tiles: each chunk's words are reloaded for the next tile as soon as the
+  // current tile has taken them (load_words inside operator()), so the loads
+  // have a whole tile of work to land.
   __device__ void prefetch(int m0, int n0, int row, int c0, int, State &st) const {
     if (MODE == MODE_RESIDUAL) return;
-    const bf16 *brow;
-    if (!draft_row(m0, row, brow)) return;
-    const int n = n0 + c0;
-    // greedy: the whole slice, so the epilogue never waits on HBM; sampling:
-    // the first chunk, later chunks are loaded one ahead
+    const bf16 *brow = nullptr;
+    if (!draft_row(m0, row, brow)) brow = nullptr;
+    load_words<BUF>(brow, n0 + c0, st.buf);
+  }
+
+  // NW 16-byte words of row `src` from column n; zeros past V or without a row.
+  template <int NW>
+  __device__ __forceinline__ void load_words(const bf16 *src, int n, uint4 *dst) const {
 #pragma unroll
-    for (int q = 0; q < BUF; ++q)
-      st.buf[q] = (n + q * 8 + 8 <= V) ? __ldg(reinterpret_cast<const uint4 *>(brow + n + q * 8))
-                                       : make_uint4(0, 0, 0, 0);
+    for (int q = 0; q < NW; ++q)
+      dst[q] = (src && n + q * 8 + 8 <= V)
+                   ? __ldg(reinterpret_cast<const uint4 *>(src + n + q * 8))
+                   : make_uint4(0, 0, 0, 0);
   }
 
   __device__ void operator()(int m0, int n0, int row, uint32_t taddr, int c0, int c1,
-                             State &st) const {
+                             int next_m0, int next_n0, State &st) const {
     constexpr float LOG2E = 1.4426950408889634f, LN2 = 0.6931471805599453f;
     const int i = m0 + row;
     bool active = i < M;
@@ -165,8 +175,14 @@ struct EpiLogits {
     } else {
       draft_row(m0, row, brow);
     }
+    // the base-logit row of this thread in the CTA's next tile (none: zeros)
+    const bf16 *nrow = nullptr;
+    if (MODE != MODE_RESIDUAL && next_m0 >= 0 && next_m0 + row < M)
+      nrow = base + (size_t)((next_m0 + row) * gamma + k - 1) * V;
+    const int nn = next_n0 + c0;
 
     float m2 = -INFINITY, s = 0.f, best = -INFINITY;
+    float z[4] = {0.f, 0.f, 0.f, 0.f};  // residual mass of the block (four partial sums)
     int idx = 0x7fffffff;
 
     if (MODE == MODE_GREEDY) {
@@ -177,9 +193,10 @@ struct EpiLogits {
         tc::tmem_ld32(taddr + (uint32_t)c, acc);
         tc::tmem_wait_ld();
         const int n = n0 + c;
+        const uint4 w4[4] = {st.buf[cc * 4], st.buf[cc * 4 + 1], st.buf[cc * 4 + 2],
+                             st.buf[cc * 4 + 3]};
+        load_words<4>(nrow, nn + cc * 32, st.buf + cc * 4);
         if (active && n < V) {
-          const uint4 w4[4] = {st.buf[cc * 4], st.buf[cc * 4 + 1], st.buf[cc * 4 + 2],
-                               st.buf[cc * 4 + 3]};
           float sv[32];
           unpack32(w4, n, V, sv);
           // four interleaved argmax chains (entries j = 4 q + p), merged with
@@ -200,14 +217,58 @@ struct EpiLogits {
           idx = pi[0];
         }
       }
-    } else {
-      const float c2 = inv_tau * LOG2E;  // scaled logits in log2 units
+    } else if (MODE == MODE_SAMPLE) {
+      // y = base + bias (unscaled); online log-sum-exp of y / tau in base 2
+      const float c2 = inv_tau * LOG2E;  // log2(e) / tau > 0
       constexpr int NQ = CH / 8;         // 16-byte words per chunk
-      uint4 nxt[NQ];
+      constexpr int NCH = SLICE / CH;
+      // TMEM loads one chunk ahead: chunk cc + 1 is in flight while cc is used
+      uint32_t accs[2][CH];
+      tc::tmem_ld<CH>(taddr + (uint32_t)c0, accs[0]);
 #pragma unroll
-      for (int q = 0; q < NQ; ++q) nxt[q] = st.buf[q];
-      if (MODE == MODE_RESIDUAL && active) load_raw<CH>(brow, n0 + c0, V, nxt);
-      float z[4] = {0.f, 0.f, 0.f, 0.f};  // residual mass of the block (four partial sums)
+      for (int cc = 0; cc < NCH; ++cc) {
+        const int c = c0 + cc * CH;
+        tc::tmem_wait_ld();
+        tc::reg_fence<CH>(accs[cc & 1]);
+        if (cc + 1 < NCH) tc::tmem_ld<CH>(taddr + (uint32_t)(c + CH), accs[(cc + 1) & 1]);
+        const uint32_t(&acc)[CH] = accs[cc & 1];
+        const int n = n0 + c;
+        uint4 cur[NQ];
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) cur[q] = st.buf[cc * NQ + q];
+        load_words<NQ>(nrow, nn + cc * CH, st.buf + cc * NQ);
+        if (active && n < V) {
+          float y[CH];
+          unpack<CH>(cur, n, V, y);
+#pragma unroll
+          for (int j = 0; j < CH; ++j) y[j] += __uint_as_float(acc[j]);
+          float mx[CH / 2];
+#pragma unroll
+          for (int j = 0; j < CH / 2; ++j) mx[j] = fmaxf(y[j], y[j + CH / 2]);
+#pragma unroll
+          for (int w = CH / 4; w >= 1; w >>= 1)
+#pragma unroll
+            for (int j = 0; j < w; ++j) mx[j] = fmaxf(mx[j], mx[j + w]);
+          const float cmax2 = mx[0] * c2;
+          if (cmax2 > m2) {
+            s *= ex2_fast(m2 - cmax2);
+            m2 = cmax2;
+          }
+          const float nm2 = -m2;
+          float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int j = 0; j < CH; ++j) ps[j & 3] += ex2_fast(fmaf(y[j], c2, nm2));
+          s += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        }
+      }
+    } else {
+      // residual mass sum_v max(0, p_t(v) - p_d(v)) at the rejected row; ids
+      // past V read -inf on both sides and add nothing
+      const float c2 = inv_tau * LOG2E;
+      constexpr int NQ = CH / 8;
+      uint4 nxt[NQ];
+      if (active) load_raw<CH>(brow, n0 + c0, V, nxt);
+      const float nt = -lse_t * LOG2E, nd = -lse_d * LOG2E;
 #pragma unroll 1
       for (int c = c0; c < c1; c += CH) {
         uint32_t acc[CH];
@@ -219,47 +280,21 @@ struct EpiLogits {
 #pragma unroll
           for (int q = 0; q < NQ; ++q) cur[q] = nxt[q];
           if (c + CH < c1) load_raw<CH>(brow, n + CH, V, nxt);  // prefetch the next chunk
-          float sv[CH];
+          uint4 tw[NQ];
+          load_raw<CH>(trow, n, V, tw);
+          float sv[CH], tv[CH];
           unpack<CH>(cur, n, V, sv);
-          if (MODE == MODE_SAMPLE) {
-            // y = base + bias (unscaled); online log-sum-exp of y / tau in base 2
-            float y[CH];
+          unpack<CH>(tw, n, V, tv);
 #pragma unroll
-            for (int j = 0; j < CH; ++j) y[j] = sv[j] + __uint_as_float(acc[j]);
-            float mx[CH / 2];
-#pragma unroll
-            for (int j = 0; j < CH / 2; ++j) mx[j] = fmaxf(y[j], y[j + CH / 2]);
-#pragma unroll
-            for (int w = CH / 4; w >= 1; w >>= 1)
-#pragma unroll
-              for (int j = 0; j < w; ++j) mx[j] = fmaxf(mx[j], mx[j + w]);
-            const float cmax2 = mx[0] * c2;  // c2 = log2(e) / tau > 0
-            if (cmax2 > m2) {
-              s *= ex2_fast(m2 - cmax2);
-              m2 = cmax2;
-            }
-            const float nm2 = -m2;
-            float ps[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int j = 0; j < CH; ++j) ps[j & 3] += ex2_fast(fmaf(y[j], c2, nm2));
-            s += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-          } else {
-            // residual mass sum_v max(0, p_t(v) - p_d(v)) at the rejected row;
-            // ids past V read -inf on both sides and add nothing
-            uint4 tw[NQ];
-            load_raw<CH>(trow, n, V, tw);
-            float tv[CH];
-            unpack<CH>(tw, n, V, tv);
-            const float nt = -lse_t * LOG2E, nd = -lse_d * LOG2E;
-#pragma unroll
-            for (int j = 0; j < CH; ++j) {
-              const float pt = ex2_fast(fmaf(tv[j], c2, nt));
-              const float pd = ex2_fast(fmaf(sv[j] + __uint_as_float(acc[j]), c2, nd));
-              z[j & 3] += fmaxf(pt - pd, 0.f);
-            }
+          for (int j = 0; j < CH; ++j) {
+            const float pt = ex2_fast(fmaf(tv[j], c2, nt));
+            const float pd = ex2_fast(fmaf(sv[j] + __uint_as_float(acc[j]), c2, nd));
+            z[j & 3] += fmaxf(pt - pd, 0.f);
           }
         }
       }
+    }
+    if (MODE != MODE_GREEDY) {
       // first level of the draw: the block score of this slice
       if (active && n0 + c0 < V) {
         const int b = (n0 + c0) / GUMBEL_BLOCK;
@@ -295,8 +330,8 @@ struct EpiLogits {
 // out[j] = base_row[v] + E . W2t[v] for v = b * GUMBEL_BLOCK + j, and -inf past
 // V: the block's logits rebuilt from the Markov bias (E = W1[x_{k-1}]).  Every
 // thread of a CTA of NT threads calls it; each warp takes GUMBEL_BLOCK / (NT/32)
-// ids and keeps all their W2t words of one pass in flight.  Ends with a
-// __syncthreads().
+// ids, and a lane has the W2t words of two passes (r = 512: all of its words)
+// in flight at once.  Ends with a __syncthreads().
 template <int NT>
 __device__ void block_logits(const bf16 *__restrict__ base_row, const bf16 *__restrict__ E,
                              const bf16 *__restrict__ W2t, int b, int V, int r,
@@ -310,15 +345,29 @@ __device__ void block_logits(const bf16 *__restrict__ base_row, const bf16 *__re
   float acc[PER];
 #pragma unroll
   for (int u = 0; u < PER; ++u) acc[u] = 0.f;
-  for (int c = lane; c < r8; c += 32) {
+  int c = lane;
+  for (; c + 32 < r8; c += 64) {
+    const uint4 a0 = e4[c], a1 = e4[c + 32];
+    uint4 w0[PER], w1[PER];
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const uint4 *rowp = reinterpret_cast<const uint4 *>(W2t + (size_t)(v0 + u) * r);
+      const bool ok = v0 + u < V;
+      w0[u] = ok ? __ldg(rowp + c) : make_uint4(0, 0, 0, 0);
+      w1[u] = ok ? __ldg(rowp + c + 32) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < PER; ++u) acc[u] = dot8_bf16(a1, w1[u], dot8_bf16(a0, w0[u], acc[u]));
+  }
+  for (; c < r8; c += 32) {  // r / 8 not a multiple of 64: one pass left
     const uint4 a = e4[c];
-    uint4 w[PER];
 #pragma unroll
-    for (int u = 0; u < PER; ++u)
-      w[u] = (v0 + u < V) ? __ldg(reinterpret_cast<const uint4 *>(W2t + (size_t)(v0 + u) * r) + c)
+    for (int u = 0; u < PER; ++u) {
+      const uint4 w = (v0 + u < V)
+                          ? __ldg(reinterpret_cast<const uint4 *>(W2t + (size_t)(v0 + u) * r) + c)
                           : make_uint4(0, 0, 0, 0);
-#pragma unroll
-    for (int u = 0; u < PER; ++u) acc[u] = dot8_bf16(a, w[u], acc[u]);
+      acc[u] = dot8_bf16(a, w, acc[u]);
+    }
   }
 #pragma unroll
   for (int u = 0; u < PER; ++u) acc[u] = warp_sum(acc[u]);

@@ -95,6 +95,8 @@ __global__ void __launch_bounds__(RP_THREADS) reduce_prep(
     const float *__restrict__ T, bf16 *__restrict__ E, float *__restrict__ conf,
     const bf16 *__restrict__ base, const bf16 *__restrict__ W2t, float inv_tau, uint64_t seed) {
   const int i = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_trigger();
+  pdl_wait();  // the vocabulary pass of step k has completed
   float m = -INFINITY, s = 0.f, best = -INFINITY, bs = 0.f;
   int idx = 0x7fffffff;
   const RowPartial *pr = part + (size_t)i * n_parts;
@@ -250,21 +252,27 @@ extern "C" int dspark_markov_draft(const dspark_dims *dims, const void *base_log
       EpiLogits<MODE_SAMPLE> epi{(const bf16 *)base_logits, nullptr, nullptr, nullptr, nullptr,
                                  ws.part, R, V, G, k, n_parts, inv_tau, seed};
       rc = gemm::launch<LogitsCfg<MODE_SAMPLE>::EPI_WARPS, LogitsCfg<MODE_SAMPLE>::BN>(
-          ws.E, W2t, R, V, r, epi, stream);
+          ws.E, W2t, R, V, r, epi, stream, nullptr, true);
       if (rc != DSPARK_OK) return rc;
-      reduce_prep<MODE_SAMPLE><<<R, RP_THREADS, 0, stream>>>(
-          ws.part, n_parts, G, V, r, k, tokens, lse_d, logp_d, (const bf16 *)W1, w_e, ws.zh, T,
-          ws.E, conf, (const bf16 *)base_logits, (const bf16 *)W2t, inv_tau, seed);
+      if (dspark_launch_pdl(reduce_prep<MODE_SAMPLE>, dim3(R), dim3(RP_THREADS), 0, stream,
+                            ws.part, n_parts, G, V, r, k, tokens, lse_d, logp_d,
+                            (const bf16 *)W1, w_e, ws.zh, T, ws.E, conf,
+                            (const bf16 *)base_logits, (const bf16 *)W2t, inv_tau,
+                            seed) != cudaSuccess)
+        return DSPARK_ERR_CUDA;
     } else {
       const int n_parts = logits_parts<MODE_GREEDY>(V);
       EpiLogits<MODE_GREEDY> epi{(const bf16 *)base_logits, nullptr, nullptr, nullptr, nullptr,
                                  ws.part, R, V, G, k, n_parts, 1.f, seed};
       rc = gemm::launch<LogitsCfg<MODE_GREEDY>::EPI_WARPS, LogitsCfg<MODE_GREEDY>::BN>(
-          ws.E, W2t, R, V, r, epi, stream);
+          ws.E, W2t, R, V, r, epi, stream, nullptr, true);
       if (rc != DSPARK_OK) return rc;
-      reduce_prep<MODE_GREEDY><<<R, RP_THREADS, 0, stream>>>(
-          ws.part, n_parts, G, V, r, k, tokens, lse_d, logp_d, (const bf16 *)W1, w_e, ws.zh, T,
-          ws.E, conf, (const bf16 *)base_logits, (const bf16 *)W2t, inv_tau, seed);
+      if (dspark_launch_pdl(reduce_prep<MODE_GREEDY>, dim3(R), dim3(RP_THREADS), 0, stream,
+                            ws.part, n_parts, G, V, r, k, tokens, lse_d, logp_d,
+                            (const bf16 *)W1, w_e, ws.zh, T, ws.E, conf,
+                            (const bf16 *)base_logits, (const bf16 *)W2t, inv_tau,
+                            seed) != cudaSuccess)
+        return DSPARK_ERR_CUDA;
     }
     DSPARK_CHECK_LAUNCH();
   }

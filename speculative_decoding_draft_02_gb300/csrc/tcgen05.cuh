@@ -52,6 +52,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// The same test, letting the thread sleep until the phase completes or up to
+// SUSPEND_HINT_NS pass, so a waiting role takes no issue slots from the others.
+constexpr uint32_t SUSPEND_HINT_NS = 20000;
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "n"(SUSPEND_HINT_NS)
+      : "memory");
+  return ok != 0;
+}
 
 // Wait for the phase of `parity` to complete.  Gives up after WAIT_LIMIT_NS or
 // when another role of the CTA has raised `abort`; returns false then.
@@ -59,8 +72,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63) == 0) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if ((it & 15) == 0) {
       if (*abort) return false;
       if (globaltimer() - t0 > WAIT_LIMIT_NS) {
         *abort = 1;
@@ -175,6 +188,15 @@ __device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[N]) {
   else tmem_ld16(taddr, r);
 }
 
+// After tmem_wait_ld: ties the registers of an earlier tmem_ld to the wait, so
+// no use of them is scheduled above it.
+template <int N>
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
+#pragma unroll
+  for (int j = 0; j < N; j += 8)
+    asm volatile("" : "+r"(r[j]), "+r"(r[j + 1]), "+r"(r[j + 2]), "+r"(r[j + 3]), "+r"(r[j + 4]),
+                 "+r"(r[j + 5]), "+r"(r[j + 6]), "+r"(r[j + 7]));
+}
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }

@@ -59,11 +59,14 @@ struct SharedCtl {
 //   static constexpr bool kRowAffine;     keep each thread on one row when possible
 //   static constexpr bool kStreamB;       B is read once: evict its tiles from L2 first
 //   __device__ void prefetch(int m0, int n0, int row, int c0, int c1, State &) const
-//       (called before the tile's accumulator is ready: start global loads)
+//       (called once, for the CTA's first tile, before its accumulator is
+//        ready: start global loads)
 //   __device__ void operator()(int m0, int n0, int row, uint32_t taddr, int c0, int c1,
-//                              State &) const
+//                              int next_m0, int next_n0, State &) const
 //       (every epilogue thread, once per tile, for its row and column slice
-//        [c0, c1); tcgen05.ld of each 32-column chunk must be warp-uniform)
+//        [c0, c1); tcgen05.ld of each 32-column chunk must be warp-uniform;
+//        next_m0 / next_n0 locate the CTA's next tile, -1 after the last, so
+//        the loads for it can start while this one is processed)
 //   __device__ void on_timeout() const.
 // PAIR: CTAs run as clusters of two over two M blocks of the same N tile; each
 // loads its own A tile and half of the B tile, multicast to both, so the B
@@ -87,23 +90,6 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
   volatile int *abort = &ctl->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (m_dev) {  // rows counted on the device by an earlier kernel (at most M)
-    const int md = *m_dev;
-    M = md < M ? (md > 0 ? md : 0) : M;
-  }
-  const int num_m = (M + BM - 1) / BM, num_n = (N + BN - 1) / BN;
-  const int k_iters = K / BK;
-  // tile sequence: t -> (m block, n block), m fastest; a pair walks pairs of M blocks
-  const uint32_t rank = PAIR ? tc::cluster_ctarank() : 0u;
-  const int num_mp = PAIR ? (num_m + 1) / 2 : num_m;
-  const int num_tiles = num_mp * num_n;
-  const int first = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-  const int stride = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
-  auto coords = [&](int t, int &m_blk, int &n_blk) {
-    const int mp = t % num_mp;
-    n_blk = t / num_mp;
-    m_blk = PAIR ? 2 * mp + (int)rank : mp;
-  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -126,6 +112,29 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
   if (PAIR) tc::cluster_sync();  // the peer's barriers exist before any multicast
   tc::fence_after_sync();
   const uint32_t tmem_base = ctl->tmem_base;
+  // everything above overlaps the previous kernel of the stream; A, the row
+  // count, the epilogue's inputs and its outputs belong to the kernels around
+  // this one
+  pdl_trigger();
+  pdl_wait();
+
+  if (m_dev) {  // rows counted on the device by an earlier kernel (at most M)
+    const int md = *m_dev;
+    M = md < M ? (md > 0 ? md : 0) : M;
+  }
+  const int num_m = (M + BM - 1) / BM, num_n = (N + BN - 1) / BN;
+  const int k_iters = K / BK;
+  // tile sequence: t -> (m block, n block), m fastest; a pair walks pairs of M blocks
+  const uint32_t rank = PAIR ? tc::cluster_ctarank() : 0u;
+  const int num_mp = PAIR ? (num_m + 1) / 2 : num_m;
+  const int num_tiles = num_mp * num_n;
+  const int first = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int stride = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  auto coords = [&](int t, int &m_blk, int &n_blk) {
+    const int mp = t % num_mp;
+    n_blk = t / num_mp;
+    m_blk = PAIR ? 2 * mp + (int)rank : mp;
+  };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -214,10 +223,20 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     typename Epi::State st;
+    if (first < num_tiles) {
+      int m_blk, n_blk;
+      coords(first, m_blk, n_blk);
+      epi.prefetch(m_blk * BM, n_blk * BN, row, c0, c0 + SLICE, st);
+    }
     for (int tile = first; tile < num_tiles; tile += stride) {
       int m_blk, n_blk;
       coords(tile, m_blk, n_blk);
-      epi.prefetch(m_blk * BM, n_blk * BN, row, c0, c0 + SLICE, st);
+      int next_m0 = -1, next_n0 = -1;
+      if (tile + stride < num_tiles) {
+        coords(tile + stride, next_m0, next_n0);
+        next_m0 *= BM;
+        next_n0 *= BN;
+      }
       // one lane polls, then the warp proceeds together (tcgen05.ld is warp-wide)
       int ok = 1;
       if (lane == 0) ok = tc::mbar_wait(&ctl->tfull[acc], acc_phase, abort) ? 1 : 0;
@@ -225,7 +244,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
       if (!ok) break;
       tc::fence_after_sync();
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
-      epi(m_blk * BM, n_blk * BN, row, taddr, c0, c0 + SLICE, st);
+      epi(m_blk * BM, n_blk * BN, row, taddr, c0, c0 + SLICE, next_m0, next_n0, st);
       tc::fence_before_sync();
       tc::mbar_arrive(&ctl->tempty[acc]);
       acc ^= 1;
@@ -249,7 +268,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
 // share B tiles by multicast (see umma_gemm_kernel).
 template <int EPI_WARPS, int BN_ = 256, bool PAIR = false, class Epi>
 int launch(const void *A, const void *B, int M, int N, int K, const Epi &epi,
-           cudaStream_t stream, const int *m_dev = nullptr) {
+           cudaStream_t stream, const int *m_dev = nullptr, bool pdl = false) {
   using G = Geo<BN_>;
   constexpr int BN = G::BN;
   static_assert(EPI_WARPS % 4 == 0 && EPI_WARPS >= 4 && EPI_WARPS <= 16 &&
@@ -263,16 +282,16 @@ int launch(const void *A, const void *B, int M, int N, int K, const Epi &epi,
   static bool attr = false;
   static int max_clusters = 0;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute cluster_attr;
-  cluster_attr.id = cudaLaunchAttributeClusterDimension;
-  cluster_attr.val.clusterDim.x = 2;
-  cluster_attr.val.clusterDim.y = 1;
-  cluster_attr.val.clusterDim.z = 1;
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = 2;
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
   cfg.blockDim = dim3(64 + 32 * EPI_WARPS);
   cfg.dynamicSmemBytes = G::SMEM_BYTES;
   cfg.stream = stream;
   if (PAIR) {
-    cfg.attrs = &cluster_attr;
+    cfg.attrs = attrs;
     cfg.numAttrs = 1;
   }
   if (!attr) {
@@ -300,6 +319,12 @@ int launch(const void *A, const void *B, int M, int N, int K, const Epi &epi,
     if (Epi::kRowAffine && grid > num_m) grid = grid / num_m * num_m;
   }
   cfg.gridDim = dim3(grid);
+  if (pdl) {  // may start while the previous kernel of the stream finishes
+    attrs[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attrs;
+    cfg.numAttrs += 1;
+  }
   if (cudaLaunchKernelEx(&cfg, kernel, ta, tb, M, N, K, m_dev, epi) != cudaSuccess)
     return DSPARK_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
