@@ -78,7 +78,9 @@ enum {
 enum {
   DSPARK_SCHED_UNCONSTRAINED = 0, /* K = argmax_K Theta(K) over every budget        */
   DSPARK_SCHED_BREAK = 1,         /* admit in sorted order while Theta increases    */
-  DSPARK_SCHED_FIXED_K = 2        /* admit the top min(k_fixed, R*gamma) candidates */
+  DSPARK_SCHED_FIXED_K = 2,       /* admit the top min(k_fixed, R*gamma) candidates */
+  DSPARK_SCHED_ASYNC = 3          /* dspark_schedule_async only: top-K with K from the
+                                     unconstrained search of two rounds earlier      */
 };
 
 /* a1 — base draft logits, "DSpark 深度解读" §二 (parallel backbone -> base logits
@@ -154,6 +156,24 @@ int dspark_schedule(const float *conf, int32_t R, int32_t gamma, const float *sp
                     int32_t n_sps, int32_t mode, int32_t k_fixed, int32_t *len,
                     int32_t *K_out, double *theta_out, float *a_out, int32_t *order_out,
                     dspark_stream_t stream);
+
+/* a5-a7, asynchronous form — "DSpark 深度解读" §三 挑战1 (Zero-Overhead
+ * Scheduling): round t-2's confidences predict round t's capacity K; round t
+ * sorts its own candidates by their actual survival products and admits the
+ * top K.  Admission is then fixed before round t's tokens exist, so it stays
+ * lossless, and every round launches with the same arguments (CUDA graphs).
+ *   k_ring int32 [3] device state, read and written by the call:
+ *          {K slot 0, K slot 1, cursor}.  The call admits K_t = k_ring[cursor]
+ *          (clamped to [0, R*gamma]), then stores this round's unconstrained
+ *          argmax_K Theta(K) in that slot and flips the cursor (0 <-> 1).
+ *          Initialise it to {K for round 0, K for round 1, 0}.
+ *   K_out  int32 [1]  out: the admitted K_t;  theta_out f64 [1]: Theta(K_t).
+ * Every other argument is that of dspark_schedule.  Calls sharing a ring must
+ * run in stream order. */
+int dspark_schedule_async(const float *conf, int32_t R, int32_t gamma, const float *sps,
+                          int32_t n_sps, int32_t *k_ring, int32_t *len, int32_t *K_out,
+                          double *theta_out, float *a_out, int32_t *order_out,
+                          dspark_stream_t stream);
 
 /* Workspace bytes dspark_verify needs for `dims`. */
 size_t dspark_verify_workspace_bytes(const dspark_dims *dims);

@@ -344,6 +344,31 @@ def schedule(conf, sps, mode: int = UNCONSTRAINED, k_fixed: int = 0) -> Dict[str
     return dict(len=lens, K=K, theta=float(th[K]), thetas=th, a=a, order=order)
 
 
+def schedule_async(conf_rounds, sps, k_round0: int, k_round1: int) -> Dict[str, np.ndarray]:
+    """Asynchronous admission over consecutive rounds  [DD §三 挑战1].
+
+    Round t-2 produces confidences and predicts round t's capacity: the
+    unconstrained optimum K*_{t-2} = argmax_K Theta(K) of its own candidates.
+    Round t sorts its candidates by their actual survival products and admits
+    the top K*_{t-2} (rounds 0 and 1 admit k_round0 and k_round1).  Returns,
+    per round, len [T, R], the admitted K_used [T], the prediction K_pred [T]
+    it hands to round t + 2, and Theta(K_used) [T].
+    """
+    pending = [int(k_round0), int(k_round1)]
+    lens, used, pred, theta = [], [], [], []
+    for t, conf in enumerate(conf_rounds):
+        k_t = pending[t % 2]                          # predicted two rounds ago
+        now = schedule(conf, sps, FIXED_K, k_t)       # top-K on this round's products
+        best = schedule(conf, sps, UNCONSTRAINED)     # this round's optimum, for t + 2
+        pending[t % 2] = best["K"]
+        lens.append(now["len"])
+        used.append(now["K"])
+        pred.append(best["K"])
+        theta.append(now["theta"])
+    return dict(len=np.array(lens), K_used=np.array(used), K_pred=np.array(pred),
+                theta=np.array(theta))
+
+
 def theta_of_lengths(a: np.ndarray, lens, sps) -> float:
     """Theta for an explicit allocation: B = sum(1 + l_r), tau = sum(1 + sum_{j<=l_r} a_{r,j})."""
     sps = to_f64(sps)

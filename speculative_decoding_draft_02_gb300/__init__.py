@@ -23,12 +23,13 @@ DSPARK_OK = 0
 SCHED_UNCONSTRAINED = 0
 SCHED_BREAK = 1
 SCHED_FIXED_K = 2
+SCHED_ASYNC = 3
 
 EXPORTS = [
     "dspark_lm_head", "dspark_pack_w2", "dspark_markov_workspace_bytes", "dspark_markov_draft",
     "dspark_draft", "dspark_schedule", "dspark_verify_workspace_bytes", "dspark_verify",
     "dspark_device_status", "dspark_error_string", "dspark_launch_count",
-    "dspark_markov_draft_static",
+    "dspark_markov_draft_static", "dspark_schedule_async",
 ]
 STATIC_SCRATCH_BYTES = 16 << 20
 
@@ -66,6 +67,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "dspark_draft": (ctypes.c_int, [DP, P, P, P, P, P, P, P, F32, U64, P, P, P, P, P, P, SZ,
                                         P]),
         "dspark_schedule": (ctypes.c_int, [P, I32, I32, P, I32, I32, I32, P, P, P, P, P, P]),
+        "dspark_schedule_async": (ctypes.c_int, [P, I32, I32, P, I32, P, P, P, P, P, P, P]),
         "dspark_verify_workspace_bytes": (SZ, [DP]),
         "dspark_verify": (ctypes.c_int, [DP, P, P, P, P, P, P, P, P, P, F32, U64, P, P, P, SZ,
                                          P]),
@@ -170,6 +172,19 @@ def dspark_schedule(conf, R, gamma, sps, mode, k_fixed, length, K_out, theta_out
         _stream(stream)), "dspark_schedule")
 
 
+def dspark_schedule_async(conf, R, gamma, sps, k_ring, length, K_out, theta_out, a_out=None,
+                          order_out=None, stream=None):
+    _check(load_library().dspark_schedule_async(
+        _ptr(conf), int(R), int(gamma), _ptr(sps), int(sps.numel()), _ptr(k_ring), _ptr(length),
+        _ptr(K_out), _ptr(theta_out), _ptr(a_out), _ptr(order_out), _stream(stream)),
+        "dspark_schedule_async")
+
+
+def async_ring(k_round0: int, k_round1: int, device="cuda") -> torch.Tensor:
+    """The device state of dspark_schedule_async: {K for round 0, K for round 1, cursor 0}."""
+    return torch.tensor([int(k_round0), int(k_round1), 0], dtype=torch.int32, device=device)
+
+
 def dspark_verify(dims, anchor, tokens, length, base_logits, W1, W2t, lse_d, logp_d, target, tau,
                   seed, accepted, bonus, workspace, stream=None):
     _check(load_library().dspark_verify(
@@ -250,8 +265,15 @@ class Round:
                      self.base, self.tokens, self.conf, self.logp_d, self.lse_d, self.ws_draft,
                      stream)
 
-    def schedule(self, sps, mode=SCHED_UNCONSTRAINED, k_fixed=0, stream=None):
+    def schedule(self, sps, mode=SCHED_UNCONSTRAINED, k_fixed=0, stream=None, k_ring=None):
+        """mode SCHED_ASYNC takes the device ring of async_ring() and ignores k_fixed."""
         d = self.head.dims
+        if mode == SCHED_ASYNC:
+            if k_ring is None:
+                raise DSparkError("SCHED_ASYNC needs k_ring (see async_ring)")
+            dspark_schedule_async(self.conf, d.R, d.gamma, sps, k_ring, self.len, self.K,
+                                  self.theta, stream=stream)
+            return
         dspark_schedule(self.conf, d.R, d.gamma, sps, mode, k_fixed, self.len, self.K, self.theta,
                         stream=stream)
 
@@ -262,21 +284,21 @@ class Round:
                       self.ws_verify, stream)
 
     def run(self, h, anchor, target, sps, tau, draft_seed, verify_seed,
-            mode=SCHED_UNCONSTRAINED, k_fixed=0, stream=None):
+            mode=SCHED_UNCONSTRAINED, k_fixed=0, stream=None, k_ring=None):
         """One whole round on device-resident inputs: draft -> schedule -> verify."""
         self.draft(h, anchor, tau, draft_seed, stream)
-        self.schedule(sps, mode, k_fixed, stream)
+        self.schedule(sps, mode, k_fixed, stream, k_ring)
         self.verify(anchor, target, tau, verify_seed, stream)
 
     def run_host(self, h_host, anchor_host, target_host, sps, tau, draft_seed, verify_seed,
                  dev_in: Dict[str, torch.Tensor], out_host: Dict[str, torch.Tensor],
-                 mode=SCHED_UNCONSTRAINED, k_fixed=0, stream=None) -> None:
+                 mode=SCHED_UNCONSTRAINED, k_fixed=0, stream=None, k_ring=None) -> None:
         """One round from pinned host inputs to pinned host outputs (copies included)."""
         dev_in["h"].copy_(h_host, non_blocking=True)
         dev_in["anchor"].copy_(anchor_host, non_blocking=True)
         dev_in["target"].copy_(target_host, non_blocking=True)
         self.run(dev_in["h"], dev_in["anchor"], dev_in["target"], sps, tau, draft_seed,
-                 verify_seed, mode, k_fixed, stream)
+                 verify_seed, mode, k_fixed, stream, k_ring)
         out_host["tokens"].copy_(self.tokens, non_blocking=True)
         out_host["len"].copy_(self.len, non_blocking=True)
         out_host["accepted"].copy_(self.accepted, non_blocking=True)

@@ -7,7 +7,9 @@
 // throughput Theta = tau * SPS(B).  The theoretical greedy admission stops at
 // the first K where Theta stops increasing (non-anticipating); §三 挑战2 drops
 // that break and searches every budget because measured SPS(B) curves are
-// stair-stepped; §三 挑战1 admits a capacity K fixed ahead of time (top-K).
+// stair-stepped; §三 挑战1 admits a capacity K fixed ahead of time (top-K), in
+// production the capacity that the unconstrained search found two rounds
+// earlier (asynchronous mode, a two-slot ring of predictions on the device).
 //
 // One CTA of 1024 threads: f32 survival products, a bitonic sort of composite
 // keys (~bits(a) << 32 | id) so that ties go to the lower (request, position),
@@ -28,7 +30,8 @@ __device__ __forceinline__ double theta_at(long K, double S, int R, const float 
 __global__ void __launch_bounds__(SCHED_THREADS) schedule_kernel(
     const float *__restrict__ conf, int R, int gamma, const float *__restrict__ sps, int mode,
     int k_fixed, int n_pad, int32_t *__restrict__ len, int32_t *__restrict__ K_out,
-    double *__restrict__ theta_out, float *__restrict__ a_out, int32_t *__restrict__ order_out) {
+    double *__restrict__ theta_out, float *__restrict__ a_out, int32_t *__restrict__ order_out,
+    int32_t *__restrict__ k_ring) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   unsigned long long *keys = reinterpret_cast<unsigned long long *>(smem_raw);
   int32_t *cnt = reinterpret_cast<int32_t *>(keys + n_pad);  // [R]
@@ -125,7 +128,7 @@ __global__ void __launch_bounds__(SCHED_THREADS) schedule_kernel(
   }
 
   long K = 0;
-  if (mode == DSPARK_SCHED_UNCONSTRAINED) {
+  if (mode == DSPARK_SCHED_UNCONSTRAINED || mode == DSPARK_SCHED_ASYNC) {
     // argmax Theta, ties to the smallest K
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
@@ -167,6 +170,18 @@ __global__ void __launch_bounds__(SCHED_THREADS) schedule_kernel(
     if (tid == 0) s_K = k_fixed < 0 ? 0 : (k_fixed > n ? n : k_fixed);
   }
   __syncthreads();
+  if (mode == DSPARK_SCHED_ASYNC) {
+    // admit the capacity predicted two rounds ago; this round's optimum s_K is
+    // the prediction for round t + 2 and takes its slot
+    if (tid == 0) {
+      const int c = k_ring[2] & 1;
+      const long use = k_ring[c];
+      k_ring[c] = (int32_t)s_K;
+      k_ring[2] = c ^ 1;
+      s_K = use < 0 ? 0 : (use > n ? n : use);
+    }
+    __syncthreads();
+  }
   K = s_K;
   if (K < 0 || K > n) K = 0;  // unreachable for finite tables; keeps every index in range
 
@@ -196,13 +211,13 @@ __global__ void __launch_bounds__(SCHED_THREADS) schedule_kernel(
 
 }  // namespace
 
-extern "C" int dspark_schedule(const float *conf, int32_t R, int32_t gamma, const float *sps,
-                               int32_t n_sps, int32_t mode, int32_t k_fixed, int32_t *len,
-                               int32_t *K_out, double *theta_out, float *a_out,
-                               int32_t *order_out, dspark_stream_t stream) {
+namespace {
+int launch_schedule(const float *conf, int32_t R, int32_t gamma, const float *sps, int32_t n_sps,
+                    int32_t mode, int32_t k_fixed, int32_t *len, int32_t *K_out,
+                    double *theta_out, float *a_out, int32_t *order_out, int32_t *k_ring,
+                    cudaStream_t stream) {
   if (!conf || !sps || !len || !K_out || !theta_out || R < 1 || gamma < 1 || gamma > 32)
     return DSPARK_ERR_ARG;
-  if (mode < DSPARK_SCHED_UNCONSTRAINED || mode > DSPARK_SCHED_FIXED_K) return DSPARK_ERR_ARG;
   const long n = (long)R * gamma;
   if (n > SCHED_MAX) return DSPARK_ERR_ARG;
   if ((long)n_sps < (long)R * (gamma + 1)) return DSPARK_ERR_SPS_SHORT;
@@ -218,10 +233,30 @@ extern "C" int dspark_schedule(const float *conf, int32_t R, int32_t gamma, cons
     attr_set = true;
   }
   schedule_kernel<<<1, SCHED_THREADS, smem, stream>>>(conf, R, gamma, sps, mode, k_fixed, n_pad,
-                                                      len, K_out, theta_out, a_out, order_out);
+                                                      len, K_out, theta_out, a_out, order_out,
+                                                      k_ring);
   DSPARK_CHECK_LAUNCH();
   dspark_count_launches(1);
   return DSPARK_OK;
+}
+}  // namespace
+
+extern "C" int dspark_schedule(const float *conf, int32_t R, int32_t gamma, const float *sps,
+                               int32_t n_sps, int32_t mode, int32_t k_fixed, int32_t *len,
+                               int32_t *K_out, double *theta_out, float *a_out,
+                               int32_t *order_out, dspark_stream_t stream) {
+  if (mode < DSPARK_SCHED_UNCONSTRAINED || mode > DSPARK_SCHED_FIXED_K) return DSPARK_ERR_ARG;
+  return launch_schedule(conf, R, gamma, sps, n_sps, mode, k_fixed, len, K_out, theta_out, a_out,
+                         order_out, nullptr, stream);
+}
+
+extern "C" int dspark_schedule_async(const float *conf, int32_t R, int32_t gamma,
+                                     const float *sps, int32_t n_sps, int32_t *k_ring,
+                                     int32_t *len, int32_t *K_out, double *theta_out,
+                                     float *a_out, int32_t *order_out, dspark_stream_t stream) {
+  if (!k_ring) return DSPARK_ERR_ARG;
+  return launch_schedule(conf, R, gamma, sps, n_sps, DSPARK_SCHED_ASYNC, 0, len, K_out, theta_out,
+                         a_out, order_out, k_ring, stream);
 }
 
 int dspark_status_sched(int clear) {

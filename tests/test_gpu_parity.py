@@ -165,6 +165,40 @@ def test_schedule_matches_oracle(R, G, mode):
         assert float(th.item()) == pytest.approx(o["thetas"][k_gpu], rel=1e-12)
 
 
+@pytest.mark.parametrize("R,G,kind", [(37, 4, "stair"), (64, 8, "concave"), (256, 5, "stair"),
+                                        (1024, 7, "stair")])
+def test_schedule_async_matches_oracle(R, G, kind):
+    """Six rounds through one device ring: each round's admitted K is the
+    optimum found two rounds earlier, its lengths the top-K of its own products."""
+    T = 6
+    rounds = [workloads.random_confidences(R, G, seed=1000 * R + 17 * t, ones_frac=0.02)
+              for t in range(T)]
+    sps = sps_for(kind, R * (G + 1))
+    k0, k1 = (R * G) // 4, (R * G) // 2
+    o = oracle.schedule_async(rounds, sps, k0, k1)
+    ring = dsp.async_ring(k0, k1)
+    length = torch.empty(R, dtype=torch.int32, device="cuda")
+    K = torch.empty(1, dtype=torch.int32, device="cuda")
+    th = torch.empty(1, dtype=torch.float64, device="cuda")
+    for t, c in enumerate(rounds):
+        before = host(ring).copy()
+        dsp.dspark_schedule_async(dev(c), R, G, dev(sps), ring, length, K, th)
+        after = host(ring)
+        k_used = int(K.item())
+        assert k_used == before[before[2] & 1]                 # the slot at the cursor
+        assert after[2] == (before[2] ^ 1)                      # cursor flipped
+        assert after[1 - (before[2] & 1)] == before[1 - (before[2] & 1)]
+        assert k_used == o["K_used"][t]
+        assert np.array_equal(host(length), o["len"][t])        # top-K: exact integers
+        assert float(th.item()) == pytest.approx(o["theta"][t], rel=1e-12)
+        k_pred = int(after[before[2] & 1])
+        if k_pred != o["K_pred"][t]:  # only a floating tie of Theta may separate them
+            ts = oracle.schedule(c, sps)["thetas"]
+            assert abs(ts[k_pred] - ts[o["K_pred"][t]]) <= 1e-12 * ts[o["K_pred"][t]]
+            return  # later rounds would follow a different (equally good) prediction
+    assert dsp.dspark_device_status() == 0
+
+
 def test_schedule_extremes():
     R, G = 50, 4
     c = workloads.random_confidences(R, G, seed=5)

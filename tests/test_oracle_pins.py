@@ -271,6 +271,58 @@ def test_unconstrained_theta_is_bruteforce_optimum(R, G):
             assert s["len"].sum() == s["K"]
 
 
+def _bruteforce_best_theta(a, sps):
+    """max over every allocation l in {0..G}^R of Theta(l), by enumeration."""
+    R, G = a.shape
+    best = -np.inf
+    for lens in itertools.product(range(G + 1), repeat=R):
+        B = sum(1 + l for l in lens)
+        tau = sum(1.0 + float(np.sum(a[r, :l], dtype=np.float64)) for r, l in enumerate(lens))
+        best = max(best, tau * float(sps[B - 1]))
+    return best
+
+
+def test_async_schedule_uses_the_prediction_of_two_rounds_back():
+    """Round t admits the top K*_{t-2} by its own survival products; K*_t is the
+    budget maximising Theta on round t alone."""
+    rng = np.random.default_rng(21)
+    R, G, T = 5, 3, 7
+    sps = _sps_tables(R * (G + 1))["stair"].astype(np.float32)
+    rounds = [(0.05 + 0.95 * rng.random((R, G))).astype(np.float32) for _ in range(T)]
+    out = oracle.schedule_async(rounds, sps, 4, 9)
+    assert out["K_used"][0] == 4 and out["K_used"][1] == 9
+    for t in range(2, T):
+        assert out["K_used"][t] == out["K_pred"][t - 2]
+    for t, c in enumerate(rounds):
+        a = oracle.survival(c)
+        lens = out["len"][t]
+        assert lens.sum() == out["K_used"][t]
+        # the admitted set is the top-K of this round's products (prefix-closed per request)
+        flat = a.reshape(-1).astype(np.float64)
+        admitted = np.zeros(R * G, bool)
+        for r in range(R):
+            admitted[r * G:r * G + lens[r]] = True
+        if admitted.any() and (~admitted).any():
+            assert flat[admitted].min() >= flat[~admitted].max()
+        # the prediction is that round's Theta optimum (brute force over allocations)
+        best = _bruteforce_best_theta(a, sps)
+        K_p = out["K_pred"][t]
+        th_p = oracle.schedule(c, sps, oracle.FIXED_K, K_p)["theta"]
+        assert th_p == pytest.approx(best, rel=1e-12)
+
+
+def test_async_schedule_with_steady_confidences_reaches_the_optimum():
+    rng = np.random.default_rng(22)
+    R, G = 4, 3
+    c = (0.05 + 0.95 * rng.random((R, G))).astype(np.float32)
+    sps = _sps_tables(R * (G + 1))["concave"].astype(np.float32)
+    out = oracle.schedule_async([c] * 5, sps, 0, R * G)
+    best = _bruteforce_best_theta(oracle.survival(c), sps)
+    assert out["theta"][0] <= best * (1 + 1e-12)       # any budget is at most the optimum
+    for t in range(2, 5):
+        assert out["theta"][t] == pytest.approx(best, rel=1e-12)
+
+
 def test_admitted_set_is_prefix_closed_and_top_k():
     rng = np.random.default_rng(7)
     c = (0.05 + 0.95 * rng.random((20, 5))).astype(np.float32)
@@ -407,6 +459,7 @@ def _markov_target_rounds(mode, V=6, G=3, N=30000, L=3, seed=0, block=2):
     start = 2
     anchor = np.full(N, start)
     emitted = [[] for _ in range(N)]
+    pending = [N * G // 3, N * G // 2]   # async mode: the first two rounds' capacities
     rnd = 0
     while min(len(e) for e in emitted) < L:
         base = np.broadcast_to(base0, (N, G, V)).copy()
@@ -424,6 +477,11 @@ def _markov_target_rounds(mode, V=6, G=3, N=30000, L=3, seed=0, block=2):
         elif mode == "fixed_k":
             lens = oracle.schedule(dr["conf"].astype(np.float32), sps, oracle.FIXED_K,
                                    N * G // 2)["len"]
+        elif mode == "async":
+            # capacity predicted two rounds earlier, top-K on this round's products
+            c32 = dr["conf"].astype(np.float32)
+            lens = oracle.schedule(c32, sps, oracle.FIXED_K, pending[rnd % 2])["len"]
+            pending[rnd % 2] = oracle.schedule(c32, sps, oracle.UNCONSTRAINED)["K"]
         res = oracle.verify(x, lens, dr["logits"], target, 1.0, seed=5000 + rnd, block=block)
         for i in range(N):
             n = res["accepted"][i]
@@ -442,7 +500,7 @@ def _markov_target_rounds(mode, V=6, G=3, N=30000, L=3, seed=0, block=2):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("mode", ["full", "random", "break", "fixed_k"])
+@pytest.mark.parametrize("mode", ["full", "random", "break", "fixed_k", "async"])
 def test_draft_schedule_verify_is_lossless(mode):
     """Chi-square: emitted tokens follow the target chain in non-anticipating modes."""
     V, L = 6, 3
