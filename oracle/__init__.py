@@ -10,5 +10,5 @@ from . import philox  # noqa: F401
 from .dspark import (  # noqa: F401
     BREAK, FIXED_K, UNCONSTRAINED, base_logits, confidence_label, draft_round,
     global_order, markov_draft, round_bf16, schedule, schedule_async, survival,
-    theta_curve, theta_of_lengths, verify,
+    expected_calibration_error, sts_fit, theta_curve, theta_of_lengths, verify,
 )

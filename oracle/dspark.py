@@ -369,6 +369,55 @@ def schedule_async(conf_rounds, sps, k_round0: int, k_round1: int) -> Dict[str, 
                 theta=np.array(theta))
 
 
+# ---------------------------------------------------------------------------
+# Sequential Temperature Scaling fit   [DD §二 设计二 STS 校准; DD stage summary]
+# ---------------------------------------------------------------------------
+
+def expected_calibration_error(prob, label, n_bins: int) -> float:
+    """ECE with n_bins equal-width bins over [0, 1]:
+    sum over bins of |B_b| / N * |mean(label in B_b) - mean(prob in B_b)|,
+    i.e. sum_b |sum_{B_b} label - sum_{B_b} prob| / N.  A value of prob falls in
+    bin min(floor(prob * n_bins), n_bins - 1), decided in float32."""
+    p32 = np.asarray(prob, dtype=np.float32)
+    b = np.minimum((p32 * np.float32(n_bins)).astype(np.int64), n_bins - 1)
+    diff = np.zeros(n_bins)
+    np.add.at(diff, b, np.asarray(label, dtype=np.float64) - p32.astype(np.float64))
+    return float(np.sum(np.abs(diff)) / p32.size)
+
+
+def sts_fit(z, accepted, T_grid, n_bins: int) -> Dict[str, np.ndarray]:
+    """Per-position temperatures fitted left to right on held-out rounds.
+
+    z [N, gamma] confidence logits w^T [h_j; W1[x_{j-1}]] (before the
+    temperature); accepted [N] drafts accepted when all gamma were verified.
+    Position j calibrates the prefix survival a_j = a_{j-1} * sigmoid(z_j / T)
+    (float32, left to right, as the scheduler takes it) against the label
+    "positions 1..j all accepted": every T of T_grid is tried with T_1..T_{j-1}
+    already fixed, and the one of least ECE is kept (ties: the earliest in the
+    grid).  Returns T [gamma] and ece [gamma] (the ECE at the chosen T).
+    """
+    z32 = np.asarray(z, dtype=np.float32)
+    acc = np.asarray(accepted, dtype=np.int64)
+    grid = np.asarray(T_grid, dtype=np.float32)
+    N, G = z32.shape
+    a_prev = np.ones(N, dtype=np.float32)
+    T_out = np.zeros(G, dtype=np.float32)
+    ece_out = np.zeros(G)
+    for j in range(G):
+        label = (acc >= j + 1).astype(np.float64)
+        best_e, best_g, best_a = np.inf, 0, None
+        for g, T in enumerate(grid):
+            c = np.float32(1.0) / (np.float32(1.0) + np.exp(-(z32[:, j] / T)))
+            a = a_prev * c if j else c
+            e = expected_calibration_error(a, label, n_bins)
+            if e < best_e:
+                best_e, best_g, best_a = e, g, a
+        T_out[j] = grid[best_g]
+        ece_out[j] = best_e
+        a_prev = best_a
+    return dict(T=T_out, ece=ece_out)
+
+
 def theta_of_lengths(a: np.ndarray, lens, sps) -> float:
     """Theta for an explicit allocation: B = sum(1 + l_r), tau = sum(1 + sum_{j<=l_r} a_{r,j})."""
     sps = to_f64(sps)

@@ -323,6 +323,52 @@ def test_async_schedule_with_steady_confidences_reaches_the_optimum():
         assert out["theta"][t] == pytest.approx(best, rel=1e-12)
 
 
+def test_ece_hand_worked_values():
+    # one sample per bin: |0-0.05| + |0-0.15| + |1-0.95| + |1-0.85| over 4
+    assert oracle.expected_calibration_error([0.05, 0.15, 0.95, 0.85], [0, 0, 1, 1], 10) == \
+        pytest.approx(0.1, abs=1e-7)
+    # one bin holding all three: |1 - (0.31 + 0.33 + 0.35)| / 3
+    assert oracle.expected_calibration_error([0.31, 0.33, 0.35], [1, 0, 0], 10) == \
+        pytest.approx(0.01 / 3, abs=1e-7)
+    # 1.0 lands in the last bin, 0.0 in the first; perfectly calibrated extremes
+    assert oracle.expected_calibration_error([1.0, 0.0], [1, 0], 15) == 0.0
+
+
+def _planted_sts_data(T_star, N, seed):
+    """Confidence logits and accepted counts drawn from a model whose prefix
+    survival is exactly prod_j sigmoid(z_j / T*_j)."""
+    rng = np.random.default_rng(seed)
+    G = len(T_star)
+    z = rng.normal(1.2, 2.0, (N, G)).astype(np.float32)
+    p = 1.0 / (1.0 + np.exp(-z.astype(np.float64) / np.asarray(T_star)))
+    ok = rng.random((N, G)) < p
+    accepted = np.where(ok.all(axis=1), G, np.argmin(ok, axis=1))
+    return z, accepted
+
+
+def test_sts_recovers_planted_temperatures():
+    T_star = [1.4, 0.7, 2.2, 1.0]
+    z, accepted = _planted_sts_data(T_star, 200_000, 31)
+    grid = np.linspace(0.5, 3.0, 51)
+    fit = oracle.sts_fit(z, accepted, grid, 15)
+    assert np.all(np.abs(fit["T"] - np.asarray(T_star)) <= 0.15), fit["T"]
+    assert np.all(fit["ece"] < 0.01)
+    # calibrating each conditional c_j against the prefix label (a plausible slip)
+    # would pick far colder temperatures from position 2 on
+    label2 = accepted >= 2
+    c2 = 1.0 / (1.0 + np.exp(-z[:, 1].astype(np.float64) / fit["T"][1]))
+    assert oracle.expected_calibration_error(c2, label2, 15) > 5 * fit["ece"][1]
+
+
+def test_sts_is_equivariant_to_logit_scale():
+    z, accepted = _planted_sts_data([1.1, 1.7, 0.9], 20_000, 32)
+    grid = np.linspace(0.5, 3.0, 26)
+    a = oracle.sts_fit(z, accepted, grid, 10)
+    b = oracle.sts_fit(z * 2, accepted, grid * 2, 10)  # z/T unchanged, exactly in float32
+    assert np.array_equal(b["T"], a["T"] * 2)
+    assert np.array_equal(b["ece"], a["ece"])
+
+
 def test_admitted_set_is_prefix_closed_and_top_k():
     rng = np.random.default_rng(7)
     c = (0.05 + 0.95 * rng.random((20, 5))).astype(np.float32)
