@@ -175,6 +175,37 @@ int dspark_schedule_async(const float *conf, int32_t R, int32_t gamma, const flo
                           double *theta_out, float *a_out, int32_t *order_out,
                           dspark_stream_t stream);
 
+/* Confidence logits before the temperature, for calibration:
+ *   z[r, j] = w_h . h[r, j] + w_e . W1[x_{j-1}]   (x_0 = anchor; w_conf = [w_h; w_e])
+ * "DSpark 深度解读" §二 设计二 Confidence Head.  h, anchor, tokens, W1, w_conf as
+ * in dspark_markov_draft (tokens: that call's output); z f32 [R, gamma] out. */
+int dspark_conf_logits(const dspark_dims *dims, const void *h, const int32_t *anchor,
+                       const int32_t *tokens, const void *W1, const void *w_conf, float *z,
+                       dspark_stream_t stream);
+
+/* Workspace bytes dspark_sts_fit needs (0 when the sizes are invalid). */
+size_t dspark_sts_workspace_bytes(int32_t N, int32_t gamma, int32_t n_grid, int32_t n_bins);
+
+/* Sequential Temperature Scaling, "DSpark 深度解读" §二 设计二 (STS 校准): the
+ * per-position temperatures T_j, fitted left to right on N held-out rounds.
+ * For j = 1..gamma, every T of T_grid is scored by the expected calibration
+ * error of the prefix survival a_j = a_{j-1} * sigmoid(z_j / T) (f32, left to
+ * right, T_1..T_{j-1} already fixed) against the label accepted >= j:
+ *   ECE = sum over n_bins equal-width bins b of |sum_{n in b}(label_n - a_n)| / N,
+ *   bin of a = min(floor(a * n_bins), n_bins - 1) in f32,
+ * and the least (the first on ties) is kept.
+ *   z        f32 [N, gamma]   logits from dspark_conf_logits
+ *   accepted int32 [N]        drafts accepted by dspark_verify with len = gamma
+ *   T_grid   f32 [n_grid]     candidate temperatures (> 0; device memory)
+ *   n_bins   1..64
+ *   T_out    f32 [gamma] out;  ece_out f64 [gamma] out: ECE at the chosen T_j
+ *   workspace device buffer of dspark_sts_workspace_bytes(...) bytes, 256-byte
+ *            aligned.  A grid value <= 0 sets DSPARK_ERR_ARG in the status word. */
+int dspark_sts_fit(const float *z, const int32_t *accepted, int32_t N, int32_t gamma,
+                   const float *T_grid, int32_t n_grid, int32_t n_bins, float *T_out,
+                   double *ece_out, void *workspace, size_t workspace_bytes,
+                   dspark_stream_t stream);
+
 /* Workspace bytes dspark_verify needs for `dims`. */
 size_t dspark_verify_workspace_bytes(const dspark_dims *dims);
 

@@ -394,7 +394,8 @@ def sts_fit(z, accepted, T_grid, n_bins: int) -> Dict[str, np.ndarray]:
     (float32, left to right, as the scheduler takes it) against the label
     "positions 1..j all accepted": every T of T_grid is tried with T_1..T_{j-1}
     already fixed, and the one of least ECE is kept (ties: the earliest in the
-    grid).  Returns T [gamma] and ece [gamma] (the ECE at the chosen T).
+    grid).  Returns T [gamma], ece [gamma] (the ECE at the chosen T) and
+    ece_grid [gamma, n_grid] (every candidate's ECE).
     """
     z32 = np.asarray(z, dtype=np.float32)
     acc = np.asarray(accepted, dtype=np.int64)
@@ -403,6 +404,7 @@ def sts_fit(z, accepted, T_grid, n_bins: int) -> Dict[str, np.ndarray]:
     a_prev = np.ones(N, dtype=np.float32)
     T_out = np.zeros(G, dtype=np.float32)
     ece_out = np.zeros(G)
+    ece_grid = np.zeros((G, grid.size))
     for j in range(G):
         label = (acc >= j + 1).astype(np.float64)
         best_e, best_g, best_a = np.inf, 0, None
@@ -410,12 +412,13 @@ def sts_fit(z, accepted, T_grid, n_bins: int) -> Dict[str, np.ndarray]:
             c = np.float32(1.0) / (np.float32(1.0) + np.exp(-(z32[:, j] / T)))
             a = a_prev * c if j else c
             e = expected_calibration_error(a, label, n_bins)
+            ece_grid[j, g] = e
             if e < best_e:
                 best_e, best_g, best_a = e, g, a
         T_out[j] = grid[best_g]
         ece_out[j] = best_e
         a_prev = best_a
-    return dict(T=T_out, ece=ece_out)
+    return dict(T=T_out, ece=ece_out, ece_grid=ece_grid)
 
 
 def theta_of_lengths(a: np.ndarray, lens, sps) -> float:

@@ -29,7 +29,8 @@ EXPORTS = [
     "dspark_lm_head", "dspark_pack_w2", "dspark_markov_workspace_bytes", "dspark_markov_draft",
     "dspark_draft", "dspark_schedule", "dspark_verify_workspace_bytes", "dspark_verify",
     "dspark_device_status", "dspark_error_string", "dspark_launch_count",
-    "dspark_markov_draft_static", "dspark_schedule_async",
+    "dspark_markov_draft_static", "dspark_schedule_async", "dspark_conf_logits",
+    "dspark_sts_workspace_bytes", "dspark_sts_fit",
 ]
 STATIC_SCRATCH_BYTES = 16 << 20
 
@@ -68,6 +69,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                         P]),
         "dspark_schedule": (ctypes.c_int, [P, I32, I32, P, I32, I32, I32, P, P, P, P, P, P]),
         "dspark_schedule_async": (ctypes.c_int, [P, I32, I32, P, I32, P, P, P, P, P, P, P]),
+        "dspark_conf_logits": (ctypes.c_int, [DP, P, P, P, P, P, P, P]),
+        "dspark_sts_workspace_bytes": (SZ, [I32, I32, I32, I32]),
+        "dspark_sts_fit": (ctypes.c_int, [P, P, I32, I32, P, I32, I32, P, P, P, SZ, P]),
         "dspark_verify_workspace_bytes": (SZ, [DP]),
         "dspark_verify": (ctypes.c_int, [DP, P, P, P, P, P, P, P, P, P, F32, U64, P, P, P, SZ,
                                          P]),
@@ -178,6 +182,27 @@ def dspark_schedule_async(conf, R, gamma, sps, k_ring, length, K_out, theta_out,
         _ptr(conf), int(R), int(gamma), _ptr(sps), int(sps.numel()), _ptr(k_ring), _ptr(length),
         _ptr(K_out), _ptr(theta_out), _ptr(a_out), _ptr(order_out), _stream(stream)),
         "dspark_schedule_async")
+
+
+def dspark_conf_logits(dims, h, anchor, tokens, W1, w_conf, z, stream=None):
+    _check(load_library().dspark_conf_logits(
+        ctypes.byref(dims), _ptr(h), _ptr(anchor), _ptr(tokens), _ptr(W1), _ptr(w_conf), _ptr(z),
+        _stream(stream)), "dspark_conf_logits")
+
+
+def dspark_sts_fit(z, accepted, T_grid, n_bins, T_out, ece_out, workspace=None, stream=None):
+    """Fit the per-position temperatures (see include/dspark.h); allocates the
+    workspace when none is given."""
+    N, G = z.shape
+    need = load_library().dspark_sts_workspace_bytes(N, G, T_grid.numel(), int(n_bins))
+    if need == 0:
+        raise DSparkError("dspark_sts_fit: invalid sizes")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=z.device)
+    _check(load_library().dspark_sts_fit(
+        _ptr(z), _ptr(accepted), int(N), int(G), _ptr(T_grid), int(T_grid.numel()), int(n_bins),
+        _ptr(T_out), _ptr(ece_out), _ptr(workspace), workspace.numel(), _stream(stream)),
+        "dspark_sts_fit")
 
 
 def async_ring(k_round0: int, k_round1: int, device="cuda") -> torch.Tensor:

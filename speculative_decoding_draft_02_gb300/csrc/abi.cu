@@ -13,6 +13,7 @@ int dspark_status_lmhead(int clear);
 int dspark_status_markov(int clear);
 int dspark_status_verify(int clear);
 int dspark_status_sched(int clear);
+int dspark_status_sts(int clear);
 
 extern "C" uint64_t dspark_launch_count(void) { return g_launches.load(); }
 
@@ -34,8 +35,9 @@ extern "C" const char *dspark_error_string(int code) {
 extern "C" int dspark_device_status(dspark_stream_t stream, int clear) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return DSPARK_ERR_CUDA;
   int first = DSPARK_OK;
-  const int vals[4] = {dspark_status_lmhead(clear), dspark_status_markov(clear),
-                       dspark_status_verify(clear), dspark_status_sched(clear)};
+  const int vals[5] = {dspark_status_lmhead(clear), dspark_status_markov(clear),
+                       dspark_status_verify(clear), dspark_status_sched(clear),
+                       dspark_status_sts(clear)};
   for (int v : vals)
     if (first == DSPARK_OK && v != DSPARK_OK) first = v;
   return first;

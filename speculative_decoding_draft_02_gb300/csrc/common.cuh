@@ -13,6 +13,7 @@ typedef __nv_bfloat16 bf16;
 // host-side plumbing shared by every translation unit (defined in abi.cu)
 // ---------------------------------------------------------------------------
 void dspark_count_launches(uint64_t n);
+int dspark_sm_count();  // SMs of the current device (defined in lm_head.cu)
 
 #define DSPARK_CHECK_LAUNCH()                                   \
   do {                                                          \

@@ -199,6 +199,55 @@ def test_schedule_async_matches_oracle(R, G, kind):
     assert dsp.dspark_device_status() == 0
 
 
+@pytest.mark.parametrize("shape", SHAPES)
+def test_conf_logits_match_oracle(shape):
+    R, G, V, r, d = shape
+    inp = _weights(R, G, V, r, d, seed=400 + V)
+    tokens = workloads.random_tokens(R, G, V, 401 + V)
+    base = np.zeros((R, G, V))
+    orc = oracle.markov_draft(base, inp["h"], inp["anchor"], inp["W1"], inp["W2"],
+                              inp["w_conf"], inp["T"], 0.0, 0, forced=tokens)
+    dims = dsp.dims_of(R, G, V, r, d)
+    z = torch.empty((R, G), dtype=torch.float32, device="cuda")
+    dsp.dspark_conf_logits(dims, dev(inp["h"], torch.bfloat16).contiguous(), dev(inp["anchor"]),
+                           dev(tokens), dev(inp["W1"], torch.bfloat16),
+                           dev(inp["w_conf"], torch.bfloat16), z)
+    got = host(z).astype(np.float64)
+    assert np.all(np.abs(got - orc["z"]) <= 1e-4 * np.maximum(1.0, np.abs(orc["z"])))
+    assert dsp.dspark_device_status() == 0
+
+
+def _planted_rounds(T_star, N, seed):
+    g = torch.Generator().manual_seed(seed)
+    G = len(T_star)
+    z = (1.2 + 2.0 * torch.randn((N, G), generator=g)).float()
+    p = torch.sigmoid(z.double() / torch.tensor(T_star, dtype=torch.float64))
+    ok = torch.rand((N, G), generator=g, dtype=torch.float64) < p
+    acc = torch.where(ok.all(dim=1), torch.full((N,), G), torch.argmin(ok.int(), dim=1))
+    return z, acc.to(torch.int32)
+
+
+@pytest.mark.parametrize("N,n_bins", [(1, 15), (777, 10), (100_000, 15), (400_000, 64)])
+def test_sts_fit_matches_oracle(N, n_bins):
+    T_star = [1.4, 0.7, 2.2, 1.0, 1.8]
+    z, acc = _planted_rounds(T_star, N, seed=N + n_bins)
+    grid = torch.linspace(0.5, 3.0, 51)
+    o = oracle.sts_fit(z.numpy(), acc.numpy(), grid.numpy(), n_bins)
+    G = len(T_star)
+    T_out = torch.empty(G, dtype=torch.float32, device="cuda")
+    ece = torch.empty(G, dtype=torch.float64, device="cuda")
+    dsp.dspark_sts_fit(dev(z), dev(acc), dev(grid), n_bins, T_out, ece)
+    got_T, got_e = host(T_out), host(ece)
+    tol = 1e-4 + 8.0 / N  # f32 sigmoid rounding may move a sample across a bin edge
+    for j in range(G):
+        if got_T[j] != o["T"][j]:  # only a near tie of two grid values may separate them
+            g = int(np.argmin(np.abs(grid.numpy() - got_T[j])))
+            assert o["ece_grid"][j, g] - o["ece"][j] <= tol, (j, got_T[j], o["T"][j])
+            break  # later positions build on a different (equally good) choice
+        assert abs(got_e[j] - o["ece"][j]) <= tol, (j, got_e[j], o["ece"][j])
+    assert dsp.dspark_device_status() == 0
+
+
 def test_schedule_extremes():
     R, G = 50, 4
     c = workloads.random_confidences(R, G, seed=5)
