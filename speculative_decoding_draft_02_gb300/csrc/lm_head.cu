@@ -7,7 +7,7 @@
 //   l0[m, v] = sum_i h[m, i] W_lm[v, i],  m = r*gamma + k - 1.
 // The contraction runs on the persistent tcgen05 GEMM (TMA-fed, f32
 // accumulation in TMEM); the epilogue rounds each accumulator row to bf16.
-#include "umma_gemm.cuh"
+#include "umma_gemm_pair.cuh"
 
 DSPARK_DECLARE_STATUS(s_status_lmhead)
 
@@ -116,12 +116,12 @@ int dspark_lm_head_tc(const dspark_dims *dims, const void *h, const void *W_lm,
   epi.C = (bf16 *)base_logits;
   epi.M = dims->R * dims->gamma;
   epi.N = dims->V;
-  // Many M blocks (large R * gamma): CTA pairs share each W_lm tile by multicast,
-  // halving the operand bytes each SM pulls from L2.  With few M blocks the
-  // single-CTA kernel reuses W_lm tiles through L2 well enough and wins.
+  // From 1024 rows on, CTA pairs (cta_group::2) on 256 x 256 tiles: a third
+  // fewer operand bytes per SM per flop, 91% of the bf16 peak at R*gamma = 1280
+  // against 86% for the single-CTA kernel.  Below that (few M blocks share each
+  // W_lm tile) the single-CTA kernel is the faster one.
   const int num_m = (epi.M + gemm::BM - 1) / gemm::BM;
-  if (num_m >= 16)
-    return gemm::launch<4, 256, true>(h, W_lm, epi.M, epi.N, dims->d, epi, stream);
+  if (num_m >= 8) return gemm::launch_pair<4>(h, W_lm, epi.M, epi.N, dims->d, epi, stream);
   return gemm::launch<4, 256, false>(h, W_lm, epi.M, epi.N, dims->d, epi, stream);
 }
 
