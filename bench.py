@@ -39,7 +39,8 @@ DEFAULT_WORKLOAD = "v4_dspark5"
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
+    # ~1 s of timed rounds at V4, so the clock sampler (200 ms) sees it several times
+    p.add_argument("--steps", type=int, default=600)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
     p.add_argument("--impl", default="dspark", choices=["dspark", "reference"])
@@ -146,7 +147,8 @@ class ClockSampler:
 
 
 # Sources that define the LM-head kernel; a profile taken on other sources is stale.
-LM_HEAD_SOURCES = ["lm_head.cu", "umma_gemm.cuh", "tcgen05.cuh", "common.cuh"]
+LM_HEAD_SOURCES = ["lm_head.cu", "umma_gemm_pair.cuh", "umma_gemm.cuh", "tcgen05.cuh",
+                   "common.cuh"]
 
 
 def kernel_source_hash(names):
