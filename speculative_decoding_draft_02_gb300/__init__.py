@@ -283,6 +283,9 @@ class Round:
         self.bonus = torch.empty((R,), dtype=torch.int32, device=device)
         self.ws_draft = workspace(dspark_markov_workspace_bytes(d), device)
         self.ws_verify = workspace(dspark_verify_workspace_bytes(d), device)
+        # run_host: the target logits come in on a side stream during the draft
+        self._copy_stream = torch.cuda.Stream(device=device)
+        self._target_ready = torch.cuda.Event()
 
     def draft(self, h, anchor, tau, seed, stream=None):
         hd = self.head
@@ -318,13 +321,29 @@ class Round:
     def run_host(self, h_host, anchor_host, target_host, sps, tau, draft_seed, verify_seed,
                  dev_in: Dict[str, torch.Tensor], out_host: Dict[str, torch.Tensor],
                  mode=SCHED_UNCONSTRAINED, k_fixed=0, stream=None, k_ring=None) -> None:
-        """One round from pinned host inputs to pinned host outputs (copies included)."""
-        dev_in["h"].copy_(h_host, non_blocking=True)
-        dev_in["anchor"].copy_(anchor_host, non_blocking=True)
-        dev_in["target"].copy_(target_host, non_blocking=True)
-        self.run(dev_in["h"], dev_in["anchor"], dev_in["target"], sps, tau, draft_seed,
-                 verify_seed, mode, k_fixed, stream, k_ring)
-        out_host["tokens"].copy_(self.tokens, non_blocking=True)
-        out_host["len"].copy_(self.len, non_blocking=True)
-        out_host["accepted"].copy_(self.accepted, non_blocking=True)
-        out_host["bonus"].copy_(self.bonus, non_blocking=True)
+        """One round from pinned host inputs to pinned host outputs (copies included).
+
+        h and the anchors are copied on `stream` ahead of the draft.  The target
+        logits, read only by verify, are copied on a side stream that starts
+        once everything already queued on `stream` (the previous round, whose
+        verify reads the same buffer) is done, so the copy runs under the draft
+        and the schedule; verify waits for it."""
+        s = stream if stream is not None else torch.cuda.current_stream()
+        c = self._copy_stream
+        with torch.cuda.stream(s):
+            dev_in["h"].copy_(h_host, non_blocking=True)
+            dev_in["anchor"].copy_(anchor_host, non_blocking=True)
+        c.wait_stream(s)
+        with torch.cuda.stream(c):
+            dev_in["target"].copy_(target_host, non_blocking=True)
+        dev_in["target"].record_stream(c)
+        self._target_ready.record(c)
+        self.draft(dev_in["h"], dev_in["anchor"], tau, draft_seed, s)
+        self.schedule(sps, mode, k_fixed, s, k_ring)
+        s.wait_event(self._target_ready)
+        self.verify(dev_in["anchor"], dev_in["target"], tau, verify_seed, s)
+        with torch.cuda.stream(s):
+            out_host["tokens"].copy_(self.tokens, non_blocking=True)
+            out_host["len"].copy_(self.len, non_blocking=True)
+            out_host["accepted"].copy_(self.accepted, non_blocking=True)
+            out_host["bonus"].copy_(self.bonus, non_blocking=True)

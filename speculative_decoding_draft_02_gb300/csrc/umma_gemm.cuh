@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&ctl->tfull[b], 1);
-      tc::mbar_init(&ctl->tempty[b], 32 * EPI_WARPS);
+      tc::mbar_init(&ctl->tempty[b], EPI_WARPS);  // one arrival per epilogue warp
     }
     tc::mbar_init(&ctl->drain, 1);
     ctl->abort = 0;
@@ -246,7 +246,8 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
       epi(m_blk * BM, n_blk * BN, row, taddr, c0, c0 + SLICE, next_m0, next_n0, st);
       tc::fence_before_sync();
-      tc::mbar_arrive(&ctl->tempty[acc]);
+      __syncwarp();  // every lane's TMEM reads are done before the warp's single arrival
+      if (lane == 0) tc::mbar_arrive(&ctl->tempty[acc]);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }

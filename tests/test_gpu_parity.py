@@ -396,3 +396,44 @@ def test_round_matches_oracle_end_to_end(name, tau, mode):
             ov = oracle.verify(orc["tokens"], o_s["len"], orc["logits"], target, tau, vs)
             compare_verify(rnd.accepted, rnd.bonus, ov, tau)
     assert dsp.dspark_device_status() == 0
+
+
+def test_run_host_matches_device_rounds():
+    """Three back-to-back rounds from pinned host buffers (the target copied on a
+    side stream under the draft) give the device-resident rounds' outputs."""
+    w = workloads.WORKLOADS["tiny"].with_(R=37, V=1000, anchor_hi=1000, n_sps=256)
+    inp = workloads.make_inputs(w)
+    R, G, V, d = w.R, w.gamma, w.V, w.d
+    head = dsp.DraftHead.from_weights(R, G, inp["W_lm"], inp["W1"], inp["W2"], inp["w_conf"],
+                                      inp["T"])
+    sps = dev(inp["sps"])
+    tau = 1.0
+    hs = [workloads.random_normal((R * G, d), 1.0, 700 + t) for t in range(3)]
+    targets = [workloads.random_normal((R, G + 1, V), 1.5, 710 + t) for t in range(3)]
+    want = []
+    rnd = dsp.Round(head)
+    for t in range(3):
+        rnd.run(dev(hs[t], torch.bfloat16).contiguous(), dev(inp["anchor"]),
+                dev(targets[t], torch.bfloat16).contiguous(), sps, tau, 11 + t, 21 + t)
+        torch.cuda.synchronize()
+        want.append({k: host(getattr(rnd, k)).copy() for k in ("tokens", "len", "accepted",
+                                                             "bonus")})
+    rnd2 = dsp.Round(head)
+    dev_in = {"h": torch.empty((R * G, d), dtype=torch.bfloat16, device="cuda"),
+              "anchor": torch.empty((R,), dtype=torch.int32, device="cuda"),
+              "target": torch.empty((R, G + 1, V), dtype=torch.bfloat16, device="cuda")}
+    a_host = inp["anchor"].to(torch.int32).pin_memory()
+    h_host = [x.to(torch.bfloat16).pin_memory() for x in hs]      # alive until the end
+    t_host = [x.to(torch.bfloat16).pin_memory() for x in targets]
+    outs = []
+    for t in range(3):  # no synchronisation between rounds
+        out_host = {k: torch.empty(getattr(rnd2, k).shape, dtype=getattr(rnd2, k).dtype,
+                                   pin_memory=True)
+                    for k in ("tokens", "len", "accepted", "bonus")}
+        rnd2.run_host(h_host[t], a_host, t_host[t], sps, tau, 11 + t, 21 + t, dev_in, out_host)
+        outs.append(out_host)
+    torch.cuda.synchronize()
+    for t in range(3):
+        for k in ("tokens", "len", "accepted", "bonus"):
+            assert np.array_equal(outs[t][k].numpy(), want[t][k]), (t, k)
+    assert dsp.dspark_device_status() == 0
