@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(RP_THREADS) reduce_prep(
   const size_t o = (size_t)i * gamma + k - 1;
   if (MODE == MODE_SAMPLE) {
     int b = s_tok;
-    if (b < 0 || b * GUMBEL_BLOCK >= V) {  // no finite block score (non-finite logits)
+    if (b < 0 || b >= (V + GUMBEL_BLOCK - 1) / GUMBEL_BLOCK) {  // no finite block score (non-finite logits)
       if (tid == 0) dspark_set_status(DSPARK_ERR_TOKEN);
       b = 0;
     }

@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(256) resample_reduce(
   __syncthreads();
   const int req = list[slot];
   const int b = s_blk;
-  if (b < 0 || b * GUMBEL_BLOCK >= V) {  // every block empty
+  if (b < 0 || b >= (V + GUMBEL_BLOCK - 1) / GUMBEL_BLOCK) {  // every block empty
     if (tid == 0) rows[req].kind = KIND_FALLBACK;
     return;
   }
