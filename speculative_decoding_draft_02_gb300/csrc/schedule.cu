@@ -27,6 +27,7 @@ __device__ __forceinline__ double theta_at(long K, double S, int R, const float 
   return ((double)R + S) * (double)sps[R + K - 1];
 }
 
+template <int E>
 __global__ void __launch_bounds__(SCHED_THREADS) schedule_kernel(
     const float *__restrict__ conf, int R, int gamma, const float *__restrict__ sps, int mode,
     int k_fixed, int n_pad, int32_t *__restrict__ len, int32_t *__restrict__ K_out,
@@ -63,18 +64,75 @@ __global__ void __launch_bounds__(SCHED_THREADS) schedule_kernel(
   for (int i = n + tid; i < n_pad; i += SCHED_THREADS) keys[i] = ~0ull;
   __syncthreads();
 
-  // a6: bitonic sort, ascending keys = descending a, ties by ascending id
-  for (int size = 2; size <= n_pad; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int t = tid; t < n_pad / 2; t += SCHED_THREADS) {
-        const int lo = 2 * t - (t & (stride - 1));
-        const int hi = lo + stride;
-        const bool up = ((lo & size) == 0);
-        const unsigned long long x = keys[lo], y = keys[hi];
-        if ((x > y) == up) { keys[lo] = y; keys[hi] = x; }
-      }
-      __syncthreads();
+  // a6: bitonic sort, ascending keys = descending a, ties by ascending id.
+  // Thread t holds keys [t*E, t*E + E) in registers (E = n_pad / 1024, at
+  // least 1; when n_pad < 1024 the slots past n_pad hold the largest key and
+  // only ever meet each other, since a stride below n_pad never crosses it).
+  // Partners closer than E are in the thread, closer than 32 E in the warp
+  // (shuffles); only the wider strides go through shared memory (n_pad keys).
+  {
+    unsigned long long k[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int i = tid * E + e;
+      k[e] = i < n_pad ? keys[i] : ~0ull;
     }
+    for (int size = 2; size <= n_pad; size <<= 1) {
+      int stride = size >> 1;
+      if (stride >= 32 * E) {
+        __syncthreads();  // every thread is done reading keys[] before it is rewritten
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+          if (tid * E + e < n_pad) keys[tid * E + e] = k[e];
+        __syncthreads();
+        for (; stride >= 32 * E; stride >>= 1) {
+          for (int t = tid; t < n_pad / 2; t += SCHED_THREADS) {
+            const int lo = 2 * t - (t & (stride - 1));
+            const int hi = lo + stride;
+            const bool up = ((lo & size) == 0);
+            const unsigned long long x = keys[lo], y = keys[hi];
+            if ((x > y) == up) { keys[lo] = y; keys[hi] = x; }
+          }
+          __syncthreads();
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) k[e] = tid * E + e < n_pad ? keys[tid * E + e] : ~0ull;
+      }
+      for (; stride >= E; stride >>= 1) {  // partner in lane ^ (stride / E), same slot
+        const int lo_bit = stride / E;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int i = tid * E + e;
+          const unsigned long long y = __shfl_xor_sync(0xffffffffu, k[e], lo_bit);
+          const bool lower = (i & stride) == 0;  // i is the lower index of its pair
+          const bool up = (i & size) == 0;
+          // ascending pairs keep the smaller key at the lower index
+          const bool take_min = lower == up;
+          k[e] = take_min ? (y < k[e] ? y : k[e]) : (y > k[e] ? y : k[e]);
+        }
+      }
+      // both partners in this thread: strides stride, stride / 2, ..., 1 (all
+      // below E), unrolled over compile-time strides so k[] stays in registers
+#pragma unroll
+      for (int st = E / 2; st >= 1; st >>= 1) {
+        if (st > stride) continue;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          if ((e & st) != 0) continue;
+          const int i = tid * E + e;
+          const bool up = (i & size) == 0;
+          const unsigned long long x = k[e], y = k[e + st];
+          if ((x > y) == up) { k[e] = y; k[e + st] = x; }
+        }
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int i = tid * E + e;
+      if (i < n_pad) keys[i] = k[e];
+    }
+    __syncthreads();
   }
 
   // a7: S_K by a block scan in f64; thread t owns sorted slots [t*per, (t+1)*per)
@@ -225,16 +283,29 @@ int launch_schedule(const float *conf, int32_t R, int32_t gamma, const float *sp
   while (n_pad < n) n_pad <<= 1;
   const size_t smem = sizeof(unsigned long long) * n_pad + sizeof(int32_t) * R;
   static bool attr_set = false;
+  const int smem_max = (int)(sizeof(unsigned long long) * SCHED_MAX + sizeof(int32_t) * SCHED_MAX);
   if (!attr_set) {
-    if (cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             sizeof(unsigned long long) * SCHED_MAX + sizeof(int32_t) * SCHED_MAX) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(schedule_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_max) != cudaSuccess ||
+        cudaFuncSetAttribute(schedule_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_max) != cudaSuccess ||
+        cudaFuncSetAttribute(schedule_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_max) != cudaSuccess ||
+        cudaFuncSetAttribute(schedule_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_max) != cudaSuccess ||
+        cudaFuncSetAttribute(schedule_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_max) != cudaSuccess)
       return DSPARK_ERR_CUDA;
     attr_set = true;
   }
-  schedule_kernel<<<1, SCHED_THREADS, smem, stream>>>(conf, R, gamma, sps, mode, k_fixed, n_pad,
-                                                      len, K_out, theta_out, a_out, order_out,
-                                                      k_ring);
+  // keys per thread: n_pad / 1024, at least one
+  auto kernel = n_pad <= 1024 ? schedule_kernel<1>
+              : n_pad == 2048 ? schedule_kernel<2>
+              : n_pad == 4096 ? schedule_kernel<4>
+              : n_pad == 8192 ? schedule_kernel<8>
+                              : schedule_kernel<16>;
+  kernel<<<1, SCHED_THREADS, smem, stream>>>(conf, R, gamma, sps, mode, k_fixed, n_pad, len,
+                                             K_out, theta_out, a_out, order_out, k_ring);
   DSPARK_CHECK_LAUNCH();
   dspark_count_launches(1);
   return DSPARK_OK;
