@@ -267,10 +267,12 @@ def run_reference(args, w, ws, rank):
     # size one step so that warmup + steps fit in about three minutes
     S = args.cpu_sample or 1
     cpu["target"] = inp["target"][:S].cpu()
+    avail = int(inp["h"].shape[0])  # requests built (all of them on a GPU machine)
     if not args.cpu_sample:
         t1 = cpu_oracle_round(w, cpu, 1)
-        S = int(max(1, min(w.R, math.floor(180.0 / (args.steps + args.warmup) / max(t1, 1e-3)))))
+        S = int(max(1, min(avail, math.floor(180.0 / (args.steps + args.warmup) / max(t1, 1e-3)))))
         cpu["target"] = inp["target"][:S].cpu()
+    S = min(S, avail)
     for _ in range(args.warmup):
         cpu_oracle_round(w, cpu, S)
     times = [cpu_oracle_round(w, cpu, S) for _ in range(args.steps)]
