@@ -266,12 +266,14 @@ def test_schedule_extremes():
 
 # ------------------------------------------------------------------ a8 ----
 
-def _verify_case(shape, tau, seed, accept_bias=0.7):
+def _verify_case(shape, tau, seed, accept_bias=0.7, lens_kind="random"):
     R, G, V, r, d = shape
     inp = _weights(R, G, V, r, d, seed=seed)
     base = workloads.random_normal((R, G, V), 1.0, seed + 1)
     tokens = workloads.random_tokens(R, G, V, seed + 2)
     lens = workloads.random_lengths(R, G, seed + 3)
+    if lens_kind == "full":
+        lens = torch.full_like(lens, G)
     noise = workloads.random_normal((R, G + 1, V), 0.3, seed + 4, dtype=torch.float32)
     if tau == 0.0:
         target = workloads.random_normal((R, G + 1, V), 1.0, seed + 5)
@@ -312,6 +314,31 @@ def test_verify_matches_oracle(shape, tau):
     assert flagged <= max(1, shape[0] // 20)
     acc = host(rnd.accepted)
     assert np.all(acc >= 0) and np.all(acc <= host(lens))
+    assert dsp.dspark_device_status() == 0
+
+
+@pytest.mark.parametrize("shape,tau", [((37, 4, 1000, 128, 320), 1.0),
+                                       ((37, 4, 1000, 128, 320), 0.0),
+                                       ((3, 32, 520, 64, 64), 1.0),
+                                       ((3, 32, 520, 64, 64), 0.0)])
+def test_verify_full_lengths(shape, tau):
+    """Every draft admitted (up to gamma = 32, the largest the library takes)."""
+    rnd, orc, lens = _verify_case(shape, tau, seed=330 + shape[1], lens_kind="full")
+    flagged = compare_verify(rnd.accepted, rnd.bonus, orc, tau)
+    assert flagged <= max(1, shape[0] // 20)
+    assert dsp.dspark_device_status() == 0
+
+
+@pytest.mark.parametrize("shape,tau", [((3, 32, 520, 64, 64), 0.0), ((3, 32, 520, 64, 64), 1.0),
+                                       ((37, 4, 1000, 128, 320), 0.05),
+                                       ((37, 4, 1000, 128, 320), 4.0)])
+def test_markov_draft_edges(shape, tau):
+    """gamma = 32; a very cold and a very hot sampling temperature."""
+    rnd, orc = _draft_case(shape, tau, seed=260 + shape[1])
+    rep = compare_draft(rnd.tokens, rnd.conf, rnd.lse_d if tau > 0 else None,
+                        rnd.logp_d if tau > 0 else None, orc, tau)
+    assert rep.compared >= shape[0]
+    assert rep.flagged <= max(2, rep.compared // (50 if tau == 0 else 25))
     assert dsp.dspark_device_status() == 0
 
 
