@@ -23,8 +23,9 @@ namespace {
 constexpr int SCHED_THREADS = 1024;
 constexpr int SCHED_MAX = 16384;
 
-__device__ __forceinline__ double theta_at(long K, double S, int R, const float *sps) {
-  return ((double)R + S) * (double)sps[R + K - 1];
+// Theta(K) = (R + S_K) * SPS(R + K), with spsK[K] = SPS(R + K).
+__device__ __forceinline__ double theta_at(long K, double S, int R, const float *spsK) {
+  return ((double)R + S) * (double)spsK[K];
 }
 
 template <int E>
@@ -34,8 +35,9 @@ __global__ void __launch_bounds__(SCHED_THREADS) schedule_kernel(
     double *__restrict__ theta_out, float *__restrict__ a_out, int32_t *__restrict__ order_out,
     int32_t *__restrict__ k_ring) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
+  // keys [n_pad] (merge sort: and a second buffer of n_pad), then cnt [R]
   unsigned long long *keys = reinterpret_cast<unsigned long long *>(smem_raw);
-  int32_t *cnt = reinterpret_cast<int32_t *>(keys + n_pad);  // [R]
+  int32_t *cnt = reinterpret_cast<int32_t *>(keys + (E == 0 ? 2 * n_pad : n_pad));
   __shared__ double warp_tot[32];
   __shared__ double red_val[32];
   __shared__ long red_k[32];
@@ -45,11 +47,20 @@ __global__ void __launch_bounds__(SCHED_THREADS) schedule_kernel(
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n = R * gamma;
 
-  // a5: survival products, f32 left to right; keys for the global order
+  // a5: survival products, f32 left to right; keys for the global order.  The
+  // merge-sort form first brings the confidences into shared memory with one
+  // coalesced pass (its second key buffer is free until the sort).
+  const float *cs = conf;
+  if constexpr (E == 0) {
+    float *stage = reinterpret_cast<float *>(keys + n_pad);
+    for (int id = tid; id < n; id += SCHED_THREADS) stage[id] = conf[id];
+    __syncthreads();
+    cs = stage;
+  }
   for (int i = tid; i < R; i += SCHED_THREADS) {
     float a = 1.f;
     for (int j = 0; j < gamma; ++j) {
-      float c = conf[(size_t)i * gamma + j];
+      float c = cs[(size_t)i * gamma + j];
       if (!(c >= 0.f && c <= 1.f)) {  // NaN or outside [0, 1]
         dspark_set_status(DSPARK_ERR_ARG);
         c = c > 1.f ? 1.f : 0.f;
@@ -64,6 +75,40 @@ __global__ void __launch_bounds__(SCHED_THREADS) schedule_kernel(
   for (int i = n + tid; i < n_pad; i += SCHED_THREADS) keys[i] = ~0ull;
   __syncthreads();
 
+  const float *spsK = sps + R - 1;  // spsK[K] = SPS(R + K), K = 0..n
+  if constexpr (E == 0) {
+    // a6 as a merge sort.  A request's keys are already in order (a_{r,j} does
+    // not increase with j and ids increase), so the R runs of gamma keys are
+    // merged pairwise, log2(R) levels.  Keys are unique (the id is in the low
+    // bits): a key's place in the merged run is its index in its own run plus
+    // the number of smaller keys in the partner run, found by binary search.
+    unsigned long long *src = keys, *dst = keys + n_pad;
+    for (int L = gamma; L < n; L <<= 1) {
+      for (int p = tid; p < n; p += SCHED_THREADS) {
+        const int a0 = p / (2 * L) * (2 * L), b0 = a0 + L;
+        const unsigned long long x = src[p];
+        int lo, hi, own;
+        if (p < b0) { lo = b0; hi = min(b0 + L, n); own = p - a0; }  // x in the left run
+        else        { lo = a0; hi = b0;             own = p - b0; }  // x in the right run
+        int l = lo, h = hi > lo ? hi : lo;  // first slot of the partner run holding a key >= x
+        while (l < h) {
+          const int m = (l + h) >> 1;
+          if (src[m] < x) l = m + 1;
+          else h = m;
+        }
+        dst[a0 + own + (l - lo)] = x;
+      }
+      __syncthreads();
+      unsigned long long *t = src;
+      src = dst;
+      dst = t;
+    }
+    keys = src;  // the sorted keys; the other buffer is free again
+    float *sp = reinterpret_cast<float *>(dst);
+    for (int K = tid; K <= n; K += SCHED_THREADS) sp[K] = sps[R + K - 1];
+    spsK = sp;
+    __syncthreads();
+  } else {
   // a6: bitonic sort, ascending keys = descending a, ties by ascending id.
   // Thread t holds keys [t*E, t*E + E) in registers (E = n_pad / 1024, at
   // least 1; when n_pad < 1024 the slots past n_pad hold the largest key and
@@ -71,7 +116,7 @@ __global__ void __launch_bounds__(SCHED_THREADS) schedule_kernel(
   // Partners closer than E are in the thread, closer than 32 E in the warp
   // (shuffles); only the wider strides go through shared memory (n_pad keys).
   {
-    unsigned long long k[E];
+    unsigned long long k[E > 0 ? E : 1];
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       const int i = tid * E + e;
@@ -134,6 +179,7 @@ __global__ void __launch_bounds__(SCHED_THREADS) schedule_kernel(
     }
     __syncthreads();
   }
+  }
 
   // a7: S_K by a block scan in f64; thread t owns sorted slots [t*per, (t+1)*per)
   const int per = (n_pad + SCHED_THREADS - 1) / SCHED_THREADS;
@@ -172,14 +218,14 @@ __global__ void __launch_bounds__(SCHED_THREADS) schedule_kernel(
   long firstDrop = 0x7fffffffffffffffL;  // smallest K with Theta(K+1) <= Theta(K)
   double prevTheta = 0.0;
   if (beg <= n) {  // sps[R + K - 1] exists for K <= n only
-    prevTheta = theta_at(beg, S, R, sps);
+    prevTheta = theta_at(beg, S, R, spsK);
     best = prevTheta;
     bestK = beg;
   }
   for (int p = beg; p < beg + per && p < n; ++p) {
     S += (double)__uint_as_float(~(unsigned)(keys[p] >> 32));
     const long K = p + 1;
-    const double th = theta_at(K, S, R, sps);
+    const double th = theta_at(K, S, R, spsK);
     if (th > best) { best = th; bestK = K; }
     if (th <= prevTheta && firstDrop > K - 1) firstDrop = K - 1;
     prevTheta = th;
@@ -251,12 +297,12 @@ __global__ void __launch_bounds__(SCHED_THREADS) schedule_kernel(
   if (order_out)
     for (int p = tid; p < n; p += SCHED_THREADS) order_out[p] = (int)(keys[p] & 0xffffffffu);
   // Theta(K): the owner of slot K recomputes it from its scan segment
-  if (tid == 0 && K == 0) s_theta = theta_at(0, 0.0, R, sps);
+  if (tid == 0 && K == 0) s_theta = theta_at(0, 0.0, R, spsK);
   {
     double S2 = S_beg;
     for (int p = beg; p < beg + per && p < n; ++p) {
       S2 += (double)__uint_as_float(~(unsigned)(keys[p] >> 32));
-      if (p + 1 == K) s_theta = theta_at(K, S2, R, sps);
+      if (p + 1 == K) s_theta = theta_at(K, S2, R, spsK);
     }
   }
   __syncthreads();
@@ -281,11 +327,15 @@ int launch_schedule(const float *conf, int32_t R, int32_t gamma, const float *sp
   if ((long)n_sps < (long)R * (gamma + 1)) return DSPARK_ERR_SPS_SHORT;
   int n_pad = 2;
   while (n_pad < n) n_pad <<= 1;
-  const size_t smem = sizeof(unsigned long long) * n_pad + sizeof(int32_t) * R;
+  // up to 8192 candidates: merge sort (two key buffers); beyond: bitonic sort
+  const bool merge = n_pad <= 8192;
+  const size_t smem = sizeof(unsigned long long) * n_pad * (merge ? 2 : 1) + sizeof(int32_t) * R;
   static bool attr_set = false;
   const int smem_max = (int)(sizeof(unsigned long long) * SCHED_MAX + sizeof(int32_t) * SCHED_MAX);
   if (!attr_set) {
-    if (cudaFuncSetAttribute(schedule_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(schedule_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_max) != cudaSuccess ||
+        cudaFuncSetAttribute(schedule_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem_max) != cudaSuccess ||
         cudaFuncSetAttribute(schedule_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem_max) != cudaSuccess ||
@@ -299,7 +349,8 @@ int launch_schedule(const float *conf, int32_t R, int32_t gamma, const float *sp
     attr_set = true;
   }
   // keys per thread: n_pad / 1024, at least one
-  auto kernel = n_pad <= 1024 ? schedule_kernel<1>
+  auto kernel = merge        ? schedule_kernel<0>
+              : n_pad <= 1024 ? schedule_kernel<1>
               : n_pad == 2048 ? schedule_kernel<2>
               : n_pad == 4096 ? schedule_kernel<4>
               : n_pad == 8192 ? schedule_kernel<8>
