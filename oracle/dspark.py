@@ -285,6 +285,84 @@ def markov_draft(base, h, anchor, W1, W2, w_conf, T, tau: float, seed: int,
 
 
 # ---------------------------------------------------------------------------
+# a2': the RNN head variant   [AR stage two, "RNN head"; DD §二 设计一]
+# ---------------------------------------------------------------------------
+
+def rnn_draft(base, h, anchor, W1, W2, W_gc, w_conf, T, tau: float, seed: int,
+              keep_scores: bool = False, block: int = GUMBEL_BLOCK) -> Dict[str, np.ndarray]:
+    """The sequential head with a gated in-block recurrent state.
+
+    The pages describe it only in words: a block-internal recurrent state,
+    updated by a gated step over the concatenation of the history (the state),
+    the previous token's embedding and the backbone hidden state.  Reading:
+      u_k  = [s_{k-1}; W1[x_{k-1}]; h_k]          (s_0 = 0, x_0 = anchor)
+      g_k  = sigmoid(W_g u_k),  c_k~ = tanh(W_c u_k),   W_gc = [W_g; W_c]  [2r, 2r + d]
+      s_k  = (1 - g_k) * s_{k-1} + g_k * c_k~
+      l_k  = base_k + s_k W2                      (the Markov head's low-rank output map)
+    The state enters each contraction rounded to bf16 (an activation, like the
+    base logits); it is carried in float64 between steps.  Sampling, the
+    confidence head (on [h_k; W1[x_{k-1}]]) and the outputs are markov_draft's.
+    """
+    base = to_f64(base)
+    h = to_f64(h)
+    anchor = to_i64(anchor)
+    W1 = to_f64(W1)
+    W2 = to_f64(W2)
+    W_gc = to_f64(W_gc)
+    w_conf = to_f64(w_conf)
+    T = to_f64(T)
+    R, G, V = base.shape
+    d = h.shape[-1]
+    r = W1.shape[1]
+    w_h, w_e = w_conf[:d], w_conf[d:]
+    req = np.arange(R)
+    tokens = np.zeros((R, G), dtype=np.int64)
+    conf = np.zeros((R, G))
+    margin = np.zeros((R, G))
+    lse = np.zeros((R, G))
+    logp = np.zeros((R, G))
+    scores = np.zeros((R, G, V)) if keep_scores else None
+    nb = (V + block - 1) // block
+    bscores = np.zeros((R, G, nb)) if keep_scores and tau != 0.0 else None
+    state = np.zeros((R, r))
+    prev = anchor.copy()
+    for k in range(1, G + 1):
+        e = W1[prev]                                              # W1[x_{k-1}]
+        u = np.concatenate([round_bf16(state), e, h[:, k - 1, :]], axis=1)
+        pre = u @ W_gc.T                                          # [R, 2r]
+        g = sigmoid(pre[:, :r])
+        cand = np.tanh(pre[:, r:])
+        state = (1.0 - g) * state + g * cand
+        ell = base[:, k - 1, :] + round_bf16(state) @ W2
+        z = h[:, k - 1, :] @ w_h + e @ w_e
+        conf[:, k - 1] = sigmoid(z / T[k - 1])
+        if tau == 0.0:
+            score = ell
+            x = np.argmax(score, axis=1)
+            margin[:, k - 1] = top2_margin(score)
+        else:
+            smp = gumbel_max(ell / tau, seed, k, req, philox.STREAM_DRAFT, block)
+            score = smp["entry_scores"]
+            x = smp["token"]
+            margin[:, k - 1] = smp["margin"]
+            if bscores is not None:
+                bscores[:, k - 1, :] = smp["block_scores"]
+            lse[:, k - 1] = logsumexp(ell / tau, axis=1)
+            logp[:, k - 1] = ell[np.arange(R), x] / tau - lse[:, k - 1]
+        tokens[:, k - 1] = x
+        if keep_scores:
+            scores[:, k - 1, :] = score
+        prev = x
+    out = dict(tokens=tokens, conf=conf, margin=margin, lse=lse, logp=logp, state=state)
+    if keep_scores:
+        out["scores"] = scores
+        if bscores is not None:
+            out["block_scores"] = bscores
+            out["block"] = block
+    return out
+
+
+# ---------------------------------------------------------------------------
 # a5-a7: survival products, global sort, Theta search   [DD §二 scheduler, §三]
 # ---------------------------------------------------------------------------
 

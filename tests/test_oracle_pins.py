@@ -117,6 +117,51 @@ def test_w2_zero_reduces_to_parallel_drafting():
     assert np.array_equal(out["tokens"], np.argmax(base, axis=2))
 
 
+def _rnn_case(R=6, G=4, V=40, r=8, d=5, seed=51):
+    rng = np.random.default_rng(seed)
+    base = rng.standard_normal((R, G, V))
+    h = rng.standard_normal((R, G, d))
+    h[:, :, 0] = 1.0                                   # a constant feature
+    anchor = rng.integers(0, V, R)
+    W1 = rng.standard_normal((V, r))
+    W2 = rng.standard_normal((r, V)) * 1.5
+    w = rng.standard_normal(d + r)
+    T = 1.0 + rng.random(G)
+    return base, h, anchor, W1, W2, w, T
+
+
+def test_rnn_head_without_weights_is_parallel_drafting():
+    base, h, anchor, W1, W2, w, T = _rnn_case()
+    r, d = W1.shape[1], h.shape[2]
+    out = oracle.rnn_draft(base, h, anchor, W1, W2, np.zeros((2 * r, 2 * r + d)), w, T, 0.0, 0)
+    assert np.array_equal(out["tokens"], np.argmax(base, axis=2))
+    assert np.all(out["state"] == 0.0)
+    # a closed gate (g -> 0 through the constant feature) keeps the zero state too
+    W_gc = np.random.default_rng(3).standard_normal((2 * r, 2 * r + d))
+    W_gc[:r, 2 * r] = -60.0
+    out = oracle.rnn_draft(base, h, anchor, W1, W2, W_gc, w, T, 0.0, 0)
+    assert np.array_equal(out["tokens"], np.argmax(base, axis=2))
+    assert np.max(np.abs(out["state"])) < 1e-20
+
+
+def test_rnn_head_with_open_gate_is_a_markov_head_on_tanh_embeddings():
+    """g -> 1 and a candidate map that passes the embedding: s_k = tanh(W1[x_{k-1}]),
+    so the draft is the Markov head's with W1 replaced by bf16(tanh(W1)) in the bias;
+    the confidence head still sees W1 itself."""
+    base, h, anchor, W1, W2, w, T = _rnn_case()
+    r, d = W1.shape[1], h.shape[2]
+    W_gc = np.zeros((2 * r, 2 * r + d))
+    W_gc[:r, 2 * r] = 60.0                             # update gate open
+    W_gc[r:, r:2 * r] = np.eye(r)                      # candidate = tanh(embedding)
+    rnn = oracle.rnn_draft(base, h, anchor, W1, W2, W_gc, w, T, 0.0, 0)
+    W1t = oracle.round_bf16(np.tanh(W1))
+    mk = oracle.markov_draft(base, h, anchor, W1t, W2, w, T, 0.0, 0)
+    assert np.array_equal(rnn["tokens"], mk["tokens"])
+    assert np.all(mk["margin"] > 1e-9)                 # no tie decides the comparison
+    mk_conf = oracle.markov_draft(base, h, anchor, W1, W2, w, T, 0.0, 0, forced=rnn["tokens"])
+    np.testing.assert_allclose(rnn["conf"], mk_conf["conf"], rtol=1e-13)
+
+
 def test_greedy_ties_pick_lowest_id():
     R, G, V = 2, 2, 9
     base = np.zeros((R, G, V))
