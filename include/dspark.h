@@ -134,6 +134,29 @@ int dspark_markov_draft(const dspark_dims *dims, const void *base_logits, const 
                         int32_t *tokens, float *conf, float *logp_d, float *lse_d,
                         void *workspace, size_t workspace_bytes, dspark_stream_t stream);
 
+/* Workspace bytes dspark_rnn_draft needs for `dims`. */
+size_t dspark_rnn_workspace_bytes(const dspark_dims *dims);
+
+/* a2-a4 with the RNN head variant instead of the Markov head, "DSpark整体架构"
+ * stage two (the pages describe it in words only: a block-internal recurrent
+ * state, gated update over the history, the previous token's embedding and
+ * the backbone hidden state).  Read as, with s_0 = 0 and x_0 = anchor:
+ *   pre_k = W_rec [s_{k-1}; W1[x_{k-1}]] + W_hid h_k          (2r values)
+ *   s_k   = (1 - g) s_{k-1} + g tanh(c), g = sigmoid(pre_k[0:r]), c = pre_k[r:2r]
+ *   l_k   = l0_k + bf16(s_k) W2      (s_{k-1} also enters W_rec in bf16)
+ * and then exactly as dspark_markov_draft (sampling, confidence head on
+ * [h_k; W1[x_{k-1}]], outputs).
+ *   W_rec  bf16 [2r, 2r]  columns [state | embedding] of the gate (rows 0..r-1)
+ *                         and candidate (rows r..2r-1) pre-activations
+ *   W_hid  bf16 [2r, d]   their hidden-state columns
+ * Every other argument is dspark_markov_draft's; the workspace is
+ * dspark_rnn_workspace_bytes(dims) bytes, 256-byte aligned. */
+int dspark_rnn_draft(const dspark_dims *dims, const void *base_logits, const void *h,
+                     const int32_t *anchor, const void *W1, const void *W2t, const void *W_rec,
+                     const void *W_hid, const void *w_conf, const float *T, float tau,
+                     uint64_t seed, int32_t *tokens, float *conf, float *logp_d, float *lse_d,
+                     void *workspace, size_t workspace_bytes, dspark_stream_t stream);
+
 /* a1-a4 in one call: dspark_lm_head into `base_logits`, then dspark_markov_draft. */
 int dspark_draft(const dspark_dims *dims, const void *h, const int32_t *anchor,
                  const void *W_lm, const void *W1, const void *W2t, const void *w_conf,

@@ -44,12 +44,14 @@ __global__ void __launch_bounds__(128) conf_hidden(const bf16 *__restrict__ h,
   if (tid == 0) zh[row] = (part[0] + part[1]) + (part[2] + part[3]);
 }
 
-// Step k: E[i] = W1[x_{k-1}], c_k = sigmoid((zh + w_e . E[i]) / T_k); one warp per request.
+// Step k: the embedding W1[x_{k-1}] into row i of e_next (row stride e_ld: the
+// Markov head's E, or the embedding columns of the RNN head's recurrent input),
+// c_k = sigmoid((zh + w_e . W1[x_{k-1}]) / T_k); one warp per request.
 __global__ void step_prep(const int32_t *__restrict__ anchor, const int32_t *__restrict__ tokens,
                           const bf16 *__restrict__ W1, const bf16 *__restrict__ w_e,
                           const float *__restrict__ zh, const float *__restrict__ T,
-                          bf16 *__restrict__ E, float *__restrict__ conf, int R, int gamma,
-                          int V, int r, int k) {
+                          bf16 *__restrict__ e_next, int e_ld, float *__restrict__ conf, int R,
+                          int gamma, int V, int r, int k) {
   const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (i >= R) return;
   int prev = (k == 1) ? anchor[i] : tokens[(size_t)i * gamma + k - 2];
@@ -58,7 +60,7 @@ __global__ void step_prep(const int32_t *__restrict__ anchor, const int32_t *__r
     prev = 0;
   }
   const uint4 *src = reinterpret_cast<const uint4 *>(W1 + (size_t)prev * r);
-  uint4 *dst = reinterpret_cast<uint4 *>(E + (size_t)i * r);
+  uint4 *dst = reinterpret_cast<uint4 *>(e_next + (size_t)i * e_ld);
   const uint4 *wr = reinterpret_cast<const uint4 *>(w_e);
   float acc = 0.f;
   for (int c = lane; c < r / 8; c += 32) {
@@ -92,8 +94,9 @@ __global__ void __launch_bounds__(RP_THREADS) reduce_prep(
     const RowPartial *__restrict__ part, int n_parts, int gamma, int V, int r, int k,
     int32_t *__restrict__ tokens, float *__restrict__ lse_out, float *__restrict__ logp_out,
     const bf16 *__restrict__ W1, const bf16 *__restrict__ w_e, const float *__restrict__ zh,
-    const float *__restrict__ T, bf16 *__restrict__ E, float *__restrict__ conf,
-    const bf16 *__restrict__ base, const bf16 *__restrict__ W2t, float inv_tau, uint64_t seed) {
+    const float *__restrict__ T, const bf16 *E, bf16 *e_next, int e_ld,  // may be one buffer
+    float *__restrict__ conf, const bf16 *__restrict__ base, const bf16 *__restrict__ W2t,
+    float inv_tau, uint64_t seed) {
   const int i = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   pdl_trigger();
   pdl_wait();  // the vocabulary pass of step k has completed
@@ -169,7 +172,7 @@ __global__ void __launch_bounds__(RP_THREADS) reduce_prep(
     prev = 0;
   }
   const uint4 *src = reinterpret_cast<const uint4 *>(W1 + (size_t)prev * r);
-  uint4 *dst = reinterpret_cast<uint4 *>(E + (size_t)i * r);
+  uint4 *dst = reinterpret_cast<uint4 *>(e_next + (size_t)i * e_ld);
   const uint4 *wr = reinterpret_cast<const uint4 *>(w_e);
   float acc = 0.f;
   for (int c = tid; c < r / 8; c += RP_THREADS) {
@@ -242,7 +245,7 @@ extern "C" int dspark_markov_draft(const dspark_dims *dims, const void *base_log
   const float inv_tau = tau > 0.f ? 1.f / tau : 1.f;
   step_prep<<<(R * 32 + 255) / 256, 256, 0, stream>>>(anchor, tokens, (const bf16 *)W1,
                                                      (const bf16 *)w_conf + d, ws.zh, T, ws.E,
-                                                     conf, R, G, V, r, 1);
+                                                     r, conf, R, G, V, r, 1);
   DSPARK_CHECK_LAUNCH();
   const bf16 *w_e = (const bf16 *)w_conf + d;
   for (int k = 1; k <= G; ++k) {
@@ -256,7 +259,7 @@ extern "C" int dspark_markov_draft(const dspark_dims *dims, const void *base_log
       if (rc != DSPARK_OK) return rc;
       if (dspark_launch_pdl(reduce_prep<MODE_SAMPLE>, dim3(R), dim3(RP_THREADS), 0, stream,
                             ws.part, n_parts, G, V, r, k, tokens, lse_d, logp_d,
-                            (const bf16 *)W1, w_e, ws.zh, T, ws.E, conf,
+                            (const bf16 *)W1, w_e, ws.zh, T, ws.E, ws.E, r, conf,
                             (const bf16 *)base_logits, (const bf16 *)W2t, inv_tau,
                             seed) != cudaSuccess)
         return DSPARK_ERR_CUDA;
@@ -269,7 +272,7 @@ extern "C" int dspark_markov_draft(const dspark_dims *dims, const void *base_log
       if (rc != DSPARK_OK) return rc;
       if (dspark_launch_pdl(reduce_prep<MODE_GREEDY>, dim3(R), dim3(RP_THREADS), 0, stream,
                             ws.part, n_parts, G, V, r, k, tokens, lse_d, logp_d,
-                            (const bf16 *)W1, w_e, ws.zh, T, ws.E, conf,
+                            (const bf16 *)W1, w_e, ws.zh, T, ws.E, ws.E, r, conf,
                             (const bf16 *)base_logits, (const bf16 *)W2t, inv_tau,
                             seed) != cudaSuccess)
         return DSPARK_ERR_CUDA;
@@ -288,6 +291,176 @@ int dspark_status_markov(int clear) {
     cudaMemcpyToSymbol(s_status_markov, &z, sizeof(int));
   }
   return v;
+}
+
+// ---------------------------------------------------------------------------
+// The RNN head variant.  "DSpark整体架构" (stage two) names a second sequential
+// head that keeps a block-internal recurrent state and updates it by a gated
+// step over the history, the previous token's embedding and the backbone
+// hidden state; the pages give no equations.  Read as:
+//   pre_k = W_rec [s_{k-1}; W1[x_{k-1}]] + W_hid h_k        (2r values; s_0 = 0)
+//   s_k   = (1 - g) s_{k-1} + g tanh(c),   g = sigmoid(pre_k[0:r]), c = pre_k[r:2r]
+//   l_k   = l0_k + s_k W2            (the Markov head's output map, s_k in bf16)
+// W_hid h_k is known for every position before the loop: one tensor-core GEMM
+// per round.  Per step: the recurrent GEMM [R, 2r] x [2r, 2r] (f32 out),
+// rnn_state, then the Markov head's vocabulary pass and reduce_prep with
+// E = bf16(s_k); reduce_prep gathers W1[x_k] into the recurrent input U.
+// ---------------------------------------------------------------------------
+namespace {
+
+// f32 accumulator rows to C [M, N] (N a multiple of 4).
+struct EpiStoreF32 {
+  float *C;
+  int M, N;
+  struct State {};
+  static constexpr bool kRowAffine = false;
+  static constexpr bool kStreamB = false;
+  __device__ void prefetch(int, int, int, int, int, State &) const {}
+  __device__ void operator()(int m0, int n0, int row, uint32_t taddr, int c0, int c1, int, int,
+                             State &) const {
+    const int m = m0 + row;
+    float *dst = C + (size_t)m * N;
+#pragma unroll 1
+    for (int c = c0; c < c1; c += 32) {
+      uint32_t v[32];
+      tc::tmem_ld32(taddr + (uint32_t)c, v);
+      tc::tmem_wait_ld();
+      if (m < M) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int n = n0 + c + 4 * q;
+          if (n + 4 <= N)
+            *reinterpret_cast<float4 *>(dst + n) =
+                make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                            __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+        }
+      }
+    }
+  }
+  __device__ void on_timeout() const { dspark_set_status(DSPARK_ERR_TIMEOUT); }
+};
+
+// s_k for every (request, state component): the f32 state, bf16(s_k) as the
+// vocabulary pass's A operand E and into the state columns of U.
+__global__ void rnn_state(const float *__restrict__ Gk, const float *__restrict__ P,
+                          float *__restrict__ state, bf16 *__restrict__ E, bf16 *__restrict__ U,
+                          int R, int gamma, int r, int k) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= R * r) return;
+  const int i = t / r, c = t % r;
+  const float *g_row = Gk + (size_t)i * 2 * r;
+  const float *p_row = P + ((size_t)i * gamma + k - 1) * 2 * r;
+  const float g = 1.f / (1.f + expf(-(g_row[c] + p_row[c])));
+  const float cand = tanhf(g_row[r + c] + p_row[r + c]);
+  const float s = (1.f - g) * state[t] + g * cand;
+  state[t] = s;
+  const bf16 sb = __float2bfloat16_rn(s);
+  E[t] = sb;
+  U[(size_t)i * 2 * r + c] = sb;
+}
+
+struct RnnWs {
+  MarkovWs mk;
+  bf16 *U;        // [R, 2r]  [bf16(s_{k-1}) | W1[x_{k-1}]]
+  float *state;   // [R, r]
+  float *Gk;      // [R, 2r]  W_rec U of the current step
+  float *P;       // [R * gamma, 2r]  W_hid h of every position
+  size_t bytes;
+};
+
+RnnWs rnn_layout(const dspark_dims *d, char *base) {
+  RnnWs w;
+  w.mk = markov_layout(d, base);
+  size_t off = w.mk.bytes;
+  const size_t R = d->R, G = d->gamma, r = d->r;
+  w.U = (bf16 *)(base + off);
+  off = dspark_align_up(off + sizeof(bf16) * R * 2 * r, 256);
+  w.state = (float *)(base + off);
+  off = dspark_align_up(off + sizeof(float) * R * r, 256);
+  w.Gk = (float *)(base + off);
+  off = dspark_align_up(off + sizeof(float) * R * 2 * r, 256);
+  w.P = (float *)(base + off);
+  off = dspark_align_up(off + sizeof(float) * R * G * 2 * r, 256);
+  w.bytes = off;
+  return w;
+}
+
+}  // namespace
+
+extern "C" size_t dspark_rnn_workspace_bytes(const dspark_dims *dims) {
+  if (!dspark_dims_ok(dims)) return 0;
+  return rnn_layout(dims, nullptr).bytes;
+}
+
+extern "C" int dspark_rnn_draft(const dspark_dims *dims, const void *base_logits, const void *h,
+                                const int32_t *anchor, const void *W1, const void *W2t,
+                                const void *W_rec, const void *W_hid, const void *w_conf,
+                                const float *T, float tau, uint64_t seed, int32_t *tokens,
+                                float *conf, float *logp_d, float *lse_d, void *workspace,
+                                size_t workspace_bytes, dspark_stream_t stream) {
+  if (!dspark_dims_ok(dims) || !base_logits || !h || !anchor || !W1 || !W2t || !W_rec ||
+      !W_hid || !w_conf || !T || !tokens || !conf || !(tau >= 0.f))
+    return DSPARK_ERR_ARG;
+  if (((uintptr_t)W2t | (uintptr_t)W1 | (uintptr_t)h | (uintptr_t)base_logits |
+       (uintptr_t)W_rec | (uintptr_t)W_hid) & 15)
+    return DSPARK_ERR_ARG;  // TMA and 16-byte vector loads
+  RnnWs ws = rnn_layout(dims, (char *)workspace);
+  if (!workspace || workspace_bytes < ws.bytes || ((uintptr_t)workspace & 255))
+    return DSPARK_ERR_WORKSPACE;
+  const int R = dims->R, G = dims->gamma, V = dims->V, r = dims->r, d = dims->d;
+  const bf16 *w_e = (const bf16 *)w_conf + d;
+  const float inv_tau = tau > 0.f ? 1.f / tau : 1.f;
+  conf_hidden<<<R * G, 128, 0, stream>>>((const bf16 *)h, (const bf16 *)w_conf, ws.mk.zh, d);
+  DSPARK_CHECK_LAUNCH();
+  // W_hid h for all positions at once
+  int rc = gemm::launch<4, 256>(h, W_hid, R * G, 2 * r, d, EpiStoreF32{ws.P, R * G, 2 * r},
+                                stream);
+  if (rc != DSPARK_OK) return rc;
+  if (cudaMemsetAsync(ws.U, 0, sizeof(bf16) * (size_t)R * 2 * r, stream) != cudaSuccess ||
+      cudaMemsetAsync(ws.state, 0, sizeof(float) * (size_t)R * r, stream) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  step_prep<<<(R * 32 + 255) / 256, 256, 0, stream>>>(anchor, tokens, (const bf16 *)W1, w_e,
+                                                     ws.mk.zh, T, ws.U + r, 2 * r, conf, R, G,
+                                                     V, r, 1);
+  DSPARK_CHECK_LAUNCH();
+  for (int k = 1; k <= G; ++k) {
+    rc = gemm::launch<4, 256>(ws.U, W_rec, R, 2 * r, 2 * r, EpiStoreF32{ws.Gk, R, 2 * r},
+                              stream, nullptr, true);
+    if (rc != DSPARK_OK) return rc;
+    rnn_state<<<(R * r + 255) / 256, 256, 0, stream>>>(ws.Gk, ws.P, ws.state, ws.mk.E, ws.U,
+                                                       R, G, r, k);
+    DSPARK_CHECK_LAUNCH();
+    if (tau > 0.f) {
+      const int n_parts = logits_parts<MODE_SAMPLE>(V);
+      EpiLogits<MODE_SAMPLE> epi{(const bf16 *)base_logits, nullptr, nullptr, nullptr, nullptr,
+                                 ws.mk.part, R, V, G, k, n_parts, inv_tau, seed};
+      rc = gemm::launch<LogitsCfg<MODE_SAMPLE>::EPI_WARPS, LogitsCfg<MODE_SAMPLE>::BN>(
+          ws.mk.E, W2t, R, V, r, epi, stream, nullptr, true);
+      if (rc != DSPARK_OK) return rc;
+      if (dspark_launch_pdl(reduce_prep<MODE_SAMPLE>, dim3(R), dim3(RP_THREADS), 0, stream,
+                            ws.mk.part, n_parts, G, V, r, k, tokens, lse_d, logp_d,
+                            (const bf16 *)W1, w_e, ws.mk.zh, T, ws.mk.E, ws.U + r, 2 * r, conf,
+                            (const bf16 *)base_logits, (const bf16 *)W2t, inv_tau,
+                            seed) != cudaSuccess)
+        return DSPARK_ERR_CUDA;
+    } else {
+      const int n_parts = logits_parts<MODE_GREEDY>(V);
+      EpiLogits<MODE_GREEDY> epi{(const bf16 *)base_logits, nullptr, nullptr, nullptr, nullptr,
+                                 ws.mk.part, R, V, G, k, n_parts, 1.f, seed};
+      rc = gemm::launch<LogitsCfg<MODE_GREEDY>::EPI_WARPS, LogitsCfg<MODE_GREEDY>::BN>(
+          ws.mk.E, W2t, R, V, r, epi, stream, nullptr, true);
+      if (rc != DSPARK_OK) return rc;
+      if (dspark_launch_pdl(reduce_prep<MODE_GREEDY>, dim3(R), dim3(RP_THREADS), 0, stream,
+                            ws.mk.part, n_parts, G, V, r, k, tokens, lse_d, logp_d,
+                            (const bf16 *)W1, w_e, ws.mk.zh, T, ws.mk.E, ws.U + r, 2 * r, conf,
+                            (const bf16 *)base_logits, (const bf16 *)W2t, inv_tau,
+                            seed) != cudaSuccess)
+        return DSPARK_ERR_CUDA;
+    }
+    DSPARK_CHECK_LAUNCH();
+  }
+  dspark_count_launches(2 + 2 * (uint64_t)G);  // + the GEMMs, counted by launch()
+  return DSPARK_OK;
 }
 
 // ---------------------------------------------------------------------------

@@ -464,3 +464,60 @@ def test_run_host_matches_device_rounds():
         for k in ("tokens", "len", "accepted", "bonus"):
             assert np.array_equal(outs[t][k].numpy(), want[t][k]), (t, k)
     assert dsp.dspark_device_status() == 0
+
+
+# ------------------------------------------------------- the RNN head -----
+
+def _rnn_weights(R, G, V, r, d, seed, scale=2.0):
+    inp = _weights(R, G, V, r, d, seed=seed)
+    g = torch.Generator().manual_seed(seed + 9)
+    W_gc = (torch.randn((2 * r, 2 * r + d), generator=g) * (scale / math.sqrt(2 * r + d)))
+    return inp, W_gc.to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("shape", [(4, 5, 1024, 64, 256), (37, 4, 1000, 128, 320),
+                                   (130, 3, 2056, 64, 192)])
+@pytest.mark.parametrize("tau", [0.0, 1.0])
+def test_rnn_draft_matches_oracle(shape, tau):
+    R, G, V, r, d = shape
+    inp, W_gc = _rnn_weights(R, G, V, r, d, seed=500 + V)
+    base = workloads.random_normal((R, G, V), 1.0, 501 + V)
+    orc = oracle.rnn_draft(base, inp["h"], inp["anchor"], inp["W1"], inp["W2"], W_gc,
+                           inp["w_conf"], inp["T"], tau, seed=4242, keep_scores=True)
+    head = dsp.DraftHead.from_weights(R, G, inp["W_lm"], inp["W1"], inp["W2"], inp["w_conf"],
+                                      inp["T"])
+    rnd = dsp.Round(head)
+    rnd.base.copy_(dev(base.reshape(R * G, V)))
+    ws = dsp.workspace(dsp.dspark_rnn_workspace_bytes(head.dims))
+    W_rec = dev(W_gc[:, :2 * r]).contiguous()
+    W_hid = dev(W_gc[:, 2 * r:]).contiguous()
+    dsp.dspark_rnn_draft(head.dims, rnd.base, dev(inp["h"], torch.bfloat16).contiguous(),
+                         dev(inp["anchor"]), head.W1, head.W2t, W_rec, W_hid, head.w_conf, head.T,
+                         tau, 4242, rnd.tokens, rnd.conf, rnd.logp_d, rnd.lse_d, ws)
+    torch.cuda.synchronize()
+    # the f32 state crosses bf16 roundings that the float64 oracle may take the
+    # other way: a wider tie band than the Markov head's 1e-3
+    rep = compare_draft(rnd.tokens, rnd.conf, rnd.lse_d if tau > 0 else None,
+                        rnd.logp_d if tau > 0 else None, orc, tau, tol_rel=3e-3)
+    assert rep.compared >= R
+    assert rep.flagged <= max(3, rep.compared // 10)
+    assert dsp.dspark_device_status() == 0
+
+
+def test_rnn_draft_without_weights_is_parallel_drafting():
+    R, G, V, r, d = 9, 3, 1000, 64, 128
+    inp, W_gc = _rnn_weights(R, G, V, r, d, seed=77)
+    base = workloads.random_normal((R, G, V), 1.0, 78)
+    head = dsp.DraftHead.from_weights(R, G, inp["W_lm"], inp["W1"], inp["W2"], inp["w_conf"],
+                                      inp["T"])
+    rnd = dsp.Round(head)
+    rnd.base.copy_(dev(base.reshape(R * G, V)))
+    ws = dsp.workspace(dsp.dspark_rnn_workspace_bytes(head.dims))
+    zero = torch.zeros((2 * r, 2 * r + d), dtype=torch.bfloat16, device="cuda")
+    dsp.dspark_rnn_draft(head.dims, rnd.base, dev(inp["h"], torch.bfloat16).contiguous(),
+                         dev(inp["anchor"]), head.W1, head.W2t, zero[:, :2 * r].contiguous(),
+                         zero[:, 2 * r:].contiguous(), head.w_conf, head.T, 0.0, 0, rnd.tokens,
+                         rnd.conf, None, None, ws)
+    want = torch.argmax(base.float(), dim=2)  # first maximum on ties
+    assert torch.equal(rnd.tokens.cpu().long(), want)
+    assert dsp.dspark_device_status() == 0
