@@ -413,8 +413,9 @@ extern "C" int dspark_rnn_draft(const dspark_dims *dims, const void *base_logits
   conf_hidden<<<R * G, 128, 0, stream>>>((const bf16 *)h, (const bf16 *)w_conf, ws.mk.zh, d);
   DSPARK_CHECK_LAUNCH();
   // W_hid h for all positions at once
-  int rc = gemm::launch<4, 256>(h, W_hid, R * G, 2 * r, d, EpiStoreF32{ws.P, R * G, 2 * r},
-                                stream);
+  // 64-wide N tiles: 2r = 1024 columns would give only a few dozen 256-wide tiles
+  int rc = gemm::launch<4, 64>(h, W_hid, R * G, 2 * r, d, EpiStoreF32{ws.P, R * G, 2 * r},
+                               stream);
   if (rc != DSPARK_OK) return rc;
   if (cudaMemsetAsync(ws.U, 0, sizeof(bf16) * (size_t)R * 2 * r, stream) != cudaSuccess ||
       cudaMemsetAsync(ws.state, 0, sizeof(float) * (size_t)R * r, stream) != cudaSuccess)
@@ -424,8 +425,8 @@ extern "C" int dspark_rnn_draft(const dspark_dims *dims, const void *base_logits
                                                      V, r, 1);
   DSPARK_CHECK_LAUNCH();
   for (int k = 1; k <= G; ++k) {
-    rc = gemm::launch<4, 256>(ws.U, W_rec, R, 2 * r, 2 * r, EpiStoreF32{ws.Gk, R, 2 * r},
-                              stream, nullptr, true);
+    rc = gemm::launch<4, 64>(ws.U, W_rec, R, 2 * r, 2 * r, EpiStoreF32{ws.Gk, R, 2 * r},
+                             stream, nullptr, true);
     if (rc != DSPARK_OK) return rc;
     rnn_state<<<(R * r + 255) / 256, 256, 0, stream>>>(ws.Gk, ws.P, ws.state, ws.mk.E, ws.U,
                                                        R, G, r, k);

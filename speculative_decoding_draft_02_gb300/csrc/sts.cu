@@ -7,8 +7,11 @@
 // cumulative prefix survival probability.  So position j picks, from a grid,
 // the T of least ECE of a_j = a_{j-1} * sigmoid(z_j / T) (f32, left to right)
 // against the label "drafts 1..j all accepted".  With n_bins equal-width bins,
-// ECE = sum_b |sum_{n in b} (label_n - a_n)| / N, so one f64 sum per
-// (grid value, bin) is all the state a position needs.
+// ECE = sum_b |sum_{n in b} (label_n - a_n)| / N, so one sum per (grid value,
+// bin) is all the state a position needs.  The sums are kept in 64-bit fixed
+// point (2^-32 units; each term rounds by at most 2^-33, so the ECE moves by at
+// most 2^-33): integer atomics, native in shared memory and independent of the
+// order in which samples arrive.
 //
 // Per position, three launches: sts_hist (n_grid x chunks CTAs; a CTA bins one
 // chunk of samples for one grid value in shared memory and adds its sums to
@@ -28,14 +31,16 @@ __device__ __forceinline__ float sigmoid_over(float z, float T) {
   return 1.f / (1.f + expf(-(z / T)));
 }
 
-// D[g][b] += sum over the CTA's samples in bin b of (label - a_j(T_g)).
+constexpr float FIX_ONE = 4294967296.f;  // 2^32: one unit of label - a
+
+// D[g][b] += sum over the CTA's samples in bin b of (label - a_j(T_g)), in 2^-32 units.
 __global__ void __launch_bounds__(STS_THREADS) sts_hist(
     const float *__restrict__ z, const int32_t *__restrict__ accepted,
     const float *__restrict__ a_prev, const float *__restrict__ grid, int N, int gamma, int j,
-    int n_bins, int chunk, double *__restrict__ D) {
-  __shared__ double sd[STS_MAX_BINS];
+    int n_bins, int chunk, unsigned long long *__restrict__ D) {
+  __shared__ unsigned long long sd[STS_MAX_BINS];
   const int g = blockIdx.x, tid = threadIdx.x;
-  for (int b = tid; b < n_bins; b += STS_THREADS) sd[b] = 0.0;
+  for (int b = tid; b < n_bins; b += STS_THREADS) sd[b] = 0ull;
   __syncthreads();
   const float T = grid[g];
   if (!(T > 0.f) && tid == 0 && blockIdx.y == 0) dspark_set_status(DSPARK_ERR_ARG);
@@ -46,17 +51,20 @@ __global__ void __launch_bounds__(STS_THREADS) sts_hist(
     const float a = j ? __fmul_rn(a_prev[n], c) : c;
     int b = (int)__fmul_rn(a, nb);
     b = b < 0 ? 0 : (b >= n_bins ? n_bins - 1 : b);
-    const double label = accepted[n] >= j + 1 ? 1.0 : 0.0;
-    atomicAdd(&sd[b], label - (double)a);
+    // label - a in fixed point: a * 2^32 is exact in f32, its rounding to an
+    // integer is the only error; negative sums wrap as two's complement
+    const long long qa = __float2ll_rn(__fmul_rn(a, FIX_ONE));
+    const long long q = (accepted[n] >= j + 1 ? (1ll << 32) : 0ll) - qa;
+    atomicAdd(&sd[b], (unsigned long long)q);
   }
   __syncthreads();
-  double *Dg = D + ((size_t)j * gridDim.x + g) * n_bins;
+  unsigned long long *Dg = D + ((size_t)j * gridDim.x + g) * n_bins;
   for (int b = tid; b < n_bins; b += STS_THREADS)
-    if (sd[b] != 0.0) atomicAdd(&Dg[b], sd[b]);
+    if (sd[b] != 0ull) atomicAdd(&Dg[b], sd[b]);
 }
 
 // ECE of every grid value at position j; the least (first on ties) is kept.
-__global__ void __launch_bounds__(STS_THREADS) sts_select(const double *__restrict__ D,
+__global__ void __launch_bounds__(STS_THREADS) sts_select(const unsigned long long *__restrict__ D,
                                                           const float *__restrict__ grid,
                                                           int n_grid, int n_bins, int N, int j,
                                                           float *__restrict__ T_out,
@@ -64,13 +72,13 @@ __global__ void __launch_bounds__(STS_THREADS) sts_select(const double *__restri
   __shared__ double sv[STS_THREADS / 32];
   __shared__ int si[STS_THREADS / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const double *Dj = D + (size_t)j * n_grid * n_bins;
+  const unsigned long long *Dj = D + (size_t)j * n_grid * n_bins;
   double best = INFINITY;
   int bg = 0x7fffffff;
   for (int g = tid; g < n_grid; g += STS_THREADS) {
     double e = 0.0;
-    for (int b = 0; b < n_bins; ++b) e += fabs(Dj[(size_t)g * n_bins + b]);
-    e /= (double)N;
+    for (int b = 0; b < n_bins; ++b) e += fabs((double)(long long)Dj[(size_t)g * n_bins + b]);
+    e = e / 4294967296.0 / (double)N;
     if (e < best) { best = e; bg = g; }  // g increases per thread: first on ties
   }
 #pragma unroll
@@ -134,7 +142,7 @@ __global__ void conf_logits(const bf16 *__restrict__ h, const int32_t *__restric
 
 struct StsWs {
   float *a_prev;
-  double *D;
+  unsigned long long *D;  // fixed-point sums [gamma][n_grid][n_bins]
   size_t bytes;
 };
 
@@ -143,8 +151,8 @@ StsWs sts_layout(int N, int gamma, int n_grid, int n_bins, char *base) {
   size_t off = 0;
   w.a_prev = (float *)(base + off);
   off = dspark_align_up(off + sizeof(float) * (size_t)N, 256);
-  w.D = (double *)(base + off);
-  off = dspark_align_up(off + sizeof(double) * (size_t)gamma * n_grid * n_bins, 256);
+  w.D = (unsigned long long *)(base + off);
+  off = dspark_align_up(off + sizeof(unsigned long long) * (size_t)gamma * n_grid * n_bins, 256);
   w.bytes = off;
   return w;
 }
@@ -171,7 +179,7 @@ extern "C" int dspark_sts_fit(const float *z, const int32_t *accepted, int32_t N
   StsWs ws = sts_layout(N, gamma, n_grid, n_bins, (char *)workspace);
   if (!workspace || workspace_bytes < ws.bytes || ((uintptr_t)workspace & 255))
     return DSPARK_ERR_WORKSPACE;
-  if (cudaMemsetAsync(ws.D, 0, sizeof(double) * (size_t)gamma * n_grid * n_bins, stream) !=
+  if (cudaMemsetAsync(ws.D, 0, sizeof(unsigned long long) * (size_t)gamma * n_grid * n_bins, stream) !=
       cudaSuccess)
     return DSPARK_ERR_CUDA;
   // about four CTAs per SM over the grid values and sample chunks
