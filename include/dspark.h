@@ -260,6 +260,15 @@ int dspark_verify(const dspark_dims *dims, const int32_t *anchor, const int32_t 
                   int32_t *bonus, void *workspace, size_t workspace_bytes,
                   dspark_stream_t stream);
 
+/* Failure detection self-test (no fault is involved).  Every device-side wait
+ * of the library is bounded in time; on expiry the kernel records
+ * DSPARK_ERR_TIMEOUT in the device status word and returns, and the context
+ * stays usable.  This call runs that path: one CTA waits, with the library's
+ * own bounded wait capped at limit_ns (1 ns .. 2 s), on an mbarrier that
+ * nothing arrives on.  Afterwards dspark_device_status reports
+ * DSPARK_ERR_TIMEOUT.  Returns DSPARK_ERR_ARG for a limit outside that range. */
+int dspark_selftest_wait_timeout(uint64_t limit_ns, dspark_stream_t stream);
+
 /* Bytes of scratch the library keeps inside itself for dspark_markov_draft_static. */
 #define DSPARK_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
 

@@ -31,7 +31,7 @@ EXPORTS = [
     "dspark_device_status", "dspark_error_string", "dspark_launch_count",
     "dspark_markov_draft_static", "dspark_schedule_async", "dspark_conf_logits",
     "dspark_sts_workspace_bytes", "dspark_sts_fit", "dspark_rnn_workspace_bytes",
-    "dspark_rnn_draft",
+    "dspark_rnn_draft", "dspark_selftest_wait_timeout",
 ]
 STATIC_SCRATCH_BYTES = 16 << 20
 
@@ -74,6 +74,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "dspark_sts_workspace_bytes": (SZ, [I32, I32, I32, I32]),
         "dspark_sts_fit": (ctypes.c_int, [P, P, I32, I32, P, I32, I32, P, P, P, SZ, P]),
         "dspark_rnn_workspace_bytes": (SZ, [DP]),
+        "dspark_selftest_wait_timeout": (ctypes.c_int, [U64, P]),
         "dspark_rnn_draft": (ctypes.c_int, [DP, P, P, P, P, P, P, P, P, P, F32, U64, P, P, P, P,
                                             P, SZ, P]),
         "dspark_verify_workspace_bytes": (SZ, [DP]),
@@ -238,6 +239,11 @@ def dspark_verify(dims, anchor, tokens, length, base_logits, W1, W2t, lse_d, log
 
 def dspark_device_status(stream=None, clear: bool = True) -> int:
     return int(load_library().dspark_device_status(_stream(stream), 1 if clear else 0))
+
+
+def dspark_selftest_wait_timeout(limit_ns: int, stream=None):
+    _check(load_library().dspark_selftest_wait_timeout(int(limit_ns), _stream(stream)),
+           "dspark_selftest_wait_timeout")
 
 
 def dspark_launch_count() -> int:

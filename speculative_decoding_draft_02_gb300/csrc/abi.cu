@@ -14,6 +14,7 @@ int dspark_status_markov(int clear);
 int dspark_status_verify(int clear);
 int dspark_status_sched(int clear);
 int dspark_status_sts(int clear);
+int dspark_status_selftest(int clear);
 
 extern "C" uint64_t dspark_launch_count(void) { return g_launches.load(); }
 
@@ -35,9 +36,9 @@ extern "C" const char *dspark_error_string(int code) {
 extern "C" int dspark_device_status(dspark_stream_t stream, int clear) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return DSPARK_ERR_CUDA;
   int first = DSPARK_OK;
-  const int vals[5] = {dspark_status_lmhead(clear), dspark_status_markov(clear),
+  const int vals[6] = {dspark_status_lmhead(clear), dspark_status_markov(clear),
                        dspark_status_verify(clear), dspark_status_sched(clear),
-                       dspark_status_sts(clear)};
+                       dspark_status_sts(clear),    dspark_status_selftest(clear)};
   for (int v : vals)
     if (first == DSPARK_OK && v != DSPARK_OK) first = v;
   return first;

@@ -66,16 +66,17 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
   return ok != 0;
 }
 
-// Wait for the phase of `parity` to complete.  Gives up after WAIT_LIMIT_NS or
+// Wait for the phase of `parity` to complete.  Gives up after limit_ns or
 // when another role of the CTA has raised `abort`; returns false then.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                          uint64_t limit_ns = WAIT_LIMIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait_sleep(bar, parity)) return true;
     if ((it & 15) == 0) {
       if (*abort) return false;
-      if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+      if (globaltimer() - t0 > limit_ns) {
         *abort = 1;
         return false;
       }

@@ -94,6 +94,27 @@ def test_null_pointers_and_short_tables_rejected(lib):
                              fake, -1.0, 0, fake, fake, fake, 1 << 30, None) == 1
 
 
+def test_new_entry_points_check_arguments_without_launch(lib):
+    d = dsp.dims_of(4, 5, 1024, 64, 256)
+    fake = ctypes.c_void_p(256)
+    # the bounded-wait self-test takes 1 ns .. 2 s
+    assert lib.dspark_selftest_wait_timeout(0, None) == 1
+    assert lib.dspark_selftest_wait_timeout(3_000_000_000, None) == 1
+    # the RNN head needs its recurrent weights, and a large enough workspace
+    assert lib.dspark_rnn_draft(ctypes.byref(d), fake, fake, fake, fake, fake, None, fake, fake,
+                                fake, 0.0, 0, fake, fake, None, None, fake, 1 << 30, None) == 1
+    assert lib.dspark_rnn_draft(ctypes.byref(d), fake, fake, fake, fake, fake, fake, fake, fake,
+                                fake, 0.0, 0, fake, fake, None, None, fake, 16, None) == 4
+    assert lib.dspark_rnn_workspace_bytes(ctypes.byref(d)) > lib.dspark_markov_workspace_bytes(
+        ctypes.byref(d))
+    # STS: at most 64 bins; the asynchronous schedule needs its ring
+    assert lib.dspark_sts_workspace_bytes(1000, 5, 51, 65) == 0
+    assert lib.dspark_sts_fit(fake, fake, 1000, 5, fake, 51, 65, fake, fake, fake, 1 << 30,
+                              None) == 1
+    assert lib.dspark_schedule_async(fake, 4, 5, fake, 24, None, fake, fake, fake, None, None,
+                                     None) == 1
+
+
 def test_binding_refuses_host_tensors():
     import torch
     d = dsp.dims_of(4, 5, 1024, 64, 256)
