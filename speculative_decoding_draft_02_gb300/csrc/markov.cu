@@ -18,14 +18,19 @@
 
 DSPARK_DECLARE_STATUS(s_status_markov)
 
+#include "markov_loop.cuh"
+
 namespace {
 
 // zh[m] = w_h . h[m] for every (request, position) row m; one CTA of 128
 // threads per row, each thread a strided quarter of the row's 16-byte words.
+// Block 0 also zeroes the loop's grid-barrier words (when given).
 __global__ void __launch_bounds__(128) conf_hidden(const bf16 *__restrict__ h,
                                                    const bf16 *__restrict__ w_conf,
-                                                   float *__restrict__ zh, int d) {
+                                                   float *__restrict__ zh, int d,
+                                                   mloop::LoopSync *sync) {
   const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (sync && row == 0 && tid == 0) *sync = mloop::LoopSync{0u, 0, {0u, 0u}};
   const uint4 *hr = reinterpret_cast<const uint4 *>(h + (size_t)row * d);
   const uint4 *wr = reinterpret_cast<const uint4 *>(w_conf);
   const int n8 = d / 8;
@@ -201,6 +206,7 @@ struct MarkovWs {
   float *zh;
   bf16 *E;
   RowPartial *part;
+  mloop::LoopSync *sync;
   size_t bytes;
 };
 
@@ -212,7 +218,12 @@ MarkovWs markov_layout(const dspark_dims *d, char *base) {
   w.E = (bf16 *)(base + off);
   off = dspark_align_up(off + sizeof(bf16) * (size_t)d->R * d->r, 256);
   w.part = (RowPartial *)(base + off);
-  off = dspark_align_up(off + sizeof(RowPartial) * (size_t)d->R * logits_parts_max(d->V), 256);
+  const size_t slots = mloop::loop_slots_max(d->V) > logits_parts_max(d->V)
+                          ? mloop::loop_slots_max(d->V)
+                          : logits_parts_max(d->V);
+  off = dspark_align_up(off + sizeof(RowPartial) * (size_t)d->R * slots, 256);
+  w.sync = (mloop::LoopSync *)(base + off);
+  off = dspark_align_up(off + sizeof(mloop::LoopSync), 256);
   w.bytes = off;
   return w;
 }
@@ -239,48 +250,28 @@ extern "C" int dspark_markov_draft(const dspark_dims *dims, const void *base_log
   if (!workspace || workspace_bytes < ws.bytes || ((uintptr_t)workspace & 255))
     return DSPARK_ERR_WORKSPACE;
   const int R = dims->R, G = dims->gamma, V = dims->V, r = dims->r, d = dims->d;
-  const int rows = R * G;
-  conf_hidden<<<rows, 128, 0, stream>>>((const bf16 *)h, (const bf16 *)w_conf, ws.zh, d);
-  DSPARK_CHECK_LAUNCH();
+  if (cudaMemsetAsync(ws.sync, 0, sizeof(mloop::LoopSync), stream) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
   const float inv_tau = tau > 0.f ? 1.f / tau : 1.f;
-  step_prep<<<(R * 32 + 255) / 256, 256, 0, stream>>>(anchor, tokens, (const bf16 *)W1,
-                                                     (const bf16 *)w_conf + d, ws.zh, T, ws.E,
-                                                     r, conf, R, G, V, r, 1);
-  DSPARK_CHECK_LAUNCH();
-  const bf16 *w_e = (const bf16 *)w_conf + d;
-  for (int k = 1; k <= G; ++k) {
-    int rc;
-    if (tau > 0.f) {
-      const int n_parts = logits_parts<MODE_SAMPLE>(V);
-      EpiLogits<MODE_SAMPLE> epi{(const bf16 *)base_logits, nullptr, nullptr, nullptr, nullptr,
-                                 ws.part, R, V, G, k, n_parts, inv_tau, seed};
-      rc = gemm::launch<LogitsCfg<MODE_SAMPLE>::EPI_WARPS, LogitsCfg<MODE_SAMPLE>::BN>(
-          ws.E, W2t, R, V, r, epi, stream, nullptr, true);
-      if (rc != DSPARK_OK) return rc;
-      if (dspark_launch_pdl(reduce_prep<MODE_SAMPLE>, dim3(R), dim3(RP_THREADS), 0, stream,
-                            ws.part, n_parts, G, V, r, k, tokens, lse_d, logp_d,
-                            (const bf16 *)W1, w_e, ws.zh, T, ws.E, ws.E, r, conf,
-                            (const bf16 *)base_logits, (const bf16 *)W2t, inv_tau,
-                            seed) != cudaSuccess)
-        return DSPARK_ERR_CUDA;
-    } else {
-      const int n_parts = logits_parts<MODE_GREEDY>(V);
-      EpiLogits<MODE_GREEDY> epi{(const bf16 *)base_logits, nullptr, nullptr, nullptr, nullptr,
-                                 ws.part, R, V, G, k, n_parts, 1.f, seed};
-      rc = gemm::launch<LogitsCfg<MODE_GREEDY>::EPI_WARPS, LogitsCfg<MODE_GREEDY>::BN>(
-          ws.E, W2t, R, V, r, epi, stream, nullptr, true);
-      if (rc != DSPARK_OK) return rc;
-      if (dspark_launch_pdl(reduce_prep<MODE_GREEDY>, dim3(R), dim3(RP_THREADS), 0, stream,
-                            ws.part, n_parts, G, V, r, k, tokens, lse_d, logp_d,
-                            (const bf16 *)W1, w_e, ws.zh, T, ws.E, ws.E, r, conf,
-                            (const bf16 *)base_logits, (const bf16 *)W2t, inv_tau,
-                            seed) != cudaSuccess)
-        return DSPARK_ERR_CUDA;
-    }
-    DSPARK_CHECK_LAUNCH();
+  // all gamma steps, with the confidence head, in one cooperative launch
+  mloop::LoopArgs la{(const bf16 *)base_logits, (const bf16 *)W1, (const bf16 *)W2t,
+                     (const bf16 *)h, (const bf16 *)w_conf, (const bf16 *)w_conf + d, anchor,
+                     ws.zh, T, ws.E, tokens, conf, lse_d, logp_d, ws.part, ws.sync, R, V, r, d, G, 0,
+                     inv_tau, seed};
+  const int sms = dspark_sm_count();
+  if (tau > 0.f) {
+    constexpr int EW = mloop::LoopCfg<MODE_SAMPLE>::EPI_WARPS;
+    const mloop::LoopGrid lg = mloop::loop_grid<MODE_SAMPLE>(R, V, sms);
+    la.n_slots = lg.n_slots;
+    // warps per request in the row phase: 4 while R is covered in one pass
+    if (R <= lg.grid * (EW / 4)) return mloop::launch_loop<MODE_SAMPLE, 4>(la, lg.grid, stream);
+    return mloop::launch_loop<MODE_SAMPLE, 2>(la, lg.grid, stream);
   }
-  dspark_count_launches(2 + (uint64_t)G);  // + one GEMM per step, counted by launch()
-  return DSPARK_OK;
+  constexpr int EW = mloop::LoopCfg<MODE_GREEDY>::EPI_WARPS;
+  const mloop::LoopGrid lg = mloop::loop_grid<MODE_GREEDY>(R, V, sms);
+  la.n_slots = lg.n_slots;
+  if (R <= lg.grid * (EW / 4)) return mloop::launch_loop<MODE_GREEDY, 4>(la, lg.grid, stream);
+  return mloop::launch_loop<MODE_GREEDY, 1>(la, lg.grid, stream);
 }
 
 int dspark_status_markov(int clear) {
@@ -410,7 +401,8 @@ extern "C" int dspark_rnn_draft(const dspark_dims *dims, const void *base_logits
   const int R = dims->R, G = dims->gamma, V = dims->V, r = dims->r, d = dims->d;
   const bf16 *w_e = (const bf16 *)w_conf + d;
   const float inv_tau = tau > 0.f ? 1.f / tau : 1.f;
-  conf_hidden<<<R * G, 128, 0, stream>>>((const bf16 *)h, (const bf16 *)w_conf, ws.mk.zh, d);
+  conf_hidden<<<R * G, 128, 0, stream>>>((const bf16 *)h, (const bf16 *)w_conf, ws.mk.zh, d,
+                                         nullptr);
   DSPARK_CHECK_LAUNCH();
   // W_hid h for all positions at once
   // 64-wide N tiles: 2r = 1024 columns would give only a few dozen 256-wide tiles

@@ -329,6 +329,19 @@ def test_verify_full_lengths(shape, tau):
     assert dsp.dspark_device_status() == 0
 
 
+@pytest.mark.parametrize("tau", [0.0, 1.0])
+def test_markov_draft_more_row_blocks_than_sms(tau):
+    """153 blocks of 128 requests: more M blocks than a GB300 has SMs, so a CTA
+    changes row block from one tile to the next and flushes a partial per tile."""
+    shape = (153 * 128, 2, 520, 64, 64)
+    rnd, orc = _draft_case(shape, tau, seed=280)
+    rep = compare_draft(rnd.tokens, rnd.conf, rnd.lse_d if tau > 0 else None,
+                        rnd.logp_d if tau > 0 else None, orc, tau)
+    assert rep.compared >= shape[0]
+    assert rep.flagged <= max(2, rep.compared // (50 if tau == 0 else 25))
+    assert dsp.dspark_device_status() == 0
+
+
 @pytest.mark.parametrize("shape,tau", [((3, 32, 520, 64, 64), 0.0), ((3, 32, 520, 64, 64), 1.0),
                                        ((37, 4, 1000, 128, 320), 0.05),
                                        ((37, 4, 1000, 128, 320), 4.0)])
