@@ -233,15 +233,24 @@ def cpu_inputs(w, inp_gpu):
     return out
 
 
+def sample_size(w, cpu, target, avail: int, target_s: float) -> int:
+    """Requests whose oracle round takes about target_s seconds, from the
+    marginal cost per request between a 1- and a 4-request probe (a round has
+    a fixed part that one probe alone would charge to its single request)."""
+    cpu["target"] = target[:4].cpu()
+    t1 = cpu_oracle_round(w, cpu, 1)
+    t4 = cpu_oracle_round(w, cpu, min(4, avail))
+    per = max((t4 - t1) / 3.0, 1e-4)
+    fixed = max(t1 - per, 0.0)
+    return int(max(1, min(avail, math.floor((target_s - fixed) / per))))
+
+
 def cpu_baseline(w, inp_gpu, S: int, target_s: float = 15.0):
     cpu = cpu_inputs(w, inp_gpu)
     cores = torch.get_num_threads()
-    # first a one-request probe to size the sample to about `target_s` seconds
-    cpu["target"] = inp_gpu["target"][:max(S, 1) if S else 1].cpu()
     if not S:
-        t1 = cpu_oracle_round(w, cpu, 1)
-        S = int(max(1, min(w.R, math.floor(target_s / max(t1, 1e-3)))))
-        cpu["target"] = inp_gpu["target"][:S].cpu()
+        S = sample_size(w, cpu, inp_gpu["target"], w.R, target_s)
+    cpu["target"] = inp_gpu["target"][:S].cpu()
     t = cpu_oracle_round(w, cpu, S)
     return {"value": S * w.gamma / t, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"one full round (LM head, {w.gamma}-step Markov loop, schedule, verify) "
@@ -266,13 +275,11 @@ def run_reference(args, w, ws, rank):
     cpu = cpu_inputs(w, inp)
     # size one step so that warmup + steps fit in about three minutes
     S = args.cpu_sample or 1
-    cpu["target"] = inp["target"][:S].cpu()
     avail = int(inp["h"].shape[0])  # requests built (all of them on a GPU machine)
     if not args.cpu_sample:
-        t1 = cpu_oracle_round(w, cpu, 1)
-        S = int(max(1, min(avail, math.floor(180.0 / (args.steps + args.warmup) / max(t1, 1e-3)))))
-        cpu["target"] = inp["target"][:S].cpu()
+        S = sample_size(w, cpu, inp["target"], avail, 180.0 / (args.steps + args.warmup))
     S = min(S, avail)
+    cpu["target"] = inp["target"][:S].cpu()
     for _ in range(args.warmup):
         cpu_oracle_round(w, cpu, S)
     times = [cpu_oracle_round(w, cpu, S) for _ in range(args.steps)]
@@ -359,8 +366,13 @@ def run_dspark(args, w, ws, rank, local):
     K_adm = int(rnd.K.item())
     acc = rnd.accepted.float().mean().item()
 
-    # roofline of the dominant kernel (the LM-head GEMM, tensor-bound)
+    # roofline of the dominant kernel (the LM-head GEMM, tensor-bound); a kernel
+    # timed inside a long loop runs under the power cap: the sustained peak
     peaks = measured_peaks()
+    long_run = ms * args.steps >= 500.0 and peaks["bf16_sustained"]
+    tc_peak = peaks["bf16_sustained"] if long_run else peaks["bf16"]
+    tc_kind = ("sustained bf16 (timed inside a loop of %.1f s)" % (ms * args.steps / 1e3)
+               if long_run else "burst bf16")
     flops = 2.0 * R * G * V * d
     ach_tf = flops / (stage["lm_head"] * 1e-3) / 1e12
     src = kernel_source_hash(LM_HEAD_SOURCES)
@@ -381,9 +393,9 @@ def run_dspark(args, w, ws, rank, local):
         "rounds_per_s": ws / (ms * 1e-3),
         "stages_ms": stage,
         "admitted_K": K_adm, "mean_accepted": acc,
-        "roofline": {"bound": "tensor", "achieved": ach_tf, "peak": peaks["bf16"],
-                     "unit": "TFLOP/s", "frac": ach_tf / peaks["bf16"], "traffic": traffic,
-                     "kernel": "lm_head", "peak_source": peaks["source"] + " burst bf16"},
+        "roofline": {"bound": "tensor", "achieved": ach_tf, "peak": tc_peak,
+                     "unit": "TFLOP/s", "frac": ach_tf / tc_peak, "traffic": traffic,
+                     "kernel": "lm_head", "peak_source": peaks["source"] + " " + tc_kind},
         "markov_loop_hbm": {"achieved": markov_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                             "frac": markov_gbs / peaks["hbm_gbs"]},
         "gpu_launches": launches,
