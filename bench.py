@@ -160,10 +160,11 @@ def kernel_source_hash(names):
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel: str, src_hash: str, units: float):
+def profiled_traffic(kernel: str, src_hash: str, units: float, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current source of that kernel (else None).  The summary states the bytes
-    of its captured launch and the units it processed; scaled by `units`."""
+    the current source of that kernel and on this workload (else None).  The
+    summary states the bytes of its captured launch and the units it processed;
+    scaled by `units`."""
     path = os.path.join(ROOT, "profiles", f"{kernel}.txt")
     if not os.path.exists(path):
         return None
@@ -172,7 +173,7 @@ def profiled_traffic(kernel: str, src_hash: str, units: float):
         if ":" in line and not line.startswith(" "):
             k, v = line.split(":", 1)
             kv[k.strip()] = v.strip()
-    if kv.get("source_hash") != src_hash:
+    if kv.get("source_hash") != src_hash or kv.get("workload", "").split()[:1] != [workload]:
         return None
     try:
         b = float(kv["dram_bytes_per_launch"])
@@ -373,12 +374,26 @@ def run_dspark(args, w, ws, rank, local):
     tc_peak = peaks["bf16_sustained"] if long_run else peaks["bf16"]
     tc_kind = ("sustained bf16 (timed inside a loop of %.1f s)" % (ms * args.steps / 1e3)
                if long_run else "burst bf16")
-    flops = 2.0 * R * G * V * d
-    ach_tf = flops / (stage["lm_head"] * 1e-3) / 1e12
+    ridge = tc_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)  # FLOP per byte where the bounds meet
+
+    def roofline(flops, nbytes, t_ms):
+        """Against the tensor peak above the ridge, against HBM below it."""
+        if flops / nbytes >= ridge:
+            ach = flops / (t_ms * 1e-3) / 1e12
+            return {"bound": "tensor", "achieved": ach, "peak": tc_peak, "unit": "TFLOP/s",
+                    "frac": ach / tc_peak, "peak_source": peaks["source"] + " " + tc_kind}
+        ach = nbytes / (t_ms * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"], "peak_source": peaks["source"] + " copy"}
+
+    # LM head: 2 M V d FLOP over W_lm, h and the base logits (M = R gamma rows)
+    lm_roof = roofline(2.0 * R * G * V * d, 2.0 * (V * d + R * G * d + R * G * V), stage["lm_head"])
     src = kernel_source_hash(LM_HEAD_SOURCES)
-    traffic = profiled_traffic("lm_head", src, R * G)
-    # the Markov loop against HBM: algorithmic bytes of one draft loop
+    lm_roof.update({"traffic": profiled_traffic("lm_head", src, R * G, w.name),
+                    "kernel": "lm_head"})
+    # the Markov loop: per step W2t, the base-logit rows and E; 2 R r V FLOP
     markov_bytes = G * (V * r * 2 + R * V * 2 + R * r * 2)
+    markov_roof = roofline(G * 2.0 * R * r * V, markov_bytes, stage["markov_loop"])
     markov_gbs = markov_bytes / (stage["markov_loop"] * 1e-3) / 1e9
 
     line = {
@@ -393,9 +408,8 @@ def run_dspark(args, w, ws, rank, local):
         "rounds_per_s": ws / (ms * 1e-3),
         "stages_ms": stage,
         "admitted_K": K_adm, "mean_accepted": acc,
-        "roofline": {"bound": "tensor", "achieved": ach_tf, "peak": tc_peak,
-                     "unit": "TFLOP/s", "frac": ach_tf / tc_peak, "traffic": traffic,
-                     "kernel": "lm_head", "peak_source": peaks["source"] + " " + tc_kind},
+        "roofline": lm_roof,
+        "markov_loop_roofline": markov_roof,
         "markov_loop_hbm": {"achieved": markov_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                             "frac": markov_gbs / peaks["hbm_gbs"]},
         "gpu_launches": launches,
