@@ -118,7 +118,8 @@ __global__ void __launch_bounds__(256) verify_rows(const bf16 *__restrict__ targ
   }
 }
 
-// Pass 2: walk each request's admitted prefix; one thread per request.
+// Pass 2: one warp per request; lane j - 1 tests admitted position j (j <= l_r)
+// and a ballot finds the first failure.
 template <int MODE>
 __global__ void verify_decide(const SegStat *__restrict__ stat, const bf16 *__restrict__ target,
                               const int32_t *__restrict__ anchor,
@@ -128,60 +129,70 @@ __global__ void verify_decide(const SegStat *__restrict__ stat, const bf16 *__re
                               int *__restrict__ count, int32_t *__restrict__ accepted,
                               int32_t *__restrict__ bonus, int R, int gamma, int V, float inv_tau,
                               uint64_t seed) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= R) return;
-  const int L = clamp_len(len, i, gamma);
+  const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (i >= R) return;  // warp-uniform
+  const int L = clamp_len(len, i, gamma);  // gamma <= 32: one lane per position
   const SegStat *st = stat + (size_t)i * (gamma + 1) * NSEG;
   const int32_t *x = tokens + (size_t)i * gamma;
-  int n = L;
+  const int j = lane + 1;  // this lane's 1-based position
   if (MODE == MODE_GREEDY) {
-    auto row_argmax = [&](int j) {  // 0-based row
+    auto row_argmax = [&](int jr) {  // 0-based row
       float b = -INFINITY;
       int id = 0x7fffffff;
       for (int g = 0; g < NSEG; ++g)
-        if (better(st[j * NSEG + g].best, st[j * NSEG + g].idx, b, id)) {
-          b = st[j * NSEG + g].best;
-          id = st[j * NSEG + g].idx;
+        if (better(st[jr * NSEG + g].best, st[jr * NSEG + g].idx, b, id)) {
+          b = st[jr * NSEG + g].best;
+          id = st[jr * NSEG + g].idx;
         }
       return id;
     };
-    for (int j = 1; j <= L; ++j)
-      if (x[j - 1] != row_argmax(j - 1)) { n = j - 1; break; }
-    accepted[i] = n;
-    bonus[i] = row_argmax(n);
+    const bool fail = j <= L && x[j - 1] != row_argmax(j - 1);
+    const unsigned bal = __ballot_sync(0xffffffffu, fail);
+    const int n = bal ? __ffs(bal) - 1 : L;  // first failing position - 1
+    if (lane == 0) {
+      accepted[i] = n;
+      bonus[i] = row_argmax(n);
+    }
     return;
   }
-  ResampleRow rr;
-  rr.kind = KIND_BONUS;
-  rr.pos = L + 1;
-  rr.prev = 0;
-  rr.lse_t = 0.f;
-  rr.lse_d = 0.f;
-  rr.pad[0] = rr.pad[1] = rr.pad[2] = 0;
-  for (int j = 1; j <= L; ++j) {
+  // sampling: accept x_j iff u * p_d(x_j) < p_t(x_j), tested in logs
+  bool fail = false;
+  float lse_t = 0.f;
+  if (j <= L) {
     float m = -INFINITY, s = 0.f;
     for (int g = 0; g < NSEG; ++g) lse_merge(m, s, st[(j - 1) * NSEG + g].m, st[(j - 1) * NSEG + g].s);
-    const float lse_t = m + logf(s);
+    lse_t = m + logf(s);
     int xj = x[j - 1];
     if (xj < 0 || xj >= V) { dspark_set_status(DSPARK_ERR_TOKEN); xj = 0; }
     const float tx = __bfloat162float(target[((size_t)i * (gamma + 1) + j - 1) * V + xj]) * inv_tau;
     const uint4 w = rng_words4(seed, 0u, (uint32_t)j, (uint32_t)i, RNG_ACCEPT);
     const float u = rng_uniform(w.x);
-    const size_t o = (size_t)i * gamma + j - 1;
-    if (logf(u) + logp_d[o] < tx - lse_t) continue;  // u * p_d(x_j) < p_t(x_j): accepted
-    n = j - 1;
-    rr.kind = KIND_RESIDUAL;
-    rr.pos = j;
-    int prev = (j == 1) ? anchor[i] : x[j - 2];
-    if (prev < 0 || prev >= V) { dspark_set_status(DSPARK_ERR_TOKEN); prev = 0; }
-    rr.prev = prev;
-    rr.lse_t = lse_t;
-    rr.lse_d = lse_d[o];
-    list[atomicAdd(count, 1)] = i;  // compacted residual rows (order irrelevant)
-    break;
+    fail = !(logf(u) + logp_d[(size_t)i * gamma + j - 1] < tx - lse_t);
   }
-  accepted[i] = n;
-  rows[i] = rr;
+  const unsigned bal = __ballot_sync(0xffffffffu, fail);
+  const int jf = bal ? __ffs(bal) : 0;  // first rejected position (1-based), 0 if none
+  if (lane == (jf ? jf - 1 : 0)) {
+    ResampleRow rr;
+    rr.pad[0] = rr.pad[1] = rr.pad[2] = 0;
+    if (jf) {
+      rr.kind = KIND_RESIDUAL;
+      rr.pos = jf;
+      int prev = (jf == 1) ? anchor[i] : x[jf - 2];
+      if (prev < 0 || prev >= V) { dspark_set_status(DSPARK_ERR_TOKEN); prev = 0; }
+      rr.prev = prev;
+      rr.lse_t = lse_t;
+      rr.lse_d = lse_d[(size_t)i * gamma + jf - 1];
+      list[atomicAdd(count, 1)] = i;  // compacted residual rows (order irrelevant)
+    } else {
+      rr.kind = KIND_BONUS;
+      rr.pos = L + 1;
+      rr.prev = 0;
+      rr.lse_t = 0.f;
+      rr.lse_d = 0.f;
+    }
+    accepted[i] = jf ? jf - 1 : L;
+    rows[i] = rr;
+  }
 }
 
 // E[slot] = W1[x_{j*-1}] of the slot's request.
@@ -276,7 +287,7 @@ __global__ void __launch_bounds__(256) resample_reduce(
 // 3), or the rejected row when its residual was empty (stream 2), drawn from
 // softmax(t / tau) in two levels.  One CTA of 512 threads per request: pass 1
 // leaves log Z_b of every 64-id block in shared memory (eight lanes per block,
-// one 16-byte word each, four words in flight), pass 2 scores the blocks (one
+// one 16-byte word each, eight words in flight), pass 2 scores the blocks (one
 // Philox call per four blocks), pass 3 draws inside the best block.
 constexpr int BONUS_THREADS = 512;
 constexpr size_t BONUS_MAX_SMEM = 220 * 1024;  // log Z_b of up to 56320 blocks: V <= 3604480
@@ -287,7 +298,7 @@ __global__ void __launch_bounds__(BONUS_THREADS) bonus_row(const ResampleRow *__
                                                            int V, float inv_tau, uint64_t seed) {
   extern __shared__ float s_lz[];  // [n_blocks]: log Z_b
   constexpr float LOG2E = 1.4426950408889634f, LN2 = 0.6931471805599453f;
-  constexpr int GROUPS = BONUS_THREADS / 8, U = 4;
+  constexpr int GROUPS = BONUS_THREADS / 8, U = 8;
   const int i = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const ResampleRow rr = rows[i];
   if (rr.kind != KIND_BONUS && rr.kind != KIND_FALLBACK) return;
@@ -431,7 +442,7 @@ extern "C" int dspark_verify(const dspark_dims *dims, const int32_t *anchor, con
   if (!sample) {
     verify_rows<MODE_GREEDY><<<rgrid, 256, 0, stream>>>(tgt, len, ws.stat, ws.count, G, V, inv_tau);
     DSPARK_CHECK_LAUNCH();
-    verify_decide<MODE_GREEDY><<<(R + 127) / 128, 128, 0, stream>>>(
+    verify_decide<MODE_GREEDY><<<(R * 32 + 255) / 256, 256, 0, stream>>>(
         ws.stat, tgt, anchor, tokens, len, lse_d, logp_d, ws.rows, ws.list, ws.count, accepted,
         bonus, R, G, V, inv_tau, seed);
     DSPARK_CHECK_LAUNCH();
@@ -447,7 +458,7 @@ extern "C" int dspark_verify(const dspark_dims *dims, const int32_t *anchor, con
     return DSPARK_ERR_CUDA;
   verify_rows<MODE_SAMPLE><<<rgrid, 256, 0, stream>>>(tgt, len, ws.stat, ws.count, G, V, inv_tau);
   DSPARK_CHECK_LAUNCH();
-  verify_decide<MODE_SAMPLE><<<(R + 127) / 128, 128, 0, stream>>>(
+  verify_decide<MODE_SAMPLE><<<(R * 32 + 255) / 256, 256, 0, stream>>>(
       ws.stat, tgt, anchor, tokens, len, lse_d, logp_d, ws.rows, ws.list, ws.count, accepted,
       bonus, R, G, V, inv_tau, seed);
   DSPARK_CHECK_LAUNCH();
