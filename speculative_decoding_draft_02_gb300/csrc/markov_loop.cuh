@@ -22,8 +22,9 @@
 //   grid barrier                (k < gamma)
 //
 // Before step 1 a prologue row phase gathers E_1 = W1[anchor] and c_1.  The
-// hidden-state part of each confidence, w_h . h_k, is taken in the row phase
-// that writes c_k.
+// hidden-state part of c_{k+1}, w_h . h_{k+1}, does not depend on x_k: the
+// epilogue warps take it at the start of step k, while the step's first
+// accumulator is computed, and the row phase only adds w_e . W1[x_k].
 //
 // W2t and the base logits do not depend on x_k: before the second barrier the
 // producer already issues the W2t halves of the next step's first stages and
