@@ -395,6 +395,20 @@ def run_dspark(args, w, ws, rank, local):
     markov_bytes = G * (V * r * 2 + R * V * 2 + R * r * 2)
     markov_roof = roofline(G * 2.0 * R * r * V, markov_bytes, stage["markov_loop"])
     markov_gbs = markov_bytes / (stage["markov_loop"] * 1e-3) / 1e9
+    # verify against HBM over the rows it reads (the round's own lengths)
+    ln = rnd.len.long().cpu()
+    acc_n = rnd.accepted.long().cpu()
+    row = V * 2
+    if w.tau > 0:
+        rejected = acc_n < ln
+        vbytes = int(ln.sum()) * row                   # target rows 1..l_r: normalisers
+        n_rej = int(rejected.sum())
+        vbytes += n_rej * (2 * row + r * 2)            # rejected row: target + base, E row
+        vbytes += (V * r * 2) if n_rej else 0           # W2t once for the residual pass
+        vbytes += int((~rejected).sum()) * row          # bonus row of the rest
+    else:
+        vbytes = int((ln + 1).sum()) * row             # rows 1..l_r + 1: argmaxes
+    verify_gbs = vbytes / (stage["verify"] * 1e-3) / 1e9
 
     line = {
         "metric": METRIC, "value": job_throughput(R * G, ms, ws), "unit": UNIT, "n_gpus": ws,
@@ -412,6 +426,8 @@ def run_dspark(args, w, ws, rank, local):
         "markov_loop_roofline": markov_roof,
         "markov_loop_hbm": {"achieved": markov_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                             "frac": markov_gbs / peaks["hbm_gbs"]},
+        "verify_hbm": {"bytes": vbytes, "achieved": verify_gbs, "peak": peaks["hbm_gbs"],
+                       "unit": "GB/s", "frac": verify_gbs / peaks["hbm_gbs"]},
         "gpu_launches": launches,
         "clocks": clk,
     }
