@@ -116,12 +116,13 @@ int dspark_lm_head_tc(const dspark_dims *dims, const void *h, const void *W_lm,
   epi.C = (bf16 *)base_logits;
   epi.M = dims->R * dims->gamma;
   epi.N = dims->V;
-  // From 1024 rows on, CTA pairs (cta_group::2) on 256 x 256 tiles: a third
-  // fewer operand bytes per SM per flop, 91% of the bf16 peak at R*gamma = 1280
-  // against 86% for the single-CTA kernel.  Below that (few M blocks share each
-  // W_lm tile) the single-CTA kernel is the faster one.
+  // From four row blocks (512 rows) on, CTA pairs (cta_group::2) on 256 x 256
+  // tiles: a third fewer operand bytes per SM per flop.  At R*gamma = 1280, 91%
+  // of the bf16 peak against 86% for the single-CTA kernel; at 512 rows
+  // (V = 151936, d = 4096) 0.383 against 0.425 ms.  Below four row blocks a
+  // pair would leave up to a quarter of its rows empty.
   const int num_m = (epi.M + gemm::BM - 1) / gemm::BM;
-  if (num_m >= 8) return gemm::launch_pair<4>(h, W_lm, epi.M, epi.N, dims->d, epi, stream);
+  if (num_m >= 4) return gemm::launch_pair<4>(h, W_lm, epi.M, epi.N, dims->d, epi, stream);
   return gemm::launch<4, 256, false>(h, W_lm, epi.M, epi.N, dims->d, epi, stream);
 }
 
