@@ -279,16 +279,19 @@ template <int RW>
 __device__ __forceinline__ void rebuild_block(const bf16 *__restrict__ base_row, const bf16 *E_row,
                                               const bf16 *__restrict__ W2t, int b, int V, int r,
                                               float *out, int wg, int lane) {
-  constexpr int PER = GUMBEL_BLOCK / RW;
-  constexpr int CHK = PER < 4 ? PER : 4;
+  // warp wg takes ids wg, wg + RW, wg + 2 RW, ... (RW need not divide 64), four
+  // at a time: each lane has their W2t words of two passes in flight
+  constexpr int CHK = 4;
   const uint4 *e4 = reinterpret_cast<const uint4 *>(E_row);
   const int r8 = r / 8;
   // this lane's first two 16-byte words of E (all of them when r <= 512)
   const uint4 e0 = lane < r8 ? __ldcg(e4 + lane) : make_uint4(0, 0, 0, 0);
   const uint4 e1 = lane + 32 < r8 ? __ldcg(e4 + lane + 32) : make_uint4(0, 0, 0, 0);
 #pragma unroll 1
-  for (int u0 = wg * PER; u0 < (wg + 1) * PER; u0 += CHK) {
-    const int v0 = b * GUMBEL_BLOCK + u0;
+  for (int t0 = 0; wg + RW * t0 < GUMBEL_BLOCK; t0 += CHK) {
+    int ids[CHK];
+#pragma unroll
+    for (int u = 0; u < CHK; ++u) ids[u] = wg + RW * (t0 + u);  // 64 or more: no id
     float acc[CHK];
 #pragma unroll
     for (int u = 0; u < CHK; ++u) acc[u] = 0.f;
@@ -299,8 +302,9 @@ __device__ __forceinline__ void rebuild_block(const bf16 *__restrict__ base_row,
       uint4 w0[CHK], w1[CHK];
 #pragma unroll
       for (int u = 0; u < CHK; ++u) {
-        const uint4 *rowp = reinterpret_cast<const uint4 *>(W2t + (size_t)(v0 + u) * r);
-        const bool ok = v0 + u < V;
+        const int v = b * GUMBEL_BLOCK + ids[u];
+        const uint4 *rowp = reinterpret_cast<const uint4 *>(W2t + (size_t)v * r);
+        const bool ok = ids[u] < GUMBEL_BLOCK && v < V;
         w0[u] = ok ? __ldg(rowp + c) : make_uint4(0, 0, 0, 0);
         w1[u] = (ok && two) ? __ldg(rowp + c + 32) : make_uint4(0, 0, 0, 0);
       }
@@ -311,8 +315,11 @@ __device__ __forceinline__ void rebuild_block(const bf16 *__restrict__ base_row,
     for (int u = 0; u < CHK; ++u) acc[u] = warp_sum(acc[u]);
     if (lane == 0) {
 #pragma unroll
-      for (int u = 0; u < CHK; ++u)
-        out[u0 + u] = v0 + u < V ? __bfloat162float(base_row[v0 + u]) + acc[u] : -INFINITY;
+      for (int u = 0; u < CHK; ++u) {
+        const int v = b * GUMBEL_BLOCK + ids[u];
+        if (ids[u] < GUMBEL_BLOCK)
+          out[ids[u]] = v < V ? __bfloat162float(base_row[v]) + acc[u] : -INFINITY;
+      }
     }
   }
 }
