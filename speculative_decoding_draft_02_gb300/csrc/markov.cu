@@ -333,17 +333,23 @@ struct EpiStoreF32 {
 };
 
 // s_k for every (request, state component): the f32 state, bf16(s_k) as the
-// vocabulary pass's A operand E and into the state columns of U.
+// vocabulary pass's A operand E and into the state columns of U.  W_rec U comes
+// as `splits` partial sums over K (rows s * m_pad + i of Gk), added in order.
 __global__ void rnn_state(const float *__restrict__ Gk, const float *__restrict__ P,
                           float *__restrict__ state, bf16 *__restrict__ E, bf16 *__restrict__ U,
-                          int R, int gamma, int r, int k) {
+                          int R, int gamma, int r, int k, int splits, int m_pad) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= R * r) return;
   const int i = t / r, c = t % r;
-  const float *g_row = Gk + (size_t)i * 2 * r;
   const float *p_row = P + ((size_t)i * gamma + k - 1) * 2 * r;
-  const float g = 1.f / (1.f + expf(-(g_row[c] + p_row[c])));
-  const float cand = tanhf(g_row[r + c] + p_row[r + c]);
+  float gg = 0.f, gc = 0.f;
+  for (int sp = 0; sp < splits; ++sp) {
+    const float *g_row = Gk + ((size_t)sp * m_pad + i) * 2 * r;
+    gg += g_row[c];
+    gc += g_row[r + c];
+  }
+  const float g = 1.f / (1.f + expf(-(gg + p_row[c])));
+  const float cand = tanhf(gc + p_row[r + c]);
   const float s = (1.f - g) * state[t] + g * cand;
   state[t] = s;
   const bf16 sb = __float2bfloat16_rn(s);
@@ -355,7 +361,8 @@ struct RnnWs {
   MarkovWs mk;
   bf16 *U;        // [R, 2r]  [bf16(s_{k-1}) | W1[x_{k-1}]]
   float *state;   // [R, r]
-  float *Gk;      // [R, 2r]  W_rec U of the current step
+  float *Gk;      // [splits * m_pad, 2r]  W_rec U of the current step, split over K
+  int splits, m_pad;
   float *P;       // [R * gamma, 2r]  W_hid h of every position
   size_t bytes;
 };
@@ -370,7 +377,11 @@ RnnWs rnn_layout(const dspark_dims *d, char *base) {
   w.state = (float *)(base + off);
   off = dspark_align_up(off + sizeof(float) * R * r, 256);
   w.Gk = (float *)(base + off);
-  off = dspark_align_up(off + sizeof(float) * R * 2 * r, 256);
+  // K = 2r in 64-deep blocks, up to four splits of equal depth
+  const int kb = (int)(2 * r / 64);
+  w.splits = kb % 4 == 0 ? 4 : (kb % 2 == 0 ? 2 : 1);
+  w.m_pad = (int)((R + 127) / 128 * 128);
+  off = dspark_align_up(off + sizeof(float) * (size_t)w.splits * w.m_pad * 2 * r, 256);
   w.P = (float *)(base + off);
   off = dspark_align_up(off + sizeof(float) * R * G * 2 * r, 256);
   w.bytes = off;
@@ -418,11 +429,13 @@ extern "C" int dspark_rnn_draft(const dspark_dims *dims, const void *base_logits
                                                      V, r, 1);
   DSPARK_CHECK_LAUNCH();
   for (int k = 1; k <= G; ++k) {
-    rc = gemm::launch<4, 64>(ws.U, W_rec, R, 2 * r, 2 * r, EpiStoreF32{ws.Gk, R, 2 * r},
-                             stream, nullptr, true);
+    // split over K: 16 k blocks (r = 512) on 32 tiles would leave most SMs idle
+    rc = gemm::launch<4, 64>(ws.U, W_rec, R, 2 * r, 2 * r,
+                             EpiStoreF32{ws.Gk, ws.splits * ws.m_pad, 2 * r}, stream, nullptr,
+                             true, ws.splits);
     if (rc != DSPARK_OK) return rc;
     rnn_state<<<(R * r + 255) / 256, 256, 0, stream>>>(ws.Gk, ws.P, ws.state, ws.mk.E, ws.U,
-                                                       R, G, r, k);
+                                                       R, G, r, k, ws.splits, ws.m_pad);
     DSPARK_CHECK_LAUNCH();
     if (tau > 0.f) {
       const int n_parts = logits_parts<MODE_SAMPLE>(V);

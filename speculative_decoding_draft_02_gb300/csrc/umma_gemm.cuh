@@ -76,7 +76,7 @@ template <class Epi, int EPI_WARPS, int BN_, bool PAIR>
 __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
                      const __grid_constant__ CUtensorMap tma_b, int M, int N, int K,
-                     const int *m_dev, Epi epi) {
+                     const int *m_dev, int ksplit, Epi epi) {
   using G = Geo<BN_>;
   constexpr int BN = G::BN, STAGES = G::STAGES, B_BYTES = G::B_BYTES;
   constexpr int STAGE_BYTES = G::STAGE_BYTES;
@@ -123,18 +123,23 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
     M = md < M ? (md > 0 ? md : 0) : M;
   }
   const int num_m = (M + BM - 1) / BM, num_n = (N + BN - 1) / BN;
-  const int k_iters = K / BK;
+  // split K (ksplit > 1): split s of a tile takes k blocks [s * k_iters, (s+1) *
+  // k_iters) and hands its partial to the epilogue as rows s * num_m * BM + ...
+  const int k_iters = K / BK / ksplit;
   // tile sequence: t -> (m block, n block), m fastest; a pair walks pairs of M blocks
   const uint32_t rank = PAIR ? tc::cluster_ctarank() : 0u;
   const int num_mp = PAIR ? (num_m + 1) / 2 : num_m;
-  const int num_tiles = num_mp * num_n;
+  const int split_tiles = num_mp * num_n;
+  const int num_tiles = split_tiles * ksplit;
   const int first = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int stride = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
   auto coords = [&](int t, int &m_blk, int &n_blk) {
-    const int mp = t % num_mp;
-    n_blk = t / num_mp;
+    const int u = t % split_tiles;
+    const int mp = u % num_mp;
+    n_blk = u / num_mp;
     m_blk = PAIR ? 2 * mp + (int)rank : mp;
   };
+  auto out_row0 = [&](int t, int m_blk) { return ((t / split_tiles) * num_m + m_blk) * BM; };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -153,18 +158,18 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
       for (int tile = first; ok && tile < num_tiles; tile += stride) {
         int m_blk, n_blk;
         coords(tile, m_blk, n_blk);
+        const int kb0 = (tile / split_tiles) * k_iters;
         for (int kb = 0; kb < k_iters; ++kb) {
           if (!tc::mbar_wait(&ctl->empty[stage], phase ^ 1, abort)) { ok = false; break; }
           tc::mbar_expect_tx(&ctl->full[stage], STAGE_BYTES);  // A + both halves of B
-          tc::tma_load_2d(sA + stage * A_BYTES, &tma_a, kb * BK, m_blk * BM, &ctl->full[stage],
-                          pol_a);
+          const int kx = (kb0 + kb) * BK;
+          tc::tma_load_2d(sA + stage * A_BYTES, &tma_a, kx, m_blk * BM, &ctl->full[stage], pol_a);
           if (PAIR)
-            tc::tma_load_2d_mcast(sB + stage * B_BYTES + rank * (B_BYTES / 2), &tma_b, kb * BK,
+            tc::tma_load_2d_mcast(sB + stage * B_BYTES + rank * (B_BYTES / 2), &tma_b, kx,
                                   n_blk * BN + (int)rank * (BN / 2), &ctl->full[stage],
                                   (uint16_t)0x3, pol_b);
           else
-            tc::tma_load_2d(sB + stage * B_BYTES, &tma_b, kb * BK, n_blk * BN, &ctl->full[stage],
-                            pol_b);
+            tc::tma_load_2d(sB + stage * B_BYTES, &tma_b, kx, n_blk * BN, &ctl->full[stage], pol_b);
           issued[stage] = (int)phase;
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
@@ -226,15 +231,16 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
     if (first < num_tiles) {
       int m_blk, n_blk;
       coords(first, m_blk, n_blk);
-      epi.prefetch(m_blk * BM, n_blk * BN, row, c0, c0 + SLICE, st);
+      epi.prefetch(out_row0(first, m_blk), n_blk * BN, row, c0, c0 + SLICE, st);
     }
     for (int tile = first; tile < num_tiles; tile += stride) {
       int m_blk, n_blk;
       coords(tile, m_blk, n_blk);
       int next_m0 = -1, next_n0 = -1;
       if (tile + stride < num_tiles) {
-        coords(tile + stride, next_m0, next_n0);
-        next_m0 *= BM;
+        int nm;
+        coords(tile + stride, nm, next_n0);
+        next_m0 = out_row0(tile + stride, nm);
         next_n0 *= BN;
       }
       // one lane polls, then the warp proceeds together (tcgen05.ld is warp-wide)
@@ -244,7 +250,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
       if (!ok) break;
       tc::fence_after_sync();
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
-      epi(m_blk * BM, n_blk * BN, row, taddr, c0, c0 + SLICE, next_m0, next_n0, st);
+      epi(out_row0(tile, m_blk), n_blk * BN, row, taddr, c0, c0 + SLICE, next_m0, next_n0, st);
       tc::fence_before_sync();
       __syncwarp();  // every lane's TMEM reads are done before the warp's single arrival
       if (lane == 0) tc::mbar_arrive(&ctl->tempty[acc]);
@@ -267,9 +273,12 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
 // only the first *m_dev of them (read on the device, so the count can come from
 // an earlier kernel in the stream).  PAIR launches clusters of two CTAs that
 // share B tiles by multicast (see umma_gemm_kernel).
+// ksplit > 1 (not with PAIR): K is split into ksplit equal parts, and the
+// epilogue receives split s's partial of M block m as rows (s * num_m + m) * BM.
 template <int EPI_WARPS, int BN_ = 256, bool PAIR = false, class Epi>
 int launch(const void *A, const void *B, int M, int N, int K, const Epi &epi,
-           cudaStream_t stream, const int *m_dev = nullptr, bool pdl = false) {
+           cudaStream_t stream, const int *m_dev = nullptr, bool pdl = false, int ksplit = 1) {
+  if (ksplit < 1 || (PAIR && ksplit != 1) || K % (BK * ksplit) != 0) return DSPARK_ERR_ARG;
   using G = Geo<BN_>;
   constexpr int BN = G::BN;
   static_assert(EPI_WARPS % 4 == 0 && EPI_WARPS >= 4 && EPI_WARPS <= 16 &&
@@ -314,7 +323,7 @@ int launch(const void *A, const void *B, int M, int N, int K, const Epi &epi,
     const int pairs = ((num_m + 1) / 2) * num_n;
     grid = 2 * (pairs < max_clusters ? pairs : max_clusters);
   } else {
-    const int tiles = num_m * num_n;
+    const int tiles = num_m * num_n * ksplit;
     grid = tiles < dspark_sm_count() ? tiles : dspark_sm_count();
     // a multiple of the M-block count keeps every CTA (and epilogue thread) on one row block
     if (Epi::kRowAffine && grid > num_m) grid = grid / num_m * num_m;
@@ -326,7 +335,7 @@ int launch(const void *A, const void *B, int M, int N, int K, const Epi &epi,
     cfg.attrs = attrs;
     cfg.numAttrs += 1;
   }
-  if (cudaLaunchKernelEx(&cfg, kernel, ta, tb, M, N, K, m_dev, epi) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, kernel, ta, tb, M, N, K, m_dev, ksplit, epi) != cudaSuccess)
     return DSPARK_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
   dspark_count_launches(1);
