@@ -334,22 +334,28 @@ struct EpiStoreF32 {
 
 // s_k for every (request, state component): the f32 state, bf16(s_k) as the
 // vocabulary pass's A operand E and into the state columns of U.  W_rec U comes
-// as `splits` partial sums over K (rows s * m_pad + i of Gk), added in order.
+// as `splits` partial sums over K (rows s * m_pad + i of Gk) and W_hid h as
+// `psplits` (rows s * pm_pad + i gamma + k - 1 of P), each added in order.
 __global__ void rnn_state(const float *__restrict__ Gk, const float *__restrict__ P,
                           float *__restrict__ state, bf16 *__restrict__ E, bf16 *__restrict__ U,
-                          int R, int gamma, int r, int k, int splits, int m_pad) {
+                          int R, int gamma, int r, int k, int splits, int m_pad, int psplits,
+                          int pm_pad) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= R * r) return;
   const int i = t / r, c = t % r;
-  const float *p_row = P + ((size_t)i * gamma + k - 1) * 2 * r;
-  float gg = 0.f, gc = 0.f;
+  float gg = 0.f, gc = 0.f, pg = 0.f, pc = 0.f;
   for (int sp = 0; sp < splits; ++sp) {
     const float *g_row = Gk + ((size_t)sp * m_pad + i) * 2 * r;
     gg += g_row[c];
     gc += g_row[r + c];
   }
-  const float g = 1.f / (1.f + expf(-(gg + p_row[c])));
-  const float cand = tanhf(gc + p_row[r + c]);
+  for (int sp = 0; sp < psplits; ++sp) {
+    const float *p_row = P + ((size_t)sp * pm_pad + (size_t)i * gamma + k - 1) * 2 * r;
+    pg += p_row[c];
+    pc += p_row[r + c];
+  }
+  const float g = 1.f / (1.f + expf(-(gg + pg)));
+  const float cand = tanhf(gc + pc);
   const float s = (1.f - g) * state[t] + g * cand;
   state[t] = s;
   const bf16 sb = __float2bfloat16_rn(s);
@@ -363,9 +369,29 @@ struct RnnWs {
   float *state;   // [R, r]
   float *Gk;      // [splits * m_pad, 2r]  W_rec U of the current step, split over K
   int splits, m_pad;
-  float *P;       // [R * gamma, 2r]  W_hid h of every position
+  float *P;       // [psplits * pm_pad, 2r]  W_hid h of every position, split over K
+  int psplits, pm_pad;
   size_t bytes;
 };
+
+// K slices for W_hid h ([R gamma, d] x [d, 2r] on 128 x 256 tiles): the divisor
+// of the 64-deep k blocks, at most 16, that minimises waves x (k blocks per
+// slice + 2 for the tile's hand-over) on GB300's 152 SMs.  The split only
+// balances the work, so a part with another SM count still gets right results.
+int rnn_hidden_splits(int M, int N, int K) {
+  const int tiles = ((M + 127) / 128) * ((N + 255) / 256), kb = K / 64, sms = 152;
+  int best = 1;
+  long best_cost = -1;
+  for (int s = 1; s <= 16; ++s) {
+    if (kb % s) continue;
+    const long cost = (long)((tiles * s + sms - 1) / sms) * (kb / s + 2);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
 
 RnnWs rnn_layout(const dspark_dims *d, char *base) {
   RnnWs w;
@@ -383,7 +409,9 @@ RnnWs rnn_layout(const dspark_dims *d, char *base) {
   w.m_pad = (int)((R + 127) / 128 * 128);
   off = dspark_align_up(off + sizeof(float) * (size_t)w.splits * w.m_pad * 2 * r, 256);
   w.P = (float *)(base + off);
-  off = dspark_align_up(off + sizeof(float) * R * G * 2 * r, 256);
+  w.psplits = rnn_hidden_splits((int)(R * G), (int)(2 * r), d->d);
+  w.pm_pad = (int)((R * G + 127) / 128 * 128);
+  off = dspark_align_up(off + sizeof(float) * (size_t)w.psplits * w.pm_pad * 2 * r, 256);
   w.bytes = off;
   return w;
 }
@@ -416,10 +444,11 @@ extern "C" int dspark_rnn_draft(const dspark_dims *dims, const void *base_logits
   conf_hidden<<<R * G, 128, 0, stream>>>((const bf16 *)h, (const bf16 *)w_conf, ws.mk.zh, d,
                                          nullptr);
   DSPARK_CHECK_LAUNCH();
-  // W_hid h for all positions at once
-  // 64-wide N tiles: 2r = 1024 columns would give only a few dozen 256-wide tiles
-  int rc = gemm::launch<4, 64>(h, W_hid, R * G, 2 * r, d, EpiStoreF32{ws.P, R * G, 2 * r},
-                               stream);
+  // W_hid h for all positions at once, split over K: 2r = 1024 columns and
+  // R gamma = 1280 rows make only 40 tiles, each 112 k blocks deep
+  int rc = gemm::launch<4, 256>(h, W_hid, R * G, 2 * r, d,
+                                EpiStoreF32{ws.P, ws.psplits * ws.pm_pad, 2 * r}, stream,
+                                nullptr, false, ws.psplits);
   if (rc != DSPARK_OK) return rc;
   if (cudaMemsetAsync(ws.U, 0, sizeof(bf16) * (size_t)R * 2 * r, stream) != cudaSuccess ||
       cudaMemsetAsync(ws.state, 0, sizeof(float) * (size_t)R * r, stream) != cudaSuccess)
@@ -435,7 +464,8 @@ extern "C" int dspark_rnn_draft(const dspark_dims *dims, const void *base_logits
                              true, ws.splits);
     if (rc != DSPARK_OK) return rc;
     rnn_state<<<(R * r + 255) / 256, 256, 0, stream>>>(ws.Gk, ws.P, ws.state, ws.mk.E, ws.U,
-                                                       R, G, r, k, ws.splits, ws.m_pad);
+                                                       R, G, r, k, ws.splits, ws.m_pad,
+                                                       ws.psplits, ws.pm_pad);
     DSPARK_CHECK_LAUNCH();
     if (tau > 0.f) {
       const int n_parts = logits_parts<MODE_SAMPLE>(V);
