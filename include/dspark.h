@@ -174,7 +174,9 @@ int dspark_draft(const dspark_dims *dims, const void *h, const int32_t *anchor,
  *   a_out  f32 [R, gamma]    out, may be NULL: survival products (f32, left to right)
  *   order_out int32 [R*gamma] out, may be NULL: candidate ids r*gamma + j-1 sorted by
  *                            a descending, ties by id ascending
- * S_K and Theta are evaluated in f64.  R*gamma <= 16384. */
+ * S_K sums the sorted products in 2^-48 units (each rounded to nearest, halves up;
+ * exact integer sums); Theta(K) = f64(R + S_K) * (f64(SPS) * 2^-48).  The argmax
+ * takes ties to the smallest K; a NaN Theta never wins.  R*gamma <= 16384. */
 int dspark_schedule(const float *conf, int32_t R, int32_t gamma, const float *sps,
                     int32_t n_sps, int32_t mode, int32_t k_fixed, int32_t *len,
                     int32_t *K_out, double *theta_out, float *a_out, int32_t *order_out,

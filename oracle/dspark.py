@@ -30,7 +30,10 @@ Readings where the pages are silent (each listed in the design notes):
     later step accumulates in float64 here.
   * Confidences are float32; survival products a_{r,j} are float32 products
     taken left to right (the scheduler's sort is decided in that precision);
-    Theta is evaluated in float64.
+    S_K is the exact sum of the sorted products each rounded to the nearest
+    multiple of 2^-48, and Theta(K) = f64(R + S_K) * (f64(SPS) * 2^-48), so
+    the argmax over K is decided in the same precision as on the device.
+    The rounding moves R + S_K by at most gamma * 2^-49 of itself.
   * Sort order: a descending, ties by (request, position) ascending.
     Theta argmax ties go to the smallest K; the break mode admits K+1 only if
     Theta(K+1) > Theta(K) strictly.
@@ -383,14 +386,28 @@ def global_order(a: np.ndarray) -> np.ndarray:
                     dtype=np.int64)
 
 
+FIX_BITS = 48  # S_K is summed in units of 2^-48
+
+
 def theta_curve(a: np.ndarray, order: np.ndarray, sps) -> np.ndarray:
-    """Theta(K) = (R + S_K) * SPS(R + K), K = 0..R*gamma, S_K = sum of the top-K a."""
+    """Theta(K) = (R + S_K) * SPS(R + K), K = 0..R*gamma, S_K = sum of the top-K a.
+
+    Each a (float32 in [0, 1]) is rounded to the nearest integer number of
+    2^-48 units, halves up: a * 2^48 is exact in float64 and so is adding 0.5
+    (for a * 2^48 below 2^-29 the sum rounds, but stays below 1).  The sums are
+    exact Python integers; R + S_K is converted to float64 once (nearest) and
+    multiplied by SPS * 2^-48 (exact scaling)."""
     R = a.shape[0]
     sps = to_f64(sps)
     sorted_a = a.reshape(-1)[order].astype(np.float64)
-    S = np.concatenate([[0.0], np.cumsum(sorted_a)])
-    K = np.arange(S.size)
-    return (R + S) * sps[R + K - 1]
+    units = np.floor(sorted_a * 2.0 ** FIX_BITS + 0.5)
+    RS = R << FIX_BITS
+    theta = np.empty(units.size + 1)
+    theta[0] = float(RS) * (sps[R - 1] * 2.0 ** -FIX_BITS)
+    for K in range(1, units.size + 1):
+        RS += int(units[K - 1])
+        theta[K] = float(RS) * (sps[R + K - 1] * 2.0 ** -FIX_BITS)
+    return theta
 
 
 def schedule(conf, sps, mode: int = UNCONSTRAINED, k_fixed: int = 0) -> Dict[str, np.ndarray]:
@@ -409,7 +426,7 @@ def schedule(conf, sps, mode: int = UNCONSTRAINED, k_fixed: int = 0) -> Dict[str
     th = theta_curve(a, order, sps)
     n = R * G
     if mode == UNCONSTRAINED:
-        K = int(np.argmax(th))
+        K = int(np.argmax(np.where(np.isnan(th), -np.inf, th)))  # a NaN entry never wins
     elif mode == BREAK:
         K = 0
         while K < n and th[K + 1] > th[K]:

@@ -13,7 +13,7 @@
 //
 // One CTA of 1024 threads: f32 survival products, a bitonic sort of composite
 // keys (~bits(a) << 32 | id) so that ties go to the lower (request, position),
-// a f64 block scan of the sorted products and the Theta search.
+// a fixed-point block scan of the sorted products and the Theta search.
 #include "common.cuh"
 
 DSPARK_DECLARE_STATUS(s_status_sched)
@@ -22,10 +22,40 @@ namespace {
 
 constexpr int SCHED_THREADS = 1024;
 constexpr int SCHED_MAX = 16384;
+constexpr int SCAN_PER = 16;  // least sorted slots per scanning thread
 
-// Theta(K) = (R + S_K) * SPS(R + K), with spsK[K] = SPS(R + K).
-__device__ __forceinline__ double theta_at(long K, double S, int R, const float *spsK) {
-  return ((double)R + S) * (double)spsK[K];
+// S_K is summed in fixed point with 2^-48 units: every survival product a in
+// [0, 1] rounded to the nearest unit, then exact 64-bit integer sums, so the
+// order of the additions does not matter and no f64 addition (slow to issue
+// and long in latency on this part) lies on a dependency chain.  Each term is
+// off by at most 2^-49, so R + S_K is within gamma * 2^-49 of the exact sum
+// relative to it.  R (1 + gamma) <= 2^15 keeps every sum below 2^63.
+constexpr int FIX_BITS = 48;
+
+// a (f32, 0 <= a <= 1) in 2^-48 units, rounded to nearest, with integer ops.
+__device__ __forceinline__ unsigned long long to_fix(float a) {
+  const uint32_t u = __float_as_uint(a);
+  const int e = (int)(u >> 23) & 0xff;
+  const int sh = e - (150 - FIX_BITS);  // a * 2^48 = m * 2^(e - 150 + 48)
+  if (e == 0 || sh < -24) return 0ull;  // below half a unit (m < 2^24)
+  const unsigned long long m = (u & 0x7fffffu) | 0x800000u;
+  if (sh >= 0) return m << sh;          // a <= 1: sh <= 25
+  return (m + (1ull << (-sh - 1))) >> (-sh);
+}
+
+// Theta(K) = (R + S_K) * SPS(R + K), with spsK[K] = SPS(R + K) and RS = R + S_K
+// in 2^-48 units.
+__device__ __forceinline__ double theta_at(long K, unsigned long long RS, const float *spsK) {
+  return (double)RS * ((double)spsK[K] * 0x1p-48);
+}
+
+// A signed 64-bit key that orders doubles as `<` does (-0 equal to +0); NaN
+// takes the least key, so it never wins the argmax.
+__device__ __forceinline__ long long theta_key(double th) {
+  const long long b = __double_as_longlong(th);
+  if ((b & 0x7fffffffffffffffLL) > 0x7ff0000000000000LL) return (long long)0x8000000000000000ULL;
+  if ((b << 1) == 0) return 0;
+  return b >= 0 ? b : (b ^ 0x7fffffffffffffffLL);
 }
 
 template <int E>
@@ -38,8 +68,8 @@ __global__ void __launch_bounds__(SCHED_THREADS) schedule_kernel(
   // keys [n_pad] (merge sort: and a second buffer of n_pad), then cnt [R]
   unsigned long long *keys = reinterpret_cast<unsigned long long *>(smem_raw);
   int32_t *cnt = reinterpret_cast<int32_t *>(keys + (E == 0 ? 2 * n_pad : n_pad));
-  __shared__ double warp_tot[32];
-  __shared__ double red_val[32];
+  __shared__ unsigned long long warp_tot[32];
+  __shared__ long long red_val[32];
   __shared__ long red_k[32];
   __shared__ long s_K;
   __shared__ double s_theta;
@@ -181,73 +211,89 @@ __global__ void __launch_bounds__(SCHED_THREADS) schedule_kernel(
   }
   }
 
-  // a7: S_K by a block scan in f64; thread t owns sorted slots [t*per, (t+1)*per)
-  const int per = (n_pad + SCHED_THREADS - 1) / SCHED_THREADS;
+  // a7: S_K by a block scan in fixed point; thread t owns sorted slots
+  // [t*per, (t+1)*per).  The slots go to as few warps as give each thread at
+  // least SCAN_PER of them; only those warps (`scanner`, warp-uniform) scan
+  // and evaluate Theta, whose f64 products are independent of one another.
+  using u64 = unsigned long long;
+  const int per = max((n_pad + SCHED_THREADS - 1) / SCHED_THREADS, SCAN_PER);
   const int beg = tid * per;
-  double local = 0.0;
-  for (int p = beg; p < beg + per && p < n; ++p)
-    local += (double)__uint_as_float(~(unsigned)(keys[p] >> 32));
-  // exclusive scan of `local` over the block
-  double incl = local;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const double y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) warp_tot[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    double w = warp_tot[lane];
-    double wi = w;
+  const int scan_warps = ((n + per - 1) / per + 31) / 32;
+  const bool scanner = warp < scan_warps;
+  auto a_at = [&](int p) { return __uint_as_float(~(unsigned)(keys[p] >> 32)); };
+  u64 incl = 0;
+  if (scanner) {
+    u64 local = 0;
+    for (int p = beg; p < beg + per && p < n; ++p) local += to_fix(a_at(p));
+    // inclusive scan of `local` over the warp
+    incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const double y = __shfl_up_sync(0xffffffffu, wi, o);
+      const u64 y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const u64 w = lane < scan_warps ? warp_tot[lane] : 0ull;
+    u64 wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const u64 y = __shfl_up_sync(0xffffffffu, wi, o);
       if (lane >= o) wi += y;
     }
     warp_tot[lane] = wi - w;  // exclusive prefix of warp totals
   }
   __syncthreads();
-  double excl = __shfl_up_sync(0xffffffffu, incl, 1);
-  if (lane == 0) excl = 0.0;
-  const double S_beg = warp_tot[warp] + excl;  // S_{beg}
-  double S = S_beg;
+  const u64 R_fix = (u64)R << FIX_BITS;
+  u64 RS_beg = R_fix;  // R + S_{beg}
 
   // Theta over K = beg .. beg+per (K = 0 handled by thread 0)
-  double best = -INFINITY;  // threads past the end never win the argmax
+  long long best = (long long)0x8000000000000000ULL;  // threads past the end never win
   long bestK = 0x7fffffffffffffffL;
   long firstDrop = 0x7fffffffffffffffL;  // smallest K with Theta(K+1) <= Theta(K)
-  double prevTheta = 0.0;
-  if (beg <= n) {  // sps[R + K - 1] exists for K <= n only
-    prevTheta = theta_at(beg, S, R, spsK);
-    best = prevTheta;
-    bestK = beg;
-  }
-  for (int p = beg; p < beg + per && p < n; ++p) {
-    S += (double)__uint_as_float(~(unsigned)(keys[p] >> 32));
-    const long K = p + 1;
-    const double th = theta_at(K, S, R, spsK);
-    if (th > best) { best = th; bestK = K; }
-    if (th <= prevTheta && firstDrop > K - 1) firstDrop = K - 1;
-    prevTheta = th;
+  if (scanner) {
+    u64 excl = __shfl_up_sync(0xffffffffu, incl, 1);
+    if (lane == 0) excl = 0ull;
+    RS_beg = R_fix + warp_tot[warp] + excl;
+    u64 RS = RS_beg;
+    double prevTheta = 0.0;
+    if (beg <= n) {  // sps[R + K - 1] exists for K <= n only
+      prevTheta = theta_at(beg, RS, spsK);
+      best = theta_key(prevTheta);
+      bestK = beg;
+    }
+    for (int p = beg; p < beg + per && p < n; ++p) {
+      RS += to_fix(a_at(p));
+      const long K = p + 1;
+      const double th = theta_at(K, RS, spsK);
+      const long long key = theta_key(th);
+      if (key > best) { best = key; bestK = K; }
+      if (th <= prevTheta && firstDrop > K - 1) firstDrop = K - 1;
+      prevTheta = th;
+    }
   }
 
   long K = 0;
   if (mode == DSPARK_SCHED_UNCONSTRAINED || mode == DSPARK_SCHED_ASYNC) {
     // argmax Theta, ties to the smallest K
+    if (scanner) {
 #pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const double b2 = __shfl_xor_sync(0xffffffffu, best, o);
-      const long k2 = __shfl_xor_sync(0xffffffffu, bestK, o);
-      if (b2 > best || (b2 == best && k2 < bestK)) { best = b2; bestK = k2; }
+      for (int o = 16; o; o >>= 1) {
+        const long long b2 = __shfl_xor_sync(0xffffffffu, best, o);
+        const long k2 = __shfl_xor_sync(0xffffffffu, bestK, o);
+        if (b2 > best || (b2 == best && k2 < bestK)) { best = b2; bestK = k2; }
+      }
     }
     if (lane == 0) { red_val[warp] = best; red_k[warp] = bestK; }
     __syncthreads();
     if (warp == 0) {
-      best = red_val[lane];
-      bestK = red_k[lane];
+      best = lane < scan_warps ? red_val[lane] : (long long)0x8000000000000000ULL;
+      bestK = lane < scan_warps ? red_k[lane] : 0x7fffffffffffffffL;
 #pragma unroll
       for (int o = 16; o; o >>= 1) {
-        const double b2 = __shfl_xor_sync(0xffffffffu, best, o);
+        const long long b2 = __shfl_xor_sync(0xffffffffu, best, o);
         const long k2 = __shfl_xor_sync(0xffffffffu, bestK, o);
         if (b2 > best || (b2 == best && k2 < bestK)) { best = b2; bestK = k2; }
       }
@@ -297,13 +343,11 @@ __global__ void __launch_bounds__(SCHED_THREADS) schedule_kernel(
   if (order_out)
     for (int p = tid; p < n; p += SCHED_THREADS) order_out[p] = (int)(keys[p] & 0xffffffffu);
   // Theta(K): the owner of slot K recomputes it from its scan segment
-  if (tid == 0 && K == 0) s_theta = theta_at(0, 0.0, R, spsK);
-  {
-    double S2 = S_beg;
-    for (int p = beg; p < beg + per && p < n; ++p) {
-      S2 += (double)__uint_as_float(~(unsigned)(keys[p] >> 32));
-      if (p + 1 == K) s_theta = theta_at(K, S2, R, spsK);
-    }
+  if (tid == 0 && K == 0) s_theta = theta_at(0, R_fix, spsK);
+  if (K > beg && K <= beg + per) {  // the owner of slot K - 1 (a scanner thread)
+    u64 RS2 = RS_beg;
+    for (int p = beg; p < K; ++p) RS2 += to_fix(a_at(p));
+    s_theta = theta_at(K, RS2, spsK);
   }
   __syncthreads();
   for (int i = tid; i < R; i += SCHED_THREADS) len[i] = cnt[i];

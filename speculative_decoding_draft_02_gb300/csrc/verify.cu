@@ -285,93 +285,151 @@ __global__ void __launch_bounds__(256) resample_reduce(
 
 // Plain target samples: the bonus row l_r + 1 when every draft passed (stream
 // 3), or the rejected row when its residual was empty (stream 2), drawn from
-// softmax(t / tau) in two levels.  One CTA of 512 threads per request: pass 1
-// leaves log Z_b of every 64-id block in shared memory (eight lanes per block,
-// one 16-byte word each, eight words in flight), pass 2 scores the blocks (one
-// Philox call per four blocks), pass 3 draws inside the best block.
-constexpr int BONUS_THREADS = 512;
+// softmax(t / tau) in two levels.  One cluster of BONUS_SPLIT CTAs per request,
+// each on a quarter of the 64-id blocks (a multiple of four blocks, so one
+// Philox call per four blocks stays in one CTA): pass 1 leaves log Z_b of its
+// blocks in shared memory (eight lanes per block, one 16-byte word each, eight
+// words in flight), pass 2 scores them (G_b = log Z_b + Gumbel of block b).
+// The CTAs exchange their best (G_b, b) through distributed shared memory, and
+// the owner of the winning block draws inside it (pass 3).  Every CTA takes
+// the same per-block arithmetic and the same total order on (G_b, b) as one
+// CTA on the whole row would, so the split does not change the draw.
+constexpr int BONUS_SPLIT = 4;
+constexpr int BONUS_THREADS = 256;
 constexpr size_t BONUS_MAX_SMEM = 220 * 1024;  // log Z_b of up to 56320 blocks: V <= 3604480
 
-__global__ void __launch_bounds__(BONUS_THREADS) bonus_row(const ResampleRow *__restrict__ rows,
-                                                           const bf16 *__restrict__ target,
-                                                           int32_t *__restrict__ bonus, int gamma,
-                                                           int V, float inv_tau, uint64_t seed) {
-  extern __shared__ float s_lz[];  // [n_blocks]: log Z_b
+__device__ __forceinline__ int bonus_quarter(int nb) {
+  return ((nb + BONUS_SPLIT - 1) / BONUS_SPLIT + 3) / 4 * 4;
+}
+
+__device__ __forceinline__ uint32_t dsmem_addr(const void *p, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(a)
+               : "r"((uint32_t)__cvta_generic_to_shared(p)), "r"(rank));
+  return a;
+}
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t a) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ int ld_dsmem_s32(uint32_t a) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void warp_best(float &best, int &idx) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const float b2 = __shfl_xor_sync(0xffffffffu, best, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
+    if (better(b2, i2, best, idx)) { best = b2; idx = i2; }
+  }
+}
+
+__global__ void __cluster_dims__(BONUS_SPLIT, 1, 1) __launch_bounds__(BONUS_THREADS)
+    bonus_row(const ResampleRow *__restrict__ rows, const bf16 *__restrict__ target,
+              int32_t *__restrict__ bonus, int gamma, int V, float inv_tau, uint64_t seed) {
+  extern __shared__ float s_lz[];  // [blocks of this CTA]: log Z_b
+  __shared__ float sb[BONUS_THREADS / 32], s_score[GUMBEL_BLOCK], s_cta_best;
+  __shared__ int si[BONUS_THREADS / 32], s_cta_idx;
   constexpr float LOG2E = 1.4426950408889634f, LN2 = 0.6931471805599453f;
   constexpr int GROUPS = BONUS_THREADS / 8, U = 8;
-  const int i = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int i = blockIdx.x / BONUS_SPLIT, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int q = (int)tc::cluster_ctarank();
   const ResampleRow rr = rows[i];
+  // the same for every CTA of the cluster: all leave here or none
   if (rr.kind != KIND_BONUS && rr.kind != KIND_FALLBACK) return;
   const uint32_t stream = rr.kind == KIND_BONUS ? RNG_BONUS : RNG_RESIDUAL;
   const bf16 *trow = target + ((size_t)i * (gamma + 1) + rr.pos - 1) * V;
-  const int nb = (V + GUMBEL_BLOCK - 1) / GUMBEL_BLOCK;
+  const int nb = (V + GUMBEL_BLOCK - 1) / GUMBEL_BLOCK, nbq = bonus_quarter(nb);
+  const int b_lo = q * nbq, b_hi = min(nb, b_lo + nbq);
   const int grp = tid >> 3, sub = tid & 7;
   const float c2 = inv_tau * LOG2E;
-  // pass 1: the trip count depends on nb only, so every lane reaches every shuffle
-  for (int b0 = 0; b0 < nb; b0 += GROUPS * U) {
-    uint4 q[U];
+  // pass 1: the trip count depends on this CTA's block range only, so every
+  // lane reaches every shuffle
+  for (int b0 = b_lo; b0 < b_hi; b0 += GROUPS * U) {
+    uint4 w4[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int b = b0 + u * GROUPS + grp, v = b * GUMBEL_BLOCK + sub * 8;
-      q[u] = (b < nb && v < V) ? __ldg(reinterpret_cast<const uint4 *>(trow + v))
-                               : make_uint4(0, 0, 0, 0);
+      w4[u] = (b < b_hi && v < V) ? __ldg(reinterpret_cast<const uint4 *>(trow + v))
+                                  : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int b = b0 + u * GROUPS + grp, v = b * GUMBEL_BLOCK + sub * 8;
-      const bool ok = b < nb && v < V;  // V % 8 == 0: a word is all inside or all past V
-      const uint32_t w[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+      const bool ok = b < b_hi && v < V;  // V % 8 == 0: a word is all inside or all past V
+      const uint32_t w[4] = {w4[u].x, w4[u].y, w4[u].z, w4[u].w};
       float x[8];
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
-        x[2 * t] = ok ? bf16_lo(w[t]) * c2 : -INFINITY;
-        x[2 * t + 1] = ok ? bf16_hi(w[t]) * c2 : -INFINITY;
+        x[2 * t] = bf16_lo(w[t]);
+        x[2 * t + 1] = bf16_hi(w[t]);
       }
+      // the maximum of the raw values, scaled once (c2 > 0 keeps the order)
       float mx = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])),
                        fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
+      mx = ok ? mx : -INFINITY;
 #pragma unroll
       for (int o = 1; o < 8; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const float ms = mx * c2;  // log2 units
       float sm = 0.f;
-      if (mx > -INFINITY) {
+      if (ok && mx > -INFINITY) {
 #pragma unroll
-        for (int t = 0; t < 8; ++t) sm += ex2_fast(x[t] - mx);
+        for (int t = 0; t < 8; ++t) sm += ex2_fast(fmaf(x[t], c2, -ms));
       }
 #pragma unroll
       for (int o = 1; o < 8; o <<= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
-      if (sub == 0 && b < nb) s_lz[b] = mx > -INFINITY ? (mx + __log2f(sm)) * LN2 : -INFINITY;
+      if (sub == 0 && b < b_hi) s_lz[b - b_lo] = mx > -INFINITY ? (ms + __log2f(sm)) * LN2 : -INFINITY;
     }
   }
   __syncthreads();
-  // pass 2: G_b = log Z_b + Gumbel(block id b, block stream)
-  float best = -INFINITY, d0 = 0.f, d1 = 0.f, d2 = 0.f;
+  // pass 2: G_b = log Z_b + Gumbel(block id b, block stream), b_lo % 4 == 0
+  float best = -INFINITY;
   int idx = 0x7fffffff;
-  for (int q4 = tid; q4 * 4 < nb; q4 += BONUS_THREADS) {
+  for (int q4 = b_lo / 4 + tid; q4 * 4 < b_hi; q4 += BONUS_THREADS) {
     const uint4 w = rng_words4(seed, (uint32_t)q4, (uint32_t)rr.pos, (uint32_t)i,
                                stream + RNG_BLOCK_OFFSET);
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       const int b = 4 * q4 + t;
-      if (b < nb && s_lz[b] > -INFINITY) {
-        const float G = s_lz[b] + rng_gumbel(ws[t]);
+      if (b < b_hi && s_lz[b - b_lo] > -INFINITY) {
+        const float G = s_lz[b - b_lo] + rng_gumbel(ws[t]);
         if (better(G, b, best, idx)) { best = G; idx = b; }
       }
     }
   }
-  warp_merge(d0, d1, best, idx, d2);
-  __shared__ float sb[BONUS_THREADS / 32], s_score[GUMBEL_BLOCK];
-  __shared__ int si[BONUS_THREADS / 32];
+  warp_best(best, idx);
   if (lane == 0) { sb[warp] = best; si[warp] = idx; }
   __syncthreads();
   if (warp == 0) {
     best = lane < BONUS_THREADS / 32 ? sb[lane] : -INFINITY;
     idx = lane < BONUS_THREADS / 32 ? si[lane] : 0x7fffffff;
-    warp_merge(d0, d1, best, idx, d2);
+    warp_best(best, idx);
+    if (lane == 0) { s_cta_best = best; s_cta_idx = idx; }
+  }
+  tc::cluster_sync();  // every CTA's best is in its shared memory
+  if (warp == 0) {
+    best = -INFINITY;
+    idx = 0x7fffffff;
+    if (lane < BONUS_SPLIT) {
+      best = ld_dsmem_f32(dsmem_addr(&s_cta_best, (uint32_t)lane));
+      idx = ld_dsmem_s32(dsmem_addr(&s_cta_idx, (uint32_t)lane));
+    }
+    warp_best(best, idx);
+  }
+  tc::cluster_sync();  // no CTA leaves while another still reads its shared memory
+  if (warp == 0) {
     int b = idx;
     if (!(best > -INFINITY) || b >= nb) {  // non-finite target row
-      if (lane == 0) dspark_set_status(DSPARK_ERR_TOKEN);
+      if (q == 0 && lane == 0) dspark_set_status(DSPARK_ERR_TOKEN);
       b = 0;
     }
+    if (b / nbq != q) return;  // another CTA owns the winning block
     // pass 3: inside block b, t / tau + Gumbel(id, entry stream)
     for (int j = lane; j < GUMBEL_BLOCK; j += 32) {
       const int v = b * GUMBEL_BLOCK + j;
@@ -449,9 +507,12 @@ extern "C" int dspark_verify(const dspark_dims *dims, const int32_t *anchor, con
     dspark_count_launches(2);
     return DSPARK_OK;
   }
-  // bonus_row keeps log Z_b of every sampler block in shared memory
-  const size_t lz_bytes = sizeof(float) * (size_t)((V + GUMBEL_BLOCK - 1) / GUMBEL_BLOCK);
-  if (lz_bytes > BONUS_MAX_SMEM) return DSPARK_ERR_TOO_LARGE;
+  // bonus_row keeps log Z_b of a quarter of the sampler blocks in shared memory
+  // (the size limit stays the one of the whole row)
+  const int nb = (V + GUMBEL_BLOCK - 1) / GUMBEL_BLOCK;
+  if (sizeof(float) * (size_t)nb > BONUS_MAX_SMEM) return DSPARK_ERR_TOO_LARGE;
+  const size_t lz_bytes =
+      sizeof(float) * (size_t)(((nb + BONUS_SPLIT - 1) / BONUS_SPLIT + 3) / 4 * 4);
   if (lz_bytes > 48 * 1024 &&
       cudaFuncSetAttribute(bonus_row, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)lz_bytes) != cudaSuccess)
@@ -475,7 +536,8 @@ extern "C" int dspark_verify(const dspark_dims *dims, const int32_t *anchor, con
                                          (const bf16 *)base_logits, tgt, ws.E,
                                          (const bf16 *)W2t, G, V, r, inv_tau, seed, bonus);
   DSPARK_CHECK_LAUNCH();
-  bonus_row<<<R, BONUS_THREADS, lz_bytes, stream>>>(ws.rows, tgt, bonus, G, V, inv_tau, seed);
+  bonus_row<<<R * BONUS_SPLIT, BONUS_THREADS, lz_bytes, stream>>>(ws.rows, tgt, bonus, G, V,
+                                                                  inv_tau, seed);
   DSPARK_CHECK_LAUNCH();
   dspark_count_launches(5);  // + the GEMM, counted by launch()
   return DSPARK_OK;

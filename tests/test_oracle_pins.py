@@ -464,6 +464,27 @@ def test_theta_closed_form_on_hand_example():
     assert oracle.schedule(c, sps, oracle.BREAK)["K"] == 3 - 1
 
 
+def test_theta_fixed_point_rounding_against_exact_rationals():
+    """S_K counts the products in 2^-48 units, each rounded to nearest with halves
+    up; Theta(K) is that sum times SPS, rounded once.  Pinned with exact
+    rationals on the half-unit boundary (2^-49 rounds up, the float below it
+    down), a product of 1 and one with a fraction of a unit."""
+    from fractions import Fraction
+    half = np.float32(2.0 ** -49)
+    a = np.array([[1.0, half, np.nextafter(half, np.float32(0)), 0.3]], dtype=np.float32)
+    sps = np.array([7.0, 3.0, 5.0, 2.0, 9.0], dtype=np.float32)
+    order = oracle.global_order(a)
+    got = oracle.dspark.theta_curve(a, order, sps)
+    units = [int(Fraction(float(a.reshape(-1)[i])) * 2 ** 48 + Fraction(1, 2)) for i in order]
+    assert units[2:] == [1, 0]                       # the boundary: half up, below half down
+    RS = 1 << 48
+    want = [float(Fraction(RS) * Fraction(float(sps[0])) / 2 ** 48)]
+    for K, u in enumerate(units, start=1):
+        RS += u
+        want.append(float(Fraction(RS) * Fraction(float(sps[K])) / 2 ** 48))
+    assert got.tolist() == want
+
+
 # ------------------------------------------------------------ a8: verify ---
 
 def test_confidence_label_identity():
