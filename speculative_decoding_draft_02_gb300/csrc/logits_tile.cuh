@@ -119,10 +119,15 @@ struct EpiLogits {
   static_assert(MODE == MODE_GREEDY || SLICE == GUMBEL_BLOCK,
                 "a sampling slice is exactly one sampler block");
 
-  // Kept by each epilogue thread across the tiles it processes.
+  // Kept by each epilogue thread across the tiles it processes.  Every tile of a
+  // CTA lies in one row block (kRowAffine), so the residual row a thread
+  // serves is looked up once.
   struct State {
     uint4 buf[BUF];  // base logits of the tile to process next, loaded ahead
+    int req;         // residual: the request of this thread's compacted row
+    bool active;
   };
+
 
   __device__ __forceinline__ bool draft_row(int m0, int row, const bf16 *&brow) const {
     const int i = m0 + row;
@@ -135,7 +140,12 @@ struct EpiLogits {
   // current tile has taken them (load_words inside operator()), so the loads
   // have a whole tile of work to land.
   __device__ void prefetch(int m0, int n0, int row, int c0, int, State &st) const {
-    if (MODE == MODE_RESIDUAL) return;
+    if (MODE == MODE_RESIDUAL) {
+      const int i = m0 + row;
+      st.active = i < *count;
+      st.req = st.active ? list[i] : i;
+      return;
+    }
     const bf16 *brow = nullptr;
     if (!draft_row(m0, row, brow)) brow = nullptr;
     load_words<BUF>(brow, n0 + c0, st.buf);
@@ -162,9 +172,9 @@ struct EpiLogits {
     const bf16 *brow = base;
     int req = i;  // request id: keys the random stream and the logit rows
     if (MODE == MODE_RESIDUAL) {
-      active = i < *count;
+      active = st.active;
       if (active) {
-        req = list[i];
+        req = st.req;
         const ResampleRow rr = rows[req];
         pos = rr.pos;
         lse_t = rr.lse_t;
@@ -266,8 +276,11 @@ struct EpiLogits {
       // past V read -inf on both sides and add nothing
       const float c2 = inv_tau * LOG2E;
       constexpr int NQ = CH / 8;
-      uint4 nxt[NQ];
-      if (active) load_raw<CH>(brow, n0 + c0, V, nxt);
+      uint4 nxt[NQ], nxt_t[NQ];  // base and target words of the next chunk
+      if (active) {
+        load_raw<CH>(brow, n0 + c0, V, nxt);
+        load_raw<CH>(trow, n0 + c0, V, nxt_t);
+      }
       const float nt = -lse_t * LOG2E, nd = -lse_d * LOG2E;
 #pragma unroll 1
       for (int c = c0; c < c1; c += CH) {
@@ -276,12 +289,16 @@ struct EpiLogits {
         tc::tmem_wait_ld();
         const int n = n0 + c;
         if (active && n < V) {
-          uint4 cur[NQ];
+          uint4 cur[NQ], tw[NQ];
 #pragma unroll
-          for (int q = 0; q < NQ; ++q) cur[q] = nxt[q];
-          if (c + CH < c1) load_raw<CH>(brow, n + CH, V, nxt);  // prefetch the next chunk
-          uint4 tw[NQ];
-          load_raw<CH>(trow, n, V, tw);
+          for (int q = 0; q < NQ; ++q) {
+            cur[q] = nxt[q];
+            tw[q] = nxt_t[q];
+          }
+          if (c + CH < c1) {  // the next chunk's words, in flight during this one
+            load_raw<CH>(brow, n + CH, V, nxt);
+            load_raw<CH>(trow, n + CH, V, nxt_t);
+          }
           float sv[CH], tv[CH];
           unpack<CH>(cur, n, V, sv);
           unpack<CH>(tw, n, V, tv);
