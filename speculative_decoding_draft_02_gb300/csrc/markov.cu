@@ -265,6 +265,7 @@ extern "C" int dspark_markov_draft(const dspark_dims *dims, const void *base_log
     la.n_slots = lg.n_slots;
     // warps per request in the row phase: as many as still cover R in one pass
     if (R <= lg.grid) return mloop::launch_loop<MODE_SAMPLE, EW>(la, lg.grid, stream);
+    if (R <= lg.grid * 2) return mloop::launch_loop<MODE_SAMPLE, EW / 2>(la, lg.grid, stream);
     if (R <= lg.grid * (EW / 4)) return mloop::launch_loop<MODE_SAMPLE, 4>(la, lg.grid, stream);
     return mloop::launch_loop<MODE_SAMPLE, 2>(la, lg.grid, stream);
   }

@@ -337,6 +337,18 @@ def test_markov_draft_more_row_blocks_than_sms(tau):
     assert dsp.dspark_device_status() == 0
 
 
+@pytest.mark.parametrize("R", [200, 400])
+def test_markov_draft_row_groups(R):
+    """Sampling on a 152-CTA grid (two row blocks): 200 requests take groups of
+    six warps per request in the row phase, 400 groups of four."""
+    shape = (R, 2, 20000, 64, 64)
+    rnd, orc = _draft_case(shape, 1.0, seed=290)
+    rep = compare_draft(rnd.tokens, rnd.conf, rnd.lse_d, rnd.logp_d, orc, 1.0)
+    assert rep.compared >= shape[0]
+    assert rep.flagged <= max(2, rep.compared // 25)
+    assert dsp.dspark_device_status() == 0
+
+
 @pytest.mark.parametrize("shape,tau", [((3, 32, 520, 64, 64), 0.0), ((3, 32, 520, 64, 64), 1.0),
                                        ((37, 4, 1000, 128, 320), 0.05),
                                        ((37, 4, 1000, 128, 320), 4.0)])
