@@ -76,6 +76,8 @@ __global__ void __launch_bounds__(SCHED_THREADS) schedule_kernel(
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n = R * gamma;
+  pdl_trigger();
+  pdl_wait();  // the confidences come from the draft
 
   // a5: survival products, f32 left to right; keys for the global order.  The
   // merge-sort form first brings the confidences into shared memory with one
@@ -399,9 +401,11 @@ int launch_schedule(const float *conf, int32_t R, int32_t gamma, const float *sp
               : n_pad == 4096 ? schedule_kernel<4>
               : n_pad == 8192 ? schedule_kernel<8>
                               : schedule_kernel<16>;
-  kernel<<<1, SCHED_THREADS, smem, stream>>>(conf, R, gamma, sps, mode, k_fixed, n_pad, len,
-                                             K_out, theta_out, a_out, order_out, k_ring);
-  DSPARK_CHECK_LAUNCH();
+  // launch and set-up overlap the tail of the draft (the kernel waits for it)
+  if (dspark_launch_pdl(kernel, dim3(1), dim3(SCHED_THREADS), smem, stream, conf, R, gamma, sps,
+                        mode, k_fixed, n_pad, len, K_out, theta_out, a_out, order_out,
+                        k_ring) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
   dspark_count_launches(1);
   return DSPARK_OK;
 }

@@ -52,6 +52,8 @@ __global__ void __launch_bounds__(256) verify_rows(const bf16 *__restrict__ targ
                                                    int *__restrict__ count, int gamma, int V,
                                                    float inv_tau) {
   const int j = blockIdx.x / NSEG, seg = blockIdx.x % NSEG, i = blockIdx.y;
+  pdl_trigger();
+  pdl_wait();  // len comes from the scheduler
   if (blockIdx.x == 0 && i == 0 && threadIdx.x == 0) *count = 0;
   const int L = clamp_len(len, i, gamma);
   if (MODE == MODE_GREEDY ? j > L : j >= L) return;
@@ -119,7 +121,9 @@ __global__ void __launch_bounds__(256) verify_rows(const bf16 *__restrict__ targ
 }
 
 // Pass 2: one warp per request; lane j - 1 tests admitted position j (j <= l_r)
-// and a ballot finds the first failure.
+// and a ballot finds the first failure.  Sampling: the warp of a rejected
+// request takes a compacted slot and copies W1[x_{j*-1}] there, the A operand
+// of the residual pass.
 template <int MODE>
 __global__ void verify_decide(const SegStat *__restrict__ stat, const bf16 *__restrict__ target,
                               const int32_t *__restrict__ anchor,
@@ -127,9 +131,12 @@ __global__ void verify_decide(const SegStat *__restrict__ stat, const bf16 *__re
                               const float *__restrict__ lse_d, const float *__restrict__ logp_d,
                               ResampleRow *__restrict__ rows, int *__restrict__ list,
                               int *__restrict__ count, int32_t *__restrict__ accepted,
-                              int32_t *__restrict__ bonus, int R, int gamma, int V, float inv_tau,
-                              uint64_t seed) {
+                              int32_t *__restrict__ bonus, const bf16 *__restrict__ W1,
+                              bf16 *__restrict__ E, int R, int gamma, int V, int r,
+                              float inv_tau, uint64_t seed) {
   const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
+  pdl_wait();  // the row statistics of verify_rows
   if (i >= R) return;  // warp-uniform
   const int L = clamp_len(len, i, gamma);  // gamma <= 32: one lane per position
   const SegStat *st = stat + (size_t)i * (gamma + 1) * NSEG;
@@ -171,18 +178,21 @@ __global__ void verify_decide(const SegStat *__restrict__ stat, const bf16 *__re
   }
   const unsigned bal = __ballot_sync(0xffffffffu, fail);
   const int jf = bal ? __ffs(bal) : 0;  // first rejected position (1-based), 0 if none
-  if (lane == (jf ? jf - 1 : 0)) {
+  const int src = jf ? jf - 1 : 0;
+  int slot = -1, prev = 0;
+  if (lane == src) {
     ResampleRow rr;
     rr.pad[0] = rr.pad[1] = rr.pad[2] = 0;
     if (jf) {
       rr.kind = KIND_RESIDUAL;
       rr.pos = jf;
-      int prev = (jf == 1) ? anchor[i] : x[jf - 2];
+      prev = (jf == 1) ? anchor[i] : x[jf - 2];
       if (prev < 0 || prev >= V) { dspark_set_status(DSPARK_ERR_TOKEN); prev = 0; }
       rr.prev = prev;
       rr.lse_t = lse_t;
       rr.lse_d = lse_d[(size_t)i * gamma + jf - 1];
-      list[atomicAdd(count, 1)] = i;  // compacted residual rows (order irrelevant)
+      slot = atomicAdd(count, 1);
+      list[slot] = i;  // compacted residual rows (order irrelevant)
     } else {
       rr.kind = KIND_BONUS;
       rr.pos = L + 1;
@@ -193,18 +203,14 @@ __global__ void verify_decide(const SegStat *__restrict__ stat, const bf16 *__re
     accepted[i] = jf ? jf - 1 : L;
     rows[i] = rr;
   }
-}
-
-// E[slot] = W1[x_{j*-1}] of the slot's request.
-__global__ void resample_gather(const ResampleRow *__restrict__ rows, const int *__restrict__ list,
-                                const int *__restrict__ count, const bf16 *__restrict__ W1,
-                                bf16 *__restrict__ E, int r) {
-  const int slot = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  if (slot >= *count) return;
-  const ResampleRow rr = rows[list[slot]];
-  uint4 *dst = reinterpret_cast<uint4 *>(E + (size_t)slot * r);
-  const uint4 *src = reinterpret_cast<const uint4 *>(W1 + (size_t)rr.prev * r);
-  for (int c = lane; c < r / 8; c += 32) dst[c] = src[c];
+  // the residual pass's A operand: E[slot] = W1[x_{j*-1}], copied by the warp
+  slot = __shfl_sync(0xffffffffu, slot, src);
+  prev = __shfl_sync(0xffffffffu, prev, src);
+  if (slot >= 0) {  // warp-uniform
+    const uint4 *from = reinterpret_cast<const uint4 *>(W1 + (size_t)prev * r);
+    uint4 *to = reinterpret_cast<uint4 *>(E + (size_t)slot * r);
+    for (int c = lane; c < r / 8; c += 32) to[c] = from[c];
+  }
 }
 
 // Residual rows: the block scores of the slices pick a block of 64 ids; inside
@@ -219,6 +225,8 @@ __global__ void __launch_bounds__(256) resample_reduce(
     const bf16 *__restrict__ target, const bf16 *__restrict__ E, const bf16 *__restrict__ W2t,
     int gamma, int V, int r, float inv_tau, uint64_t seed, int32_t *__restrict__ bonus) {
   const int slot = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_trigger();
+  pdl_wait();  // the residual pass's partials
   if (slot >= *count) return;
   float best = -INFINITY, d0 = 0.f, d1 = 0.f, d2 = 0.f;
   int idx = 0x7fffffff;
@@ -339,6 +347,8 @@ __global__ void __cluster_dims__(BONUS_SPLIT, 1, 1) __launch_bounds__(BONUS_THRE
   constexpr int GROUPS = BONUS_THREADS / 8, U = 8;
   const int i = blockIdx.x / BONUS_SPLIT, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int q = (int)tc::cluster_ctarank();
+  pdl_trigger();
+  pdl_wait();  // the rows' kinds, final once resample_reduce has run
   const ResampleRow rr = rows[i];
   // the same for every CTA of the cluster: all leave here or none
   if (rr.kind != KIND_BONUS && rr.kind != KIND_FALLBACK) return;
@@ -498,12 +508,13 @@ extern "C" int dspark_verify(const dspark_dims *dims, const int32_t *anchor, con
   const dim3 rgrid(NSEG * (G + 1), R);
   const bf16 *tgt = (const bf16 *)target;
   if (!sample) {
-    verify_rows<MODE_GREEDY><<<rgrid, 256, 0, stream>>>(tgt, len, ws.stat, ws.count, G, V, inv_tau);
-    DSPARK_CHECK_LAUNCH();
-    verify_decide<MODE_GREEDY><<<(R * 32 + 255) / 256, 256, 0, stream>>>(
-        ws.stat, tgt, anchor, tokens, len, lse_d, logp_d, ws.rows, ws.list, ws.count, accepted,
-        bonus, R, G, V, inv_tau, seed);
-    DSPARK_CHECK_LAUNCH();
+    if (dspark_launch_pdl(verify_rows<MODE_GREEDY>, rgrid, dim3(256), 0, stream, tgt, len,
+                          ws.stat, ws.count, G, V, inv_tau) != cudaSuccess ||
+        dspark_launch_pdl(verify_decide<MODE_GREEDY>, dim3((R * 32 + 255) / 256), dim3(256), 0,
+                          stream, ws.stat, tgt, anchor, tokens, len, lse_d, logp_d, ws.rows,
+                          ws.list, ws.count, accepted, bonus, (const bf16 *)nullptr,
+                          (bf16 *)nullptr, R, G, V, r, inv_tau, seed) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
     dspark_count_launches(2);
     return DSPARK_OK;
   }
@@ -517,29 +528,30 @@ extern "C" int dspark_verify(const dspark_dims *dims, const int32_t *anchor, con
       cudaFuncSetAttribute(bonus_row, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)lz_bytes) != cudaSuccess)
     return DSPARK_ERR_CUDA;
-  verify_rows<MODE_SAMPLE><<<rgrid, 256, 0, stream>>>(tgt, len, ws.stat, ws.count, G, V, inv_tau);
-  DSPARK_CHECK_LAUNCH();
-  verify_decide<MODE_SAMPLE><<<(R * 32 + 255) / 256, 256, 0, stream>>>(
-      ws.stat, tgt, anchor, tokens, len, lse_d, logp_d, ws.rows, ws.list, ws.count, accepted,
-      bonus, R, G, V, inv_tau, seed);
-  DSPARK_CHECK_LAUNCH();
-  resample_gather<<<(R * 32 + 255) / 256, 256, 0, stream>>>(ws.rows, ws.list, ws.count,
-                                                          (const bf16 *)W1, ws.E, r);
-  DSPARK_CHECK_LAUNCH();
+  // each kernel's launch and set-up overlap the tail of the one before
+  // (programmatic serialisation; every kernel waits before touching memory)
+  if (dspark_launch_pdl(verify_rows<MODE_SAMPLE>, rgrid, dim3(256), 0, stream, tgt, len, ws.stat,
+                        ws.count, G, V, inv_tau) != cudaSuccess ||
+      dspark_launch_pdl(verify_decide<MODE_SAMPLE>, dim3((R * 32 + 255) / 256), dim3(256), 0,
+                        stream, ws.stat, tgt, anchor, tokens, len, lse_d, logp_d, ws.rows,
+                        ws.list, ws.count, accepted, bonus, (const bf16 *)W1, ws.E, R, G, V, r,
+                        inv_tau, seed) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
   const int n_parts = logits_parts<MODE_RESIDUAL>(V);
   EpiLogits<MODE_RESIDUAL> epi{(const bf16 *)base_logits, tgt, ws.rows, ws.list, ws.count,
                                ws.part, R, V, G, 0, n_parts, inv_tau, seed};
   const int rc = gemm::launch<LogitsCfg<MODE_RESIDUAL>::EPI_WARPS, LogitsCfg<MODE_RESIDUAL>::BN>(
-      ws.E, W2t, R, V, r, epi, stream, ws.count);
+      ws.E, W2t, R, V, r, epi, stream, ws.count, true);
   if (rc != DSPARK_OK) return rc;
-  resample_reduce<<<R, 256, 0, stream>>>(ws.rows, ws.list, ws.count, ws.part, n_parts,
-                                         (const bf16 *)base_logits, tgt, ws.E,
-                                         (const bf16 *)W2t, G, V, r, inv_tau, seed, bonus);
-  DSPARK_CHECK_LAUNCH();
-  bonus_row<<<R * BONUS_SPLIT, BONUS_THREADS, lz_bytes, stream>>>(ws.rows, tgt, bonus, G, V,
-                                                                  inv_tau, seed);
-  DSPARK_CHECK_LAUNCH();
-  dspark_count_launches(5);  // + the GEMM, counted by launch()
+  if (dspark_launch_pdl(resample_reduce, dim3(R), dim3(256), 0, stream, ws.rows,
+                        (const int *)ws.list, (const int *)ws.count, (const RowPartial *)ws.part,
+                        n_parts, (const bf16 *)base_logits, tgt, (const bf16 *)ws.E,
+                        (const bf16 *)W2t, G, V, r, inv_tau, seed, bonus) != cudaSuccess ||
+      dspark_launch_pdl(bonus_row, dim3(R * BONUS_SPLIT), dim3(BONUS_THREADS), lz_bytes, stream,
+                        (const ResampleRow *)ws.rows, tgt, bonus, G, V, inv_tau,
+                        seed) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  dspark_count_launches(4);  // + the GEMM, counted by launch()
   return DSPARK_OK;
 }
 
