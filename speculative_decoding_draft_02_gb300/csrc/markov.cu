@@ -342,6 +342,8 @@ __global__ void rnn_state(const float *__restrict__ Gk, const float *__restrict_
                           int R, int gamma, int r, int k, int splits, int m_pad, int psplits,
                           int pm_pad) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  pdl_trigger();
+  pdl_wait();  // the recurrent GEMM's partials
   if (t >= R * r) return;
   const int i = t / r, c = t % r;
   float gg = 0.f, gc = 0.f, pg = 0.f, pc = 0.f;
@@ -449,7 +451,7 @@ extern "C" int dspark_rnn_draft(const dspark_dims *dims, const void *base_logits
   // R gamma = 1280 rows make only 40 tiles, each 112 k blocks deep
   int rc = gemm::launch<4, 256>(h, W_hid, R * G, 2 * r, d,
                                 EpiStoreF32{ws.P, ws.psplits * ws.pm_pad, 2 * r}, stream,
-                                nullptr, false, ws.psplits);
+                                nullptr, true, ws.psplits);
   if (rc != DSPARK_OK) return rc;
   if (cudaMemsetAsync(ws.U, 0, sizeof(bf16) * (size_t)R * 2 * r, stream) != cudaSuccess ||
       cudaMemsetAsync(ws.state, 0, sizeof(float) * (size_t)R * r, stream) != cudaSuccess)
@@ -464,10 +466,10 @@ extern "C" int dspark_rnn_draft(const dspark_dims *dims, const void *base_logits
                              EpiStoreF32{ws.Gk, ws.splits * ws.m_pad, 2 * r}, stream, nullptr,
                              true, ws.splits);
     if (rc != DSPARK_OK) return rc;
-    rnn_state<<<(R * r + 255) / 256, 256, 0, stream>>>(ws.Gk, ws.P, ws.state, ws.mk.E, ws.U,
-                                                       R, G, r, k, ws.splits, ws.m_pad,
-                                                       ws.psplits, ws.pm_pad);
-    DSPARK_CHECK_LAUNCH();
+    if (dspark_launch_pdl(rnn_state, dim3((R * r + 255) / 256), dim3(256), 0, stream,
+                          (const float *)ws.Gk, (const float *)ws.P, ws.state, ws.mk.E, ws.U, R,
+                          G, r, k, ws.splits, ws.m_pad, ws.psplits, ws.pm_pad) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
     if (tau > 0.f) {
       const int n_parts = logits_parts<MODE_SAMPLE>(V);
       EpiLogits<MODE_SAMPLE> epi{(const bf16 *)base_logits, nullptr, nullptr, nullptr, nullptr,
