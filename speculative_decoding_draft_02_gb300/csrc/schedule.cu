@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(SCHED_THREADS) schedule_kernel(
   // Theta over K = beg .. beg+per (K = 0 handled by thread 0)
   long long best = (long long)0x8000000000000000ULL;  // threads past the end never win
   long bestK = 0x7fffffffffffffffL;
-  long firstDrop = 0x7fffffffffffffffL;  // smallest K with Theta(K+1) <= Theta(K)
+  long firstDrop = 0x7fffffffffffffffL;  // smallest K with Theta(K+1) > Theta(K) false
   if (scanner) {
     u64 excl = __shfl_up_sync(0xffffffffu, incl, 1);
     if (lane == 0) excl = 0ull;
@@ -272,7 +272,8 @@ __global__ void __launch_bounds__(SCHED_THREADS) schedule_kernel(
       const double th = theta_at(K, RS, spsK);
       const long long key = theta_key(th);
       if (key > best) { best = key; bestK = K; }
-      if (th <= prevTheta && firstDrop > K - 1) firstDrop = K - 1;
+      // break admits K only while Theta strictly rises (a NaN stops it)
+      if (!(th > prevTheta) && firstDrop > K - 1) firstDrop = K - 1;
       prevTheta = th;
     }
   }

@@ -259,6 +259,47 @@ def test_schedule_extremes():
         assert sorted_order_ok(oracle.schedule(c, sps)["order"], oracle.survival(c))
 
 
+def _schedule_gpu(c, R, G, sps, mode, kf=0):
+    length = torch.empty(R, dtype=torch.int32, device="cuda")
+    K = torch.empty(1, dtype=torch.int32, device="cuda")
+    th = torch.empty(1, dtype=torch.float64, device="cuda")
+    dsp.dspark_schedule(dev(c), R, G, dev(sps), mode, kf, length, K, th)
+    return int(K.item()), host(length), float(th.item())
+
+
+def test_schedule_at_the_size_limit_with_every_product_one():
+    """R gamma = 16384 candidates, all survival products 1: the largest fixed-point
+    sum, R + S_K = 2^15 units of 2^48 at K = n."""
+    R, G = 16384, 1
+    c = torch.ones((R, G), dtype=torch.float32)
+    for kind in SPS_KINDS:
+        sps = sps_for(kind, R * (G + 1))
+        for mode in (0, 1):
+            o = oracle.schedule(c, sps, mode)
+            k, length, th = _schedule_gpu(c, R, G, sps, mode)
+            assert k == o["K"] and th == o["theta"], (kind, mode)
+            assert np.array_equal(length, o["len"])
+    assert dsp.dspark_device_status() == 0
+
+
+def test_schedule_with_nan_in_the_sps_table():
+    """A NaN Theta never wins the argmax; break mode stops at it."""
+    R, G = 40, 4
+    c = workloads.random_confidences(R, G, seed=9)
+    sps = sps_for("concave", R * (G + 1)).clone()
+    best = oracle.schedule(c, sps)["K"]
+    for at in (best, 3):
+        bad = sps.clone()
+        bad[R + at - 1] = float("nan")  # Theta(at) is NaN
+        for mode in (0, 1):
+            o = oracle.schedule(c, bad, mode)
+            k, length, th = _schedule_gpu(c, R, G, bad, mode)
+            assert k == o["K"], (at, mode)
+            assert np.array_equal(length, o["len"])
+            assert th == o["theta"] or (np.isnan(th) and np.isnan(o["theta"]))
+    assert dsp.dspark_device_status() == 0
+
+
 # ------------------------------------------------------------------ a8 ----
 
 def _verify_case(shape, tau, seed, accept_bias=0.7, lens_kind="random"):
