@@ -46,6 +46,9 @@ def parse():
     p.add_argument("--impl", default="dspark", choices=["dspark", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--fused-variant", action="store_true",
+                   help="also time the fused single-contraction draft step (a measured "
+                        "variant; the main line is unchanged)")
     p.add_argument("--cpu-sample", type=int, default=0,
                    help="requests in the CPU-oracle sample (0 = sized automatically)")
     return p.parse_args()
@@ -431,6 +434,36 @@ def run_dspark(args, w, ws, rank, local):
         "gpu_launches": launches,
         "clocks": clk,
     }
+
+    if args.fused_variant:
+        # the fused single-contraction draft step in place of LM head + Markov loop:
+        # per step one GEMM [R, d + r] x [d + r, V] (W_lm and W2t streamed each step)
+        W_cat = torch.empty((V, d + r), dtype=torch.bfloat16, device="cuda")
+        dsp.dspark_pack_fused(dims, head.W_lm, head.W2t, W_cat)
+        fws = dsp.workspace(dsp.dspark_fused_workspace_bytes(dims))
+
+        def fused():
+            dsp.dspark_fused_draft(dims, h, anchor, W_cat, head.W1, head.w_conf, head.T, tau, ds,
+                                   rnd.tokens, rnd.conf, rnd.logp_d, rnd.lse_d, fws)
+
+        for _ in range(3):
+            fused()
+        torch.cuda.synchronize()
+        n_f = max(3, min(args.steps, 50))
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(n_f):
+            fused()
+        f1.record(stream)
+        torch.cuda.synchronize()
+        dsp.check_device_status()
+        fms = f0.elapsed_time(f1) / n_f
+        fbytes = G * (V * (d + r) * 2 + R * (d + r) * 2)
+        line["fused_variant"] = {
+            "draft_ms": fms, "lm_head_plus_loop_ms": stage["lm_head"] + stage["markov_loop"],
+            "draft_bytes": fbytes, "hbm_frac": fbytes / (fms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "tensor_frac": G * 2.0 * R * (d + r) * V / (fms * 1e-3) / 1e12 / tc_peak}
+        del W_cat, fws
 
     if not args.no_e2e:
         # end to end through the public API from pinned host buffers

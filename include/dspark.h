@@ -157,6 +157,24 @@ int dspark_rnn_draft(const dspark_dims *dims, const void *base_logits, const voi
                      uint64_t seed, int32_t *tokens, float *conf, float *logp_d, float *lse_d,
                      void *workspace, size_t workspace_bytes, dspark_stream_t stream);
 
+/* Fused single-contraction draft step, a measured variant of a1 + a2
+ * ("DSpark 深度解读" §二 设计一: the draft logits are the shared LM head's plus
+ * the Markov bias).  Per step k one contraction
+ *   l_k = [h_k; W1[x_{k-1}]] . [W_lm; W2t]^T    (f32 accumulation, no bf16 base)
+ * replaces the round's LM head plus the bias pass: the base logits never reach
+ * HBM, but W_lm is streamed gamma times.  Sampling, the confidence head and
+ * the outputs are dspark_markov_draft's.
+ *   W_cat  bf16 [V, d + r]  row v = [W_lm[v] | W2t[v]], made by dspark_pack_fused
+ * The workspace is dspark_fused_workspace_bytes(dims) bytes, 256-byte aligned. */
+size_t dspark_fused_workspace_bytes(const dspark_dims *dims);
+int dspark_pack_fused(const dspark_dims *dims, const void *W_lm, const void *W2t, void *W_cat,
+                      dspark_stream_t stream);
+int dspark_fused_draft(const dspark_dims *dims, const void *h, const int32_t *anchor,
+                       const void *W_cat, const void *W1, const void *w_conf, const float *T,
+                       float tau, uint64_t seed, int32_t *tokens, float *conf, float *logp_d,
+                       float *lse_d, void *workspace, size_t workspace_bytes,
+                       dspark_stream_t stream);
+
 /* a1-a4 in one call: dspark_lm_head into `base_logits`, then dspark_markov_draft. */
 int dspark_draft(const dspark_dims *dims, const void *h, const int32_t *anchor,
                  const void *W_lm, const void *W1, const void *W2t, const void *w_conf,

@@ -9,6 +9,7 @@ library and never imports it.
 from . import philox  # noqa: F401
 from .dspark import (  # noqa: F401
     BREAK, FIXED_K, UNCONSTRAINED, base_logits, confidence_label, draft_round,
-    global_order, markov_draft, rnn_draft, round_bf16, schedule, schedule_async, survival,
+    fused_draft, global_order, markov_draft, rnn_draft, round_bf16, schedule, schedule_async,
+    survival,
     expected_calibration_error, sts_fit, theta_curve, theta_of_lengths, verify,
 )

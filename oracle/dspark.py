@@ -288,8 +288,25 @@ def markov_draft(base, h, anchor, W1, W2, w_conf, T, tau: float, seed: int,
 
 
 # ---------------------------------------------------------------------------
+# a1 + a2 fused: one contraction per step   [DD §二 设计一]
+# ---------------------------------------------------------------------------
+
+
+def fused_draft(h, anchor, W_lm, W1, W2, w_conf, T, tau: float, seed: int,
+                **kw) -> Dict[str, np.ndarray]:
+    """The same draft head with the base logits never materialised.
+
+    One contraction per step, [h_k; W1[x_{k-1}]] . [W_lm; W2]^T, gives the whole
+    draft logit, so h_k . W_lm is not rounded to bf16 as the LM head's stored
+    output is; everything else is markov_draft's."""
+    return markov_draft(base_logits(h, W_lm, bf16_out=False), h, anchor, W1, W2, w_conf, T,
+                        tau, seed, **kw)
+
+
+# ---------------------------------------------------------------------------
 # a2': the RNN head variant   [AR stage two, "RNN head"; DD §二 设计一]
 # ---------------------------------------------------------------------------
+
 
 def rnn_draft(base, h, anchor, W1, W2, W_gc, w_conf, T, tau: float, seed: int,
               keep_scores: bool = False, block: int = GUMBEL_BLOCK) -> Dict[str, np.ndarray]:

@@ -31,7 +31,8 @@ EXPORTS = [
     "dspark_device_status", "dspark_error_string", "dspark_launch_count",
     "dspark_markov_draft_static", "dspark_schedule_async", "dspark_conf_logits",
     "dspark_sts_workspace_bytes", "dspark_sts_fit", "dspark_rnn_workspace_bytes",
-    "dspark_rnn_draft", "dspark_selftest_wait_timeout",
+    "dspark_rnn_draft", "dspark_selftest_wait_timeout", "dspark_fused_workspace_bytes",
+    "dspark_pack_fused", "dspark_fused_draft",
 ]
 STATIC_SCRATCH_BYTES = 16 << 20
 
@@ -74,6 +75,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "dspark_sts_workspace_bytes": (SZ, [I32, I32, I32, I32]),
         "dspark_sts_fit": (ctypes.c_int, [P, P, I32, I32, P, I32, I32, P, P, P, SZ, P]),
         "dspark_rnn_workspace_bytes": (SZ, [DP]),
+        "dspark_fused_workspace_bytes": (SZ, [DP]),
+        "dspark_pack_fused": (ctypes.c_int, [DP, P, P, P, P]),
+        "dspark_fused_draft": (ctypes.c_int, [DP, P, P, P, P, P, P, F32, U64, P, P, P, P, P, SZ,
+                                              P]),
         "dspark_selftest_wait_timeout": (ctypes.c_int, [U64, P]),
         "dspark_rnn_draft": (ctypes.c_int, [DP, P, P, P, P, P, P, P, P, P, F32, U64, P, P, P, P,
                                             P, SZ, P]),
@@ -206,6 +211,23 @@ def dspark_rnn_draft(dims, base_logits, h, anchor, W1, W2t, W_rec, W_hid, w_conf
         _ptr(W_rec), _ptr(W_hid), _ptr(w_conf), _ptr(T), float(tau), _u64(seed), _ptr(tokens),
         _ptr(conf), _ptr(logp_d), _ptr(lse_d), _ptr(workspace), workspace.numel(),
         _stream(stream)), "dspark_rnn_draft")
+
+
+def dspark_fused_workspace_bytes(dims) -> int:
+    return int(load_library().dspark_fused_workspace_bytes(ctypes.byref(dims)))
+
+
+def dspark_pack_fused(dims, W_lm, W2t, W_cat, stream=None):
+    _check(load_library().dspark_pack_fused(ctypes.byref(dims), _ptr(W_lm), _ptr(W2t),
+                                            _ptr(W_cat), _stream(stream)), "dspark_pack_fused")
+
+
+def dspark_fused_draft(dims, h, anchor, W_cat, W1, w_conf, T, tau, seed, tokens, conf, logp_d,
+                       lse_d, workspace, stream=None):
+    _check(load_library().dspark_fused_draft(
+        ctypes.byref(dims), _ptr(h), _ptr(anchor), _ptr(W_cat), _ptr(W1), _ptr(w_conf), _ptr(T),
+        float(tau), _u64(seed), _ptr(tokens), _ptr(conf), _ptr(logp_d), _ptr(lse_d),
+        _ptr(workspace), workspace.numel(), _stream(stream)), "dspark_fused_draft")
 
 
 def dspark_sts_fit(z, accepted, T_grid, n_bins, T_out, ece_out, workspace=None, stream=None):

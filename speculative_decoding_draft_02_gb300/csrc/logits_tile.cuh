@@ -129,9 +129,11 @@ struct EpiLogits {
   };
 
 
+  // base == nullptr: no base logits (the fused single-contraction step, whose
+  // A operand carries h and the GEMM adds h . W_lm itself); they read as zeros
   __device__ __forceinline__ bool draft_row(int m0, int row, const bf16 *&brow) const {
     const int i = m0 + row;
-    brow = base + (size_t)(i * gamma + k - 1) * V;
+    brow = base ? base + (size_t)(i * gamma + k - 1) * V : nullptr;
     return i < M;
   }
 
@@ -187,7 +189,7 @@ struct EpiLogits {
     }
     // the base-logit row of this thread in the CTA's next tile (none: zeros)
     const bf16 *nrow = nullptr;
-    if (MODE != MODE_RESIDUAL && next_m0 >= 0 && next_m0 + row < M)
+    if (MODE != MODE_RESIDUAL && base && next_m0 >= 0 && next_m0 + row < M)
       nrow = base + (size_t)((next_m0 + row) * gamma + k - 1) * V;
     const int nn = next_n0 + c0;
 
@@ -345,7 +347,9 @@ struct EpiLogits {
 // ---------------------------------------------------------------------------
 
 // out[j] = base_row[v] + E . W2t[v] for v = b * GUMBEL_BLOCK + j, and -inf past
-// V: the block's logits rebuilt from the Markov bias (E = W1[x_{k-1}]).  Every
+// V: the block's logits rebuilt from the Markov bias (E = W1[x_{k-1}]), or with
+// base_row == nullptr the whole logit of a fused step (E = [h; W1[x_{k-1}]]
+// against rows [W_lm; W2t], r their common length).  Every
 // thread of a CTA of NT threads calls it; each warp takes GUMBEL_BLOCK / (NT/32)
 // ids, and a lane has the W2t words of two passes (r = 512: all of its words)
 // in flight at once.  Ends with a __syncthreads().
@@ -392,7 +396,8 @@ __device__ void block_logits(const bf16 *__restrict__ base_row, const bf16 *__re
 #pragma unroll
     for (int u = 0; u < PER; ++u)
       out[warp * PER + u] =
-          v0 + u < V ? __bfloat162float(base_row[v0 + u]) + acc[u] : -INFINITY;
+          v0 + u < V ? (base_row ? __bfloat162float(base_row[v0 + u]) : 0.f) + acc[u]
+                     : -INFINITY;
   }
   __syncthreads();
 }

@@ -90,8 +90,10 @@ __global__ void step_prep(const int32_t *__restrict__ anchor, const int32_t *__r
 // then (k < gamma) prepare step k+1: E[i] = W1[x_k] and the confidence c_{k+1}.
 // One CTA of RP_THREADS threads per request.  Greedy: the partials carry the
 // argmax.  Sampling: they carry block scores; the best block's 64 logits are
-// rebuilt (base logit + W1[x_{k-1}] . W2t[v], E still holds W1[x_{k-1}] here),
-// x_k is drawn among them and log p_d(x_k) = l_k[x_k] / tau - lse_k.
+// rebuilt (base logit + W1[x_{k-1}] . W2t[v], E still holds W1[x_{k-1}] here;
+// for the fused step, no base and E row [h_k; W1[x_{k-1}]] of length e_k and
+// stride e_row_ld against W2t = [W_lm; W2t]), x_k is drawn among them and
+// log p_d(x_k) = l_k[x_k] / tau - lse_k.
 constexpr int RP_THREADS = 256;
 
 template <int MODE>
@@ -99,7 +101,8 @@ __global__ void __launch_bounds__(RP_THREADS) reduce_prep(
     const RowPartial *__restrict__ part, int n_parts, int gamma, int V, int r, int k,
     int32_t *__restrict__ tokens, float *__restrict__ lse_out, float *__restrict__ logp_out,
     const bf16 *__restrict__ W1, const bf16 *__restrict__ w_e, const float *__restrict__ zh,
-    const float *__restrict__ T, const bf16 *E, bf16 *e_next, int e_ld,  // may be one buffer
+    const float *__restrict__ T, const bf16 *E, int e_row_ld, int e_k, bf16 *e_next,
+    int e_ld,  // E and e_next may share a buffer
     float *__restrict__ conf, const bf16 *__restrict__ base, const bf16 *__restrict__ W2t,
     float inv_tau, uint64_t seed) {
   const int i = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -148,7 +151,8 @@ __global__ void __launch_bounds__(RP_THREADS) reduce_prep(
       if (tid == 0) dspark_set_status(DSPARK_ERR_TOKEN);
       b = 0;
     }
-    block_logits<RP_THREADS>(base + o * V, E + (size_t)i * r, W2t, b, V, r, s_logit);
+    block_logits<RP_THREADS>(base ? base + o * V : nullptr, E + (size_t)i * e_row_ld, W2t, b, V,
+                             e_k, s_logit);
     if (warp == 0) {
       for (int j = lane; j < GUMBEL_BLOCK; j += 32) s_score[j] = s_logit[j] * inv_tau;
       __syncwarp();
@@ -479,7 +483,8 @@ extern "C" int dspark_rnn_draft(const dspark_dims *dims, const void *base_logits
       if (rc != DSPARK_OK) return rc;
       if (dspark_launch_pdl(reduce_prep<MODE_SAMPLE>, dim3(R), dim3(RP_THREADS), 0, stream,
                             ws.mk.part, n_parts, G, V, r, k, tokens, lse_d, logp_d,
-                            (const bf16 *)W1, w_e, ws.mk.zh, T, ws.mk.E, ws.U + r, 2 * r, conf,
+                            (const bf16 *)W1, w_e, ws.mk.zh, T, (const bf16 *)ws.mk.E, r, r,
+                            ws.U + r, 2 * r, conf,
                             (const bf16 *)base_logits, (const bf16 *)W2t, inv_tau,
                             seed) != cudaSuccess)
         return DSPARK_ERR_CUDA;
@@ -492,7 +497,8 @@ extern "C" int dspark_rnn_draft(const dspark_dims *dims, const void *base_logits
       if (rc != DSPARK_OK) return rc;
       if (dspark_launch_pdl(reduce_prep<MODE_GREEDY>, dim3(R), dim3(RP_THREADS), 0, stream,
                             ws.mk.part, n_parts, G, V, r, k, tokens, lse_d, logp_d,
-                            (const bf16 *)W1, w_e, ws.mk.zh, T, ws.mk.E, ws.U + r, 2 * r, conf,
+                            (const bf16 *)W1, w_e, ws.mk.zh, T, (const bf16 *)ws.mk.E, r, r,
+                            ws.U + r, 2 * r, conf,
                             (const bf16 *)base_logits, (const bf16 *)W2t, inv_tau,
                             seed) != cudaSuccess)
         return DSPARK_ERR_CUDA;
@@ -500,6 +506,121 @@ extern "C" int dspark_rnn_draft(const dspark_dims *dims, const void *base_logits
     DSPARK_CHECK_LAUNCH();
   }
   dspark_count_launches(2 + 2 * (uint64_t)G);  // + the GEMMs, counted by launch()
+  return DSPARK_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Fused single-contraction step, a measured variant: per step k the logits
+// come from one contraction [h_k; W1[x_{k-1}]] . [W_lm; W2]^T, so the base
+// logits never reach HBM, at the price of streaming W_lm once per step instead
+// of once per round ("DSpark 深度解读" §二 设计一 reads the draft logits as the
+// shared LM head's plus the Markov bias; this computes the same sum in one
+// GEMM).  Per step: A_k = [h_k | W1[x_{k-1}]] (a strided copy of h_k and the
+// embedding gather), the tcgen05 GEMM with the draft epilogue and no base
+// logits, then reduce_prep.
+// ---------------------------------------------------------------------------
+namespace {
+
+struct FusedWs {
+  MarkovWs mk;
+  bf16 *A;  // [R, d + r]
+  size_t bytes;
+};
+
+FusedWs fused_layout(const dspark_dims *d, char *base) {
+  FusedWs w;
+  w.mk = markov_layout(d, base);
+  size_t off = w.mk.bytes;
+  w.A = (bf16 *)(base + off);
+  off = dspark_align_up(off + sizeof(bf16) * (size_t)d->R * (d->d + d->r), 256);
+  w.bytes = off;
+  return w;
+}
+
+// d and r are multiples of 64, so d + r is a whole number of 64-deep k blocks
+bool fused_dims_ok(const dspark_dims *d) { return dspark_dims_ok(d); }
+
+}  // namespace
+
+extern "C" size_t dspark_fused_workspace_bytes(const dspark_dims *dims) {
+  if (!fused_dims_ok(dims)) return 0;
+  return fused_layout(dims, nullptr).bytes;
+}
+
+extern "C" int dspark_pack_fused(const dspark_dims *dims, const void *W_lm, const void *W2t,
+                                 void *W_cat, dspark_stream_t stream) {
+  if (!fused_dims_ok(dims) || !W_lm || !W2t || !W_cat) return DSPARK_ERR_ARG;
+  const size_t V = dims->V, d = dims->d, r = dims->r, ld = (d + r) * sizeof(bf16);
+  if (cudaMemcpy2DAsync(W_cat, ld, W_lm, d * sizeof(bf16), d * sizeof(bf16), V,
+                        cudaMemcpyDeviceToDevice, stream) != cudaSuccess ||
+      cudaMemcpy2DAsync((char *)W_cat + d * sizeof(bf16), ld, W2t, r * sizeof(bf16),
+                        r * sizeof(bf16), V, cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  return DSPARK_OK;
+}
+
+extern "C" int dspark_fused_draft(const dspark_dims *dims, const void *h, const int32_t *anchor,
+                                  const void *W_cat, const void *W1, const void *w_conf,
+                                  const float *T, float tau, uint64_t seed, int32_t *tokens,
+                                  float *conf, float *logp_d, float *lse_d, void *workspace,
+                                  size_t workspace_bytes, dspark_stream_t stream) {
+  if (!fused_dims_ok(dims) || !h || !anchor || !W_cat || !W1 || !w_conf || !T || !tokens ||
+      !conf || !(tau >= 0.f))
+    return DSPARK_ERR_ARG;
+  if (((uintptr_t)W_cat | (uintptr_t)W1 | (uintptr_t)h) & 15)
+    return DSPARK_ERR_ARG;  // TMA and 16-byte vector loads
+  FusedWs ws = fused_layout(dims, (char *)workspace);
+  if (!workspace || workspace_bytes < ws.bytes || ((uintptr_t)workspace & 255))
+    return DSPARK_ERR_WORKSPACE;
+  const int R = dims->R, G = dims->gamma, V = dims->V, r = dims->r, d = dims->d;
+  const int K = d + r;
+  const bf16 *w_e = (const bf16 *)w_conf + d;
+  const float inv_tau = tau > 0.f ? 1.f / tau : 1.f;
+  conf_hidden<<<R * G, 128, 0, stream>>>((const bf16 *)h, (const bf16 *)w_conf, ws.mk.zh, d,
+                                         nullptr);
+  DSPARK_CHECK_LAUNCH();
+  // E_1 = W1[anchor] into the embedding columns of A, and c_1
+  step_prep<<<(R * 32 + 255) / 256, 256, 0, stream>>>(anchor, tokens, (const bf16 *)W1, w_e,
+                                                     ws.mk.zh, T, ws.A + d, K, conf, R, G, V,
+                                                     r, 1);
+  DSPARK_CHECK_LAUNCH();
+  for (int k = 1; k <= G; ++k) {
+    // h_k into the first d columns of A (reduce_prep of step k-1 is done with A)
+    if (cudaMemcpy2DAsync(ws.A, (size_t)K * sizeof(bf16),
+                          (const bf16 *)h + (size_t)(k - 1) * d, (size_t)G * d * sizeof(bf16),
+                          (size_t)d * sizeof(bf16), R, cudaMemcpyDeviceToDevice,
+                          stream) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
+    int rc;
+    if (tau > 0.f) {
+      const int n_parts = logits_parts<MODE_SAMPLE>(V);
+      EpiLogits<MODE_SAMPLE> epi{nullptr, nullptr, nullptr, nullptr, nullptr, ws.mk.part,
+                                 R, V, G, k, n_parts, inv_tau, seed};
+      rc = gemm::launch<LogitsCfg<MODE_SAMPLE>::EPI_WARPS, LogitsCfg<MODE_SAMPLE>::BN>(
+          ws.A, W_cat, R, V, K, epi, stream, nullptr, true);
+      if (rc != DSPARK_OK) return rc;
+      if (dspark_launch_pdl(reduce_prep<MODE_SAMPLE>, dim3(R), dim3(RP_THREADS), 0, stream,
+                            ws.mk.part, n_parts, G, V, r, k, tokens, lse_d, logp_d,
+                            (const bf16 *)W1, w_e, ws.mk.zh, T, (const bf16 *)ws.A, K, K,
+                            ws.A + d, K, conf, (const bf16 *)nullptr, (const bf16 *)W_cat,
+                            inv_tau, seed) != cudaSuccess)
+        return DSPARK_ERR_CUDA;
+    } else {
+      const int n_parts = logits_parts<MODE_GREEDY>(V);
+      EpiLogits<MODE_GREEDY> epi{nullptr, nullptr, nullptr, nullptr, nullptr, ws.mk.part,
+                                 R, V, G, k, n_parts, 1.f, seed};
+      rc = gemm::launch<LogitsCfg<MODE_GREEDY>::EPI_WARPS, LogitsCfg<MODE_GREEDY>::BN>(
+          ws.A, W_cat, R, V, K, epi, stream, nullptr, true);
+      if (rc != DSPARK_OK) return rc;
+      if (dspark_launch_pdl(reduce_prep<MODE_GREEDY>, dim3(R), dim3(RP_THREADS), 0, stream,
+                            ws.mk.part, n_parts, G, V, r, k, tokens, lse_d, logp_d,
+                            (const bf16 *)W1, w_e, ws.mk.zh, T, (const bf16 *)ws.A, K, K,
+                            ws.A + d, K, conf, (const bf16 *)nullptr, (const bf16 *)W_cat,
+                            inv_tau, seed) != cudaSuccess)
+        return DSPARK_ERR_CUDA;
+    }
+  }
+  dspark_count_launches(2 + (uint64_t)G);  // + the GEMMs, counted by launch()
   return DSPARK_OK;
 }
 

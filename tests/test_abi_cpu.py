@@ -107,6 +107,14 @@ def test_new_entry_points_check_arguments_without_launch(lib):
                                 fake, 0.0, 0, fake, fake, None, None, fake, 16, None) == 4
     assert lib.dspark_rnn_workspace_bytes(ctypes.byref(d)) > lib.dspark_markov_workspace_bytes(
         ctypes.byref(d))
+    # the fused single-contraction step needs the packed weights and its workspace
+    assert lib.dspark_fused_draft(ctypes.byref(d), fake, fake, None, fake, fake, fake, 0.0, 0,
+                                  fake, fake, None, None, fake, 1 << 30, None) == 1
+    assert lib.dspark_fused_draft(ctypes.byref(d), fake, fake, fake, fake, fake, fake, 0.0, 0,
+                                  fake, fake, None, None, fake, 16, None) == 4
+    assert lib.dspark_pack_fused(ctypes.byref(d), fake, None, fake, None) == 1
+    assert lib.dspark_fused_workspace_bytes(ctypes.byref(d)) > lib.dspark_markov_workspace_bytes(
+        ctypes.byref(d))
     # STS: at most 64 bins; the asynchronous schedule needs its ring
     assert lib.dspark_sts_workspace_bytes(1000, 5, 51, 65) == 0
     assert lib.dspark_sts_fit(fake, fake, 1000, 5, fake, 51, 65, fake, fake, fake, 1 << 30,

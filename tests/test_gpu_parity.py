@@ -378,6 +378,34 @@ def test_markov_draft_more_row_blocks_than_sms(tau):
     assert dsp.dspark_device_status() == 0
 
 
+@pytest.mark.parametrize("shape", [(4, 5, 1024, 64, 256), (37, 4, 1000, 128, 320),
+                                   (130, 2, 2056, 64, 192)])
+@pytest.mark.parametrize("tau", [0.0, 1.0])
+def test_fused_draft_matches_oracle(shape, tau):
+    """The fused single-contraction step against the oracle's statement of it
+    (base logits h . W_lm exact, never rounded to bf16)."""
+    R, G, V, r, d = shape
+    seed = 240 + V
+    inp = _weights(R, G, V, r, d, seed=seed)
+    orc = oracle.fused_draft(inp["h"], inp["anchor"], inp["W_lm"], inp["W1"], inp["W2"],
+                             inp["w_conf"], inp["T"], tau, seed=12345 + seed, keep_scores=True)
+    head = dsp.DraftHead.from_weights(R, G, inp["W_lm"], inp["W1"], inp["W2"], inp["w_conf"],
+                                      inp["T"])
+    W_cat = torch.empty((V, d + r), dtype=torch.bfloat16, device="cuda")
+    dsp.dspark_pack_fused(head.dims, head.W_lm, head.W2t, W_cat)
+    assert torch.equal(W_cat[:, :d], head.W_lm) and torch.equal(W_cat[:, d:], head.W2t)
+    rnd = dsp.Round(head)
+    ws = dsp.workspace(dsp.dspark_fused_workspace_bytes(head.dims))
+    dsp.dspark_fused_draft(head.dims, dev(inp["h"], torch.bfloat16).contiguous(),
+                           dev(inp["anchor"]), W_cat, head.W1, head.w_conf, head.T, tau,
+                           12345 + seed, rnd.tokens, rnd.conf, rnd.logp_d, rnd.lse_d, ws)
+    rep = compare_draft(rnd.tokens, rnd.conf, rnd.lse_d if tau > 0 else None,
+                        rnd.logp_d if tau > 0 else None, orc, tau)
+    assert rep.compared >= R
+    assert rep.flagged <= max(2, rep.compared // (50 if tau == 0 else 25))
+    assert dsp.dspark_device_status() == 0
+
+
 @pytest.mark.parametrize("R", [200, 400])
 def test_markov_draft_row_groups(R):
     """Sampling on a 152-CTA grid (two row blocks): 200 requests take groups of

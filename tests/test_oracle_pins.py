@@ -117,6 +117,41 @@ def test_w2_zero_reduces_to_parallel_drafting():
     assert np.array_equal(out["tokens"], np.argmax(base, axis=2))
 
 
+def test_fused_step_keeps_the_base_logit_unrounded():
+    """One contraction per step gives h . W_lm exactly: 257.5 and 257.75 stay
+    apart (the second wins), where the LM head's bf16 output rounds both to 258
+    and the tie goes to the first id."""
+    h = np.ones((1, 1, 2))
+    W_lm = np.array([[256.0, 1.5], [256.0, 1.75]])   # every weight exact in bf16
+    W1, W2 = np.zeros((2, 8)), np.zeros((8, 2))        # no Markov bias
+    w, T, anchor = np.zeros(2 + 8), np.ones(1), np.zeros(1, dtype=np.int64)
+    fused = oracle.fused_draft(h, anchor, W_lm, W1, W2, w, T, 0.0, 0)
+    stored = oracle.markov_draft(oracle.base_logits(h, W_lm), h, anchor, W1, W2, w, T, 0.0, 0)
+    assert fused["tokens"][0, 0] == 1 and stored["tokens"][0, 0] == 0
+
+
+@pytest.mark.parametrize("tau", [0.0, 1.0])
+def test_fused_step_equals_the_markov_head_when_base_logits_are_bf16_exact(tau):
+    """Small-integer h and W_lm make every h . W_lm an integer below 256, exact in
+    bf16: then the fused step and LM head + Markov head draw the same tokens and
+    confidences (the same random streams)."""
+    rng = np.random.default_rng(61)
+    R, G, V, r, d = 3, 4, 130, 8, 6
+    h = rng.integers(-2, 3, (R, G, d)).astype(np.float64)
+    W_lm = rng.integers(-3, 4, (V, d)).astype(np.float64)
+    W1 = rng.standard_normal((V, r))
+    W2 = rng.standard_normal((r, V))
+    w = rng.standard_normal(d + r)
+    T = 1.0 + rng.random(G)
+    anchor = rng.integers(0, V, R)
+    base = oracle.base_logits(h, W_lm)
+    assert np.array_equal(base, h @ W_lm.T)           # exact: the bf16 rounding is a no-op
+    fused = oracle.fused_draft(h, anchor, W_lm, W1, W2, w, T, tau, 7)
+    stored = oracle.markov_draft(base, h, anchor, W1, W2, w, T, tau, 7)
+    assert np.array_equal(fused["tokens"], stored["tokens"])
+    np.testing.assert_array_equal(fused["conf"], stored["conf"])
+
+
 def _rnn_case(R=6, G=4, V=40, r=8, d=5, seed=51):
     rng = np.random.default_rng(seed)
     base = rng.standard_normal((R, G, V))
