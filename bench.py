@@ -168,7 +168,7 @@ def profiled_traffic(kernel: str, src_hash: str, units: float, workload: str):
     the current source of that kernel and on this workload (else None).  The
     summary states the bytes of its captured launch and the units it processed;
     scaled by `units`."""
-    path = os.path.join(ROOT, "profiles", f"{kernel}.txt")
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.txt")
     if not os.path.exists(path):
         return None
     kv = {}
