@@ -54,7 +54,7 @@ __device__ __forceinline__ double theta_at(long K, unsigned long long RS, const 
 __device__ __forceinline__ long long theta_key(double th) {
   const long long b = __double_as_longlong(th);
   if ((b & 0x7fffffffffffffffLL) > 0x7ff0000000000000LL) return (long long)0x8000000000000000ULL;
-  if ((b << 1) == 0) return 0;
+  if (((unsigned long long)b << 1) == 0ull) return 0;  // +0 and -0
   return b >= 0 ? b : (b ^ 0x7fffffffffffffffLL);
 }
 
