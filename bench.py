@@ -279,7 +279,7 @@ def run_reference(args, w, ws, rank):
     cpu = cpu_inputs(w, inp)
     # size one step so that warmup + steps fit in about three minutes
     S = args.cpu_sample or 1
-    avail = int(inp["h"].shape[0])  # requests built (all of them on a GPU machine)
+    avail = int(inp["h"].shape[0])  # requests built (all of them when CUDA builds the inputs)
     if not args.cpu_sample:
         S = sample_size(w, cpu, inp["target"], avail, 180.0 / (args.steps + args.warmup))
     S = min(S, avail)
