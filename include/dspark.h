@@ -41,6 +41,25 @@
  *   - Random draws use Philox4x32-10 keyed by (seed) with counter
  *     (v >> 2, position, request, stream), word v & 3, u = ((w >> 9) + 0.5) 2^-23;
  *     streams: 0 draft Gumbel, 1 accept uniform, 2 residual Gumbel, 3 bonus Gumbel.
+ *
+ * Departures from the planned boundary (draft / schedule / verify / status):
+ *   - W2 enters once, through dspark_pack_w2, as W2t [V, r]; every later call
+ *     takes W2t.  Both operands of the bias contraction are then K-major, as the
+ *     tensor-core path needs, and no call pays a transpose of r*V*2 bytes.
+ *   - The draft writes no draft-logit rows (pd_logits [R, gamma, V]): the loop
+ *     keeps the logits on chip.  It returns log p_d(x_k) and lse_k per position,
+ *     which is all the acceptance test needs; on the one rejected row of a
+ *     request, dspark_verify rebuilds p_d from the draft's own operands
+ *     (base_logits, W1, W2t, lse_d).  Writing and re-reading the rows would add
+ *     2 * R*gamma*V*2 bytes of traffic per round (662 MB at R=256, gamma=5,
+ *     V=129280).
+ *   - Theta is returned as f64: it is computed from an exact fixed-point S_K,
+ *     and f64 carries that value without a second rounding.
+ *   - The status call is dspark_device_status(stream, clear): it reads the one
+ *     word every kernel of the library writes, and clearing is the caller's
+ *     choice.
+ *   - The LM head is also a call of its own (dspark_lm_head), and the base
+ *     logits are a caller-owned buffer, because verify reads them again.
  */
 #ifndef DSPARK_H
 #define DSPARK_H
@@ -96,7 +115,8 @@ int dspark_lm_head(const dspark_dims *dims, const void *h, const void *W_lm,
 /* Layout preparation for the Markov factor W2 (done once per weight load).
  *   W2   bf16 [r, V]   as the pages define it (B = W1[x] W2)
  *   W2t  bf16 [V, r]   out: W2t[v, i] = W2[i, v]  (rank-contiguous rows)
- * Every later call takes W2t. */
+ * Every later call takes W2t (a departure from taking W2 itself: the bias
+ * contraction's operands must both be K-major for TMA and tcgen05). */
 int dspark_pack_w2(const dspark_dims *dims, const void *W2, void *W2t, dspark_stream_t stream);
 
 /* Workspace bytes dspark_markov_draft / dspark_draft need for `dims`. */
@@ -125,7 +145,9 @@ size_t dspark_markov_workspace_bytes(const dspark_dims *dims);
  *   T           f32  [gamma]        per-position STS temperatures (> 0)
  *   tokens      int32 [R, gamma]    out
  *   conf        f32  [R, gamma]     out
- *   logp_d, lse_d f32 [R, gamma]    out, may be NULL (needed by sampling verify)
+ *   logp_d, lse_d f32 [R, gamma]    out, may be NULL (needed by sampling verify);
+ *               they replace draft-logit rows as the draft's output for verify:
+ *               the logits are never written to memory
  *   workspace   device buffer of dspark_markov_workspace_bytes(dims) bytes,
  *               256-byte aligned; contents on entry are ignored. */
 int dspark_markov_draft(const dspark_dims *dims, const void *base_logits, const void *h,
@@ -194,7 +216,9 @@ int dspark_draft(const dspark_dims *dims, const void *h, const int32_t *anchor,
  *                            a descending, ties by id ascending
  * S_K sums the sorted products in 2^-48 units (each rounded to nearest, halves up;
  * exact integer sums); Theta(K) = f64(R + S_K) * (f64(SPS) * 2^-48).  The argmax
- * takes ties to the smallest K; a NaN Theta never wins.  R*gamma <= 16384. */
+ * takes ties to the smallest K; a NaN Theta never wins.  R*gamma <= 16384.
+ * theta_out is f64 rather than f32, so the exact fixed-point S_K reaches the
+ * caller without a second rounding. */
 int dspark_schedule(const float *conf, int32_t R, int32_t gamma, const float *sps,
                     int32_t n_sps, int32_t mode, int32_t k_fixed, int32_t *len,
                     int32_t *K_out, double *theta_out, float *a_out, int32_t *order_out,
@@ -266,7 +290,8 @@ size_t dspark_verify_workspace_bytes(const dspark_dims *dims);
  *             Returns DSPARK_ERR_TOO_LARGE when tau > 0 and V > 3604480.
  *   anchor   int32 [R];  tokens int32 [R, gamma];  len int32 [R] (0..gamma)
  *   base_logits bf16 [R*gamma, V], W1 bf16 [V, r], W2t bf16 [V, r]: the draft's
- *            operands, used to rebuild p_d on the rejected row (tau > 0 only)
+ *            operands, used to rebuild p_d on the rejected row (tau > 0 only), in
+ *            place of draft-logit rows that the draft does not write
  *   lse_d, logp_d f32 [R, gamma] from dspark_markov_draft (tau > 0 only)
  *   target   bf16 [R, gamma + 1, V]  target logits; row j-1 scores position j
  *   accepted int32 [R] out: accepted draft tokens n_r (0..l_r)
@@ -306,7 +331,9 @@ int dspark_selftest_wait_timeout(uint64_t limit_ns, dspark_stream_t stream);
  *   shape (R=256, gamma=5, V=129280, r=512) needs about 8.6 MB.
  *   The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.
+ *   before any stream capture.  The address is kept until the process exits,
+ *   so a device reset (cudaDeviceReset) followed by further calls is not
+ *   supported.
  *   Every call shares the one array: calls whose work overlaps on the GPU
  *   (other streams, other host threads) race and must be serialised by the
  *   caller.  Nothing in the array needs to start at zero. */
@@ -317,7 +344,9 @@ int dspark_markov_draft_static(const dspark_dims *dims, const void *base_logits,
                                dspark_stream_t stream);
 
 /* Synchronises `stream`, returns the sticky device status word (DSPARK_OK or a
- * DSPARK_ERR_* code) and clears it when clear != 0. */
+ * DSPARK_ERR_* code) and clears it when clear != 0.  (Planned as
+ * dspark_last_device_status(stream); the clear flag lets a caller keep the word
+ * across several reads.) */
 int dspark_device_status(dspark_stream_t stream, int clear);
 
 /* Human-readable name of a return / status code (static string). */

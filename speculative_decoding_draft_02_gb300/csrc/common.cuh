@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/dspark.h"
 
 typedef __nv_bfloat16 bf16;
@@ -27,6 +29,31 @@ static inline int dspark_dims_ok(const dspark_dims *d) {
 }
 
 static inline size_t dspark_align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// One-time settings of a device (a kernel's shared-memory limit, an occupancy
+// query): cudaFuncSetAttribute and the like act on the current device only, so
+// a process that drives several GPUs needs them once per device.  `init` runs
+// under the lock, with the device current, until it returns a value >= 0,
+// which is then kept for that device; a negative value is returned and not kept.
+constexpr int DSPARK_MAX_DEVICES = 64;
+struct DsparkPerDevice {
+  std::mutex mu;
+  bool done[DSPARK_MAX_DEVICES];
+  int value[DSPARK_MAX_DEVICES];
+};
+template <class F>
+static inline int dspark_per_device(DsparkPerDevice &s, F init) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= DSPARK_MAX_DEVICES) return -1;
+  std::lock_guard<std::mutex> lock(s.mu);
+  if (!s.done[dev]) {
+    const int v = init();
+    if (v < 0) return v;
+    s.value[dev] = v;
+    s.done[dev] = true;
+  }
+  return s.value[dev];
+}
 
 // Launch with the programmatic stream-serialisation attribute (see pdl_wait).
 template <class... KArgs, class... Args>

@@ -100,14 +100,15 @@ int dspark_make_tmap_bf16(CUtensorMap *map, const void *base, uint64_t rows, uin
 }
 
 int dspark_sm_count() {
-  static int sms = 0;
-  if (!sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 1;
-  }
-  return sms;
+  static DsparkPerDevice sms;
+  const int n = dspark_per_device(sms, [] {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      return -1;
+    return v;
+  });
+  return n > 0 ? n : 1;
 }
 
 int dspark_lm_head_tc(const dspark_dims *dims, const void *h, const void *W_lm,
@@ -123,7 +124,7 @@ int dspark_lm_head_tc(const dspark_dims *dims, const void *h, const void *W_lm,
   // pair would leave up to a quarter of its rows empty.
   const int num_m = (epi.M + gemm::BM - 1) / gemm::BM;
   if (num_m >= 4) return gemm::launch_pair<4>(h, W_lm, epi.M, epi.N, dims->d, epi, stream);
-  return gemm::launch<4, 256, false>(h, W_lm, epi.M, epi.N, dims->d, epi, stream);
+  return gemm::launch<4, 256>(h, W_lm, epi.M, epi.N, dims->d, epi, stream);
 }
 
 extern "C" int dspark_pack_w2(const dspark_dims *dims, const void *W2, void *W2t,

@@ -868,17 +868,15 @@ int launch_loop(const LoopArgs &args, int grid, cudaStream_t stream) {
   if (dspark_make_tmap_bf16(&tb, args.W2t, (uint64_t)args.V, (uint64_t)args.r,
                             LoopCfg<MODE>::BN) != 0)
     return DSPARK_ERR_CUDA;
-  static bool attr = false;
-  if (!attr) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) {
-      if (getenv("DSPARK_DEBUG"))
-        fprintf(stderr, "dspark: markov loop smem attribute: %s\n", cudaGetErrorString(e));
-      return DSPARK_ERR_CUDA;
-    }
-    attr = true;
-  }
+  static DsparkPerDevice attr;
+  if (dspark_per_device(attr, [&] {
+        const cudaError_t e =
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess && getenv("DSPARK_DEBUG"))
+          fprintf(stderr, "dspark: markov loop smem attribute: %s\n", cudaGetErrorString(e));
+        return e == cudaSuccess ? 1 : -1;
+      }) < 0)
+    return DSPARK_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeCooperative;  // every CTA resident: the grid barriers need it

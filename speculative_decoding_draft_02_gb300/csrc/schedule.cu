@@ -11,9 +11,11 @@
 // production the capacity that the unconstrained search found two rounds
 // earlier (asynchronous mode, a two-slot ring of predictions on the device).
 //
-// One CTA of 1024 threads: f32 survival products, a bitonic sort of composite
-// keys (~bits(a) << 32 | id) so that ties go to the lower (request, position),
-// a fixed-point block scan of the sorted products and the Theta search.
+// One CTA of 1024 threads: f32 survival products, a sort of composite keys
+// (~bits(a) << 32 | id) so that ties go to the lower (request, position) -- a
+// merge of the per-request runs (each already in order) up to 8192 keys, a
+// bitonic sort above -- a fixed-point block scan of the sorted products and the
+// Theta search.
 #include "common.cuh"
 
 DSPARK_DECLARE_STATUS(s_status_sched)
@@ -377,24 +379,17 @@ int launch_schedule(const float *conf, int32_t R, int32_t gamma, const float *sp
   // up to 8192 candidates: merge sort (two key buffers); beyond: bitonic sort
   const bool merge = n_pad <= 8192;
   const size_t smem = sizeof(unsigned long long) * n_pad * (merge ? 2 : 1) + sizeof(int32_t) * R;
-  static bool attr_set = false;
   const int smem_max = (int)(sizeof(unsigned long long) * SCHED_MAX + sizeof(int32_t) * SCHED_MAX);
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(schedule_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem_max) != cudaSuccess ||
-        cudaFuncSetAttribute(schedule_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem_max) != cudaSuccess ||
-        cudaFuncSetAttribute(schedule_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem_max) != cudaSuccess ||
-        cudaFuncSetAttribute(schedule_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem_max) != cudaSuccess ||
-        cudaFuncSetAttribute(schedule_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem_max) != cudaSuccess ||
-        cudaFuncSetAttribute(schedule_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem_max) != cudaSuccess)
-      return DSPARK_ERR_CUDA;
-    attr_set = true;
-  }
+  static DsparkPerDevice attr;
+  if (dspark_per_device(attr, [&] {
+        for (auto k : {schedule_kernel<0>, schedule_kernel<1>, schedule_kernel<2>,
+                       schedule_kernel<4>, schedule_kernel<8>, schedule_kernel<16>})
+          if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) !=
+              cudaSuccess)
+            return -1;
+        return 1;
+      }) < 0)
+    return DSPARK_ERR_CUDA;
   // keys per thread: n_pad / 1024, at least one
   auto kernel = merge        ? schedule_kernel<0>
               : n_pad <= 1024 ? schedule_kernel<1>

@@ -68,11 +68,7 @@ struct SharedCtl {
 //        next_m0 / next_n0 locate the CTA's next tile, -1 after the last, so
 //        the loads for it can start while this one is processed)
 //   __device__ void on_timeout() const.
-// PAIR: CTAs run as clusters of two over two M blocks of the same N tile; each
-// loads its own A tile and half of the B tile, multicast to both, so the B
-// bytes brought from L2 per SM are halved.  A stage is reused only after both
-// CTAs' MMAs released it (their commits are multicast to both empty barriers).
-template <class Epi, int EPI_WARPS, int BN_, bool PAIR>
+template <class Epi, int EPI_WARPS, int BN_>
 __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
                      const __grid_constant__ CUtensorMap tma_b, int M, int N, int K,
@@ -94,7 +90,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       tc::mbar_init(&ctl->full[s], 1);
-      tc::mbar_init(&ctl->empty[s], PAIR ? 2 : 1);
+      tc::mbar_init(&ctl->empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&ctl->tfull[b], 1);
@@ -109,7 +105,6 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
   if (warp == 1) tc::tmem_alloc(&ctl->tmem_base, TMEM_COLS);
   tc::fence_before_sync();
   __syncthreads();
-  if (PAIR) tc::cluster_sync();  // the peer's barriers exist before any multicast
   tc::fence_after_sync();
   const uint32_t tmem_base = ctl->tmem_base;
   // everything above overlaps the previous kernel of the stream; A, the row
@@ -126,18 +121,15 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
   // split K (ksplit > 1): split s of a tile takes k blocks [s * k_iters, (s+1) *
   // k_iters) and hands its partial to the epilogue as rows s * num_m * BM + ...
   const int k_iters = K / BK / ksplit;
-  // tile sequence: t -> (m block, n block), m fastest; a pair walks pairs of M blocks
-  const uint32_t rank = PAIR ? tc::cluster_ctarank() : 0u;
-  const int num_mp = PAIR ? (num_m + 1) / 2 : num_m;
-  const int split_tiles = num_mp * num_n;
+  // tile sequence: t -> (m block, n block), m fastest
+  const int split_tiles = num_m * num_n;
   const int num_tiles = split_tiles * ksplit;
-  const int first = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-  const int stride = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const int first = (int)blockIdx.x;
+  const int stride = (int)gridDim.x;
   auto coords = [&](int t, int &m_blk, int &n_blk) {
     const int u = t % split_tiles;
-    const int mp = u % num_mp;
-    n_blk = u / num_mp;
-    m_blk = PAIR ? 2 * mp + (int)rank : mp;
+    m_blk = u % num_m;
+    n_blk = u / num_m;
   };
   auto out_row0 = [&](int t, int m_blk) { return ((t / split_tiles) * num_m + m_blk) * BM; };
 
@@ -146,10 +138,8 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
       // ------------------------------------------------ TMA producer ----
       const uint64_t pol_a = tc::policy_evict_last();   // A tiles are re-read
       // B: streamed once (LM head) or re-read by other M blocks and later steps
-      // (a pair fetches each B line once per cluster; with several clusters on one
-      // N tile the lines must survive until the last of them reads them)
       const uint64_t pol_b =
-          (Epi::kStreamB && !PAIR) ? tc::policy_evict_first() : tc::policy_evict_normal();
+          Epi::kStreamB ? tc::policy_evict_first() : tc::policy_evict_normal();
       int stage = 0;
       uint32_t phase = 0;
       int issued[STAGES];
@@ -161,15 +151,10 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
         const int kb0 = (tile / split_tiles) * k_iters;
         for (int kb = 0; kb < k_iters; ++kb) {
           if (!tc::mbar_wait(&ctl->empty[stage], phase ^ 1, abort)) { ok = false; break; }
-          tc::mbar_expect_tx(&ctl->full[stage], STAGE_BYTES);  // A + both halves of B
+          tc::mbar_expect_tx(&ctl->full[stage], STAGE_BYTES);  // A + B
           const int kx = (kb0 + kb) * BK;
           tc::tma_load_2d(sA + stage * A_BYTES, &tma_a, kx, m_blk * BM, &ctl->full[stage], pol_a);
-          if (PAIR)
-            tc::tma_load_2d_mcast(sB + stage * B_BYTES + rank * (B_BYTES / 2), &tma_b, kx,
-                                  n_blk * BN + (int)rank * (BN / 2), &ctl->full[stage],
-                                  (uint16_t)0x3, pol_b);
-          else
-            tc::tma_load_2d(sB + stage * B_BYTES, &tma_b, kx, n_blk * BN, &ctl->full[stage], pol_b);
+          tc::tma_load_2d(sB + stage * B_BYTES, &tma_b, kx, n_blk * BN, &ctl->full[stage], pol_b);
           issued[stage] = (int)phase;
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
@@ -202,10 +187,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
           for (int k = 0; k < BK / 16; ++k)  // +32 B per 16-element K step
             tc::umma_bf16(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc,
                           (kb | k) != 0 ? 1u : 0u);
-          if (PAIR)
-            tc::umma_commit_mcast(&ctl->empty[stage], (uint16_t)0x3);  // both CTAs' slots
-          else
-            tc::umma_commit(&ctl->empty[stage]);
+          tc::umma_commit(&ctl->empty[stage]);
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
@@ -261,7 +243,6 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
 
   tc::fence_before_sync();
   __syncthreads();
-  if (PAIR) tc::cluster_sync();  // no peer multicast or commit still targets this CTA
   if (ctl->abort && threadIdx.x == 0) epi.on_timeout();
   if (warp == 1) {
     tc::fence_after_sync();
@@ -271,69 +252,49 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
 
 // M rows of A are described to TMA; when m_dev is given the kernel processes
 // only the first *m_dev of them (read on the device, so the count can come from
-// an earlier kernel in the stream).  PAIR launches clusters of two CTAs that
-// share B tiles by multicast (see umma_gemm_kernel).
-// ksplit > 1 (not with PAIR): K is split into ksplit equal parts, and the
+// an earlier kernel in the stream).
+// ksplit > 1: K is split into ksplit equal parts, and the
 // epilogue receives split s's partial of M block m as rows (s * num_m + m) * BM.
-template <int EPI_WARPS, int BN_ = 256, bool PAIR = false, class Epi>
+template <int EPI_WARPS, int BN_ = 256, class Epi>
 int launch(const void *A, const void *B, int M, int N, int K, const Epi &epi,
            cudaStream_t stream, const int *m_dev = nullptr, bool pdl = false, int ksplit = 1) {
-  if (ksplit < 1 || (PAIR && ksplit != 1) || K % (BK * ksplit) != 0) return DSPARK_ERR_ARG;
+  if (ksplit < 1 || K % (BK * ksplit) != 0) return DSPARK_ERR_ARG;
   using G = Geo<BN_>;
   constexpr int BN = G::BN;
   static_assert(EPI_WARPS % 4 == 0 && EPI_WARPS >= 4 && EPI_WARPS <= 16 &&
                     BN % (EPI_WARPS / 4) == 0 && (BN / (EPI_WARPS / 4)) % 32 == 0,
                 "epilogue warps: 4 per TMEM lane quarter group, slices of whole 32-column loads");
-  auto kernel = umma_gemm_kernel<Epi, EPI_WARPS, BN_, PAIR>;
+  auto kernel = umma_gemm_kernel<Epi, EPI_WARPS, BN_>;
   CUtensorMap ta, tb;
   if (dspark_make_tmap_bf16(&ta, A, (uint64_t)M, (uint64_t)K, BM) != 0) return DSPARK_ERR_CUDA;
-  if (dspark_make_tmap_bf16(&tb, B, (uint64_t)N, (uint64_t)K, PAIR ? BN / 2 : BN) != 0)
+  if (dspark_make_tmap_bf16(&tb, B, (uint64_t)N, (uint64_t)K, BN) != 0)
     return DSPARK_ERR_CUDA;
-  static bool attr = false;
-  static int max_clusters = 0;
+  static DsparkPerDevice attr;
+  if (dspark_per_device(attr, [&] {
+        return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)G::SMEM_BYTES) == cudaSuccess
+                   ? 1
+                   : -1;
+      }) < 0)
+    return DSPARK_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attrs[2];
-  attrs[0].id = cudaLaunchAttributeClusterDimension;
-  attrs[0].val.clusterDim.x = 2;
-  attrs[0].val.clusterDim.y = 1;
-  attrs[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attrs[1];
   cfg.blockDim = dim3(64 + 32 * EPI_WARPS);
   cfg.dynamicSmemBytes = G::SMEM_BYTES;
   cfg.stream = stream;
-  if (PAIR) {
-    cfg.attrs = attrs;
-    cfg.numAttrs = 1;
-  }
-  if (!attr) {
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)G::SMEM_BYTES) != cudaSuccess)
-      return DSPARK_ERR_CUDA;
-    if (PAIR) {
-      cfg.gridDim = dim3(2 * (dspark_sm_count() / 2));
-      if (cudaOccupancyMaxActiveClusters(&max_clusters, kernel, &cfg) != cudaSuccess ||
-          max_clusters < 1)
-        return DSPARK_ERR_CUDA;
-    }
-    attr = true;
-  }
   const int num_m = (M + BM - 1) / BM;
   const int num_n = (N + BN - 1) / BN;
-  int grid;
-  if (PAIR) {
-    const int pairs = ((num_m + 1) / 2) * num_n;
-    grid = 2 * (pairs < max_clusters ? pairs : max_clusters);
-  } else {
-    const int tiles = num_m * num_n * ksplit;
-    grid = tiles < dspark_sm_count() ? tiles : dspark_sm_count();
-    // a multiple of the M-block count keeps every CTA (and epilogue thread) on one row block
-    if (Epi::kRowAffine && grid > num_m) grid = grid / num_m * num_m;
-  }
+  const int sms = dspark_sm_count();
+  const int tiles = num_m * num_n * ksplit;
+  int grid = tiles < sms ? tiles : sms;
+  // a multiple of the M-block count keeps every CTA (and epilogue thread) on one row block
+  if (Epi::kRowAffine && grid > num_m) grid = grid / num_m * num_m;
   cfg.gridDim = dim3(grid);
   if (pdl) {  // may start while the previous kernel of the stream finishes
-    attrs[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attrs[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+    attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attrs;
-    cfg.numAttrs += 1;
+    cfg.numAttrs = 1;
   }
   if (cudaLaunchKernelEx(&cfg, kernel, ta, tb, M, N, K, m_dev, ksplit, epi) != cudaSuccess)
     return DSPARK_ERR_CUDA;

@@ -234,8 +234,6 @@ int launch_pair(const void *A, const void *B, int M, int N, int K, const Epi &ep
   CUtensorMap ta, tb;
   if (dspark_make_tmap_bf16(&ta, A, (uint64_t)M, (uint64_t)K, BM) != 0) return DSPARK_ERR_CUDA;
   if (dspark_make_tmap_bf16(&tb, B, (uint64_t)N, (uint64_t)K, G::BNH) != 0) return DSPARK_ERR_CUDA;
-  static bool attr = false;
-  static int max_clusters = 0;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeClusterDimension;
@@ -247,16 +245,19 @@ int launch_pair(const void *A, const void *B, int M, int N, int K, const Epi &ep
   cfg.stream = stream;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  if (!attr) {
+  // the shared-memory limit and the number of co-resident clusters, per device
+  static DsparkPerDevice clusters;
+  const int max_clusters = dspark_per_device(clusters, [&] {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)G::SMEM_BYTES) != cudaSuccess)
-      return DSPARK_ERR_CUDA;
-    cfg.gridDim = dim3(2 * (dspark_sm_count() / 2));
-    if (cudaOccupancyMaxActiveClusters(&max_clusters, kernel, &cfg) != cudaSuccess ||
-        max_clusters < 1)
-      return DSPARK_ERR_CUDA;
-    attr = true;
-  }
+      return -1;
+    cudaLaunchConfig_t q = cfg;
+    q.gridDim = dim3(2 * (dspark_sm_count() / 2));
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &q) != cudaSuccess || n < 1) return -1;
+    return n;
+  });
+  if (max_clusters < 1) return DSPARK_ERR_CUDA;
   const int num_m = (M + BM - 1) / BM;
   const int tiles = ((num_m + 1) / 2) * ((N + G::BN - 1) / G::BN);
   cfg.gridDim = dim3(2 * (tiles < max_clusters ? tiles : max_clusters));
