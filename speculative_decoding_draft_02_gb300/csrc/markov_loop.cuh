@@ -116,6 +116,19 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void *p, uint32_t bytes) 
 __device__ __forceinline__ void named_bar(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+// A named barrier that also returns, to every participant, the OR of `pred`
+// over them: one decision that all of them act on alike.
+__device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+constexpr int BAR_STOP = 15;  // named barrier of the stop decision (row groups use 2 ..)
 
 // Generic-proxy stores of this thread become visible to later TMA (async proxy)
 // reads of global memory.
@@ -782,16 +795,20 @@ __global__ void __launch_bounds__(64 + 32 * LoopCfg<MODE>::EPI_WARPS, 1) markov_
           run_n = -1;
         }
       }
-      // ---- grid barrier: every partial of step k is written
+      // ---- grid barrier: every partial of step k is written.  One thread
+      // decides whether to go on and every epilogue thread gets that decision
+      // (a flag raised meanwhile by another role is seen by the next wait), so
+      // all of them meet the same named barriers.
       named_bar(1, EPI_THREADS);
+      bool give_up = false;
       if (ew == 0 && lane == 0) {
         if (*abort || !grid_barrier(a.sync, (unsigned)(2 * k) * gridDim.x)) {
           *abort = 1;
           atomicExch(&a.sync->abort, 1);
+          give_up = true;
         }
       }
-      named_bar(1, EPI_THREADS);
-      if (*abort) break;
+      if (named_bar_or(BAR_STOP, EPI_THREADS, give_up)) break;
       row_phase<MODE, RW, EPI_WARPS>(a, k, scr[g], g, wg, lane, groups);
       if (k < gamma) {
         // ---- grid barrier: every E row of step k+1 is written; the producer may load them
