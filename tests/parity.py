@@ -25,6 +25,21 @@ import torch
 import oracle
 
 
+# Tie band of a token decision, relative to the score's magnitude.  The CUDA
+# path and the oracle compute the same scores to about 1e-6 (f32 sums of the
+# same bf16 products, f32 logarithms of the same Philox words), so a band of
+# 1e-4 leaves a hundredfold margin and flags only genuine near-ties.
+TOL_DRAFT = 1e-4
+
+
+def flag_budget(compared: int) -> int:
+    """Near-ties allowed among `compared` token decisions.  With a tie band of
+    1e-4 of scores of order 1-10 and top-2 gaps of order 0.1 or more, fewer
+    than one decision in a thousand falls in it; 1 % leaves room for the two
+    levels of a sampled token and small shapes."""
+    return max(1, compared // 100)
+
+
 def host(x):
     if isinstance(x, torch.Tensor):
         x = x.detach().cpu()
@@ -44,9 +59,23 @@ class DraftReport:
     notes: list = field(default_factory=list)
 
 
+def _shift_band(shift_row, s, tau, cand):
+    """Twice the largest logit difference (over the candidate entries `cand`)
+    between the two sides' base logits, in score units."""
+    if shift_row is None or not np.any(cand):
+        return 0.0
+    return 2.0 * float(np.max(shift_row[cand])) / (tau if tau > 0 else 1.0)
+
+
 def compare_draft(gpu_tokens, gpu_conf, gpu_lse, gpu_logp, orc, tau, tol_rel=1e-3,
-                  conf_rtol=1e-2, requests=None) -> DraftReport:
-    """Walk each request's chain; see module docstring.  `orc` from oracle.markov_draft(keep_scores)."""
+                  conf_rtol=1e-2, requests=None, shift=None) -> DraftReport:
+    """Walk each request's chain; see module docstring.  `orc` from oracle.markov_draft(keep_scores).
+
+    `shift` [requests, gamma, V], optional: where the two sides' base logits
+    differ (|GPU - oracle|, e.g. one bf16 step of a value the LM head's f32 sum
+    rounded the other way), a decision among the entries near the top can move
+    by up to that much, so its tie band widens by twice the largest such
+    difference among them."""
     gt = host(gpu_tokens).astype(np.int64)
     gc = host(gpu_conf).astype(np.float64)
     gl = None if gpu_lse is None else host(gpu_lse).astype(np.float64)
@@ -63,12 +92,19 @@ def compare_draft(gpu_tokens, gpu_conf, gpu_lse, gpu_logp, orc, tau, tol_rel=1e-
             s = orc["scores"][oi, k]
             smax = float(s.max())
             two_level = tau > 0 and "block_scores" in orc
+            sh = None if shift is None else shift[oi, k]
             if two_level:
                 bs = orc["block_scores"][oi, k]
                 bmax = float(bs.max())
                 tol = tol_rel * max(1.0, abs(smax), abs(bmax))
+                if sh is not None:  # every entry of a block near the top
+                    blk = orc["block"]
+                    near = np.repeat(bs >= bmax - 0.5, blk)[:s.size]
+                    tol += _shift_band(sh, s, tau, near)
             else:
                 tol = tol_rel * max(1.0, abs(smax))
+                if sh is not None:
+                    tol += _shift_band(sh, s, tau, s >= smax - 0.5)
             g = int(gt[i, k])
             assert 0 <= g < s.size
             rep.compared += 1

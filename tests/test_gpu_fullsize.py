@@ -12,13 +12,13 @@ import torch
 
 import oracle
 import workloads
-from parity import compare_draft, compare_verify, host
+from parity import TOL_DRAFT, compare_draft, compare_verify, flag_budget, host
 
 pytestmark = pytest.mark.gpu
 
 dsp = pytest.importorskip("speculative_decoding_draft_02_gb300")
 
-SAMPLED = 3  # requests re-derived by the oracle per case
+SAMPLED = 16  # requests re-derived by the oracle per case (plus the first and last)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -32,8 +32,8 @@ def _lib():
 
 def _sample_ids(R, seed):
     rng = np.random.default_rng(seed)
-    ids = sorted(set([0, R - 1] + list(rng.integers(0, R, SAMPLED))))
-    return np.array(ids[:SAMPLED + 1])
+    pick = rng.choice(R, size=min(R, SAMPLED), replace=False)
+    return np.array(sorted(set([0, R - 1] + pick.tolist())))
 
 
 @pytest.mark.parametrize("name,tau", [("v4_dspark5", 1.0), ("qwen3_8b", 1.0), ("qwen3_4b", 0.0),
@@ -57,11 +57,18 @@ def test_draft_full_size_sampled_requests(name, tau):
     orc = oracle.markov_draft(base_s, h_s, inp["anchor"][ids].cpu(), inp["W1"].cpu(),
                               inp["W2"].cpu(), inp["w_conf"].cpu(), inp["T"].cpu(), tau,
                               inp["draft_seed"], keep_scores=True, requests=ids)
-    rep = compare_draft(rnd.tokens, rnd.conf, rnd.lse_d if tau > 0 else None,
-                        rnd.logp_d if tau > 0 else None, orc, tau, tol_rel=1e-2, requests=ids)
-    assert rep.compared >= len(ids)
-    # the base logits themselves, on the sampled rows
+    # the LM head sums in f32 and the oracle in f64, so a base logit near a bf16
+    # rounding boundary can land one bf16 step away: the tie band of a decision
+    # widens by the differences seen among the entries near its top
     got = host(rnd.base.view(R, G, V)[ids]).astype(np.float64)
+    rep = compare_draft(rnd.tokens, rnd.conf, rnd.lse_d if tau > 0 else None,
+                        rnd.logp_d if tau > 0 else None, orc, tau, tol_rel=TOL_DRAFT,
+                        requests=ids, shift=np.abs(got - base_s))
+    print(f"{name} tau={tau}: {rep.flagged} of {rep.compared} decisions in the tie band, "
+          f"{int(np.sum(got != base_s))} of {got.size} base logits one bf16 step apart")
+    assert rep.compared >= len(ids)
+    assert rep.flagged <= flag_budget(rep.compared)
+    # the base logits themselves, on the sampled rows
     exact = oracle.base_logits(h_s.reshape(-1, d), W_lm, bf16_out=False,
                                vocab_chunk=16384).reshape(len(ids), G, V)
     err = np.abs(got - exact)
@@ -87,15 +94,16 @@ def test_schedule_full_size(name, mode):
     dsp.dspark_schedule(c.cuda(), R, G, sps.cuda(), mode, kf, rnd_len, K, th, a, order)
     assert np.array_equal(host(a), o["a"])
     assert np.array_equal(host(order), o["order"])
-    k_gpu = int(K.item())
-    assert abs(o["thetas"][k_gpu] - o["theta"]) <= 1e-12 * o["theta"]
-    if k_gpu == o["K"]:
-        assert np.array_equal(host(rnd_len), o["len"])
+    # the same fixed-point sums and float64 products on both sides: bit-exact
+    assert int(K.item()) == o["K"]
+    assert np.array_equal(host(rnd_len), o["len"])
+    assert float(th.item()) == o["theta"]
     if mode == 0 and name in ("v4_dspark5", "stress"):
         assert 0 < o["K"] < R * G  # the staircase tables give an interior optimum
 
 
-@pytest.mark.parametrize("name,tau", [("v4_dspark5", 1.0), ("stress", 0.0)])
+@pytest.mark.parametrize("name,tau", [("v4_dspark5", 1.0), ("stress", 0.0), ("qwen3_8b", 1.0),
+                                      ("qwen3_4b", 0.0), ("qwen3_4b", 1.0)])
 def test_verify_full_size_sampled_requests(name, tau):
     w = workloads.WORKLOADS[name]
     R, G, V = w.R, w.gamma, w.V
@@ -141,6 +149,7 @@ def test_verify_full_size_sampled_requests(name, tau):
     orc = oracle.verify(tokens[ids].cpu(), lens[ids].cpu(), dl, target[ids].cpu(), tau,
                         w.seed + 77, requests=ids)
     flagged = compare_verify(rnd.accepted[ids], rnd.bonus[ids], orc, tau)
+    print(f"verify {name} tau={tau}: {flagged} of {len(ids)} requests in a tie band")
     assert flagged <= 1
     acc = host(rnd.accepted)
     assert np.all(acc >= 0) and np.all(acc <= host(lens))

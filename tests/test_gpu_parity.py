@@ -11,8 +11,8 @@ import torch
 
 import oracle
 import workloads
-from parity import (compare_draft, compare_verify, host, schedule_is_robust,
-                    sorted_order_ok)
+from parity import (TOL_DRAFT, compare_draft, compare_verify, flag_budget, host,
+                    schedule_is_robust, sorted_order_ok)
 
 pytestmark = pytest.mark.gpu
 
@@ -103,10 +103,10 @@ def _draft_case(shape, tau, seed):
 def test_markov_draft_matches_oracle(shape, tau):
     rnd, orc = _draft_case(shape, tau, seed=200 + shape[2])
     rep = compare_draft(rnd.tokens, rnd.conf, rnd.lse_d if tau > 0 else None,
-                        rnd.logp_d if tau > 0 else None, orc, tau)
+                        rnd.logp_d if tau > 0 else None, orc, tau, tol_rel=TOL_DRAFT)
+    print(f"{shape} tau={tau}: {rep.flagged} of {rep.compared} decisions in the tie band")
     assert rep.compared >= shape[0]
-    # a sampled token is two decisions (block, then id), each with its tie band
-    assert rep.flagged <= max(2, rep.compared // (50 if tau == 0 else 25))
+    assert rep.flagged <= flag_budget(rep.compared)
     assert dsp.dspark_device_status() == 0
 
 
@@ -347,7 +347,8 @@ def _verify_case(shape, tau, seed, accept_bias=0.7, lens_kind="random"):
 def test_verify_matches_oracle(shape, tau):
     rnd, orc, lens = _verify_case(shape, tau, seed=300 + shape[2])
     flagged = compare_verify(rnd.accepted, rnd.bonus, orc, tau)
-    assert flagged <= max(1, shape[0] // 20)
+    print(f"verify {shape} tau={tau}: {flagged} of {shape[0]} requests in a tie band")
+    assert flagged <= max(1, shape[0] // 50)
     acc = host(rnd.accepted)
     assert np.all(acc >= 0) and np.all(acc <= host(lens))
     assert dsp.dspark_device_status() == 0
@@ -361,7 +362,8 @@ def test_verify_full_lengths(shape, tau):
     """Every draft admitted (up to gamma = 32, the largest the library takes)."""
     rnd, orc, lens = _verify_case(shape, tau, seed=330 + shape[1], lens_kind="full")
     flagged = compare_verify(rnd.accepted, rnd.bonus, orc, tau)
-    assert flagged <= max(1, shape[0] // 20)
+    print(f"verify {shape} tau={tau}: {flagged} of {shape[0]} requests in a tie band")
+    assert flagged <= max(1, shape[0] // 50)
     assert dsp.dspark_device_status() == 0
 
 
@@ -372,9 +374,10 @@ def test_markov_draft_more_row_blocks_than_sms(tau):
     shape = (153 * 128, 2, 520, 64, 64)
     rnd, orc = _draft_case(shape, tau, seed=280)
     rep = compare_draft(rnd.tokens, rnd.conf, rnd.lse_d if tau > 0 else None,
-                        rnd.logp_d if tau > 0 else None, orc, tau)
+                        rnd.logp_d if tau > 0 else None, orc, tau, tol_rel=TOL_DRAFT)
+    print(f"{shape} tau={tau}: {rep.flagged} of {rep.compared} in the tie band")
     assert rep.compared >= shape[0]
-    assert rep.flagged <= max(2, rep.compared // (50 if tau == 0 else 25))
+    assert rep.flagged <= flag_budget(rep.compared)
     assert dsp.dspark_device_status() == 0
 
 
@@ -400,9 +403,10 @@ def test_fused_draft_matches_oracle(shape, tau):
                            dev(inp["anchor"]), W_cat, head.W1, head.w_conf, head.T, tau,
                            12345 + seed, rnd.tokens, rnd.conf, rnd.logp_d, rnd.lse_d, ws)
     rep = compare_draft(rnd.tokens, rnd.conf, rnd.lse_d if tau > 0 else None,
-                        rnd.logp_d if tau > 0 else None, orc, tau)
+                        rnd.logp_d if tau > 0 else None, orc, tau, tol_rel=TOL_DRAFT)
+    print(f"fused {shape} tau={tau}: {rep.flagged} of {rep.compared} in the tie band")
     assert rep.compared >= R
-    assert rep.flagged <= max(2, rep.compared // (50 if tau == 0 else 25))
+    assert rep.flagged <= flag_budget(rep.compared)
     assert dsp.dspark_device_status() == 0
 
 
@@ -412,9 +416,11 @@ def test_markov_draft_row_groups(R):
     six warps per request in the row phase, 400 groups of four."""
     shape = (R, 2, 20000, 64, 64)
     rnd, orc = _draft_case(shape, 1.0, seed=290)
-    rep = compare_draft(rnd.tokens, rnd.conf, rnd.lse_d, rnd.logp_d, orc, 1.0)
+    rep = compare_draft(rnd.tokens, rnd.conf, rnd.lse_d, rnd.logp_d, orc, 1.0,
+                        tol_rel=TOL_DRAFT)
+    print(f"{shape}: {rep.flagged} of {rep.compared} in the tie band")
     assert rep.compared >= shape[0]
-    assert rep.flagged <= max(2, rep.compared // 25)
+    assert rep.flagged <= flag_budget(rep.compared)
     assert dsp.dspark_device_status() == 0
 
 
@@ -425,9 +431,10 @@ def test_markov_draft_edges(shape, tau):
     """gamma = 32; a very cold and a very hot sampling temperature."""
     rnd, orc = _draft_case(shape, tau, seed=260 + shape[1])
     rep = compare_draft(rnd.tokens, rnd.conf, rnd.lse_d if tau > 0 else None,
-                        rnd.logp_d if tau > 0 else None, orc, tau)
+                        rnd.logp_d if tau > 0 else None, orc, tau, tol_rel=TOL_DRAFT)
+    print(f"{shape} tau={tau}: {rep.flagged} of {rep.compared} in the tie band")
     assert rep.compared >= shape[0]
-    assert rep.flagged <= max(2, rep.compared // (50 if tau == 0 else 25))
+    assert rep.flagged <= flag_budget(rep.compared)
     assert dsp.dspark_device_status() == 0
 
 
@@ -478,12 +485,26 @@ def test_device_status_reports_bad_tokens_and_lengths():
 
 # ------------------------------------------------------------ the round ---
 
+# the Qwen3-8B-shaped case with its vocabulary cut to 4104 (a ragged 64-id
+# block) and d to 256: tau = 1, T_k = 1 + 0.1 k, the concave SPS table
+ROUND_CASES = {"tiny": workloads.WORKLOADS["tiny"],
+               "qwen3_8b_small": workloads.WORKLOADS["qwen3_8b"].with_(V=4104, d=256,
+                                                                       anchor_hi=4104)}
+
+
 @pytest.mark.parametrize("name,tau,mode", [("tiny", 0.0, 0), ("tiny", 1.0, 1),
-                                           ("tiny", 0.7, 2)])
+                                           ("tiny", 0.7, 2), ("qwen3_8b_small", 1.0, 0),
+                                           ("qwen3_8b_small", 1.0, 1),
+                                           ("qwen3_8b_small", 1.0, 2)])
 def test_round_matches_oracle_end_to_end(name, tau, mode):
-    w = workloads.WORKLOADS[name]
+    """One whole round through Round.run, then each later stage on the oracle's
+    own inputs: the scheduler on the oracle's confidences (bit-exact), and the
+    verifier on the oracle's tokens and lengths (exact outside the tie bands).
+    The oracle never sees a CUDA output; the CUDA stages see the oracle's."""
+    w = ROUND_CASES[name]
     inp = workloads.make_inputs(w)
     R, G, V, d = w.R, w.gamma, w.V, w.d
+    kf = R * G // 2
     orc_base = oracle.base_logits(inp["h"], inp["W_lm"])
     nxt = oracle.base_logits(inp["h_next"], inp["W_lm"])
     target_np = np.concatenate([orc_base, nxt[:, None, :]], axis=1) + host(inp["noise"])
@@ -498,19 +519,38 @@ def test_round_matches_oracle_end_to_end(name, tau, mode):
     h = dev(inp["h"], torch.bfloat16).contiguous()
     anchor = dev(inp["anchor"])
     sps = dev(inp["sps"])
-    rnd.run(h, anchor, dev(target).contiguous(), sps, tau, ds, vs, mode=mode, k_fixed=R * G // 2)
+    tgt = dev(target).contiguous()
+    rnd.run(h, anchor, tgt, sps, tau, ds, vs, mode=mode, k_fixed=kf)
     torch.cuda.synchronize()
+    assert dsp.dspark_device_status() == 0
     rep = compare_draft(rnd.tokens, rnd.conf, rnd.lse_d if tau > 0 else None,
-                        rnd.logp_d if tau > 0 else None, orc, tau, tol_rel=1e-2)
-    same_tokens = np.array_equal(host(rnd.tokens), orc["tokens"])
-    if same_tokens:
-        # the GPU schedules its own confidences (equal to the oracle's within
-        # rounding); compare with the oracle's schedule where that is robust
-        o_s = oracle.schedule(orc["conf"].astype(np.float32), inp["sps"], mode, R * G // 2)
-        if schedule_is_robust(o_s, rel=1e-4):
-            assert np.array_equal(host(rnd.len), o_s["len"])
-            ov = oracle.verify(orc["tokens"], o_s["len"], orc["logits"], target, tau, vs)
-            compare_verify(rnd.accepted, rnd.bonus, ov, tau)
+                        rnd.logp_d if tau > 0 else None, orc, tau, tol_rel=TOL_DRAFT)
+    print(f"{name} tau={tau} mode={mode}: draft {rep.flagged} of {rep.compared} in the tie band")
+    assert rep.flagged <= flag_budget(rep.compared)
+    c_o = orc["conf"].astype(np.float32)
+    o_s = oracle.schedule(c_o, inp["sps"], mode, kf)
+    acc = host(rnd.accepted)
+    assert np.all(acc >= 0) and np.all(acc <= host(rnd.len))
+    if np.array_equal(host(rnd.tokens), orc["tokens"]) and schedule_is_robust(o_s, rel=1e-4):
+        assert np.array_equal(host(rnd.len), o_s["len"])  # the round's own schedule
+    # the scheduler on the oracle's confidences: every output bit-exact
+    dsp.dspark_schedule(dev(torch.tensor(c_o)), R, G, sps, mode, kf, rnd.len, rnd.K, rnd.theta)
+    assert int(rnd.K.item()) == o_s["K"]
+    assert np.array_equal(host(rnd.len), o_s["len"])
+    assert float(rnd.theta.item()) == o_s["theta"]
+    # the verifier on the oracle's base logits, tokens, lengths and draft
+    # log-probabilities
+    rnd.base.copy_(dev(torch.tensor(orc_base.reshape(R * G, V), dtype=torch.float32),
+                       torch.bfloat16))
+    rnd.tokens.copy_(dev(torch.tensor(orc["tokens"], dtype=torch.int32)))
+    rnd.lse_d.copy_(dev(torch.tensor(orc["lse"], dtype=torch.float32)))
+    rnd.logp_d.copy_(dev(torch.tensor(orc["logp"], dtype=torch.float32)))
+    rnd.verify(anchor, tgt, tau, vs)
+    torch.cuda.synchronize()
+    ov = oracle.verify(orc["tokens"], o_s["len"], orc["logits"], target, tau, vs)
+    flagged = compare_verify(rnd.accepted, rnd.bonus, ov, tau)
+    print(f"  verify: {flagged} of {R} requests in a tie band")
+    assert flagged <= max(1, R // 50)
     assert dsp.dspark_device_status() == 0
 
 

@@ -197,6 +197,50 @@ def test_rnn_head_with_open_gate_is_a_markov_head_on_tanh_embeddings():
     np.testing.assert_allclose(rnn["conf"], mk_conf["conf"], rtol=1e-13)
 
 
+def test_rnn_head_two_steps_in_closed_form():
+    """One request, two steps, rank 1, worked by hand.  The gate row sees only
+    the constant feature with weight ln 3, so g = sigmoid(ln 3) = 3/4; the
+    candidate row takes 3/4 of the state (in bf16), the embedding and 1/4 of the
+    constant feature.  With W1[anchor = 2] = 1/2 and W1[5] = -1/4:
+      s_1 = 1/4 * 0   + 3/4 * tanh(0 + 1/2 + 1/4)            = 3/4 tanh(3/4)
+      s_2 = 1/4 * s_1 + 3/4 * tanh(3/4 bf16(s_1) - 1/4 + 1/4)
+    and the logit of id 0 at step k is bf16(s_k) * W2[0, 0] (its base logit is
+    0).  A dropped carry, a swapped gate half, g and 1 - g exchanged, or an
+    unrounded state would each give a different number."""
+    import torch
+    V, r, d = 8, 1, 1
+    base = np.zeros((1, 2, V))
+    base[0, 0, 5] = 10.0                               # x_1 = 5
+    base[0, 1, 6] = 10.0                               # x_2 = 6
+    h = np.ones((1, 2, d))
+    W1 = np.zeros((V, r))
+    W1[2, 0], W1[5, 0] = 0.5, -0.25
+    W2 = np.zeros((r, V))
+    W2[0, 0] = 0.375
+    W_gc = np.array([[0.0, 0.0, math.log(3.0)],       # gate:      [state, embedding, h]
+                     [0.75, 1.0, 0.25]])               # candidate: [state, embedding, h]
+    out = oracle.rnn_draft(base, h, np.array([2]), W1, W2, W_gc, np.zeros(d + r), np.ones(2),
+                           0.0, 0, keep_scores=True)
+    bf = lambda x: torch.tensor(x, dtype=torch.float64).to(torch.bfloat16).double().item()
+    s1 = 0.75 * math.tanh(0.75)
+    s2 = 0.25 * s1 + 0.75 * math.tanh(0.75 * bf(s1))
+    assert out["tokens"].tolist() == [[5, 6]]
+    assert out["state"][0, 0] == pytest.approx(s2, abs=1e-15)
+    assert out["scores"][0, 0, 0] == pytest.approx(bf(s1) * 0.375, abs=1e-15)
+    assert out["scores"][0, 1, 0] == pytest.approx(bf(s2) * 0.375, abs=1e-15)
+    # the slips this pin tells apart from the reading
+    slips = {"no carry": 0.75 * math.tanh(0.75 * bf(s1)),
+             "gate and 1 - gate exchanged": 0.75 * 0.25 * math.tanh(0.75)
+             + 0.25 * math.tanh(0.75 * bf(0.25 * math.tanh(0.75))),
+             "unrounded state": 0.25 * s1 + 0.75 * math.tanh(0.75 * s1)}
+    sg = lambda x: 1.0 / (1.0 + math.exp(-x))
+    w1 = sg(0.75) * math.tanh(math.log(3.0))           # rows exchanged: g from the
+    slips["gate and candidate rows exchanged"] = (      # candidate row, tanh(ln 3) candidate
+        (1 - sg(0.75 * bf(w1))) * w1 + sg(0.75 * bf(w1)) * math.tanh(math.log(3.0)))
+    for name, wrong in slips.items():
+        assert abs(wrong - s2) > 1e-6, name
+
+
 def test_greedy_ties_pick_lowest_id():
     R, G, V = 2, 2, 9
     base = np.zeros((R, G, V))
@@ -518,6 +562,63 @@ def test_theta_fixed_point_rounding_against_exact_rationals():
         RS += u
         want.append(float(Fraction(RS) * Fraction(float(sps[K])) / 2 ** 48))
     assert got.tolist() == want
+
+
+def _exact_thetas(a, order, sps):
+    """Theta(K) in exact rationals from the float32 products and table entries."""
+    from fractions import Fraction
+    R = a.shape[0]
+    flat = a.reshape(-1)
+    S = Fraction(0)
+    out = [Fraction(R) * Fraction(float(sps[R - 1]))]
+    for K, i in enumerate(order, start=1):
+        S += Fraction(float(flat[i]))
+        out.append((R + S) * Fraction(float(sps[R + K - 1])))
+    return out
+
+
+def test_fixed_point_theta_decides_as_exact_arithmetic_outside_its_rounding_band():
+    """The fixed-point S_K moves R + S_K by at most gamma 2^-49 of itself, and
+    the two float64 roundings add 2^-52.  Wherever the exact optimum beats every
+    other budget by more than twice that, the fixed-point argmax (and the break
+    mode's first drop) is the exact one.  Random confidences, some equal to 1
+    and some repeated, over linear, concave, stepped and random tables."""
+    from fractions import Fraction
+    rng = np.random.default_rng(21)
+    decided = 0
+    for case in range(300):
+        R = int(rng.integers(1, 30))
+        G = int(rng.integers(1, 9))
+        c = rng.uniform(0.3, 1.0, (R, G)).astype(np.float32)
+        c[rng.random((R, G)) < 0.1] = 1.0
+        if case % 3 == 0:                              # repeated values: ties in the sort
+            c = np.round(c * 8) / 8
+        n = R * (G + 1)
+        B = np.arange(1, n + 1, dtype=np.float64)
+        kind = case % 4
+        if kind == 0:
+            sps = 1000.0 * (1.0 - (B - 1) / (2.0 * n))
+        elif kind == 1:
+            sps = 1000.0 * (1.0 - 0.75 * ((B - 1) / n) ** 2)
+        elif kind == 2:
+            sps = 1000.0 / (1.0 + 0.15 * np.floor((B - 1) / max(1, n // 7)))
+        else:
+            sps = np.sort(rng.uniform(100, 1000, n))[::-1]
+        sps = sps.astype(np.float32)
+        o = oracle.schedule(c, sps, oracle.UNCONSTRAINED)
+        ex = _exact_thetas(o["a"], o["order"], sps)
+        k_exact = max(range(len(ex)), key=lambda K: (ex[K], -K))
+        eps = Fraction(G, 2 ** 49) + Fraction(1, 2 ** 52)
+        others = [ex[K] for K in range(len(ex)) if K != k_exact]
+        if not others or all(ex[k_exact] > t * (1 + 2 * eps) for t in others):
+            assert o["K"] == k_exact, case
+            decided += 1
+        # break mode: the first K whose next budget does not raise Theta
+        steps = [ex[K + 1] / ex[K] - 1 for K in range(len(ex) - 1)]
+        if all(abs(x) > 2 * eps for x in steps):
+            kb = next((K for K, x in enumerate(steps) if x < 0), len(ex) - 1)
+            assert oracle.schedule(c, sps, oracle.BREAK)["K"] == kb, case
+    assert decided > 250
 
 
 # ------------------------------------------------------------ a8: verify ---
