@@ -49,6 +49,10 @@ def parse():
     p.add_argument("--fused-variant", action="store_true",
                    help="also time the fused single-contraction draft step (a measured "
                         "variant; the main line is unchanged)")
+    p.add_argument("--rnn-variant", action="store_true",
+                   help="also time the RNN-head draft (a measured variant) against the loop")
+    p.add_argument("--sts-fit", action="store_true",
+                   help="also time one STS fit over 1M synthetic held-out rounds")
     p.add_argument("--cpu-sample", type=int, default=0,
                    help="requests in the CPU-oracle sample (0 = sized automatically)")
     return p.parse_args()
@@ -354,10 +358,13 @@ def run_dspark(args, w, ws, rank, local):
     barrier(ws)
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # NVTX range "timed": a profiler can capture exactly the timed rounds
+    torch.cuda.nvtx.range_push("timed")
     start.record(stream)
     for i in range(args.steps):
         step(evs[i])
     end.record(stream)
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     barrier(ws)
     launches = dsp.dspark_launch_count() - n0
@@ -451,10 +458,12 @@ def run_dspark(args, w, ws, rank, local):
         torch.cuda.synchronize()
         n_f = max(3, min(args.steps, 50))
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.nvtx.range_push("fused")
         f0.record(stream)
         for _ in range(n_f):
             fused()
         f1.record(stream)
+        torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
         dsp.check_device_status()
         fms = f0.elapsed_time(f1) / n_f
@@ -464,6 +473,64 @@ def run_dspark(args, w, ws, rank, local):
             "draft_bytes": fbytes, "hbm_frac": fbytes / (fms * 1e-3) / 1e9 / peaks["hbm_gbs"],
             "tensor_frac": G * 2.0 * R * (d + r) * V / (fms * 1e-3) / 1e12 / tc_peak}
         del W_cat, fws
+
+    if args.rnn_variant:
+        # the RNN head in place of the Markov head (untrained weights of the
+        # stated shapes: W_rec [2r, 2r], W_hid [2r, d], std 1/sqrt(fan-in))
+        g = torch.Generator(device="cuda").manual_seed(w.seed + 17)
+        W_rec = (torch.randn((2 * r, 2 * r), generator=g, device="cuda") /
+                 math.sqrt(2 * r)).to(torch.bfloat16)
+        W_hid = (torch.randn((2 * r, d), generator=g, device="cuda") /
+                 math.sqrt(d)).to(torch.bfloat16)
+        rws = dsp.workspace(dsp.dspark_rnn_workspace_bytes(dims))
+
+        def rnn():
+            dsp.dspark_rnn_draft(dims, rnd.base, h, anchor, head.W1, head.W2t, W_rec, W_hid,
+                                 head.w_conf, head.T, tau, ds, rnd.tokens, rnd.conf, rnd.logp_d,
+                                 rnd.lse_d, rws)
+
+        for _ in range(3):
+            rnn()
+        torch.cuda.synchronize()
+        n_r = max(3, min(args.steps, 50))
+        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.nvtx.range_push("rnn")
+        r0.record(stream)
+        for _ in range(n_r):
+            rnn()
+        r1.record(stream)
+        torch.cuda.nvtx.range_pop()
+        torch.cuda.synchronize()
+        dsp.check_device_status()
+        line["rnn_variant"] = {"draft_ms": r0.elapsed_time(r1) / n_r,
+                               "markov_loop_ms": stage["markov_loop"]}
+        del W_rec, W_hid, rws
+
+    if args.sts_fit:
+        # one Sequential Temperature Scaling fit: 1M held-out rounds, gamma
+        # positions, 51 temperatures, 15 bins (synthetic logits and acceptances)
+        N = 1 << 20
+        g = torch.Generator(device="cuda").manual_seed(w.seed + 29)
+        z = (1.2 + 2.0 * torch.randn((N, G), generator=g, device="cuda")).contiguous()
+        accepted = torch.randint(0, G + 1, (N,), generator=g, device="cuda", dtype=torch.int32)
+        grid = torch.linspace(0.5, 3.0, 51, device="cuda")
+        T_out = torch.empty(G, dtype=torch.float32, device="cuda")
+        ece = torch.empty(G, dtype=torch.float64, device="cuda")
+        sws = dsp.workspace(dsp.dspark_sts_workspace_bytes(N, G, 51, 15))
+        for _ in range(3):
+            dsp.dspark_sts_fit(z, accepted, grid, 15, T_out, ece, sws)
+        torch.cuda.synchronize()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.nvtx.range_push("sts")
+        s0.record(stream)
+        for _ in range(10):
+            dsp.dspark_sts_fit(z, accepted, grid, 15, T_out, ece, sws)
+        s1.record(stream)
+        torch.cuda.nvtx.range_pop()
+        torch.cuda.synchronize()
+        dsp.check_device_status()
+        line["sts_fit"] = {"ms": s0.elapsed_time(s1) / 10, "rounds": N, "grid": 51, "bins": 15}
+        del z, accepted, sws
 
     if not args.no_e2e:
         # end to end through the public API from pinned host buffers

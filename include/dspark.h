@@ -91,7 +91,7 @@ enum {
   DSPARK_ERR_LENGTH = 6,     /* device status: verify length outside [0, gamma]     */
   DSPARK_ERR_TIMEOUT = 7,    /* device status: a bounded device-side wait ran out   */
   DSPARK_ERR_TOO_LARGE = 8   /* problem exceeds a fixed library limit (static scratch,
-                                sampling verify with V > 3604480)                  */
+                                sampling verify with V > 13107200)                 */
 };
 
 enum {
@@ -287,7 +287,7 @@ size_t dspark_verify_workspace_bytes(const dspark_dims *dims);
  *             draw is the two-level Gumbel-max of dspark_markov_draft (entry
  *             stream s, block stream s + 4); a residual that is empty in
  *             floating point is replaced by p_t itself (streams 2 and 6).
- *             Returns DSPARK_ERR_TOO_LARGE when tau > 0 and V > 3604480.
+ *             Returns DSPARK_ERR_TOO_LARGE when tau > 0 and V > 13107200.
  *   anchor   int32 [R];  tokens int32 [R, gamma];  len int32 [R] (0..gamma)
  *   base_logits bf16 [R*gamma, V], W1 bf16 [V, r], W2t bf16 [V, r]: the draft's
  *            operands, used to rebuild p_d on the rejected row (tau > 0 only), in

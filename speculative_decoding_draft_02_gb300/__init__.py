@@ -230,6 +230,11 @@ def dspark_fused_draft(dims, h, anchor, W_cat, W1, w_conf, T, tau, seed, tokens,
         _ptr(workspace), workspace.numel(), _stream(stream)), "dspark_fused_draft")
 
 
+def dspark_sts_workspace_bytes(N: int, gamma: int, n_grid: int, n_bins: int) -> int:
+    return int(load_library().dspark_sts_workspace_bytes(int(N), int(gamma), int(n_grid),
+                                                         int(n_bins)))
+
+
 def dspark_sts_fit(z, accepted, T_grid, n_bins, T_out, ece_out, workspace=None, stream=None):
     """Fit the per-position temperatures (see include/dspark.h); allocates the
     workspace when none is given."""

@@ -9,11 +9,14 @@
 // Greedy (tau = 0): accept iff x_j = argmax t_j; emit the argmax of the first
 // failing row (or of row l_r + 1).
 //
-// Pass 1 (verify_rows) scans each target row 1..l_r+1 once: its argmax, its
-// log-sum-exp and the drafted token's logit.  Pass 2 (verify_decide) walks each
-// request.  Sampling only: pass 3 rebuilds p_d on the rejected row through the
-// same fused vocabulary pass as the draft (bias + base logits, on chip) and
-// draws the residual, or draws the bonus from the target row.
+// Pass 1 (verify_rows) scans each target row 1..l_r+1 once: greedy, its
+// argmax; sampling, the log-sum-exp of rows 1..l_r (the acceptance test's
+// normalisers) and, for row l_r + 1, the first level of the bonus draw (each
+// 64-id block's log-mass plus its Gumbel).  Pass 2 (verify_decide) walks each
+// request and, when every draft passed, draws the bonus inside the winning
+// block.  Sampling only: pass 3 rebuilds p_d on the rejected row through the
+// same fused vocabulary pass as the draft (bias + base logits, on chip), and
+// pass 4 draws the residual.
 #include "logits_tile.cuh"
 
 DSPARK_DECLARE_STATUS(s_status_verify)
@@ -22,12 +25,13 @@ namespace {
 
 constexpr int NSEG = 4;  // CTAs per target row in the first pass
 
-// Per (request, row, segment): online log-sum-exp of t / tau (sampling) or the
-// argmax (greedy) over one quarter of the vocabulary.
+// Per (request, row, segment): online log-sum-exp of t / tau (sampling rows
+// 1..l_r), the argmax (greedy), or the best block score and its block
+// (sampling, the bonus row l_r + 1) over one quarter of the vocabulary.
 struct __align__(16) SegStat {
-  float m, s;      // sampling
-  float best;      // greedy
-  int32_t idx;     // greedy
+  float m, s;      // sampling: log-sum-exp
+  float best;      // greedy: max logit; sampling bonus row: best block score
+  int32_t idx;     // its id or block
 };
 
 __device__ __forceinline__ int clamp_len(const int32_t *len, int i, int gamma) {
@@ -39,24 +43,149 @@ __device__ __forceinline__ int clamp_len(const int32_t *len, int i, int gamma) {
   return L;
 }
 
-__device__ __forceinline__ int seg_len(int V) { return ((V + NSEG - 1) / NSEG + 7) / 8 * 8; }
+// Segments hold whole groups of four sampler blocks (256 ids), so a block's
+// log-mass, and one Philox call's four block words, are one CTA's.
+__device__ __forceinline__ int seg_len(int V) {
+  return ((V + NSEG - 1) / NSEG + 4 * GUMBEL_BLOCK - 1) / (4 * GUMBEL_BLOCK) * (4 * GUMBEL_BLOCK);
+}
+
+__device__ __forceinline__ void block_best_reduce(float &best, int &idx) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const float b2 = __shfl_xor_sync(0xffffffffu, best, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
+    if (better(b2, i2, best, idx)) { best = b2; idx = i2; }
+  }
+}
+
+// The first level of a two-level draw from softmax(row / tau) over segment
+// `seg`'s sampler blocks: G_b = log Z_b + Gumbel(block id b, stream + 4) at
+// (pos, req); the best (G_b, b) goes to out->best, out->idx.  Pass 1 leaves
+// log Z_b of every block of the segment in s_lz (dynamic shared memory): eight
+// lanes take a block (one 16-byte word each), eight words in flight per lane.
+// Pass 2 scores them, four blocks per thread from one Philox call (segments
+// start on a multiple of four blocks).  Called by a whole CTA of 256.
+__device__ void seg_block_scores(const bf16 *__restrict__ row, int V, int seg, float inv_tau,
+                                 uint64_t seed, int pos, int req, uint32_t stream,
+                                 SegStat *out) {
+  extern __shared__ float s_lz[];
+  constexpr float LOG2E = 1.4426950408889634f, LN2 = 0.6931471805599453f;
+  constexpr int GROUPS = 256 / 8, U = 8;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int grp = tid >> 3, sub = tid & 7;
+  const int sl = seg_len(V), nb = (V + GUMBEL_BLOCK - 1) / GUMBEL_BLOCK;
+  const int b_lo = seg * sl / GUMBEL_BLOCK;
+  const int b_hi = min(nb, b_lo + sl / GUMBEL_BLOCK);
+  const float c2 = inv_tau * LOG2E;
+  // pass 1: the trip count depends on the segment only: every lane reaches every shuffle
+  for (int b0 = b_lo; b0 < b_hi; b0 += GROUPS * U) {
+    uint4 w4[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int b = b0 + u * GROUPS + grp, v = b * GUMBEL_BLOCK + sub * 8;
+      w4[u] = (b < b_hi && v < V) ? __ldg(reinterpret_cast<const uint4 *>(row + v))
+                                  : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int b = b0 + u * GROUPS + grp, v = b * GUMBEL_BLOCK + sub * 8;
+      const bool ok = b < b_hi && v < V;  // V % 8 == 0: a word is all inside or all past V
+      const uint32_t w[4] = {w4[u].x, w4[u].y, w4[u].z, w4[u].w};
+      float x[8];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        x[2 * t] = bf16_lo(w[t]);
+        x[2 * t + 1] = bf16_hi(w[t]);
+      }
+      // the maximum of the raw values, scaled once (c2 > 0 keeps the order)
+      float mx = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])),
+                       fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
+      mx = ok ? mx : -INFINITY;
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const float ms = mx * c2;  // log2 units
+      float sm = 0.f;
+      if (ok && mx > -INFINITY) {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) sm += ex2_fast(fmaf(x[t], c2, -ms));
+      }
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
+      if (sub == 0 && b < b_hi)
+        s_lz[b - b_lo] = mx > -INFINITY ? (ms + __log2f(sm)) * LN2 : -INFINITY;
+    }
+  }
+  __syncthreads();
+  // pass 2: G_b = log Z_b + Gumbel(block id b, block stream), b_lo % 4 == 0
+  float best = -INFINITY;
+  int idx = 0x7fffffff;
+  for (int q4 = b_lo / 4 + tid; q4 * 4 < b_hi; q4 += 256) {
+    const uint4 g4 = rng_words4(seed, (uint32_t)q4, (uint32_t)pos, (uint32_t)req,
+                                stream + RNG_BLOCK_OFFSET);
+    const uint32_t ws[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int b = 4 * q4 + t;
+      if (b < b_hi && s_lz[b - b_lo] > -INFINITY) {
+        const float G = s_lz[b - b_lo] + rng_gumbel(ws[t]);
+        if (better(G, b, best, idx)) { best = G; idx = b; }
+      }
+    }
+  }
+  block_best_reduce(best, idx);
+  __shared__ float sb[8];
+  __shared__ int si[8];
+  if (lane == 0) { sb[warp] = best; si[warp] = idx; }
+  __syncthreads();
+  if (warp == 0) {
+    best = lane < 8 ? sb[lane] : -INFINITY;
+    idx = lane < 8 ? si[lane] : 0x7fffffff;
+    block_best_reduce(best, idx);
+    if (lane == 0) {
+      SegStat st;
+      st.m = -INFINITY; st.s = 0.f; st.best = best; st.idx = idx;
+      *out = st;
+    }
+  }
+  __syncthreads();  // s_lz, sb, si are free for the next call
+}
+
+// Dynamic shared memory of seg_block_scores: log Z_b of one segment's blocks.
+static inline size_t seg_lz_bytes(int V) {
+  const int sl = ((V + NSEG - 1) / NSEG + 4 * GUMBEL_BLOCK - 1) / (4 * GUMBEL_BLOCK) *
+                 (4 * GUMBEL_BLOCK);
+  return sizeof(float) * (size_t)(sl / GUMBEL_BLOCK);
+}
+constexpr size_t SEG_LZ_MAX = 200 * 1024;  // V up to about 13 million
+
+__device__ __forceinline__ void bonus_blocks(const bf16 *__restrict__ row, int V, int seg,
+                                             float inv_tau, uint64_t seed, int pos, int req,
+                                             SegStat *out) {
+  seg_block_scores(row, V, seg, inv_tau, seed, pos, req, RNG_BONUS, out);
+}
 
 // Pass 1: grid (NSEG * (gamma+1), R).  Greedy scans rows 1..l_r+1 (their
 // argmaxes decide acceptance and give the correction or bonus token); sampling
-// scans rows 1..l_r (their normalisers enter the acceptance test; the bonus
-// row needs none).  Block (0, 0) also clears the residual-row counter.
+// scans rows 1..l_r (their normalisers enter the acceptance test) and the
+// bonus row l_r + 1 (block scores: the bonus draw's first level, on the bonus
+// stream).  Block (0, 0) also clears the residual-row counter.
 template <int MODE>
 __global__ void __launch_bounds__(256) verify_rows(const bf16 *__restrict__ target,
                                                    const int32_t *__restrict__ len,
                                                    SegStat *__restrict__ stat,
                                                    int *__restrict__ count, int gamma, int V,
-                                                   float inv_tau) {
+                                                   float inv_tau, uint64_t seed) {
   const int j = blockIdx.x / NSEG, seg = blockIdx.x % NSEG, i = blockIdx.y;
   pdl_trigger();
   pdl_wait();  // len comes from the scheduler
   if (blockIdx.x == 0 && i == 0 && threadIdx.x == 0) *count = 0;
   const int L = clamp_len(len, i, gamma);
-  if (MODE == MODE_GREEDY ? j > L : j >= L) return;
+  if (j > L) return;
+  if (MODE == MODE_SAMPLE && j == L) {
+    bonus_blocks(target + ((size_t)i * (gamma + 1) + j) * V, V, seg, inv_tau, seed, j + 1, i,
+                 stat + ((size_t)i * (gamma + 1) + j) * NSEG + seg);
+    return;
+  }
   const int sl = seg_len(V), v_beg = seg * sl, v_end = min(V, v_beg + sl);
   const bf16 *row = target + ((size_t)i * (gamma + 1) + j) * V;
   const uint4 *row4 = reinterpret_cast<const uint4 *>(row);
@@ -85,16 +214,15 @@ __global__ void __launch_bounds__(256) verify_rows(const bf16 *__restrict__ targ
       for (int t = 0; t < 8; ++t) s += ex2_fast(vals[t] * c2 - m);
     }
   };
-  // four independent 16-byte loads in flight per thread
+  // eight independent 16-byte loads in flight per thread
   const int c_end = v_end / 8, step = blockDim.x;
   int c = v_beg / 8 + threadIdx.x;
-  for (; c + 3 * step < c_end; c += 4 * step) {
-    const uint4 q0 = __ldg(row4 + c), q1 = __ldg(row4 + c + step);
-    const uint4 q2 = __ldg(row4 + c + 2 * step), q3 = __ldg(row4 + c + 3 * step);
-    consume(q0, c);
-    consume(q1, c + step);
-    consume(q2, c + 2 * step);
-    consume(q3, c + 3 * step);
+  for (; c + 7 * step < c_end; c += 8 * step) {
+    uint4 q[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) q[u] = __ldg(row4 + c + u * step);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) consume(q[u], c + u * step);
   }
   for (; c < c_end; c += step) consume(__ldg(row4 + c), c);
   constexpr float LN2 = 0.6931471805599453f;
@@ -203,6 +331,30 @@ __global__ void verify_decide(const SegStat *__restrict__ stat, const bf16 *__re
     accepted[i] = jf ? jf - 1 : L;
     rows[i] = rr;
   }
+  if (!jf) {  // warp-uniform: every draft passed, the bonus comes from row l_r + 1
+    // the winning block of pass 1's block scores, then the ids inside it:
+    // t / tau + Gumbel(id, bonus stream) at position l_r + 1
+    const SegStat *sb = st + (size_t)L * NSEG;
+    float gb = -INFINITY;
+    int b = 0x7fffffff;
+    for (int g = 0; g < NSEG; ++g)
+      if (better(sb[g].best, sb[g].idx, gb, b)) { gb = sb[g].best; b = sb[g].idx; }
+    const int nb = (V + GUMBEL_BLOCK - 1) / GUMBEL_BLOCK;
+    if (!(gb > -INFINITY) || b >= nb) {  // non-finite target row
+      if (lane == 0) dspark_set_status(DSPARK_ERR_TOKEN);
+      b = 0;
+    }
+    __shared__ float s_score[256 / 32][GUMBEL_BLOCK];
+    float *sc = s_score[(threadIdx.x >> 5)];
+    const bf16 *trow = target + ((size_t)i * (gamma + 1) + L) * V;
+    for (int e = lane; e < GUMBEL_BLOCK; e += 32) {
+      const int v = b * GUMBEL_BLOCK + e;
+      sc[e] = v < V ? __bfloat162float(trow[v]) * inv_tau : -INFINITY;
+    }
+    __syncwarp();
+    const int tok = block_pick(sc, b, V, seed, (uint32_t)(L + 1), (uint32_t)i, RNG_BONUS);
+    if (lane == 0) bonus[i] = tok >= 0 ? tok : b * GUMBEL_BLOCK;
+  }
   // the residual pass's A operand: E[slot] = W1[x_{j*-1}], copied by the warp
   slot = __shfl_sync(0xffffffffu, slot, src);
   prev = __shfl_sync(0xffffffffu, prev, src);
@@ -216,9 +368,9 @@ __global__ void verify_decide(const SegStat *__restrict__ stat, const bf16 *__re
 // Residual rows: the block scores of the slices pick a block of 64 ids; inside
 // it the residual q = max(0, p_t - p_d) is rebuilt (target row, base logits and
 // the Markov bias W1[x_{j*-1}] . W2t[v]) and the corrected token is drawn from
-// log q + Gumbel.  A row whose residual came out empty is handed to the plain
-// target sample.  One CTA of 256 threads per compacted row, eight partial
-// loads in flight per thread.
+// log q + Gumbel.  A row whose residual came out empty is drawn from p_t
+// instead.  One CTA of 256 threads per compacted row, eight partial loads in
+// flight per thread.
 __global__ void __launch_bounds__(256) resample_reduce(
     ResampleRow *__restrict__ rows, const int *__restrict__ list, const int *__restrict__ count,
     const RowPartial *__restrict__ part, int n_parts, const bf16 *__restrict__ base,
@@ -262,192 +414,63 @@ __global__ void __launch_bounds__(256) resample_reduce(
   }
   __syncthreads();
   const int req = list[slot];
-  const int b = s_blk;
-  if (b < 0 || b >= (V + GUMBEL_BLOCK - 1) / GUMBEL_BLOCK) {  // every block empty
-    if (tid == 0) rows[req].kind = KIND_FALLBACK;
-    return;
-  }
   const ResampleRow rr = rows[req];
-  block_logits<256>(base + ((size_t)req * gamma + rr.pos - 1) * V, E + (size_t)slot * r, W2t, b,
-                    V, r, s_logit);
-  if (warp == 0) {
-    const bf16 *trow = target + ((size_t)req * (gamma + 1) + rr.pos - 1) * V;
-    for (int j = lane; j < GUMBEL_BLOCK; j += 32) {
-      const int v = b * GUMBEL_BLOCK + j;
-      float sc = -INFINITY;
-      if (v < V) {
-        const float pt = __expf(__bfloat162float(trow[v]) * inv_tau - rr.lse_t);
-        const float pd = __expf(s_logit[j] * inv_tau - rr.lse_d);
-        if (pt > pd) sc = __logf(pt - pd);
+  const bf16 *trow = target + ((size_t)req * (gamma + 1) + rr.pos - 1) * V;
+  const int nb = (V + GUMBEL_BLOCK - 1) / GUMBEL_BLOCK;
+  __shared__ int s_fb;
+  const int b = s_blk;
+  bool fallback = b < 0 || b >= nb;  // every block's residual empty (CTA-uniform)
+  if (!fallback) {
+    block_logits<256>(base + ((size_t)req * gamma + rr.pos - 1) * V, E + (size_t)slot * r, W2t,
+                      b, V, r, s_logit);
+    if (warp == 0) {
+      for (int j = lane; j < GUMBEL_BLOCK; j += 32) {
+        const int v = b * GUMBEL_BLOCK + j;
+        float sc = -INFINITY;
+        if (v < V) {
+          const float pt = __expf(__bfloat162float(trow[v]) * inv_tau - rr.lse_t);
+          const float pd = __expf(s_logit[j] * inv_tau - rr.lse_d);
+          if (pt > pd) sc = __logf(pt - pd);
+        }
+        s_score[j] = sc;
       }
-      s_score[j] = sc;
-    }
-    __syncwarp();
-    const int tok = block_pick(s_score, b, V, seed, (uint32_t)rr.pos, (uint32_t)req, RNG_RESIDUAL);
-    if (lane == 0) {
-      if (tok >= 0) bonus[req] = tok;
-      else rows[req].kind = KIND_FALLBACK;  // the block's mass was rounding only
-    }
-  }
-}
-
-// Plain target samples: the bonus row l_r + 1 when every draft passed (stream
-// 3), or the rejected row when its residual was empty (stream 2), drawn from
-// softmax(t / tau) in two levels.  One cluster of BONUS_SPLIT CTAs per request,
-// each on a quarter of the 64-id blocks (a multiple of four blocks, so one
-// Philox call per four blocks stays in one CTA): pass 1 leaves log Z_b of its
-// blocks in shared memory (eight lanes per block, one 16-byte word each, eight
-// words in flight), pass 2 scores them (G_b = log Z_b + Gumbel of block b).
-// The CTAs exchange their best (G_b, b) through distributed shared memory, and
-// the owner of the winning block draws inside it (pass 3).  Every CTA takes
-// the same per-block arithmetic and the same total order on (G_b, b) as one
-// CTA on the whole row would, so the split does not change the draw.
-constexpr int BONUS_SPLIT = 4;
-constexpr int BONUS_THREADS = 256;
-constexpr size_t BONUS_MAX_SMEM = 220 * 1024;  // log Z_b of up to 56320 blocks: V <= 3604480
-
-__device__ __forceinline__ int bonus_quarter(int nb) {
-  return ((nb + BONUS_SPLIT - 1) / BONUS_SPLIT + 3) / 4 * 4;
-}
-
-__device__ __forceinline__ uint32_t dsmem_addr(const void *p, uint32_t rank) {
-  uint32_t a;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
-               : "=r"(a)
-               : "r"((uint32_t)__cvta_generic_to_shared(p)), "r"(rank));
-  return a;
-}
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t a) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
-  return v;
-}
-__device__ __forceinline__ int ld_dsmem_s32(uint32_t a) {
-  int v;
-  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void warp_best(float &best, int &idx) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    const float b2 = __shfl_xor_sync(0xffffffffu, best, o);
-    const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
-    if (better(b2, i2, best, idx)) { best = b2; idx = i2; }
-  }
-}
-
-__global__ void __cluster_dims__(BONUS_SPLIT, 1, 1) __launch_bounds__(BONUS_THREADS)
-    bonus_row(const ResampleRow *__restrict__ rows, const bf16 *__restrict__ target,
-              int32_t *__restrict__ bonus, int gamma, int V, float inv_tau, uint64_t seed) {
-  extern __shared__ float s_lz[];  // [blocks of this CTA]: log Z_b
-  __shared__ float sb[BONUS_THREADS / 32], s_score[GUMBEL_BLOCK], s_cta_best;
-  __shared__ int si[BONUS_THREADS / 32], s_cta_idx;
-  constexpr float LOG2E = 1.4426950408889634f, LN2 = 0.6931471805599453f;
-  constexpr int GROUPS = BONUS_THREADS / 8, U = 8;
-  const int i = blockIdx.x / BONUS_SPLIT, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int q = (int)tc::cluster_ctarank();
-  pdl_trigger();
-  pdl_wait();  // the rows' kinds, final once resample_reduce has run
-  const ResampleRow rr = rows[i];
-  // the same for every CTA of the cluster: all leave here or none
-  if (rr.kind != KIND_BONUS && rr.kind != KIND_FALLBACK) return;
-  const uint32_t stream = rr.kind == KIND_BONUS ? RNG_BONUS : RNG_RESIDUAL;
-  const bf16 *trow = target + ((size_t)i * (gamma + 1) + rr.pos - 1) * V;
-  const int nb = (V + GUMBEL_BLOCK - 1) / GUMBEL_BLOCK, nbq = bonus_quarter(nb);
-  const int b_lo = q * nbq, b_hi = min(nb, b_lo + nbq);
-  const int grp = tid >> 3, sub = tid & 7;
-  const float c2 = inv_tau * LOG2E;
-  // pass 1: the trip count depends on this CTA's block range only, so every
-  // lane reaches every shuffle
-  for (int b0 = b_lo; b0 < b_hi; b0 += GROUPS * U) {
-    uint4 w4[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int b = b0 + u * GROUPS + grp, v = b * GUMBEL_BLOCK + sub * 8;
-      w4[u] = (b < b_hi && v < V) ? __ldg(reinterpret_cast<const uint4 *>(trow + v))
-                                  : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int b = b0 + u * GROUPS + grp, v = b * GUMBEL_BLOCK + sub * 8;
-      const bool ok = b < b_hi && v < V;  // V % 8 == 0: a word is all inside or all past V
-      const uint32_t w[4] = {w4[u].x, w4[u].y, w4[u].z, w4[u].w};
-      float x[8];
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        x[2 * t] = bf16_lo(w[t]);
-        x[2 * t + 1] = bf16_hi(w[t]);
-      }
-      // the maximum of the raw values, scaled once (c2 > 0 keeps the order)
-      float mx = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])),
-                       fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
-      mx = ok ? mx : -INFINITY;
-#pragma unroll
-      for (int o = 1; o < 8; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      const float ms = mx * c2;  // log2 units
-      float sm = 0.f;
-      if (ok && mx > -INFINITY) {
-#pragma unroll
-        for (int t = 0; t < 8; ++t) sm += ex2_fast(fmaf(x[t], c2, -ms));
-      }
-#pragma unroll
-      for (int o = 1; o < 8; o <<= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
-      if (sub == 0 && b < b_hi) s_lz[b - b_lo] = mx > -INFINITY ? (ms + __log2f(sm)) * LN2 : -INFINITY;
-    }
-  }
-  __syncthreads();
-  // pass 2: G_b = log Z_b + Gumbel(block id b, block stream), b_lo % 4 == 0
-  float best = -INFINITY;
-  int idx = 0x7fffffff;
-  for (int q4 = b_lo / 4 + tid; q4 * 4 < b_hi; q4 += BONUS_THREADS) {
-    const uint4 w = rng_words4(seed, (uint32_t)q4, (uint32_t)rr.pos, (uint32_t)i,
-                               stream + RNG_BLOCK_OFFSET);
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const int b = 4 * q4 + t;
-      if (b < b_hi && s_lz[b - b_lo] > -INFINITY) {
-        const float G = s_lz[b - b_lo] + rng_gumbel(ws[t]);
-        if (better(G, b, best, idx)) { best = G; idx = b; }
+      __syncwarp();
+      const int tok = block_pick(s_score, b, V, seed, (uint32_t)rr.pos, (uint32_t)req, RNG_RESIDUAL);
+      if (lane == 0) {
+        if (tok >= 0) bonus[req] = tok;
+        s_fb = tok < 0;  // the block's mass was rounding only
       }
     }
+    __syncthreads();
+    fallback = s_fb;
   }
-  warp_best(best, idx);
-  if (lane == 0) { sb[warp] = best; si[warp] = idx; }
-  __syncthreads();
-  if (warp == 0) {
-    best = lane < BONUS_THREADS / 32 ? sb[lane] : -INFINITY;
-    idx = lane < BONUS_THREADS / 32 ? si[lane] : 0x7fffffff;
-    warp_best(best, idx);
-    if (lane == 0) { s_cta_best = best; s_cta_idx = idx; }
-  }
-  tc::cluster_sync();  // every CTA's best is in its shared memory
-  if (warp == 0) {
-    best = -INFINITY;
-    idx = 0x7fffffff;
-    if (lane < BONUS_SPLIT) {
-      best = ld_dsmem_f32(dsmem_addr(&s_cta_best, (uint32_t)lane));
-      idx = ld_dsmem_s32(dsmem_addr(&s_cta_idx, (uint32_t)lane));
+  if (fallback) {
+    // the residual max(0, p_t - p_d) is empty in floating point (impossible in
+    // exact arithmetic): the row is drawn from p_t itself, on the residual
+    // stream, in the same two levels (block scores over the whole row, then
+    // the ids of the winning block)
+    __shared__ SegStat s_seg[NSEG];
+    if (tid == 0) rows[req].kind = KIND_FALLBACK;
+    for (int g = 0; g < NSEG; ++g)
+      seg_block_scores(trow, V, g, inv_tau, seed, rr.pos, req, RNG_RESIDUAL, &s_seg[g]);
+    if (warp == 0) {
+      float gb = -INFINITY;
+      int bb = 0x7fffffff;
+      for (int g = 0; g < NSEG; ++g)
+        if (better(s_seg[g].best, s_seg[g].idx, gb, bb)) { gb = s_seg[g].best; bb = s_seg[g].idx; }
+      if (!(gb > -INFINITY) || bb >= nb) {  // non-finite target row
+        if (lane == 0) dspark_set_status(DSPARK_ERR_TOKEN);
+        bb = 0;
+      }
+      for (int j = lane; j < GUMBEL_BLOCK; j += 32) {
+        const int v = bb * GUMBEL_BLOCK + j;
+        s_score[j] = v < V ? __bfloat162float(trow[v]) * inv_tau : -INFINITY;
+      }
+      __syncwarp();
+      const int tok = block_pick(s_score, bb, V, seed, (uint32_t)rr.pos, (uint32_t)req,
+                                 RNG_RESIDUAL);
+      if (lane == 0) bonus[req] = tok >= 0 ? tok : bb * GUMBEL_BLOCK;
     }
-    warp_best(best, idx);
-  }
-  tc::cluster_sync();  // no CTA leaves while another still reads its shared memory
-  if (warp == 0) {
-    int b = idx;
-    if (!(best > -INFINITY) || b >= nb) {  // non-finite target row
-      if (q == 0 && lane == 0) dspark_set_status(DSPARK_ERR_TOKEN);
-      b = 0;
-    }
-    if (b / nbq != q) return;  // another CTA owns the winning block
-    // pass 3: inside block b, t / tau + Gumbel(id, entry stream)
-    for (int j = lane; j < GUMBEL_BLOCK; j += 32) {
-      const int v = b * GUMBEL_BLOCK + j;
-      s_score[j] = v < V ? __bfloat162float(trow[v]) * inv_tau : -INFINITY;
-    }
-    __syncwarp();
-    const int tok = block_pick(s_score, b, V, seed, (uint32_t)rr.pos, (uint32_t)i, stream);
-    if (lane == 0) bonus[i] = tok >= 0 ? tok : b * GUMBEL_BLOCK;
   }
 }
 
@@ -509,7 +532,7 @@ extern "C" int dspark_verify(const dspark_dims *dims, const int32_t *anchor, con
   const bf16 *tgt = (const bf16 *)target;
   if (!sample) {
     if (dspark_launch_pdl(verify_rows<MODE_GREEDY>, rgrid, dim3(256), 0, stream, tgt, len,
-                          ws.stat, ws.count, G, V, inv_tau) != cudaSuccess ||
+                          ws.stat, ws.count, G, V, inv_tau, seed) != cudaSuccess ||
         dspark_launch_pdl(verify_decide<MODE_GREEDY>, dim3((R * 32 + 255) / 256), dim3(256), 0,
                           stream, ws.stat, tgt, anchor, tokens, len, lse_d, logp_d, ws.rows,
                           ws.list, ws.count, accepted, bonus, (const bf16 *)nullptr,
@@ -518,20 +541,25 @@ extern "C" int dspark_verify(const dspark_dims *dims, const int32_t *anchor, con
     dspark_count_launches(2);
     return DSPARK_OK;
   }
-  // bonus_row keeps log Z_b of a quarter of the sampler blocks in shared memory
-  // (the size limit stays the one of the whole row)
-  const int nb = (V + GUMBEL_BLOCK - 1) / GUMBEL_BLOCK;
-  if (sizeof(float) * (size_t)nb > BONUS_MAX_SMEM) return DSPARK_ERR_TOO_LARGE;
-  const size_t lz_bytes =
-      sizeof(float) * (size_t)(((nb + BONUS_SPLIT - 1) / BONUS_SPLIT + 3) / 4 * 4);
-  if (lz_bytes > 48 * 1024 &&
-      cudaFuncSetAttribute(bonus_row, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)lz_bytes) != cudaSuccess)
+  // the block scores keep one segment's log-masses in shared memory
+  const size_t lz = seg_lz_bytes(V);
+  if (lz > SEG_LZ_MAX) return DSPARK_ERR_TOO_LARGE;
+  static DsparkPerDevice smem_attr;
+  if (dspark_per_device(smem_attr, [] {
+        return cudaFuncSetAttribute(verify_rows<MODE_SAMPLE>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)SEG_LZ_MAX) == cudaSuccess &&
+                       cudaFuncSetAttribute(resample_reduce,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            (int)SEG_LZ_MAX) == cudaSuccess
+                   ? 1
+                   : -1;
+      }) < 0)
     return DSPARK_ERR_CUDA;
   // each kernel's launch and set-up overlap the tail of the one before
   // (programmatic serialisation; every kernel waits before touching memory)
-  if (dspark_launch_pdl(verify_rows<MODE_SAMPLE>, rgrid, dim3(256), 0, stream, tgt, len, ws.stat,
-                        ws.count, G, V, inv_tau) != cudaSuccess ||
+  if (dspark_launch_pdl(verify_rows<MODE_SAMPLE>, rgrid, dim3(256), lz, stream, tgt, len, ws.stat,
+                        ws.count, G, V, inv_tau, seed) != cudaSuccess ||
       dspark_launch_pdl(verify_decide<MODE_SAMPLE>, dim3((R * 32 + 255) / 256), dim3(256), 0,
                         stream, ws.stat, tgt, anchor, tokens, len, lse_d, logp_d, ws.rows,
                         ws.list, ws.count, accepted, bonus, (const bf16 *)W1, ws.E, R, G, V, r,
@@ -543,15 +571,12 @@ extern "C" int dspark_verify(const dspark_dims *dims, const int32_t *anchor, con
   const int rc = gemm::launch<LogitsCfg<MODE_RESIDUAL>::EPI_WARPS, LogitsCfg<MODE_RESIDUAL>::BN>(
       ws.E, W2t, R, V, r, epi, stream, ws.count, true);
   if (rc != DSPARK_OK) return rc;
-  if (dspark_launch_pdl(resample_reduce, dim3(R), dim3(256), 0, stream, ws.rows,
+  if (dspark_launch_pdl(resample_reduce, dim3(R), dim3(256), lz, stream, ws.rows,
                         (const int *)ws.list, (const int *)ws.count, (const RowPartial *)ws.part,
                         n_parts, (const bf16 *)base_logits, tgt, (const bf16 *)ws.E,
-                        (const bf16 *)W2t, G, V, r, inv_tau, seed, bonus) != cudaSuccess ||
-      dspark_launch_pdl(bonus_row, dim3(R * BONUS_SPLIT), dim3(BONUS_THREADS), lz_bytes, stream,
-                        (const ResampleRow *)ws.rows, tgt, bonus, G, V, inv_tau,
-                        seed) != cudaSuccess)
+                        (const bf16 *)W2t, G, V, r, inv_tau, seed, bonus) != cudaSuccess)
     return DSPARK_ERR_CUDA;
-  dspark_count_launches(4);  // + the GEMM, counted by launch()
+  dspark_count_launches(3);  // + the GEMM, counted by launch()
   return DSPARK_OK;
 }
 
