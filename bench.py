@@ -182,10 +182,10 @@ def profiled_traffic(kernel: str, src_hash: str, units: float, workload: str):
             kv[k.strip()] = v.strip()
     if kv.get("source_hash") != src_hash or kv.get("workload", "").split()[:1] != [workload]:
         return None
-    try:
-        b = float(kv["dram_bytes_per_launch"])
-        u = float(kv.get("units_per_launch", units))
-    except (KeyError, ValueError):
+    try:  # "units_per_launch: 1280  (what they are)"
+        b = float(kv["dram_bytes_per_launch"].split()[0])
+        u = float(str(kv.get("units_per_launch", units)).split()[0])
+    except (KeyError, ValueError, IndexError):
         return None
     return b * units / u
 
