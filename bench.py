@@ -14,6 +14,7 @@ Prints one JSON line (rank 0).  `value` is drafted tokens/s over all ranks.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import math
@@ -39,7 +40,7 @@ DEFAULT_WORKLOAD = "v4_dspark5"
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    # ~1 s of timed rounds at V4, so the clock sampler (200 ms) sees it several times
+    # ~1 s of timed rounds at V4, so the clock sampler (20 ms) sees it many times
     p.add_argument("--steps", type=int, default=600)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
@@ -108,21 +109,28 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clocks and throttle reasons, sampled every 20 ms from before the
+    warm-up on; stop() keeps the samples stamped inside the timed region (the
+    one nearest its middle when the region is shorter than the period)."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.proc = None
         self.gpu = gpu_index
+        self.t0 = self.t1 = None
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
+
+    def region(self, t0, t1):
+        """Host wall-clock bounds (datetime) of the timed region."""
+        self.t0, self.t1 = t0, t1
 
     def stop(self):
         if self.proc is None:
@@ -133,24 +141,32 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, mx, reasons = [], [], set()
+        rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in out.strip().splitlines():
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f")
+                rows.append((ts, float(f[2]), float(f[3]),
+                             {n for n, v in zip(names, f[6:10]) if v.lower().startswith("active")}))
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
+        if not rows:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        inside = rows
+        if self.t0 is not None:
+            inside = [r for r in rows if self.t0 <= r[0] <= self.t1]
+            if not inside:
+                mid = self.t0 + (self.t1 - self.t0) / 2
+                inside = [min(rows, key=lambda r: abs((r[0] - mid).total_seconds()))]
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": sorted(set().union(*(r[3] for r in inside))),
+                "samples": len(inside),
+                "window_ms": None if self.t0 is None else
+                round((self.t1 - self.t0).total_seconds() * 1e3, 1)}
 
 
 # Sources that define the LM-head kernel; a profile taken on other sources is stale.
@@ -346,6 +362,7 @@ def run_dspark(args, w, ws, rank, local):
         if ev is not None:
             ev[4].record(stream)
 
+    clocks = ClockSampler(local) if rank == 0 else None
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize()
@@ -353,21 +370,24 @@ def run_dspark(args, w, ws, rank, local):
 
     # timed region: K whole rounds, events around each stage on the launching stream
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
-    clocks = ClockSampler(local) if rank == 0 else None
     n0 = dsp.dspark_launch_count()
     barrier(ws)
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     # NVTX range "timed": a profiler can capture exactly the timed rounds
     torch.cuda.nvtx.range_push("timed")
+    t_host0 = datetime.datetime.now()
     start.record(stream)
     for i in range(args.steps):
         step(evs[i])
     end.record(stream)
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
+    t_host1 = datetime.datetime.now()
     barrier(ws)
     launches = dsp.dspark_launch_count() - n0
+    if clocks:
+        clocks.region(t_host0, t_host1)
     clk = clocks.stop() if clocks else None
     ms = start.elapsed_time(end) / args.steps
     ms = max_over_ranks(ms, ws)
