@@ -41,6 +41,12 @@ Readings where the pages are silent (each listed in the design notes):
     u * p_d(x_j) < p_t(x_j); on the first rejection sample from
     norm(max(0, p_t - p_d)); if every draft is accepted, sample the bonus from
     target row l_r + 1.  Greedy: accept iff x_j = argmax t_j.
+  * The residual draw is by rejection from p_t: trial q proposes y ~ p_t and
+    keeps it iff u_q p_t(y) < p_t(y) - p_d(y), so a kept y has law
+    max(0, p_t - p_d) / sum(max(0, p_t - p_d)) exactly (von Neumann's
+    rejection method with envelope p_t, whose ratio max(0, p_t - p_d) / p_t is
+    at most 1).  The first kept of RESIDUAL_TRIALS trials is the token; when
+    none is kept, the residual is formed explicitly and drawn by Gumbel-max.
 """
 from __future__ import annotations
 
@@ -113,6 +119,7 @@ def _block_logsumexp(x: np.ndarray) -> np.ndarray:
 # ---------------------------------------------------------------------------
 
 GUMBEL_BLOCK = 64
+RESIDUAL_TRIALS = 64   # proposals from p_t per rejected row before the explicit residual
 
 
 def gumbel_max(score, seed: int, position, request, stream: int,
@@ -563,8 +570,11 @@ def verify(tokens, lens, draft_logits, target, tau: float, seed: int,
     Returns accepted [R], bonus [R], and diagnostics: accept_margin [R, gamma]
     (log u + log p_d - log p_t at each tested position, nan elsewhere) and
     final_margin [R] (top-2 gap of the score that picked the bonus; sampling:
-    the margin of gumbel_max), and final_kind [R] (0 greedy, 1 residual,
-    2 bonus row, 3 residual that was empty, drawn from p_t instead).
+    the margin of gumbel_max, and for residual trials the smallest of every
+    evaluated trial's proposal margin and |1 - p_d/p_t - u|), final_kind [R]
+    (0 greedy, 1 residual drawn explicitly, 2 bonus row, 3 residual that was
+    empty, drawn from p_t instead, 4 residual kept by a trial) and trials [R]
+    (residual trials evaluated).
     """
     tokens = to_i64(tokens)
     lens = to_i64(lens)
@@ -578,6 +588,7 @@ def verify(tokens, lens, draft_logits, target, tau: float, seed: int,
     acc_margin = np.full((R, G), np.nan)
     final_margin = np.zeros(R)
     final_kind = np.zeros(R, dtype=np.int64)
+    trials = np.zeros(R, dtype=np.int64)
     for i in range(R):
         L = int(lens[i])
         rq = int(req[i])
@@ -607,16 +618,36 @@ def verify(tokens, lens, draft_logits, target, tau: float, seed: int,
             n = j - 1
             p_t = np.exp(lt - lse_t)
             p_d = np.exp(ld - lse_d)
-            q = np.maximum(p_t - p_d, 0.0)
+            rejected = True
+            # the residual by rejection from p_t: keep y_q iff u_q < 1 - p_d(y_q) / p_t(y_q)
+            margin = np.inf
+            for q in range(RESIDUAL_TRIALS):
+                s = philox.STREAM_TRIAL0 + 8 * q
+                prop = gumbel_max(lt, seed, j, rq, s, block)
+                y = int(prop["token"][0])
+                if y < 0:                                # no finite target entry
+                    break
+                trials[i] += 1
+                uq = float(philox.uniform(seed, j, rq, s + 1, 0))
+                keep = 1.0 - p_d[y] / p_t[y] - uq if p_t[y] > 0.0 else -np.inf
+                margin = min(margin, prop["margin"][0], abs(keep))
+                if keep > 0.0:
+                    bonus[i] = y
+                    final_kind[i] = 4
+                    break
+            if final_kind[i] == 4:
+                final_margin[i] = margin
+                break
+            # no trial kept: the explicit residual, drawn by Gumbel-max
+            qr = np.maximum(p_t - p_d, 0.0)
             with np.errstate(divide="ignore"):
-                smp = gumbel_max(np.log(q), seed, j, rq, philox.STREAM_RESIDUAL, block)
+                smp = gumbel_max(np.log(qr), seed, j, rq, philox.STREAM_RESIDUAL, block)
             final_kind[i] = 1
             if smp["token"][0] < 0:                      # empty residual: draw from p_t
                 smp = gumbel_max(lt, seed, j, rq, philox.STREAM_RESIDUAL, block)
                 final_kind[i] = 3
             bonus[i] = int(smp["token"][0])
-            final_margin[i] = smp["margin"][0]
-            rejected = True
+            final_margin[i] = min(margin, smp["margin"][0])
             break
         if not rejected:
             smp = gumbel_max(target[i, L] / tau, seed, L + 1, rq, philox.STREAM_BONUS, block)
@@ -625,7 +656,7 @@ def verify(tokens, lens, draft_logits, target, tau: float, seed: int,
             final_kind[i] = 2
         accepted[i] = n
     return dict(accepted=accepted, bonus=bonus, accept_margin=acc_margin,
-                final_margin=final_margin, final_kind=final_kind)
+                final_margin=final_margin, final_kind=final_kind, trials=trials)
 
 
 # ---------------------------------------------------------------------------

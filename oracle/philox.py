@@ -20,6 +20,9 @@ written independently draws the same numbers:
 Streams: 0 draft Gumbel, 1 accept uniform (v = 0), 2 residual Gumbel, 3 bonus Gumbel;
 the block-level Gumbels of a draw in stream s use stream s + 4 (4 draft,
 6 residual, 7 bonus; v = the block index; see oracle.dspark.gumbel_max).
+Residual trial q (q = 0, 1, ...; see oracle.dspark.verify) uses stream 16 + 8q
+for its proposal's Gumbels (16 + 8q + 4 at the block level) and 16 + 8q + 1
+for its acceptance uniform (v = 0).
 """
 from __future__ import annotations
 
@@ -36,6 +39,7 @@ STREAM_ACCEPT = 1
 STREAM_RESIDUAL = 2
 STREAM_BONUS = 3
 BLOCK_STREAM_OFFSET = 4   # block-level draws of stream s use stream s + 4
+STREAM_TRIAL0 = 16        # residual trial q: streams 16 + 8q (+1 uniform, +4 block level)
 
 
 def philox4x32_10(c0, c1, c2, c3, k0: int, k1: int):

@@ -656,6 +656,75 @@ def test_acceptance_rate_equals_confidence_label():
     assert abs(wrong - label) > 8 * math.sqrt(label * (1 - label) / N)
 
 
+def _one_position_verify(ld, lt, N, seed, block=64):
+    """N requests of one admitted position: drafts sampled from softmax(ld),
+    target row softmax(lt).  Returns the verify result and p_d, p_t."""
+    V = ld.size
+    base = np.broadcast_to(ld, (N, 1, V)).copy()
+    dr = oracle.markov_draft(base, np.zeros((N, 1, 1)), np.zeros(N, int), np.zeros((V, 1)),
+                             np.zeros((1, V)), np.zeros(2), np.ones(1), 1.0, seed=seed,
+                             block=block)
+    target = np.broadcast_to(np.stack([lt, lt]), (N, 2, V)).copy()
+    res = oracle.verify(dr["tokens"], np.ones(N, int), base, target, 1.0, seed=seed + 1,
+                        block=block)
+    pd = np.exp(ld - oracle.dspark.logsumexp(ld))
+    pt = np.exp(lt - oracle.dspark.logsumexp(lt))
+    return res, pd, pt
+
+
+def test_residual_draw_follows_the_residual_law():
+    """On rejection the corrected token follows norm(max(0, p_t - p_d)) (the
+    residual of speculative sampling), with the sampler's blocks of 3 ids over
+    V = 7 (both levels and a ragged block), and the draws come from the trials."""
+    ld = np.array([1.1, -0.3, 0.4, 2.0, -1.2, 0.0, 0.7])
+    lt = np.array([0.2, 0.9, -0.5, 1.0, 0.3, 1.4, -0.8])
+    res, pd, pt = _one_position_verify(ld, lt, 20000, 31, block=3)
+    rej = res["accepted"] == 0
+    q = np.maximum(pt - pd, 0.0)
+    q /= q.sum()
+    counts = np.bincount(res["bonus"][rej], minlength=ld.size)
+    assert rej.sum() > 4000
+    assert counts[q == 0].sum() == 0  # ids with p_d >= p_t are never the correction
+    keep = q > 0
+    assert stats.chisquare(counts[keep], rej.sum() * q[keep]).pvalue > 1e-4
+    assert np.all(res["final_kind"][rej] == 4)
+    # a trial that kept every proposal would give the target row itself
+    assert stats.chisquare(counts, rej.sum() * pt).pvalue < 1e-8
+
+
+def test_residual_trials_are_geometric_in_the_residual_mass():
+    """Each trial keeps its proposal with probability sum(max(0, p_t - p_d)), so
+    the trials of a rejected row are geometric with that mean inverse: a kept
+    proposal that skipped the test, or a test with the ratio reversed, moves it."""
+    ld = np.array([0.5, 0.1, -0.2, 0.8, 0.0])
+    lt = np.array([0.6, -0.1, 0.1, 0.7, -0.2])
+    res, pd, pt = _one_position_verify(ld, lt, 30000, 41)
+    rej = res["accepted"] == 0
+    z = np.maximum(pt - pd, 0.0).sum()
+    n = res["trials"][rej]
+    assert 0.05 < z < 0.2 and n.size > 1500
+    sem = math.sqrt((1 - z) / z ** 2 / n.size)
+    assert abs(n.mean() - 1 / z) < 4 * sem
+    assert np.all(res["trials"][~rej] == 0)
+
+
+def test_residual_without_trials_is_the_explicit_draw(monkeypatch):
+    """With no trials every rejected row takes the explicit residual, drawn by
+    Gumbel-max from log max(0, p_t - p_d): the same law."""
+    monkeypatch.setattr(oracle.dspark, "RESIDUAL_TRIALS", 0)
+    ld = np.array([1.1, -0.3, 0.4, 2.0, -1.2, 0.0, 0.7])
+    lt = np.array([0.2, 0.9, -0.5, 1.0, 0.3, 1.4, -0.8])
+    res, pd, pt = _one_position_verify(ld, lt, 15000, 51)
+    rej = res["accepted"] == 0
+    q = np.maximum(pt - pd, 0.0)
+    q /= q.sum()
+    counts = np.bincount(res["bonus"][rej], minlength=ld.size)
+    keep = q > 0
+    assert counts[~keep].sum() == 0
+    assert stats.chisquare(counts[keep], rej.sum() * q[keep]).pvalue > 1e-4
+    assert np.all(res["final_kind"][rej] == 1) and np.all(res["trials"] == 0)
+
+
 def test_greedy_verify_accepts_own_argmax():
     rng = np.random.default_rng(13)
     R, G, V = 6, 4, 50
