@@ -432,10 +432,12 @@ def run_dspark(args, w, ws, rank, local):
     if w.tau > 0:
         rejected = acc_n < ln
         vbytes = int(ln.sum()) * row                   # target rows 1..l_r: normalisers
-        n_rej = int(rejected.sum())
-        vbytes += n_rej * (2 * row + r * 2)            # rejected row: target + base, E row
-        vbytes += (V * r * 2) if n_rej else 0           # W2t once for the residual pass
+        n_rej, n_expl = dsp.dspark_verify_residual_rows(head.dims, rnd.ws_verify)
+        vbytes += n_rej * row                           # rejected row: rescanned for its trials
+        vbytes += n_expl * (2 * row + r * 2)            # explicit residual: target + base, E row
+        vbytes += (V * r * 2) if n_expl else 0          # W2t once for the explicit pass
         vbytes += int((~rejected).sum()) * row          # bonus row of the rest
+        # (each trial's 256 target ids, W2t row and base logit, ~1.5 KB, not counted)
     else:
         vbytes = int((ln + 1).sum()) * row             # rows 1..l_r + 1: argmaxes
     verify_gbs = vbytes / (stage["verify"] * 1e-3) / 1e9

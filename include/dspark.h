@@ -40,7 +40,8 @@
  *     read with dspark_device_status().
  *   - Random draws use Philox4x32-10 keyed by (seed) with counter
  *     (v >> 2, position, request, stream), word v & 3, u = ((w >> 9) + 0.5) 2^-23;
- *     streams: 0 draft Gumbel, 1 accept uniform, 2 residual Gumbel, 3 bonus Gumbel.
+ *     streams: 0 draft Gumbel, 1 accept uniform, 2 residual Gumbel, 3 bonus Gumbel;
+ *     residual trial q: 16 + 8q Gumbel, 16 + 8q + 1 uniform.
  *
  * Departures from the planned boundary (draft / schedule / verify / status):
  *   - W2 enters once, through dspark_pack_w2, as W2t [V, r]; every later call
@@ -281,12 +282,17 @@ size_t dspark_verify_workspace_bytes(const dspark_dims *dims);
  *   tau == 0: accept x_j iff x_j == argmax_v t_j[v]; the first mismatch row's
  *             argmax (or row l_r + 1 when all match) is the bonus token.
  *   tau > 0:  accept x_j iff u * p_d(x_j) < p_t(x_j), u = U(seed; r, j, stream 1);
- *             on the first rejection sample norm(max(0, p_t - p_d)) at that row
- *             (Gumbel streams 2 and 6); when all l_r are accepted sample target
- *             row l_r + 1 (streams 3 and 7).  p = softmax(logits / tau).  Each
- *             draw is the two-level Gumbel-max of dspark_markov_draft (entry
- *             stream s, block stream s + 4); a residual that is empty in
- *             floating point is replaced by p_t itself (streams 2 and 6).
+ *             on the first rejection sample norm(max(0, p_t - p_d)) at that row;
+ *             when all l_r are accepted sample target row l_r + 1 (streams 3
+ *             and 7).  p = softmax(logits / tau).  Each draw is the two-level
+ *             Gumbel-max of dspark_markov_draft (entry stream s, block stream
+ *             s + 4).  The residual is drawn by rejection from p_t: trial
+ *             q = 0, 1, .. proposes y ~ p_t (streams 16 + 8q and 20 + 8q) and
+ *             keeps it iff u_q < 1 - p_d(y) / p_t(y), u_q = U(stream 17 + 8q);
+ *             the first kept proposal is the token.  After 64 unkept trials the
+ *             residual is formed over the whole row and drawn on streams 2 and
+ *             6; a residual that is empty in floating point is replaced by p_t
+ *             itself (streams 2 and 6).
  *             Returns DSPARK_ERR_TOO_LARGE when tau > 0 and V > 13107200.
  *   anchor   int32 [R];  tokens int32 [R, gamma];  len int32 [R] (0..gamma)
  *   base_logits bf16 [R*gamma, V], W1 bf16 [V, r], W2t bf16 [V, r]: the draft's
@@ -304,6 +310,17 @@ int dspark_verify(const dspark_dims *dims, const int32_t *anchor, const int32_t 
                   const void *target, float tau, uint64_t seed, int32_t *accepted,
                   int32_t *bonus, void *workspace, size_t workspace_bytes,
                   dspark_stream_t stream);
+
+/* After a sampling dspark_verify on `stream` (and with its workspace): how many
+ * requests were rejected at some position (their corrected token came from the
+ * residual) and how many of those kept none of their 64 rejection trials, so
+ * that the residual was formed over the whole row (one W2t pass for all of
+ * them).  rejected, explicit_rows: host int32 out.  Copies two device counters
+ * and synchronises the stream.  Returns DSPARK_ERR_WORKSPACE for a workspace
+ * shorter than dspark_verify_workspace_bytes(dims). */
+int dspark_verify_residual_rows(const dspark_dims *dims, const void *workspace,
+                                size_t workspace_bytes, int32_t *rejected,
+                                int32_t *explicit_rows, dspark_stream_t stream);
 
 /* Failure detection self-test (no fault is involved).  Every device-side wait
  * of the library is bounded in time; on expiry the kernel records

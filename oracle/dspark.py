@@ -47,6 +47,8 @@ Readings where the pages are silent (each listed in the design notes):
     rejection method with envelope p_t, whose ratio max(0, p_t - p_d) / p_t is
     at most 1).  The first kept of RESIDUAL_TRIALS trials is the token; when
     none is kept, the residual is formed explicitly and drawn by Gumbel-max.
+    A proposal is the two-level draw with blocks of four sampler blocks
+    (256 ids), so its first level needs a quarter of the random words.
 """
 from __future__ import annotations
 
@@ -120,6 +122,7 @@ def _block_logsumexp(x: np.ndarray) -> np.ndarray:
 
 GUMBEL_BLOCK = 64
 RESIDUAL_TRIALS = 64   # proposals from p_t per rejected row before the explicit residual
+TRIAL_BLOCKS = 4       # sampler blocks per block of a trial proposal
 
 
 def gumbel_max(score, seed: int, position, request, stream: int,
@@ -623,7 +626,7 @@ def verify(tokens, lens, draft_logits, target, tau: float, seed: int,
             margin = np.inf
             for q in range(RESIDUAL_TRIALS):
                 s = philox.STREAM_TRIAL0 + 8 * q
-                prop = gumbel_max(lt, seed, j, rq, s, block)
+                prop = gumbel_max(lt, seed, j, rq, s, TRIAL_BLOCKS * block)
                 y = int(prop["token"][0])
                 if y < 0:                                # no finite target entry
                     break

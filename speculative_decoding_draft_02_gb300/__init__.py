@@ -32,7 +32,7 @@ EXPORTS = [
     "dspark_markov_draft_static", "dspark_schedule_async", "dspark_conf_logits",
     "dspark_sts_workspace_bytes", "dspark_sts_fit", "dspark_rnn_workspace_bytes",
     "dspark_rnn_draft", "dspark_selftest_wait_timeout", "dspark_fused_workspace_bytes",
-    "dspark_pack_fused", "dspark_fused_draft",
+    "dspark_pack_fused", "dspark_fused_draft", "dspark_verify_residual_rows",
 ]
 STATIC_SCRATCH_BYTES = 16 << 20
 
@@ -87,6 +87,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                          P]),
         "dspark_markov_draft_static": (ctypes.c_int, [DP, P, P, P, P, P, P, P, F32, U64, P, P, P,
                                                       P, P]),
+        "dspark_verify_residual_rows": (ctypes.c_int, [DP, P, SZ, P, P, P]),
         "dspark_device_status": (ctypes.c_int, [P, ctypes.c_int]),
         "dspark_error_string": (ctypes.c_char_p, [ctypes.c_int]),
         "dspark_launch_count": (U64, []),
@@ -262,6 +263,15 @@ def dspark_verify(dims, anchor, tokens, length, base_logits, W1, W2t, lse_d, log
         _ptr(W1), _ptr(W2t), _ptr(lse_d), _ptr(logp_d), _ptr(target), float(tau), _u64(seed),
         _ptr(accepted), _ptr(bonus), _ptr(workspace), workspace.numel(), _stream(stream)),
         "dspark_verify")
+
+
+def dspark_verify_residual_rows(dims, workspace, stream=None):
+    """(rejected, explicit_rows) of the last sampling dspark_verify on `workspace`."""
+    rej, expl = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(load_library().dspark_verify_residual_rows(
+        ctypes.byref(dims), _ptr(workspace), workspace.numel(), ctypes.byref(rej),
+        ctypes.byref(expl), _stream(stream)), "dspark_verify_residual_rows")
+    return int(rej.value), int(expl.value)
 
 
 def dspark_device_status(stream=None, clear: bool = True) -> int:

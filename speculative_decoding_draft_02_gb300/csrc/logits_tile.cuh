@@ -19,9 +19,11 @@
 #include "umma_gemm.cuh"
 
 enum TileMode { MODE_GREEDY = 0, MODE_SAMPLE = 1, MODE_RESIDUAL = 2 };
-enum RowKind { KIND_NONE = 0, KIND_RESIDUAL = 1, KIND_BONUS = 2, KIND_FALLBACK = 3 };
+enum RowKind { KIND_NONE = 0, KIND_RESIDUAL = 1, KIND_BONUS = 2, KIND_FALLBACK = 3,
+               KIND_TRIAL = 4 };
 // KIND_FALLBACK: the residual max(0, p_t - p_d) of the rejected row was empty in
 // floating point; the row is then sampled from p_t itself (residual stream).
+// KIND_TRIAL: a rejection trial from p_t kept its proposal (no explicit pass).
 
 // Per-request context of a verification resample.
 struct __align__(16) ResampleRow {

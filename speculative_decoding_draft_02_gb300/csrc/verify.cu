@@ -14,9 +14,12 @@
 // normalisers) and, for row l_r + 1, the first level of the bonus draw (each
 // 64-id block's log-mass plus its Gumbel).  Pass 2 (verify_decide) walks each
 // request and, when every draft passed, draws the bonus inside the winning
-// block.  Sampling only: pass 3 rebuilds p_d on the rejected row through the
-// same fused vocabulary pass as the draft (bias + base logits, on chip), and
-// pass 4 draws the residual.
+// block.  Sampling only: pass 3 (residual_trials) draws each rejected row's
+// residual norm(max(0, p_t - p_d)) by rejection from p_t, which needs p_d at
+// the proposed ids only (one W2t row each).  A row none of whose trials keeps
+// its proposal (rare unless p_t and p_d nearly agree) takes the explicit
+// route: pass 4 rebuilds p_d on the row through the same fused vocabulary pass
+// as the draft (bias + base logits, on chip), and pass 5 draws the residual.
 #include "logits_tile.cuh"
 
 DSPARK_DECLARE_STATUS(s_status_verify)
@@ -65,19 +68,19 @@ __device__ __forceinline__ void block_best_reduce(float &best, int &idx) {
 // lanes take a block (one 16-byte word each), eight words in flight per lane.
 // Pass 2 scores them, four blocks per thread from one Philox call (segments
 // start on a multiple of four blocks).  Called by a whole CTA of 256.
-__device__ void seg_block_scores(const bf16 *__restrict__ row, int V, int seg, float inv_tau,
-                                 uint64_t seed, int pos, int req, uint32_t stream,
-                                 SegStat *out) {
-  extern __shared__ float s_lz[];
+// log Z_b of sampler blocks [b_lo, b_hi) of a row of logits / tau into
+// out[b - b_lo] (-inf for a block with no finite weight): eight lanes take a
+// block (one 16-byte word each), eight words in flight per lane.  Called by a
+// whole CTA of NT threads; ends with a CTA barrier, after which out is complete.
+template <int NT>
+__device__ void block_lz(const bf16 *__restrict__ row, int V, int b_lo, int b_hi, float inv_tau,
+                         float *out) {
   constexpr float LOG2E = 1.4426950408889634f, LN2 = 0.6931471805599453f;
-  constexpr int GROUPS = 256 / 8, U = 8;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int GROUPS = NT / 8, U = 8;
+  const int tid = threadIdx.x;
   const int grp = tid >> 3, sub = tid & 7;
-  const int sl = seg_len(V), nb = (V + GUMBEL_BLOCK - 1) / GUMBEL_BLOCK;
-  const int b_lo = seg * sl / GUMBEL_BLOCK;
-  const int b_hi = min(nb, b_lo + sl / GUMBEL_BLOCK);
   const float c2 = inv_tau * LOG2E;
-  // pass 1: the trip count depends on the segment only: every lane reaches every shuffle
+  // the trip count depends on the block range only: every lane reaches every shuffle
   for (int b0 = b_lo; b0 < b_hi; b0 += GROUPS * U) {
     uint4 w4[U];
 #pragma unroll
@@ -112,10 +115,22 @@ __device__ void seg_block_scores(const bf16 *__restrict__ row, int V, int seg, f
 #pragma unroll
       for (int o = 1; o < 8; o <<= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
       if (sub == 0 && b < b_hi)
-        s_lz[b - b_lo] = mx > -INFINITY ? (ms + __log2f(sm)) * LN2 : -INFINITY;
+        out[b - b_lo] = mx > -INFINITY ? (ms + __log2f(sm)) * LN2 : -INFINITY;
     }
   }
   __syncthreads();
+}
+
+__device__ void seg_block_scores(const bf16 *__restrict__ row, int V, int seg, float inv_tau,
+                                 uint64_t seed, int pos, int req, uint32_t stream,
+                                 SegStat *out) {
+  extern __shared__ float s_lz[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int sl = seg_len(V), nb = (V + GUMBEL_BLOCK - 1) / GUMBEL_BLOCK;
+  const int b_lo = seg * sl / GUMBEL_BLOCK;
+  const int b_hi = min(nb, b_lo + sl / GUMBEL_BLOCK);
+  // pass 1: the blocks' log-masses
+  block_lz<256>(row, V, b_lo, b_hi, inv_tau, s_lz);
   // pass 2: G_b = log Z_b + Gumbel(block id b, block stream), b_lo % 4 == 0
   float best = -INFINITY;
   int idx = 0x7fffffff;
@@ -168,17 +183,21 @@ __device__ __forceinline__ void bonus_blocks(const bf16 *__restrict__ row, int V
 // argmaxes decide acceptance and give the correction or bonus token); sampling
 // scans rows 1..l_r (their normalisers enter the acceptance test) and the
 // bonus row l_r + 1 (block scores: the bonus draw's first level, on the bonus
-// stream).  Block (0, 0) also clears the residual-row counter.
+// stream).  Block (0, 0) also clears the residual-row counters.
 template <int MODE>
 __global__ void __launch_bounds__(256) verify_rows(const bf16 *__restrict__ target,
                                                    const int32_t *__restrict__ len,
                                                    SegStat *__restrict__ stat,
-                                                   int *__restrict__ count, int gamma, int V,
+                                                   int *__restrict__ count,
+                                                   int *__restrict__ count_fb, int gamma, int V,
                                                    float inv_tau, uint64_t seed) {
   const int j = blockIdx.x / NSEG, seg = blockIdx.x % NSEG, i = blockIdx.y;
   pdl_trigger();
   pdl_wait();  // len comes from the scheduler
-  if (blockIdx.x == 0 && i == 0 && threadIdx.x == 0) *count = 0;
+  if (blockIdx.x == 0 && i == 0 && threadIdx.x == 0) {
+    *count = 0;
+    *count_fb = 0;
+  }
   const int L = clamp_len(len, i, gamma);
   if (j > L) return;
   if (MODE == MODE_SAMPLE && j == L) {
@@ -249,9 +268,8 @@ __global__ void __launch_bounds__(256) verify_rows(const bf16 *__restrict__ targ
 }
 
 // Pass 2: one warp per request; lane j - 1 tests admitted position j (j <= l_r)
-// and a ballot finds the first failure.  Sampling: the warp of a rejected
-// request takes a compacted slot and copies W1[x_{j*-1}] there, the A operand
-// of the residual pass.
+// and a ballot finds the first failure.  Sampling: a rejected request takes a
+// compacted slot of the residual passes.
 template <int MODE>
 __global__ void verify_decide(const SegStat *__restrict__ stat, const bf16 *__restrict__ target,
                               const int32_t *__restrict__ anchor,
@@ -259,8 +277,7 @@ __global__ void verify_decide(const SegStat *__restrict__ stat, const bf16 *__re
                               const float *__restrict__ lse_d, const float *__restrict__ logp_d,
                               ResampleRow *__restrict__ rows, int *__restrict__ list,
                               int *__restrict__ count, int32_t *__restrict__ accepted,
-                              int32_t *__restrict__ bonus, const bf16 *__restrict__ W1,
-                              bf16 *__restrict__ E, int R, int gamma, int V, int r,
+                              int32_t *__restrict__ bonus, int R, int gamma, int V,
                               float inv_tau, uint64_t seed) {
   const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   pdl_trigger();
@@ -307,20 +324,18 @@ __global__ void verify_decide(const SegStat *__restrict__ stat, const bf16 *__re
   const unsigned bal = __ballot_sync(0xffffffffu, fail);
   const int jf = bal ? __ffs(bal) : 0;  // first rejected position (1-based), 0 if none
   const int src = jf ? jf - 1 : 0;
-  int slot = -1, prev = 0;
   if (lane == src) {
     ResampleRow rr;
     rr.pad[0] = rr.pad[1] = rr.pad[2] = 0;
     if (jf) {
       rr.kind = KIND_RESIDUAL;
       rr.pos = jf;
-      prev = (jf == 1) ? anchor[i] : x[jf - 2];
+      int prev = (jf == 1) ? anchor[i] : x[jf - 2];
       if (prev < 0 || prev >= V) { dspark_set_status(DSPARK_ERR_TOKEN); prev = 0; }
       rr.prev = prev;
       rr.lse_t = lse_t;
       rr.lse_d = lse_d[(size_t)i * gamma + jf - 1];
-      slot = atomicAdd(count, 1);
-      list[slot] = i;  // compacted residual rows (order irrelevant)
+      list[atomicAdd(count, 1)] = i;  // compacted residual rows (order irrelevant)
     } else {
       rr.kind = KIND_BONUS;
       rr.pos = L + 1;
@@ -355,17 +370,9 @@ __global__ void verify_decide(const SegStat *__restrict__ stat, const bf16 *__re
     const int tok = block_pick(sc, b, V, seed, (uint32_t)(L + 1), (uint32_t)i, RNG_BONUS);
     if (lane == 0) bonus[i] = tok >= 0 ? tok : b * GUMBEL_BLOCK;
   }
-  // the residual pass's A operand: E[slot] = W1[x_{j*-1}], copied by the warp
-  slot = __shfl_sync(0xffffffffu, slot, src);
-  prev = __shfl_sync(0xffffffffu, prev, src);
-  if (slot >= 0) {  // warp-uniform
-    const uint4 *from = reinterpret_cast<const uint4 *>(W1 + (size_t)prev * r);
-    uint4 *to = reinterpret_cast<uint4 *>(E + (size_t)slot * r);
-    for (int c = lane; c < r / 8; c += 32) to[c] = from[c];
-  }
 }
 
-// Residual rows: the block scores of the slices pick a block of 64 ids; inside
+// Pass 5, the rows no trial settled: the block scores of the slices pick a block of 64 ids; inside
 // it the residual q = max(0, p_t - p_d) is rebuilt (target row, base logits and
 // the Markov bias W1[x_{j*-1}] . W2t[v]) and the corrected token is drawn from
 // log q + Gumbel.  A row whose residual came out empty is drawn from p_t
@@ -474,11 +481,147 @@ __global__ void __launch_bounds__(256) resample_reduce(
   }
 }
 
+// Rejection trials from p_t per rejected row before the explicit residual.
+constexpr int RESIDUAL_TRIALS = 64;
+constexpr int TRIAL_WARPS = 32;  // trials in flight per row (one per warp)
+constexpr int TRIAL_THREADS = 32 * TRIAL_WARPS;
+constexpr int TRIAL_BLOCK = 4 * GUMBEL_BLOCK;  // ids per block of a proposal
+
+// Pass 3, one CTA per rejected row (compacted by verify_decide): the residual
+// norm(max(0, p_t - p_d)) by rejection from p_t.  The row's log-masses over
+// blocks of TRIAL_BLOCK ids go to lz once; then rounds of TRIAL_WARPS trials,
+// one per warp: trial q draws y_q ~ p_t in two levels (block by log Z_b +
+// Gumbel(b) on stream RNG_TRIAL0 + 8q + RNG_BLOCK_OFFSET, id inside it by
+// t_v / tau + Gumbel(v) on RNG_TRIAL0 + 8q) and keeps it iff
+// u_q < 1 - p_d(y_q) / p_t(y_q), u_q on RNG_TRIAL0 + 8q + 1, where p_d(y)
+// needs only the base logit, W1[x_{j*-1}] . W2t[y] and lse_d.  The first kept
+// trial in q order is the corrected token.  A row that keeps none of its
+// RESIDUAL_TRIALS goes to the explicit residual pass: compacted into list_fb,
+// with E_fb = W1[x_{j*-1}] as its A operand.
+__global__ void __launch_bounds__(TRIAL_THREADS) residual_trials(
+    ResampleRow *__restrict__ rows, const int *__restrict__ list, const int *__restrict__ count,
+    const bf16 *__restrict__ base, const bf16 *__restrict__ target, const bf16 *__restrict__ W1,
+    const bf16 *__restrict__ W2t, float *__restrict__ lz, int gamma, int V, int r,
+    float inv_tau, uint64_t seed, int32_t *__restrict__ bonus, int *__restrict__ list_fb,
+    int *__restrict__ count_fb, bf16 *__restrict__ E_fb) {
+  const int slot = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_trigger();
+  pdl_wait();  // the compacted rows of verify_decide
+  if (slot >= *count) return;
+  const int req = list[slot];
+  const ResampleRow rr = rows[req];
+  const int nb = (V + GUMBEL_BLOCK - 1) / GUMBEL_BLOCK;
+  const int nq = (V + TRIAL_BLOCK - 1) / TRIAL_BLOCK;
+  const uint32_t pos = (uint32_t)rr.pos;
+  const bf16 *trow = target + ((size_t)req * (gamma + 1) + rr.pos - 1) * V;
+  const bf16 *brow = base + ((size_t)req * gamma + rr.pos - 1) * V;
+  const uint4 *e4 = reinterpret_cast<const uint4 *>(W1 + (size_t)rr.prev * r);
+  // the log-masses of the sampler blocks, then of blocks of four of them
+  float *lz64 = lz + (size_t)slot * (nb + nq), *lz256 = lz64 + nb;
+  block_lz<TRIAL_THREADS>(trow, V, 0, nb, inv_tau, lz64);  // ends with a CTA barrier
+  for (int c = tid; c < nq; c += TRIAL_THREADS) {
+    float m = -INFINITY;
+    for (int t = 4 * c; t < 4 * c + 4 && t < nb; ++t) m = fmaxf(m, lz64[t]);
+    float sm = 0.f;
+    if (m > -INFINITY)
+      for (int t = 4 * c; t < 4 * c + 4 && t < nb; ++t) sm += expf(lz64[t] - m);
+    lz256[c] = m > -INFINITY ? m + logf(sm) : -INFINITY;
+  }
+  __syncthreads();
+  __shared__ int s_kept[TRIAL_WARPS];
+  int tok = -1;
+  for (int q0 = 0; q0 < RESIDUAL_TRIALS; q0 += TRIAL_WARPS) {  // CTA-uniform trip count
+    const uint32_t st = RNG_TRIAL0 + 8u * (uint32_t)(q0 + warp);
+    // y ~ p_t, first level: the best block score over the row
+    float best = -INFINITY;
+    int b = 0x7fffffff;
+    for (int q4 = lane; 4 * q4 < nq; q4 += 32) {
+      const uint4 g4 = rng_words4(seed, (uint32_t)q4, pos, (uint32_t)req, st + RNG_BLOCK_OFFSET);
+      const uint32_t ws[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int bb = 4 * q4 + t;
+        const float l = bb < nq ? lz256[bb] : -INFINITY;
+        if (l > -INFINITY) {
+          const float G = l + rng_gumbel(ws[t]);
+          if (better(G, bb, best, b)) { best = G; b = bb; }
+        }
+      }
+    }
+    block_best_reduce(best, b);
+    int y = -1;
+    if (best > -INFINITY) {  // warp-uniform: second level, eight ids of block b per lane
+      const int v0 = b * TRIAL_BLOCK + 8 * lane;
+      float e = -INFINITY;
+      int id = 0x7fffffff;
+      if (v0 < V) {  // V % 8 == 0: the eight ids are all inside or all past V
+        const uint4 w = __ldg(reinterpret_cast<const uint4 *>(trow + v0));
+        const uint4 ga = rng_words4(seed, (uint32_t)(v0 >> 2), pos, (uint32_t)req, st);
+        const uint4 gb = rng_words4(seed, (uint32_t)(v0 >> 2) + 1u, pos, (uint32_t)req, st);
+        const uint32_t tw[4] = {w.x, w.y, w.z, w.w};
+        const uint32_t gw[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const float tv = (t & 1) ? bf16_hi(tw[t >> 1]) : bf16_lo(tw[t >> 1]);
+          const float sc = tv * inv_tau;
+          if (sc > -INFINITY) {
+            const float ev = sc + rng_gumbel(gw[t]);
+            if (better(ev, v0 + t, e, id)) { e = ev; id = v0 + t; }
+          }
+        }
+      }
+      block_best_reduce(e, id);
+      y = e > -INFINITY ? id : -1;
+    }
+    int kept = -1;
+    if (y >= 0) {  // warp-uniform: the acceptance test, p_d(y) / p_t(y) in logs
+      const uint4 *w4 = reinterpret_cast<const uint4 *>(W2t + (size_t)y * r);
+      float dot = 0.f;
+      for (int c = lane; c < r / 8; c += 32) dot = dot8_bf16(__ldg(e4 + c), __ldg(w4 + c), dot);
+      dot = warp_sum(dot);
+      const float ld = (__bfloat162float(brow[y]) + dot) * inv_tau - rr.lse_d;
+      const float lt = __bfloat162float(trow[y]) * inv_tau - rr.lse_t;
+      const float u = rng_uniform(rng_words4(seed, 0u, pos, (uint32_t)req, st + 1).x);
+      if (1.f - expf(ld - lt) - u > 0.f) kept = y;
+    }
+    if (lane == 0) s_kept[warp] = kept;
+    __syncthreads();
+    int t = -1;
+#pragma unroll
+    for (int w = 0; w < TRIAL_WARPS; ++w)
+      if (t < 0) t = s_kept[w];  // the first kept trial in q order
+    __syncthreads();  // s_kept is rewritten by the next round
+    if (t >= 0) {
+      tok = t;
+      break;
+    }
+  }
+  if (tok >= 0) {
+    if (tid == 0) {
+      bonus[req] = tok;
+      rows[req].kind = KIND_TRIAL;
+    }
+    return;
+  }
+  // no trial kept its proposal: the explicit residual pass takes the row
+  __shared__ int s_fs;
+  if (tid == 0) {
+    s_fs = atomicAdd(count_fb, 1);
+    list_fb[s_fs] = req;
+  }
+  __syncthreads();
+  uint4 *to = reinterpret_cast<uint4 *>(E_fb + (size_t)s_fs * r);
+  for (int c = tid; c < r / 8; c += TRIAL_THREADS) to[c] = __ldg(e4 + c);
+}
+
 struct VerifyWs {
   SegStat *stat;
   ResampleRow *rows;
   int *list;
   int *count;
+  int *list_fb;   // rows left to the explicit residual pass
+  int *count_fb;
+  float *lz;      // [R, V / 64 + V / 256] block log-masses of the rejected rows' target rows
   bf16 *E;
   RowPartial *part;
   size_t bytes;
@@ -495,6 +638,13 @@ VerifyWs verify_layout(const dspark_dims *d, char *base) {
   off = dspark_align_up(off + sizeof(int) * (size_t)d->R, 256);
   w.count = (int *)(base + off);
   off = dspark_align_up(off + sizeof(int), 256);
+  w.list_fb = (int *)(base + off);
+  off = dspark_align_up(off + sizeof(int) * (size_t)d->R, 256);
+  w.count_fb = (int *)(base + off);
+  off = dspark_align_up(off + sizeof(int), 256);
+  w.lz = (float *)(base + off);
+  const size_t nb = (size_t)(d->V + GUMBEL_BLOCK - 1) / GUMBEL_BLOCK;
+  off = dspark_align_up(off + sizeof(float) * (size_t)d->R * (nb + (nb + 3) / 4), 256);
   w.E = (bf16 *)(base + off);
   off = dspark_align_up(off + sizeof(bf16) * (size_t)d->R * d->r, 256);
   w.part = (RowPartial *)(base + off);
@@ -532,11 +682,11 @@ extern "C" int dspark_verify(const dspark_dims *dims, const int32_t *anchor, con
   const bf16 *tgt = (const bf16 *)target;
   if (!sample) {
     if (dspark_launch_pdl(verify_rows<MODE_GREEDY>, rgrid, dim3(256), 0, stream, tgt, len,
-                          ws.stat, ws.count, G, V, inv_tau, seed) != cudaSuccess ||
+                          ws.stat, ws.count, ws.count_fb, G, V, inv_tau, seed) != cudaSuccess ||
         dspark_launch_pdl(verify_decide<MODE_GREEDY>, dim3((R * 32 + 255) / 256), dim3(256), 0,
                           stream, ws.stat, tgt, anchor, tokens, len, lse_d, logp_d, ws.rows,
-                          ws.list, ws.count, accepted, bonus, (const bf16 *)nullptr,
-                          (bf16 *)nullptr, R, G, V, r, inv_tau, seed) != cudaSuccess)
+                          ws.list, ws.count, accepted, bonus, R, G, V, inv_tau,
+                          seed) != cudaSuccess)
       return DSPARK_ERR_CUDA;
     dspark_count_launches(2);
     return DSPARK_OK;
@@ -559,24 +709,50 @@ extern "C" int dspark_verify(const dspark_dims *dims, const int32_t *anchor, con
   // each kernel's launch and set-up overlap the tail of the one before
   // (programmatic serialisation; every kernel waits before touching memory)
   if (dspark_launch_pdl(verify_rows<MODE_SAMPLE>, rgrid, dim3(256), lz, stream, tgt, len, ws.stat,
-                        ws.count, G, V, inv_tau, seed) != cudaSuccess ||
+                        ws.count, ws.count_fb, G, V, inv_tau, seed) != cudaSuccess ||
       dspark_launch_pdl(verify_decide<MODE_SAMPLE>, dim3((R * 32 + 255) / 256), dim3(256), 0,
                         stream, ws.stat, tgt, anchor, tokens, len, lse_d, logp_d, ws.rows,
-                        ws.list, ws.count, accepted, bonus, (const bf16 *)W1, ws.E, R, G, V, r,
-                        inv_tau, seed) != cudaSuccess)
+                        ws.list, ws.count, accepted, bonus, R, G, V, inv_tau,
+                        seed) != cudaSuccess ||
+      dspark_launch_pdl(residual_trials, dim3(R), dim3(TRIAL_THREADS), 0, stream, ws.rows,
+                        (const int *)ws.list, (const int *)ws.count, (const bf16 *)base_logits,
+                        tgt, (const bf16 *)W1, (const bf16 *)W2t, ws.lz, G, V, r, inv_tau, seed,
+                        bonus, ws.list_fb, ws.count_fb, ws.E) != cudaSuccess)
     return DSPARK_ERR_CUDA;
+  // the explicit residual, for the rows no trial settled (usually none: the
+  // GEMM then finds no rows and the reduction no slot)
   const int n_parts = logits_parts<MODE_RESIDUAL>(V);
-  EpiLogits<MODE_RESIDUAL> epi{(const bf16 *)base_logits, tgt, ws.rows, ws.list, ws.count,
+  EpiLogits<MODE_RESIDUAL> epi{(const bf16 *)base_logits, tgt, ws.rows, ws.list_fb, ws.count_fb,
                                ws.part, R, V, G, 0, n_parts, inv_tau, seed};
   const int rc = gemm::launch<LogitsCfg<MODE_RESIDUAL>::EPI_WARPS, LogitsCfg<MODE_RESIDUAL>::BN>(
-      ws.E, W2t, R, V, r, epi, stream, ws.count, true);
+      ws.E, W2t, R, V, r, epi, stream, ws.count_fb, true);
   if (rc != DSPARK_OK) return rc;
   if (dspark_launch_pdl(resample_reduce, dim3(R), dim3(256), lz, stream, ws.rows,
-                        (const int *)ws.list, (const int *)ws.count, (const RowPartial *)ws.part,
-                        n_parts, (const bf16 *)base_logits, tgt, (const bf16 *)ws.E,
-                        (const bf16 *)W2t, G, V, r, inv_tau, seed, bonus) != cudaSuccess)
+                        (const int *)ws.list_fb, (const int *)ws.count_fb,
+                        (const RowPartial *)ws.part, n_parts, (const bf16 *)base_logits, tgt,
+                        (const bf16 *)ws.E, (const bf16 *)W2t, G, V, r, inv_tau, seed,
+                        bonus) != cudaSuccess)
     return DSPARK_ERR_CUDA;
-  dspark_count_launches(3);  // + the GEMM, counted by launch()
+  dspark_count_launches(4);  // + the GEMM, counted by launch()
+  return DSPARK_OK;
+}
+
+extern "C" int dspark_verify_residual_rows(const dspark_dims *dims, const void *workspace,
+                                          size_t workspace_bytes, int32_t *rejected,
+                                          int32_t *explicit_rows, dspark_stream_t stream) {
+  if (!dspark_dims_ok(dims) || !rejected || !explicit_rows) return DSPARK_ERR_ARG;
+  const VerifyWs ws = verify_layout(dims, (char *)workspace);
+  if (!workspace || workspace_bytes < ws.bytes || ((uintptr_t)workspace & 255))
+    return DSPARK_ERR_WORKSPACE;
+  int v[2] = {0, 0};
+  if (cudaMemcpyAsync(&v[0], ws.count, sizeof(int), cudaMemcpyDeviceToHost, stream) !=
+          cudaSuccess ||
+      cudaMemcpyAsync(&v[1], ws.count_fb, sizeof(int), cudaMemcpyDeviceToHost, stream) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  *rejected = v[0];
+  *explicit_rows = v[1];
   return DSPARK_OK;
 }
 

@@ -302,7 +302,7 @@ def test_schedule_with_nan_in_the_sps_table():
 
 # ------------------------------------------------------------------ a8 ----
 
-def _verify_case(shape, tau, seed, accept_bias=0.7, lens_kind="random"):
+def _verify_case(shape, tau, seed, accept_bias=0.7, lens_kind="random", noise_std=0.3):
     R, G, V, r, d = shape
     inp = _weights(R, G, V, r, d, seed=seed)
     base = workloads.random_normal((R, G, V), 1.0, seed + 1)
@@ -310,7 +310,7 @@ def _verify_case(shape, tau, seed, accept_bias=0.7, lens_kind="random"):
     lens = workloads.random_lengths(R, G, seed + 3)
     if lens_kind == "full":
         lens = torch.full_like(lens, G)
-    noise = workloads.random_normal((R, G + 1, V), 0.3, seed + 4, dtype=torch.float32)
+    noise = workloads.random_normal((R, G + 1, V), noise_std, seed + 4, dtype=torch.float32)
     if tau == 0.0:
         target = workloads.random_normal((R, G + 1, V), 1.0, seed + 5)
         # make runs of accepted tokens likely: drafts equal the target argmax mostly
@@ -352,6 +352,26 @@ def test_verify_matches_oracle(shape, tau):
     acc = host(rnd.accepted)
     assert np.all(acc >= 0) and np.all(acc <= host(lens))
     assert dsp.dspark_device_status() == 0
+
+
+def test_verify_rows_no_trial_settles_take_the_explicit_residual():
+    """Target within a few hundredths of the draft: a rejected row's residual
+    mass is about 1 %, so most of its 64 trials keep nothing and the row goes
+    on to the explicit residual pass (the oracle's kind 1); the trials settle
+    the rest (kind 4).  Both routes against the oracle."""
+    shape = (768, 4, 1000, 128, 320)
+    rnd, orc, lens = _verify_case(shape, 1.0, seed=351, noise_std=0.03)
+    kinds = np.bincount(orc["final_kind"], minlength=5)
+    print(f"oracle kinds (greedy, explicit, bonus, empty, trial): {kinds.tolist()}")
+    assert kinds[1] >= 2 and kinds[4] >= 1
+    flagged = compare_verify(rnd.accepted, rnd.bonus, orc, 1.0)
+    print(f"verify {shape}: {flagged} of {shape[0]} requests in a tie band")
+    assert flagged <= max(1, shape[0] // 50)
+    assert dsp.dspark_device_status() == 0
+    rejected, explicit = dsp.dspark_verify_residual_rows(rnd.head.dims, rnd.ws_verify)
+    print(f"device: {rejected} rejected rows, {explicit} to the explicit pass")
+    assert abs(rejected - int(kinds[1] + kinds[3] + kinds[4])) <= flagged
+    assert abs(explicit - int(kinds[1] + kinds[3])) <= flagged
 
 
 @pytest.mark.parametrize("shape,tau", [((37, 4, 1000, 128, 320), 1.0),
