@@ -12,14 +12,15 @@
 // Pass 1 (verify_rows) scans each target row 1..l_r+1 once: greedy, its
 // argmax; sampling, the log-sum-exp of rows 1..l_r (the acceptance test's
 // normalisers) and, for row l_r + 1, the first level of the bonus draw (each
-// 64-id block's log-mass plus its Gumbel).  Pass 2 (verify_decide) walks each
-// request and, when every draft passed, draws the bonus inside the winning
-// block.  Sampling only: pass 3 (residual_trials) draws each rejected row's
-// residual norm(max(0, p_t - p_d)) by rejection from p_t, which needs p_d at
-// the proposed ids only (one W2t row each).  A row none of whose trials keeps
-// its proposal (rare unless p_t and p_d nearly agree) takes the explicit
-// route: pass 4 rebuilds p_d on the row through the same fused vocabulary pass
-// as the draft (bias + base logits, on chip), and pass 5 draws the residual.
+// 64-id block's log-mass plus its Gumbel).  The last CTA of each request to
+// finish its row then decides the request: the acceptance ballot, and the
+// bonus drawn inside the winning block, or (sampling) the request joins the
+// rejected rows.  Pass 2 (residual_trials) draws each rejected row's residual
+// norm(max(0, p_t - p_d)) by rejection from p_t, which needs p_d at the
+// proposed ids only (one W2t row each).  A row none of whose trials keeps its
+// proposal (rare unless p_t and p_d nearly agree) takes the explicit route:
+// pass 3 rebuilds p_d on the row through the same fused vocabulary pass as the
+// draft (bias + base logits, on chip), and pass 4 draws the residual.
 #include "logits_tile.cuh"
 
 DSPARK_DECLARE_STATUS(s_status_verify)
@@ -179,200 +180,234 @@ __device__ __forceinline__ void bonus_blocks(const bf16 *__restrict__ row, int V
   seg_block_scores(row, V, seg, inv_tau, seed, pos, req, RNG_BONUS, out);
 }
 
-// Pass 1: grid (NSEG * (gamma+1), R).  Greedy scans rows 1..l_r+1 (their
-// argmaxes decide acceptance and give the correction or bonus token); sampling
-// scans rows 1..l_r (their normalisers enter the acceptance test) and the
-// bonus row l_r + 1 (block scores: the bonus draw's first level, on the bonus
-// stream).  Block (0, 0) also clears the residual-row counters.
-template <int MODE>
-__global__ void __launch_bounds__(256) verify_rows(const bf16 *__restrict__ target,
-                                                   const int32_t *__restrict__ len,
-                                                   SegStat *__restrict__ stat,
-                                                   int *__restrict__ count,
-                                                   int *__restrict__ count_fb, int gamma, int V,
-                                                   float inv_tau, uint64_t seed) {
-  const int j = blockIdx.x / NSEG, seg = blockIdx.x % NSEG, i = blockIdx.y;
-  pdl_trigger();
-  pdl_wait();  // len comes from the scheduler
-  if (blockIdx.x == 0 && i == 0 && threadIdx.x == 0) {
-    *count = 0;
-    *count_fb = 0;
-  }
-  const int L = clamp_len(len, i, gamma);
-  if (j > L) return;
-  if (MODE == MODE_SAMPLE && j == L) {
-    bonus_blocks(target + ((size_t)i * (gamma + 1) + j) * V, V, seg, inv_tau, seed, j + 1, i,
-                 stat + ((size_t)i * (gamma + 1) + j) * NSEG + seg);
-    return;
-  }
-  const int sl = seg_len(V), v_beg = seg * sl, v_end = min(V, v_beg + sl);
-  const bf16 *row = target + ((size_t)i * (gamma + 1) + j) * V;
-  const uint4 *row4 = reinterpret_cast<const uint4 *>(row);
-  float m = -INFINITY, s = 0.f, best = -INFINITY, bs = 0.f;
-  int idx = 0x7fffffff;
-  const float c2 = inv_tau * 1.4426950408889634f;
-  auto consume = [&](const uint4 q, int c) {
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-    float vals[8];
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      vals[2 * t] = bf16_lo(w[t]);
-      vals[2 * t + 1] = bf16_hi(w[t]);
-    }
-    if (MODE == MODE_GREEDY) {
-#pragma unroll
-      for (int t = 0; t < 8; ++t)
-        if (vals[t] > best) { best = vals[t]; idx = c * 8 + t; }  // ids increase per thread
-    } else {
-      float cm = vals[0];
-#pragma unroll
-      for (int t = 1; t < 8; ++t) cm = fmaxf(cm, vals[t]);
-      cm *= c2;  // log2 units
-      if (cm > m) { s *= ex2_fast(m - cm); m = cm; }
-#pragma unroll
-      for (int t = 0; t < 8; ++t) s += ex2_fast(vals[t] * c2 - m);
-    }
-  };
-  // eight independent 16-byte loads in flight per thread
-  const int c_end = v_end / 8, step = blockDim.x;
-  int c = v_beg / 8 + threadIdx.x;
-  for (; c + 7 * step < c_end; c += 8 * step) {
-    uint4 q[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) q[u] = __ldg(row4 + c + u * step);
-#pragma unroll
-    for (int u = 0; u < 8; ++u) consume(q[u], c + u * step);
-  }
-  for (; c < c_end; c += step) consume(__ldg(row4 + c), c);
-  constexpr float LN2 = 0.6931471805599453f;
-  m = m > -INFINITY ? m * LN2 : m;  // back to natural units
-  warp_merge(m, s, best, idx, bs);
-  __shared__ float sm[8], ss[8], sb[8];
-  __shared__ int si[8];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) { sm[warp] = m; ss[warp] = s; sb[warp] = best; si[warp] = idx; }
-  __syncthreads();
-  if (warp == 0) {
-    const int nw = blockDim.x >> 5;
-    m = lane < nw ? sm[lane] : -INFINITY;
-    s = lane < nw ? ss[lane] : 0.f;
-    best = lane < nw ? sb[lane] : -INFINITY;
-    idx = lane < nw ? si[lane] : 0x7fffffff;
-    warp_merge(m, s, best, idx, bs);
-    if (lane == 0) {
-      SegStat st;
-      st.m = m; st.s = s; st.best = best; st.idx = idx;
-      stat[((size_t)i * (gamma + 1) + j) * NSEG + seg] = st;
-    }
-  }
-}
+// Arguments of the first pass (and of the decision its last CTA per request takes).
+struct VerifyArgs {
+  const bf16 *target;           // [R, gamma + 1, V]
+  const int32_t *len;           // [R]
+  const int32_t *anchor;        // [R]
+  const int32_t *tokens;        // [R, gamma]
+  const float *lse_d, *logp_d;  // [R, gamma]
+  const bf16 *base;             // [R * gamma, V]
+  const bf16 *W1, *W2t;         // [V, r]
+  SegStat *stat;                // [R, gamma + 1, NSEG]
+  int *done;                    // [R]  arrivals of a request's row CTAs (zeroed per call)
+  int *count;                   // rejected requests
+  int *list;                    // [R]  those requests, compacted
+  ResampleRow *rows;            // [R]
+  int32_t *accepted, *bonus;    // [R]
+  int R, gamma, V, r;
+  float inv_tau;
+  uint64_t seed;
+};
 
-// Pass 2: one warp per request; lane j - 1 tests admitted position j (j <= l_r)
-// and a ballot finds the first failure.  Sampling: a rejected request takes a
-// compacted slot of the residual passes.
+// The decision of request i from its rows' statistics, by the last CTA of the
+// request to finish its row: warp 0 tests admitted position j on lane j - 1
+// and a ballot finds the first failure.  Greedy: the argmaxes decide.
+// Sampling: every draft passed, the bonus is drawn inside the bonus row's
+// winning block; else the request joins the rejected rows of the trial pass.
 template <int MODE>
-__global__ void verify_decide(const SegStat *__restrict__ stat, const bf16 *__restrict__ target,
-                              const int32_t *__restrict__ anchor,
-                              const int32_t *__restrict__ tokens, const int32_t *__restrict__ len,
-                              const float *__restrict__ lse_d, const float *__restrict__ logp_d,
-                              ResampleRow *__restrict__ rows, int *__restrict__ list,
-                              int *__restrict__ count, int32_t *__restrict__ accepted,
-                              int32_t *__restrict__ bonus, int R, int gamma, int V,
-                              float inv_tau, uint64_t seed) {
-  const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  pdl_trigger();
-  pdl_wait();  // the row statistics of verify_rows
-  if (i >= R) return;  // warp-uniform
-  const int L = clamp_len(len, i, gamma);  // gamma <= 32: one lane per position
-  const SegStat *st = stat + (size_t)i * (gamma + 1) * NSEG;
-  const int32_t *x = tokens + (size_t)i * gamma;
-  const int j = lane + 1;  // this lane's 1-based position
+__device__ void decide_request(const VerifyArgs &a, int i, int L) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int gamma = a.gamma, V = a.V;
+  const SegStat *st = a.stat + (size_t)i * (gamma + 1) * NSEG;
+  const int32_t *x = a.tokens + (size_t)i * gamma;
+  const int j = lane + 1;  // this lane's 1-based position (gamma <= 32)
+  auto load = [&](int k) {  // another CTA's statistics: from L2
+    SegStat v;
+    const float4 f = __ldcg(reinterpret_cast<const float4 *>(st + k));
+    v.m = f.x; v.s = f.y; v.best = f.z; v.idx = __float_as_int(f.w);
+    return v;
+  };
   if (MODE == MODE_GREEDY) {
+    if (warp != 0) return;
     auto row_argmax = [&](int jr) {  // 0-based row
       float b = -INFINITY;
       int id = 0x7fffffff;
-      for (int g = 0; g < NSEG; ++g)
-        if (better(st[jr * NSEG + g].best, st[jr * NSEG + g].idx, b, id)) {
-          b = st[jr * NSEG + g].best;
-          id = st[jr * NSEG + g].idx;
-        }
+      for (int g = 0; g < NSEG; ++g) {
+        const SegStat v = load(jr * NSEG + g);
+        if (better(v.best, v.idx, b, id)) { b = v.best; id = v.idx; }
+      }
       return id;
     };
     const bool fail = j <= L && x[j - 1] != row_argmax(j - 1);
     const unsigned bal = __ballot_sync(0xffffffffu, fail);
     const int n = bal ? __ffs(bal) - 1 : L;  // first failing position - 1
+    const int tok = row_argmax(n);
     if (lane == 0) {
-      accepted[i] = n;
-      bonus[i] = row_argmax(n);
+      a.accepted[i] = n;
+      a.bonus[i] = tok;
     }
     return;
   }
-  // sampling: accept x_j iff u * p_d(x_j) < p_t(x_j), tested in logs
-  bool fail = false;
-  float lse_t = 0.f;
-  if (j <= L) {
-    float m = -INFINITY, s = 0.f;
-    for (int g = 0; g < NSEG; ++g) lse_merge(m, s, st[(j - 1) * NSEG + g].m, st[(j - 1) * NSEG + g].s);
-    lse_t = m + logf(s);
-    int xj = x[j - 1];
-    if (xj < 0 || xj >= V) { dspark_set_status(DSPARK_ERR_TOKEN); xj = 0; }
-    const float tx = __bfloat162float(target[((size_t)i * (gamma + 1) + j - 1) * V + xj]) * inv_tau;
-    const uint4 w = rng_words4(seed, 0u, (uint32_t)j, (uint32_t)i, RNG_ACCEPT);
-    const float u = rng_uniform(w.x);
-    fail = !(logf(u) + logp_d[(size_t)i * gamma + j - 1] < tx - lse_t);
-  }
-  const unsigned bal = __ballot_sync(0xffffffffu, fail);
-  const int jf = bal ? __ffs(bal) : 0;  // first rejected position (1-based), 0 if none
-  const int src = jf ? jf - 1 : 0;
-  if (lane == src) {
-    ResampleRow rr;
-    rr.pad[0] = rr.pad[1] = rr.pad[2] = 0;
-    if (jf) {
-      rr.kind = KIND_RESIDUAL;
-      rr.pos = jf;
-      int prev = (jf == 1) ? anchor[i] : x[jf - 2];
-      if (prev < 0 || prev >= V) { dspark_set_status(DSPARK_ERR_TOKEN); prev = 0; }
-      rr.prev = prev;
-      rr.lse_t = lse_t;
-      rr.lse_d = lse_d[(size_t)i * gamma + jf - 1];
-      list[atomicAdd(count, 1)] = i;  // compacted residual rows (order irrelevant)
-    } else {
-      rr.kind = KIND_BONUS;
-      rr.pos = L + 1;
-      rr.prev = 0;
-      rr.lse_t = 0.f;
-      rr.lse_d = 0.f;
+  if (warp == 0) {
+    // sampling: accept x_j iff u * p_d(x_j) < p_t(x_j), tested in logs
+    bool fail = false;
+    float lse_t = 0.f;
+    if (j <= L) {
+      float m = -INFINITY, s = 0.f;
+      for (int g = 0; g < NSEG; ++g) {
+        const SegStat v = load((j - 1) * NSEG + g);
+        lse_merge(m, s, v.m, v.s);
+      }
+      lse_t = m + logf(s);
+      int xj = x[j - 1];
+      if (xj < 0 || xj >= V) { dspark_set_status(DSPARK_ERR_TOKEN); xj = 0; }
+      const float tx =
+          __bfloat162float(a.target[((size_t)i * (gamma + 1) + j - 1) * V + xj]) * a.inv_tau;
+      const uint4 w = rng_words4(a.seed, 0u, (uint32_t)j, (uint32_t)i, RNG_ACCEPT);
+      const float u = rng_uniform(w.x);
+      fail = !(logf(u) + a.logp_d[(size_t)i * gamma + j - 1] < tx - lse_t);
     }
-    accepted[i] = jf ? jf - 1 : L;
-    rows[i] = rr;
-  }
-  if (!jf) {  // warp-uniform: every draft passed, the bonus comes from row l_r + 1
-    // the winning block of pass 1's block scores, then the ids inside it:
-    // t / tau + Gumbel(id, bonus stream) at position l_r + 1
-    const SegStat *sb = st + (size_t)L * NSEG;
-    float gb = -INFINITY;
-    int b = 0x7fffffff;
-    for (int g = 0; g < NSEG; ++g)
-      if (better(sb[g].best, sb[g].idx, gb, b)) { gb = sb[g].best; b = sb[g].idx; }
-    const int nb = (V + GUMBEL_BLOCK - 1) / GUMBEL_BLOCK;
-    if (!(gb > -INFINITY) || b >= nb) {  // non-finite target row
-      if (lane == 0) dspark_set_status(DSPARK_ERR_TOKEN);
-      b = 0;
+    const unsigned bal = __ballot_sync(0xffffffffu, fail);
+    const int jf = bal ? __ffs(bal) : 0;  // first rejected position (1-based), 0 if none
+    const int src = jf ? jf - 1 : 0;
+    if (lane == src) {
+      ResampleRow rr;
+      rr.pad[0] = rr.pad[1] = rr.pad[2] = 0;
+      if (jf) {
+        rr.kind = KIND_RESIDUAL;
+        rr.pos = jf;
+        int prev = (jf == 1) ? a.anchor[i] : x[jf - 2];
+        if (prev < 0 || prev >= V) { dspark_set_status(DSPARK_ERR_TOKEN); prev = 0; }
+        rr.prev = prev;
+        rr.lse_t = lse_t;
+        rr.lse_d = a.lse_d[(size_t)i * gamma + jf - 1];
+        a.list[atomicAdd(a.count, 1)] = i;  // compacted rejected rows (order irrelevant)
+      } else {
+        rr.kind = KIND_BONUS;
+        rr.pos = L + 1;
+        rr.prev = 0;
+        rr.lse_t = 0.f;
+        rr.lse_d = 0.f;
+      }
+      a.accepted[i] = jf ? jf - 1 : L;
+      a.rows[i] = rr;
     }
-    __shared__ float s_score[256 / 32][GUMBEL_BLOCK];
-    float *sc = s_score[(threadIdx.x >> 5)];
-    const bf16 *trow = target + ((size_t)i * (gamma + 1) + L) * V;
-    for (int e = lane; e < GUMBEL_BLOCK; e += 32) {
-      const int v = b * GUMBEL_BLOCK + e;
-      sc[e] = v < V ? __bfloat162float(trow[v]) * inv_tau : -INFINITY;
+    if (!jf) {  // warp-uniform: every draft passed, the bonus comes from row l_r + 1
+      // the winning block of the bonus row's block scores, then the ids inside
+      // it: t / tau + Gumbel(id, bonus stream) at position l_r + 1
+      float gb = -INFINITY;
+      int b = 0x7fffffff;
+      for (int g = 0; g < NSEG; ++g) {
+        const SegStat v = load(L * NSEG + g);
+        if (better(v.best, v.idx, gb, b)) { gb = v.best; b = v.idx; }
+      }
+      const int nb = (V + GUMBEL_BLOCK - 1) / GUMBEL_BLOCK;
+      if (!(gb > -INFINITY) || b >= nb) {  // non-finite target row
+        if (lane == 0) dspark_set_status(DSPARK_ERR_TOKEN);
+        b = 0;
+      }
+      __shared__ float s_score[GUMBEL_BLOCK];
+      const bf16 *trow = a.target + ((size_t)i * (gamma + 1) + L) * V;
+      for (int e = lane; e < GUMBEL_BLOCK; e += 32) {
+        const int v = b * GUMBEL_BLOCK + e;
+        s_score[e] = v < V ? __bfloat162float(trow[v]) * a.inv_tau : -INFINITY;
+      }
+      __syncwarp();
+      const int tok =
+          block_pick(s_score, b, V, a.seed, (uint32_t)(L + 1), (uint32_t)i, RNG_BONUS);
+      if (lane == 0) a.bonus[i] = tok >= 0 ? tok : b * GUMBEL_BLOCK;
     }
-    __syncwarp();
-    const int tok = block_pick(sc, b, V, seed, (uint32_t)(L + 1), (uint32_t)i, RNG_BONUS);
-    if (lane == 0) bonus[i] = tok >= 0 ? tok : b * GUMBEL_BLOCK;
   }
 }
 
-// Pass 5, the rows no trial settled: the block scores of the slices pick a block of 64 ids; inside
+// Pass 1: grid (NSEG * (gamma+1), R).  Greedy scans rows 1..l_r+1 (their
+// argmaxes decide acceptance and give the correction or bonus token); sampling
+// scans rows 1..l_r (their normalisers enter the acceptance test) and the
+// bonus row l_r + 1 (block scores: the bonus draw's first level, on the bonus
+// stream).  Each CTA then counts itself in for its request; the last of the
+// request's NSEG (l_r + 1) CTAs takes the request's decision (decide_request),
+// so the decision of one request overlaps the scans of the others and no CTA
+// ever waits for another.
+template <int MODE>
+__global__ void __launch_bounds__(256) verify_rows(const __grid_constant__ VerifyArgs a) {
+  const int j = blockIdx.x / NSEG, seg = blockIdx.x % NSEG, i = blockIdx.y;
+  const int gamma = a.gamma, V = a.V;
+  const float inv_tau = a.inv_tau;
+  pdl_trigger();
+  pdl_wait();  // len comes from the scheduler
+  const int L = clamp_len(a.len, i, gamma);
+  if (j > L) return;
+  SegStat *out = a.stat + ((size_t)i * (gamma + 1) + j) * NSEG + seg;
+  if (MODE == MODE_SAMPLE && j == L) {
+    bonus_blocks(a.target + ((size_t)i * (gamma + 1) + j) * V, V, seg, inv_tau, a.seed, j + 1,
+                 i, out);
+  } else {
+    const int sl = seg_len(V), v_beg = seg * sl, v_end = min(V, v_beg + sl);
+    const bf16 *row = a.target + ((size_t)i * (gamma + 1) + j) * V;
+    const uint4 *row4 = reinterpret_cast<const uint4 *>(row);
+    float m = -INFINITY, s = 0.f, best = -INFINITY, bs = 0.f;
+    int idx = 0x7fffffff;
+    const float c2 = inv_tau * 1.4426950408889634f;
+    auto consume = [&](const uint4 q, int c) {
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+      float vals[8];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        vals[2 * t] = bf16_lo(w[t]);
+        vals[2 * t + 1] = bf16_hi(w[t]);
+      }
+      if (MODE == MODE_GREEDY) {
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+          if (vals[t] > best) { best = vals[t]; idx = c * 8 + t; }  // ids increase per thread
+      } else {
+        float cm = vals[0];
+#pragma unroll
+        for (int t = 1; t < 8; ++t) cm = fmaxf(cm, vals[t]);
+        cm *= c2;  // log2 units
+        if (cm > m) { s *= ex2_fast(m - cm); m = cm; }
+#pragma unroll
+        for (int t = 0; t < 8; ++t) s += ex2_fast(vals[t] * c2 - m);
+      }
+    };
+    // eight independent 16-byte loads in flight per thread
+    const int c_end = v_end / 8, step = blockDim.x;
+    int c = v_beg / 8 + threadIdx.x;
+    for (; c + 7 * step < c_end; c += 8 * step) {
+      uint4 q[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) q[u] = __ldg(row4 + c + u * step);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) consume(q[u], c + u * step);
+    }
+    for (; c < c_end; c += step) consume(__ldg(row4 + c), c);
+    constexpr float LN2 = 0.6931471805599453f;
+    m = m > -INFINITY ? m * LN2 : m;  // back to natural units
+    warp_merge(m, s, best, idx, bs);
+    __shared__ float sm[8], ss[8], sb[8];
+    __shared__ int si[8];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) { sm[warp] = m; ss[warp] = s; sb[warp] = best; si[warp] = idx; }
+    __syncthreads();
+    if (warp == 0) {
+      const int nw = blockDim.x >> 5;
+      m = lane < nw ? sm[lane] : -INFINITY;
+      s = lane < nw ? ss[lane] : 0.f;
+      best = lane < nw ? sb[lane] : -INFINITY;
+      idx = lane < nw ? si[lane] : 0x7fffffff;
+      warp_merge(m, s, best, idx, bs);
+      if (lane == 0) {
+        SegStat st;
+        st.m = m; st.s = s; st.best = best; st.idx = idx;
+        *out = st;
+      }
+    }
+  }
+  // thread 0 wrote this CTA's statistics: it makes them visible, then counts
+  // the CTA in; the last of the request's CTAs decides
+  __shared__ int s_last;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(a.done + i, 1) == NSEG * (L + 1) - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();  // the other CTAs' statistics, read below through L2
+  decide_request<MODE>(a, i, L);
+}
+
+// Pass 4, the rows no trial settled: the block scores of the slices pick a block of 64 ids; inside
 // it the residual q = max(0, p_t - p_d) is rebuilt (target row, base logits and
 // the Markov bias W1[x_{j*-1}] . W2t[v]) and the corrected token is drawn from
 // log q + Gumbel.  A row whose residual came out empty is drawn from p_t
@@ -487,7 +522,7 @@ constexpr int TRIAL_WARPS = 32;  // trials in flight per row (one per warp)
 constexpr int TRIAL_THREADS = 32 * TRIAL_WARPS;
 constexpr int TRIAL_BLOCK = 4 * GUMBEL_BLOCK;  // ids per block of a proposal
 
-// Pass 3, one CTA per rejected row (compacted by verify_decide): the residual
+// Pass 2, one CTA per rejected row (compacted by the decisions of pass 1): the residual
 // norm(max(0, p_t - p_d)) by rejection from p_t.  The row's log-masses over
 // blocks of TRIAL_BLOCK ids go to lz once; then rounds of TRIAL_WARPS trials,
 // one per warp: trial q draws y_q ~ p_t in two levels (block by log Z_b +
@@ -506,7 +541,7 @@ __global__ void __launch_bounds__(TRIAL_THREADS) residual_trials(
     int *__restrict__ count_fb, bf16 *__restrict__ E_fb) {
   const int slot = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   pdl_trigger();
-  pdl_wait();  // the compacted rows of verify_decide
+  pdl_wait();  // the compacted rows of pass 1
   if (slot >= *count) return;
   const int req = list[slot];
   const ResampleRow rr = rows[req];
@@ -617,10 +652,11 @@ __global__ void __launch_bounds__(TRIAL_THREADS) residual_trials(
 struct VerifyWs {
   SegStat *stat;
   ResampleRow *rows;
-  int *list;
-  int *count;
-  int *list_fb;   // rows left to the explicit residual pass
-  int *count_fb;
+  int *done;      // [R] arrivals per request, then count and count_fb: zeroed per call
+  int *count;     // rejected requests
+  int *count_fb;  // of them, the rows left to the explicit residual pass
+  int *list;      // [R] the rejected requests
+  int *list_fb;   // [R] the explicit pass's rows
   float *lz;      // [R, V / 64 + V / 256] block log-masses of the rejected rows' target rows
   bf16 *E;
   RowPartial *part;
@@ -634,14 +670,14 @@ VerifyWs verify_layout(const dspark_dims *d, char *base) {
   off = dspark_align_up(off + sizeof(SegStat) * (size_t)d->R * (d->gamma + 1) * NSEG, 256);
   w.rows = (ResampleRow *)(base + off);
   off = dspark_align_up(off + sizeof(ResampleRow) * (size_t)d->R, 256);
+  w.done = (int *)(base + off);
+  w.count = w.done + d->R;
+  w.count_fb = w.done + d->R + 1;
+  off = dspark_align_up(off + sizeof(int) * ((size_t)d->R + 2), 256);
   w.list = (int *)(base + off);
   off = dspark_align_up(off + sizeof(int) * (size_t)d->R, 256);
-  w.count = (int *)(base + off);
-  off = dspark_align_up(off + sizeof(int), 256);
   w.list_fb = (int *)(base + off);
   off = dspark_align_up(off + sizeof(int) * (size_t)d->R, 256);
-  w.count_fb = (int *)(base + off);
-  off = dspark_align_up(off + sizeof(int), 256);
   w.lz = (float *)(base + off);
   const size_t nb = (size_t)(d->V + GUMBEL_BLOCK - 1) / GUMBEL_BLOCK;
   off = dspark_align_up(off + sizeof(float) * (size_t)d->R * (nb + (nb + 3) / 4), 256);
@@ -680,15 +716,17 @@ extern "C" int dspark_verify(const dspark_dims *dims, const int32_t *anchor, con
   const float inv_tau = sample ? 1.f / tau : 1.f;
   const dim3 rgrid(NSEG * (G + 1), R);
   const bf16 *tgt = (const bf16 *)target;
+  // the arrival counters and the residual-row counts start at zero
+  if (cudaMemsetAsync(ws.done, 0, sizeof(int) * ((size_t)R + 2), stream) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  VerifyArgs va{tgt, len, anchor, tokens, lse_d, logp_d, (const bf16 *)base_logits,
+                (const bf16 *)W1, (const bf16 *)W2t, ws.stat, ws.done, ws.count, ws.list, ws.rows,
+                accepted, bonus, R, G, V, r, inv_tau, seed};
   if (!sample) {
-    if (dspark_launch_pdl(verify_rows<MODE_GREEDY>, rgrid, dim3(256), 0, stream, tgt, len,
-                          ws.stat, ws.count, ws.count_fb, G, V, inv_tau, seed) != cudaSuccess ||
-        dspark_launch_pdl(verify_decide<MODE_GREEDY>, dim3((R * 32 + 255) / 256), dim3(256), 0,
-                          stream, ws.stat, tgt, anchor, tokens, len, lse_d, logp_d, ws.rows,
-                          ws.list, ws.count, accepted, bonus, R, G, V, inv_tau,
-                          seed) != cudaSuccess)
+    if (dspark_launch_pdl(verify_rows<MODE_GREEDY>, rgrid, dim3(256), 0, stream, va) !=
+        cudaSuccess)
       return DSPARK_ERR_CUDA;
-    dspark_count_launches(2);
+    dspark_count_launches(1);
     return DSPARK_OK;
   }
   // the block scores keep one segment's log-masses in shared memory
@@ -708,12 +746,8 @@ extern "C" int dspark_verify(const dspark_dims *dims, const int32_t *anchor, con
     return DSPARK_ERR_CUDA;
   // each kernel's launch and set-up overlap the tail of the one before
   // (programmatic serialisation; every kernel waits before touching memory)
-  if (dspark_launch_pdl(verify_rows<MODE_SAMPLE>, rgrid, dim3(256), lz, stream, tgt, len, ws.stat,
-                        ws.count, ws.count_fb, G, V, inv_tau, seed) != cudaSuccess ||
-      dspark_launch_pdl(verify_decide<MODE_SAMPLE>, dim3((R * 32 + 255) / 256), dim3(256), 0,
-                        stream, ws.stat, tgt, anchor, tokens, len, lse_d, logp_d, ws.rows,
-                        ws.list, ws.count, accepted, bonus, R, G, V, inv_tau,
-                        seed) != cudaSuccess ||
+  if (dspark_launch_pdl(verify_rows<MODE_SAMPLE>, rgrid, dim3(256), lz, stream, va) !=
+          cudaSuccess ||
       dspark_launch_pdl(residual_trials, dim3(R), dim3(TRIAL_THREADS), 0, stream, ws.rows,
                         (const int *)ws.list, (const int *)ws.count, (const bf16 *)base_logits,
                         tgt, (const bf16 *)W1, (const bf16 *)W2t, ws.lz, G, V, r, inv_tau, seed,
@@ -733,7 +767,7 @@ extern "C" int dspark_verify(const dspark_dims *dims, const int32_t *anchor, con
                         (const bf16 *)ws.E, (const bf16 *)W2t, G, V, r, inv_tau, seed,
                         bonus) != cudaSuccess)
     return DSPARK_ERR_CUDA;
-  dspark_count_launches(4);  // + the GEMM, counted by launch()
+  dspark_count_launches(3);  // + the GEMM, counted by launch()
   return DSPARK_OK;
 }
 
