@@ -41,7 +41,8 @@
  *   - Random draws use Philox4x32-10 keyed by (seed) with counter
  *     (v >> 2, position, request, stream), word v & 3, u = ((w >> 9) + 0.5) 2^-23;
  *     streams: 0 draft Gumbel, 1 accept uniform, 2 residual Gumbel, 3 bonus Gumbel;
- *     residual trial q: 16 + 8q Gumbel, 16 + 8q + 1 uniform.
+ *     residual trial q: 16 + 8q id Gumbel, 20 + 8q block Gumbel, 21 + 8q
+ *     super-block Gumbel, 17 + 8q uniform.
  *
  * Departures from the planned boundary (draft / schedule / verify / status):
  *   - W2 enters once, through dspark_pack_w2, as W2t [V, r]; every later call
@@ -287,8 +288,10 @@ size_t dspark_verify_workspace_bytes(const dspark_dims *dims);
  *             and 7).  p = softmax(logits / tau).  Each draw is the two-level
  *             Gumbel-max of dspark_markov_draft (entry stream s, block stream
  *             s + 4).  The residual is drawn by rejection from p_t: trial
- *             q = 0, 1, .. proposes y ~ p_t (streams 16 + 8q and 20 + 8q) and
- *             keeps it iff u_q < 1 - p_d(y) / p_t(y), u_q = U(stream 17 + 8q);
+ *             q = 0, 1, .. proposes y ~ p_t by Gumbel-max in three levels
+ *             (super-blocks of 1024 ids on stream 21 + 8q, their 64-id blocks
+ *             on 20 + 8q, ids on 16 + 8q) and keeps it iff
+ *             u_q < 1 - p_d(y) / p_t(y), u_q = U(stream 17 + 8q);
  *             the first kept proposal is the token.  After 64 unkept trials the
  *             residual is formed over the whole row and drawn on streams 2 and
  *             6; a residual that is empty in floating point is replaced by p_t

@@ -47,8 +47,10 @@ Readings where the pages are silent (each listed in the design notes):
     rejection method with envelope p_t, whose ratio max(0, p_t - p_d) / p_t is
     at most 1).  The first kept of RESIDUAL_TRIALS trials is the token; when
     none is kept, the residual is formed explicitly and drawn by Gumbel-max.
-    A proposal is the two-level draw with blocks of four sampler blocks
-    (256 ids), so its first level needs a quarter of the random words.
+    A proposal is a three-level Gumbel-max draw (gumbel_max_trial): over
+    super-blocks of 16 sampler blocks (1024 ids), over the sampler blocks of
+    the winning super-block, then over the ids of the winning block, so a
+    trial needs a few hundred random words rather than one per block.
 """
 from __future__ import annotations
 
@@ -122,7 +124,7 @@ def _block_logsumexp(x: np.ndarray) -> np.ndarray:
 
 GUMBEL_BLOCK = 64
 RESIDUAL_TRIALS = 64   # proposals from p_t per rejected row before the explicit residual
-TRIAL_BLOCKS = 4       # sampler blocks per block of a trial proposal
+TRIAL_SUPER = 16       # sampler blocks per first-level block of a trial proposal
 
 
 def gumbel_max(score, seed: int, position, request, stream: int,
@@ -180,6 +182,55 @@ def gumbel_max(score, seed: int, position, request, stream: int,
         m_i = top2_margin(gi) if gi.size > 1 else np.inf
         margin[n] = min(m_b, m_i)
     return dict(token=token, margin=margin, block_scores=G, entry_scores=e)
+
+
+def gumbel_max_trial(score, seed: int, position: int, request: int, stream: int,
+                     block: int = GUMBEL_BLOCK, sup: int = TRIAL_SUPER) -> Dict[str, float]:
+    """One draw from softmax(score) (score [V] float64 log-weights) in three levels:
+
+      1. super-blocks of sup * block consecutive ids: S* = argmax_S log Z_S + g_S,
+         g_S the Gumbel of super-block id S in stream `stream + 5`;
+      2. blocks of `block` ids inside S*: b* = argmax_b log Z_b + g_b, g_b the
+         Gumbel of block id b (numbered over the whole vocabulary) in stream
+         `stream + 4`;
+      3. ids inside b*: argmax_v score_v + g_v, g_v the Gumbel of id v in stream
+         `stream`.
+    Lowest index on ties; parts of zero mass never win.  Max-stability makes
+    each level pick its part with probability proportional to its mass given the
+    level above, so the token has probability softmax(score)_v (the top-down
+    construction of gumbel_max, one level deeper).  Returns token (-1 when every
+    entry is -inf) and margin (the smallest of the three levels' top-2 gaps).
+    """
+    score = to_f64(score).reshape(-1)
+    V = score.size
+    nb = (V + block - 1) // block
+    ns = (nb + sup - 1) // sup
+    padded = np.full(ns * sup * block, -np.inf)
+    padded[:V] = score
+    lz_b = _block_logsumexp(padded.reshape(ns * sup, block))          # [ns * sup]
+    lz_s = _block_logsumexp(lz_b.reshape(ns, sup))                     # [ns]
+    out = dict(token=-1, margin=np.inf)
+
+    def pick(vals, ids, st):
+        g = philox.gumbel(seed, position, request, st, np.asarray(ids, dtype=np.uint64))
+        e = vals + g
+        fin = np.isfinite(vals)
+        if not np.any(fin):
+            return -1, np.inf
+        k = int(np.argmax(np.where(fin, e, -np.inf)))
+        ef = e[fin]
+        return int(ids[k]), (top2_margin(ef) if ef.size > 1 else np.inf)
+
+    S, m1 = pick(lz_s, np.arange(ns), stream + 5)
+    if S < 0:
+        return out
+    bs = np.arange(S * sup, min(nb, S * sup + sup))
+    b, m2 = pick(lz_b[bs], bs, stream + 4)
+    vs = np.arange(b * block, min(V, b * block + block))
+    v, m3 = pick(score[vs], vs, stream)
+    out["token"] = v
+    out["margin"] = min(m1, m2, m3)
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -626,14 +677,14 @@ def verify(tokens, lens, draft_logits, target, tau: float, seed: int,
             margin = np.inf
             for q in range(RESIDUAL_TRIALS):
                 s = philox.STREAM_TRIAL0 + 8 * q
-                prop = gumbel_max(lt, seed, j, rq, s, TRIAL_BLOCKS * block)
-                y = int(prop["token"][0])
+                prop = gumbel_max_trial(lt, seed, j, rq, s, block, TRIAL_SUPER)
+                y = int(prop["token"])
                 if y < 0:                                # no finite target entry
                     break
                 trials[i] += 1
                 uq = float(philox.uniform(seed, j, rq, s + 1, 0))
                 keep = 1.0 - p_d[y] / p_t[y] - uq if p_t[y] > 0.0 else -np.inf
-                margin = min(margin, prop["margin"][0], abs(keep))
+                margin = min(margin, prop["margin"], abs(keep))
                 if keep > 0.0:
                     bonus[i] = y
                     final_kind[i] = 4

@@ -21,7 +21,8 @@ Streams: 0 draft Gumbel, 1 accept uniform (v = 0), 2 residual Gumbel, 3 bonus Gu
 the block-level Gumbels of a draw in stream s use stream s + 4 (4 draft,
 6 residual, 7 bonus; v = the block index; see oracle.dspark.gumbel_max).
 Residual trial q (q = 0, 1, ...; see oracle.dspark.verify) uses stream 16 + 8q
-for its proposal's Gumbels (16 + 8q + 4 at the block level) and 16 + 8q + 1
+for its proposal's id Gumbels, 16 + 8q + 4 for its block Gumbels, 16 + 8q + 5
+for its super-block Gumbels (oracle.dspark.gumbel_max_trial) and 16 + 8q + 1
 for its acceptance uniform (v = 0).
 """
 from __future__ import annotations
@@ -39,7 +40,7 @@ STREAM_ACCEPT = 1
 STREAM_RESIDUAL = 2
 STREAM_BONUS = 3
 BLOCK_STREAM_OFFSET = 4   # block-level draws of stream s use stream s + 4
-STREAM_TRIAL0 = 16        # residual trial q: streams 16 + 8q (+1 uniform, +4 block level)
+STREAM_TRIAL0 = 16        # residual trial q: streams 16 + 8q (+1 uniform, +4 blocks, +5 super-blocks)
 
 
 def philox4x32_10(c0, c1, c2, c3, k0: int, k1: int):

@@ -136,9 +136,10 @@ struct PhiloxKeys {
 // law makes this an exact sample (Maddison, Tarlow, Minka, "A* Sampling",
 // NIPS 2014, top-down Gumbel processes).
 // The residual's rejection trial q draws its proposal on stream RNG_TRIAL0 + 8q
-// (block level + RNG_BLOCK_OFFSET) and its acceptance uniform on RNG_TRIAL0 + 8q + 1.
+// (ids; sampler blocks + RNG_BLOCK_OFFSET, super-blocks + RNG_SUPER_OFFSET) and
+// its acceptance uniform on RNG_TRIAL0 + 8q + 1.
 enum { RNG_DRAFT = 0, RNG_ACCEPT = 1, RNG_RESIDUAL = 2, RNG_BONUS = 3, RNG_BLOCK_OFFSET = 4,
-       RNG_TRIAL0 = 16 };
+       RNG_SUPER_OFFSET = 5, RNG_TRIAL0 = 16 };
 constexpr int GUMBEL_BLOCK = 64;
 
 // The four words for vocabulary slots 4*q .. 4*q+3 at (position, request, stream).

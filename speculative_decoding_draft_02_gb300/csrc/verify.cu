@@ -520,13 +520,15 @@ __global__ void __launch_bounds__(256) resample_reduce(
 constexpr int RESIDUAL_TRIALS = 64;
 constexpr int TRIAL_WARPS = 32;  // trials in flight per row (one per warp)
 constexpr int TRIAL_THREADS = 32 * TRIAL_WARPS;
-constexpr int TRIAL_BLOCK = 4 * GUMBEL_BLOCK;  // ids per block of a proposal
+constexpr int TRIAL_SUPER = 16;  // sampler blocks per first-level block of a proposal
 
-// Pass 2, one CTA per rejected row (compacted by the decisions of pass 1): the residual
-// norm(max(0, p_t - p_d)) by rejection from p_t.  The row's log-masses over
-// blocks of TRIAL_BLOCK ids go to lz once; then rounds of TRIAL_WARPS trials,
-// one per warp: trial q draws y_q ~ p_t in two levels (block by log Z_b +
-// Gumbel(b) on stream RNG_TRIAL0 + 8q + RNG_BLOCK_OFFSET, id inside it by
+// Pass 2, one CTA per rejected row (compacted by the decisions of pass 1): the
+// residual norm(max(0, p_t - p_d)) by rejection from p_t.  The row's
+// log-masses over sampler blocks and over super-blocks of TRIAL_SUPER of them
+// go to lz once; then rounds of TRIAL_WARPS trials, one per warp: trial q
+// draws y_q ~ p_t in three levels (super-block by log Z_S + Gumbel(S) on
+// stream RNG_TRIAL0 + 8q + RNG_SUPER_OFFSET, sampler block inside it by
+// log Z_b + Gumbel(b) on RNG_TRIAL0 + 8q + RNG_BLOCK_OFFSET, id inside that by
 // t_v / tau + Gumbel(v) on RNG_TRIAL0 + 8q) and keeps it iff
 // u_q < 1 - p_d(y_q) / p_t(y_q), u_q on RNG_TRIAL0 + 8q + 1, where p_d(y)
 // needs only the base logit, W1[x_{j*-1}] . W2t[y] and lse_d.  The first kept
@@ -546,67 +548,76 @@ __global__ void __launch_bounds__(TRIAL_THREADS) residual_trials(
   const int req = list[slot];
   const ResampleRow rr = rows[req];
   const int nb = (V + GUMBEL_BLOCK - 1) / GUMBEL_BLOCK;
-  const int nq = (V + TRIAL_BLOCK - 1) / TRIAL_BLOCK;
+  const int ns = (nb + TRIAL_SUPER - 1) / TRIAL_SUPER;
   const uint32_t pos = (uint32_t)rr.pos;
   const bf16 *trow = target + ((size_t)req * (gamma + 1) + rr.pos - 1) * V;
   const bf16 *brow = base + ((size_t)req * gamma + rr.pos - 1) * V;
   const uint4 *e4 = reinterpret_cast<const uint4 *>(W1 + (size_t)rr.prev * r);
-  // the log-masses of the sampler blocks, then of blocks of four of them
-  float *lz64 = lz + (size_t)slot * (nb + nq), *lz256 = lz64 + nb;
+  // the log-masses of the sampler blocks, then of super-blocks of TRIAL_SUPER of them
+  float *lz64 = lz + (size_t)slot * (nb + ns), *lzs = lz64 + nb;
   block_lz<TRIAL_THREADS>(trow, V, 0, nb, inv_tau, lz64);  // ends with a CTA barrier
-  for (int c = tid; c < nq; c += TRIAL_THREADS) {
+  for (int c = tid; c < ns; c += TRIAL_THREADS) {
+    const int t1 = min(nb, TRIAL_SUPER * c + TRIAL_SUPER);
     float m = -INFINITY;
-    for (int t = 4 * c; t < 4 * c + 4 && t < nb; ++t) m = fmaxf(m, lz64[t]);
+    for (int t = TRIAL_SUPER * c; t < t1; ++t) m = fmaxf(m, lz64[t]);
     float sm = 0.f;
     if (m > -INFINITY)
-      for (int t = 4 * c; t < 4 * c + 4 && t < nb; ++t) sm += expf(lz64[t] - m);
-    lz256[c] = m > -INFINITY ? m + logf(sm) : -INFINITY;
+      for (int t = TRIAL_SUPER * c; t < t1; ++t) sm += expf(lz64[t] - m);
+    lzs[c] = m > -INFINITY ? m + logf(sm) : -INFINITY;
   }
   __syncthreads();
   __shared__ int s_kept[TRIAL_WARPS];
   int tok = -1;
   for (int q0 = 0; q0 < RESIDUAL_TRIALS; q0 += TRIAL_WARPS) {  // CTA-uniform trip count
     const uint32_t st = RNG_TRIAL0 + 8u * (uint32_t)(q0 + warp);
-    // y ~ p_t, first level: the best block score over the row
+    // y ~ p_t in three levels; first, the super-block
     float best = -INFINITY;
-    int b = 0x7fffffff;
-    for (int q4 = lane; 4 * q4 < nq; q4 += 32) {
-      const uint4 g4 = rng_words4(seed, (uint32_t)q4, pos, (uint32_t)req, st + RNG_BLOCK_OFFSET);
+    int sb = 0x7fffffff;
+    for (int q4 = lane; 4 * q4 < ns; q4 += 32) {
+      const uint4 g4 = rng_words4(seed, (uint32_t)q4, pos, (uint32_t)req, st + RNG_SUPER_OFFSET);
       const uint32_t ws[4] = {g4.x, g4.y, g4.z, g4.w};
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
-        const int bb = 4 * q4 + t;
-        const float l = bb < nq ? lz256[bb] : -INFINITY;
+        const int S = 4 * q4 + t;
+        const float l = S < ns ? lzs[S] : -INFINITY;
         if (l > -INFINITY) {
           const float G = l + rng_gumbel(ws[t]);
-          if (better(G, bb, best, b)) { best = G; b = bb; }
+          if (better(G, S, best, sb)) { best = G; sb = S; }
         }
       }
     }
-    block_best_reduce(best, b);
+    block_best_reduce(best, sb);
     int y = -1;
-    if (best > -INFINITY) {  // warp-uniform: second level, eight ids of block b per lane
-      const int v0 = b * TRIAL_BLOCK + 8 * lane;
-      float e = -INFINITY;
-      int id = 0x7fffffff;
-      if (v0 < V) {  // V % 8 == 0: the eight ids are all inside or all past V
-        const uint4 w = __ldg(reinterpret_cast<const uint4 *>(trow + v0));
-        const uint4 ga = rng_words4(seed, (uint32_t)(v0 >> 2), pos, (uint32_t)req, st);
-        const uint4 gb = rng_words4(seed, (uint32_t)(v0 >> 2) + 1u, pos, (uint32_t)req, st);
-        const uint32_t tw[4] = {w.x, w.y, w.z, w.w};
-        const uint32_t gw[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const float tv = (t & 1) ? bf16_hi(tw[t >> 1]) : bf16_lo(tw[t >> 1]);
-          const float sc = tv * inv_tau;
-          if (sc > -INFINITY) {
-            const float ev = sc + rng_gumbel(gw[t]);
-            if (better(ev, v0 + t, e, id)) { e = ev; id = v0 + t; }
+    if (best > -INFINITY) {  // warp-uniform
+      // the sampler block inside super-block sb: one per lane
+      const int b = sb * TRIAL_SUPER + lane;
+      const float l = (lane < TRIAL_SUPER && b < nb) ? lz64[b] : -INFINITY;
+      float e2 = -INFINITY;
+      int b2 = 0x7fffffff;
+      if (l > -INFINITY) {
+        const uint4 g4 = rng_words4(seed, (uint32_t)(b >> 2), pos, (uint32_t)req,
+                                    st + RNG_BLOCK_OFFSET);
+        e2 = l + rng_gumbel(uint4_get(g4, b & 3));
+        b2 = b;
+      }
+      block_best_reduce(e2, b2);
+      if (e2 > -INFINITY) {  // warp-uniform: the ids of block b2, two per lane
+        const int v = b2 * GUMBEL_BLOCK + 2 * lane;
+        float e3 = -INFINITY;
+        int id = 0x7fffffff;
+        if (v < V) {  // V is even: both ids inside
+          const uint32_t w = __ldg(reinterpret_cast<const uint32_t *>(trow + v));
+          const uint4 g4 = rng_words4(seed, (uint32_t)(v >> 2), pos, (uint32_t)req, st);
+          const float s0 = bf16_lo(w) * inv_tau, s1 = bf16_hi(w) * inv_tau;
+          if (s0 > -INFINITY) { e3 = s0 + rng_gumbel(uint4_get(g4, v & 3)); id = v; }
+          if (s1 > -INFINITY) {
+            const float ev = s1 + rng_gumbel(uint4_get(g4, (v & 3) + 1));
+            if (better(ev, v + 1, e3, id)) { e3 = ev; id = v + 1; }
           }
         }
+        block_best_reduce(e3, id);
+        y = e3 > -INFINITY ? id : -1;
       }
-      block_best_reduce(e, id);
-      y = e > -INFINITY ? id : -1;
     }
     int kept = -1;
     if (y >= 0) {  // warp-uniform: the acceptance test, p_d(y) / p_t(y) in logs
@@ -657,7 +668,7 @@ struct VerifyWs {
   int *count_fb;  // of them, the rows left to the explicit residual pass
   int *list;      // [R] the rejected requests
   int *list_fb;   // [R] the explicit pass's rows
-  float *lz;      // [R, V / 64 + V / 256] block log-masses of the rejected rows' target rows
+  float *lz;      // [R, V / 64 + V / 1024] log-masses of the rejected rows' target rows
   bf16 *E;
   RowPartial *part;
   size_t bytes;
@@ -680,7 +691,8 @@ VerifyWs verify_layout(const dspark_dims *d, char *base) {
   off = dspark_align_up(off + sizeof(int) * (size_t)d->R, 256);
   w.lz = (float *)(base + off);
   const size_t nb = (size_t)(d->V + GUMBEL_BLOCK - 1) / GUMBEL_BLOCK;
-  off = dspark_align_up(off + sizeof(float) * (size_t)d->R * (nb + (nb + 3) / 4), 256);
+  off = dspark_align_up(
+      off + sizeof(float) * (size_t)d->R * (nb + (nb + TRIAL_SUPER - 1) / TRIAL_SUPER), 256);
   w.E = (bf16 *)(base + off);
   off = dspark_align_up(off + sizeof(bf16) * (size_t)d->R * d->r, 256);
   w.part = (RowPartial *)(base + off);

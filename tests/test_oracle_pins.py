@@ -672,10 +672,31 @@ def _one_position_verify(ld, lt, N, seed, block=64):
     return res, pd, pt
 
 
-def test_residual_draw_follows_the_residual_law():
+@pytest.mark.parametrize("block,sup", [(1, 4), (2, 4)])
+def test_three_level_trial_draw_follows_softmax(block, sup):
+    """The residual trials' proposal (super-blocks, blocks, ids) samples
+    softmax(score): V = 42 with ragged super-blocks and blocks and three ids at
+    -inf, which never come up."""
+    V, N = 42, 15000
+    rng = np.random.default_rng(61)
+    score = rng.standard_normal(V) * 1.1
+    score[[3, 17, 41]] = -np.inf
+    toks = np.array([oracle.dspark.gumbel_max_trial(score, 11, 2, n, 16, block, sup)["token"]
+                     for n in range(N)])
+    counts = np.bincount(toks, minlength=V)
+    p = np.exp(score - oracle.dspark.logsumexp(score))
+    assert counts[[3, 17, 41]].sum() == 0
+    keep = p > 0
+    assert stats.chisquare(counts[keep], N * p[keep]).pvalue > 1e-4
+
+
+@pytest.mark.parametrize("sup", [16, 1])
+def test_residual_draw_follows_the_residual_law(monkeypatch, sup):
     """On rejection the corrected token follows norm(max(0, p_t - p_d)) (the
     residual of speculative sampling), with the sampler's blocks of 3 ids over
-    V = 7 (both levels and a ragged block), and the draws come from the trials."""
+    V = 7 (a ragged block; with super-blocks of one block, three of them), and
+    the draws come from the trials."""
+    monkeypatch.setattr(oracle.dspark, "TRIAL_SUPER", sup)
     ld = np.array([1.1, -0.3, 0.4, 2.0, -1.2, 0.0, 0.7])
     lt = np.array([0.2, 0.9, -0.5, 1.0, 0.3, 1.4, -0.8])
     res, pd, pt = _one_position_verify(ld, lt, 20000, 31, block=3)
