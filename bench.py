@@ -439,6 +439,7 @@ def run_dspark(args, w, ws, rank, local):
         vbytes += int((~rejected).sum()) * row          # bonus row of the rest
         # (each trial's 256 target ids, W2t row and base logit, ~1.5 KB, not counted)
     else:
+        n_rej = n_expl = 0
         vbytes = int((ln + 1).sum()) * row             # rows 1..l_r + 1: argmaxes
     verify_gbs = vbytes / (stage["verify"] * 1e-3) / 1e9
 
@@ -459,7 +460,9 @@ def run_dspark(args, w, ws, rank, local):
         "markov_loop_hbm": {"achieved": markov_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                             "frac": markov_gbs / peaks["hbm_gbs"]},
         "verify_hbm": {"bytes": vbytes, "achieved": verify_gbs, "peak": peaks["hbm_gbs"],
-                       "unit": "GB/s", "frac": verify_gbs / peaks["hbm_gbs"]},
+                       "unit": "GB/s", "frac": verify_gbs / peaks["hbm_gbs"],
+                       **({"rejected_rows": n_rej, "explicit_rows": n_expl} if w.tau > 0
+                          else {})},
         "gpu_launches": launches,
         "clocks": clk,
     }
