@@ -7,6 +7,7 @@ mistake (dropped term, wrong sign or index, transposed operand) fails here.
 import itertools
 import math
 import os
+import zlib
 
 import numpy as np
 import pytest
@@ -842,7 +843,7 @@ def _markov_target_rounds(mode, V=6, G=3, N=30000, L=3, seed=0, block=2):
 def test_draft_schedule_verify_is_lossless(mode):
     """Chi-square: emitted tokens follow the target chain in non-anticipating modes."""
     V, L = 6, 3
-    first, joint = _markov_target_rounds(mode, V=V, L=L, N=24000, seed=hash(mode) % 1000)
+    first, joint = _markov_target_rounds(mode, V=V, L=L, N=16000, seed=zlib.crc32(mode.encode()) % 1000)
     cells = np.ravel_multi_index(first.T, [V] * L)
     counts = np.bincount(cells, minlength=V ** L)
     exp = joint.reshape(-1) * first.shape[0]
