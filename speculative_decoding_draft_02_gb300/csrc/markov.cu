@@ -206,6 +206,9 @@ __global__ void __launch_bounds__(RP_THREADS) reduce_prep(
   }
 }
 
+// Row blocks (of 128 requests) from which the greedy loop keeps E resident.
+constexpr int ERES_MIN_ROW_BLOCKS = 4;
+
 struct MarkovWs {
   float *zh;
   bf16 *E;
@@ -267,6 +270,10 @@ extern "C" int dspark_markov_draft(const dspark_dims *dims, const void *base_log
     constexpr int EW = mloop::LoopCfg<MODE_SAMPLE>::EPI_WARPS;
     const mloop::LoopGrid lg = mloop::loop_grid<MODE_SAMPLE>(R, V, sms);
     la.n_slots = lg.n_slots;
+    const int num_m = (R + gemm::BM - 1) / gemm::BM;
+    if (num_m >= ERES_MIN_ROW_BLOCKS && lg.grid >= num_m && lg.grid % num_m == 0 &&
+        r <= mloop::ERES_KB * gemm::BK && R > lg.grid * (EW / 4))
+      return mloop::launch_loop<MODE_SAMPLE, 2, true>(la, lg.grid, stream);
     // warps per request in the row phase: as many as still cover R in one pass
     if (R <= lg.grid) return mloop::launch_loop<MODE_SAMPLE, EW>(la, lg.grid, stream);
     if (R <= lg.grid * 2) return mloop::launch_loop<MODE_SAMPLE, EW / 2>(la, lg.grid, stream);
@@ -276,6 +283,15 @@ extern "C" int dspark_markov_draft(const dspark_dims *dims, const void *base_log
   constexpr int EW = mloop::LoopCfg<MODE_GREEDY>::EPI_WARPS;
   const mloop::LoopGrid lg = mloop::loop_grid<MODE_GREEDY>(R, V, sms);
   la.n_slots = lg.n_slots;
+  // resident E for batches of several row blocks: every W2t tile then serves
+  // several CTAs from L2, and the tiles' E re-reads were a third of the pass's
+  // L2 traffic (each CTA stays on one row block, and E fits up to r = 512)
+  // (at four row blocks or more R exceeds two requests per CTA, so the row
+  // phase takes one warp per request)
+  const int num_m = (R + gemm::BM - 1) / gemm::BM;
+  if (num_m >= ERES_MIN_ROW_BLOCKS && lg.grid >= num_m && lg.grid % num_m == 0 &&
+      r <= mloop::ERES_KB * gemm::BK)
+    return mloop::launch_loop<MODE_GREEDY, 1, true>(la, lg.grid, stream);
   if (R <= lg.grid * (EW / 4)) return mloop::launch_loop<MODE_GREEDY, 4>(la, lg.grid, stream);
   return mloop::launch_loop<MODE_GREEDY, 1>(la, lg.grid, stream);
 }

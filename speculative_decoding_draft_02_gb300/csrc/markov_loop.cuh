@@ -94,19 +94,30 @@ struct LoopCtl {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t go;     // the grid barrier after a row phase has passed: E may be loaded
+  uint64_t efull;  // resident-E form: the step's E tile has landed
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
 };
 
-// Shared scratch of one row group.
-template <int RW>
+// Shared scratch of one row group (NS: room for a rebuilt block's logits,
+// which only sampling needs).
+template <int RW, int NS>
 struct RowScratch {
-  float score[GUMBEL_BLOCK];  // the winning block's logits, then logits / tau
+  float score[NS];  // the winning block's logits, then logits / tau
   float m[RW], s[RW], b[RW], dot[RW];
   int i[RW];
   int tok;
 };
+template <int MODE, int RW>
+using Scratch = RowScratch<RW, MODE == MODE_SAMPLE ? GUMBEL_BLOCK : 1>;
+
+// Resident-E form of the loop (many row blocks): each CTA keeps its row block's
+// E (r / 64 k blocks of 128 x 64, up to r = 512) in shared memory for the whole
+// step, and only W2t streams through a ring of ERES_STAGES stages.  A greedy
+// 128 x 256 tile then moves 256 KB from L2 instead of 384 KB.
+constexpr int ERES_KB = 8;
+constexpr int ERES_STAGES = 3;
 
 // Bring `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2.
 __device__ __forceinline__ void bulk_prefetch_l2(const void *p, uint32_t bytes) {
@@ -394,10 +405,10 @@ __device__ __forceinline__ void hidden_dots(const LoopArgs &a, int p, int gw, in
 // position p + 1's pass) and c = sigmoid((w_h . h[i, p] + w_e . W1[prev]) / T[p]),
 // "DSpark 深度解读" §二 设计二; zh_part is this thread's part of w_h . h[i, p].
 // Called by the RT threads of a row group.
-template <int RW>
+template <int RW, class Scr>
 __device__ __forceinline__ void embed_conf(const LoopArgs &a, int i, int p, int prev,
-                                           float zh_part, RowScratch<RW> &S, int wg, int lane,
-                                           int tg, int group_bar) {
+                                           float zh_part, Scr &S, int wg, int lane, int tg,
+                                           int group_bar) {
   constexpr int RT = 32 * RW;
   const int r = a.r;
   if (prev < 0 || prev >= a.V) {
@@ -429,7 +440,7 @@ __device__ __forceinline__ void embed_conf(const LoopArgs &a, int i, int p, int 
 // Row phase of step k for one group of RW epilogue warps (group g of the CTA,
 // `groups` groups in the grid).  See the file comment.
 template <int MODE, int RW, int EPI_WARPS>
-__device__ void row_phase(const LoopArgs &a, int k, RowScratch<RW> &S, int g, int wg, int lane,
+__device__ void row_phase(const LoopArgs &a, int k, Scratch<MODE, RW> &S, int g, int wg, int lane,
                           int groups) {
   constexpr int RT = 32 * RW;
   const int tg = wg * 32 + lane;
@@ -529,9 +540,8 @@ __device__ void row_phase(const LoopArgs &a, int k, RowScratch<RW> &S, int g, in
 // Registers are split over the SM's four quadrants (16384 each): 18 warps
 // (sampling) leave 96 per thread, 10 warps (greedy) 168.
 // Before step 1: E[i] = W1[anchor_i] and c_1 for the group's requests.
-template <int RW, int EPI_WARPS>
-__device__ void prologue_rows(const LoopArgs &a, RowScratch<RW> &S, int g, int wg, int lane,
-                              int groups) {
+template <int RW, int EPI_WARPS, class Scr>
+__device__ void prologue_rows(const LoopArgs &a, Scr &S, int g, int wg, int lane, int groups) {
   const int tg = wg * 32 + lane;
   for (int i = blockIdx.x * (EPI_WARPS / RW) + g; i < a.R; i += groups) {
     embed_conf<RW>(a, i, 0, a.anchor[i], hidden_dot_part<RW>(a, i, 0, tg), S, wg, lane, tg,
@@ -541,7 +551,20 @@ __device__ void prologue_rows(const LoopArgs &a, RowScratch<RW> &S, int g, int w
   }
 }
 
-template <int MODE, int RW>
+// Shared-memory geometry of a loop kernel: the A region (ring stages, or the
+// resident E), the W2t stages, then the barriers and the row groups' scratch.
+template <int MODE, int RW, bool ERES>
+struct LoopSmem {
+  using G = gemm::Geo<LoopCfg<MODE>::BN>;
+  static constexpr int NSTAGE = ERES ? ERES_STAGES : G::STAGES;
+  static constexpr size_t A_REGION = (size_t)(ERES ? ERES_KB : NSTAGE) * A_BYTES;
+  static constexpr size_t B_REGION = (size_t)NSTAGE * G::B_BYTES;
+  static constexpr size_t CTL = A_REGION + B_REGION;
+  static constexpr size_t BYTES = 1024 + CTL + 512 +
+                                  sizeof(Scratch<MODE, RW>) * (LoopCfg<MODE>::EPI_WARPS / RW);
+};
+
+template <int MODE, int RW, bool ERES>
 __global__ void __launch_bounds__(64 + 32 * LoopCfg<MODE>::EPI_WARPS, 1) markov_loop_kernel(const __grid_constant__ CUtensorMap tma_a,
                        const __grid_constant__ CUtensorMap tma_b, const __grid_constant__ LoopArgs a) {
   constexpr int EPI_WARPS = LoopCfg<MODE>::EPI_WARPS;
@@ -550,17 +573,20 @@ __global__ void __launch_bounds__(64 + 32 * LoopCfg<MODE>::EPI_WARPS, 1) markov_
   constexpr int SLICE = LoopCfg<MODE>::SLICE;
   constexpr int RG = EPI_WARPS / RW;  // row groups per CTA
   using G = gemm::Geo<LoopCfg<MODE>::BN>;
-  constexpr int BN = G::BN, STAGES = G::STAGES, B_BYTES = G::B_BYTES;
+  using L = LoopSmem<MODE, RW, ERES>;
+  constexpr int BN = G::BN, STAGES = L::NSTAGE, B_BYTES = G::B_BYTES;
   constexpr int STAGE_BYTES = G::STAGE_BYTES;
   constexpr uint32_t TMEM_COLS = G::TMEM_COLS;
   static_assert(EPI_WARPS % RW == 0, "row groups split the epilogue warps");
+  static_assert(sizeof(LoopCtl<STAGES>) <= 512, "barrier block");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sbase = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *sA = sbase;
-  uint8_t *sB = sbase + STAGES * A_BYTES;
-  LoopCtl<STAGES> *ctl = reinterpret_cast<LoopCtl<STAGES> *>(sbase + STAGES * STAGE_BYTES);
-  RowScratch<RW> *scr = reinterpret_cast<RowScratch<RW> *>(sbase + STAGES * STAGE_BYTES + 512);
+  uint8_t *sA = sbase;  // ring: stage s at s * A_BYTES; resident E: k block kb at kb * A_BYTES
+  uint8_t *sB = sbase + L::A_REGION;
+  LoopCtl<STAGES> *ctl = reinterpret_cast<LoopCtl<STAGES> *>(sbase + L::CTL);
+  using Scr = Scratch<MODE, RW>;
+  Scr *scr = reinterpret_cast<Scr *>(sbase + L::CTL + 512);
   volatile int *abort = &ctl->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -574,6 +600,7 @@ __global__ void __launch_bounds__(64 + 32 * LoopCfg<MODE>::EPI_WARPS, 1) markov_
       tc::mbar_init(&ctl->tempty[b], EPI_WARPS);
     }
     tc::mbar_init(&ctl->go, 1);
+    tc::mbar_init(&ctl->efull, 1);
     tc::mbar_init(&ctl->drain, 1);
     ctl->abort = 0;
     tc::fence_barrier_init();
@@ -605,6 +632,8 @@ __global__ void __launch_bounds__(64 + 32 * LoopCfg<MODE>::EPI_WARPS, 1) markov_
       uint32_t phase = 0;
       int issued[STAGES];
       for (int s = 0; s < STAGES; ++s) issued[s] = -1;
+      int e_issued = -1;  // resident E: parity of the last E load armed
+      constexpr uint32_t FULL_BYTES = ERES ? B_BYTES : STAGE_BYTES;
       bool ok = true;
       for (int k = 1; ok && k <= gamma; ++k) {
         bool first_tile = true;
@@ -620,7 +649,7 @@ __global__ void __launch_bounds__(64 + 32 * LoopCfg<MODE>::EPI_WARPS, 1) markov_
             const int s0 = stage;
             for (; kb < nd; ++kb) {
               if (!tc::mbar_wait(&ctl->empty[stage], phase ^ 1, abort)) { ok = false; break; }
-              tc::mbar_expect_tx(&ctl->full[stage], STAGE_BYTES);
+              tc::mbar_expect_tx(&ctl->full[stage], FULL_BYTES);
               tc::tma_load_2d(sB + stage * B_BYTES, &tma_b, kb * BK, n_blk * BN, &ctl->full[stage],
                               pol_b);
               issued[stage] = (int)phase;
@@ -630,18 +659,33 @@ __global__ void __launch_bounds__(64 + 32 * LoopCfg<MODE>::EPI_WARPS, 1) markov_
             // every armed stage completes before the CTA exits
             if (ok && !tc::mbar_wait(&ctl->go, (uint32_t)((k - 1) & 1), abort)) ok = false;
             fence_proxy_async_global();
-            for (int j = 0, s = s0; j < kb; ++j) {
-              tc::tma_load_2d(sA + s * A_BYTES, &tma_a, j * BK, m_blk * BM, &ctl->full[s], pol_a);
-              if (++s == STAGES) s = 0;
+            if (ERES) {
+              // the step's E tile, resident for all of the step's tiles (the
+              // previous step's MMAs have all completed: the grid barrier
+              // behind go came after every accumulator was consumed)
+              if (ok) {
+                tc::mbar_expect_tx(&ctl->efull, (uint32_t)(k_iters * A_BYTES));
+                for (int j = 0; j < k_iters; ++j)
+                  tc::tma_load_2d(sA + j * A_BYTES, &tma_a, j * BK, m_blk * BM, &ctl->efull,
+                                  pol_a);
+                e_issued = (k - 1) & 1;
+              }
+            } else {
+              for (int j = 0, s = s0; j < kb; ++j) {
+                tc::tma_load_2d(sA + s * A_BYTES, &tma_a, j * BK, m_blk * BM, &ctl->full[s],
+                                pol_a);
+                if (++s == STAGES) s = 0;
+              }
             }
             if (!ok) break;
           }
           first_tile = false;
           for (; kb < k_iters; ++kb) {
             if (!tc::mbar_wait(&ctl->empty[stage], phase ^ 1, abort)) { ok = false; break; }
-            tc::mbar_expect_tx(&ctl->full[stage], STAGE_BYTES);
-            tc::tma_load_2d(sA + stage * A_BYTES, &tma_a, kb * BK, m_blk * BM, &ctl->full[stage],
-                            pol_a);
+            tc::mbar_expect_tx(&ctl->full[stage], FULL_BYTES);
+            if (!ERES)
+              tc::tma_load_2d(sA + stage * A_BYTES, &tma_a, kb * BK, m_blk * BM,
+                              &ctl->full[stage], pol_a);
             tc::tma_load_2d(sB + stage * B_BYTES, &tma_b, kb * BK, n_blk * BN, &ctl->full[stage],
                             pol_b);
             issued[stage] = (int)phase;
@@ -653,6 +697,7 @@ __global__ void __launch_bounds__(64 + 32 * LoopCfg<MODE>::EPI_WARPS, 1) markov_
       volatile int never = 0;
       for (int s = 0; s < STAGES; ++s)
         if (issued[s] >= 0) tc::mbar_wait(&ctl->full[s], (uint32_t)issued[s], &never);
+      if (ERES && e_issued >= 0) tc::mbar_wait(&ctl->efull, (uint32_t)e_issued, &never);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -665,6 +710,10 @@ __global__ void __launch_bounds__(64 + 32 * LoopCfg<MODE>::EPI_WARPS, 1) markov_
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int k = 1; ok && k <= gamma; ++k) {
+        if (ERES) {  // the step's resident E tile
+          if (!tc::mbar_wait(&ctl->efull, (uint32_t)((k - 1) & 1), abort)) { ok = false; break; }
+          tc::fence_after_sync();
+        }
         for (int tile = first; ok && tile < num_tiles; tile += stride) {
           if (!tc::mbar_wait(&ctl->tempty[acc], acc_phase ^ 1, abort)) { ok = false; break; }
           tc::fence_after_sync();
@@ -672,7 +721,8 @@ __global__ void __launch_bounds__(64 + 32 * LoopCfg<MODE>::EPI_WARPS, 1) markov_
           for (int kb = 0; kb < k_iters; ++kb) {
             if (!tc::mbar_wait(&ctl->full[stage], phase, abort)) { ok = false; break; }
             tc::fence_after_sync();
-            const uint64_t a_desc = tc::smem_desc_sw128(sA + stage * A_BYTES);
+            const uint64_t a_desc =
+                tc::smem_desc_sw128(sA + (ERES ? kb : stage) * A_BYTES);
             const uint64_t b_desc = tc::smem_desc_sw128(sB + stage * B_BYTES);
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk)
@@ -837,11 +887,9 @@ __global__ void __launch_bounds__(64 + 32 * LoopCfg<MODE>::EPI_WARPS, 1) markov_
   }
 }
 
-template <int MODE, int RW>
+template <int MODE, int RW, bool ERES>
 constexpr size_t loop_smem_bytes() {
-  using G = gemm::Geo<LoopCfg<MODE>::BN>;
-  return 1024 + (size_t)G::STAGES * G::STAGE_BYTES + 512 +
-         sizeof(RowScratch<RW>) * (LoopCfg<MODE>::EPI_WARPS / RW);
+  return LoopSmem<MODE, RW, ERES>::BYTES;
 }
 
 // Grid of the loop: at most one CTA per SM, a multiple of the M-block count
@@ -874,10 +922,10 @@ inline size_t loop_slots_max(int V) {
   return g > t ? g : t;
 }
 
-template <int MODE, int RW>
+template <int MODE, int RW, bool ERES = false>
 int launch_loop(const LoopArgs &args, int grid, cudaStream_t stream) {
-  auto kernel = markov_loop_kernel<MODE, RW>;
-  constexpr size_t smem = loop_smem_bytes<MODE, RW>();
+  auto kernel = markov_loop_kernel<MODE, RW, ERES>;
+  constexpr size_t smem = loop_smem_bytes<MODE, RW, ERES>();
   static_assert(smem <= gemm::SMEM_LIMIT, "shared memory of the loop kernel");
   CUtensorMap ta, tb;
   if (dspark_make_tmap_bf16(&ta, args.E, (uint64_t)args.R, (uint64_t)args.r, BM) != 0)

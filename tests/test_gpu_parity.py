@@ -444,6 +444,22 @@ def test_markov_draft_row_groups(R):
     assert dsp.dspark_device_status() == 0
 
 
+@pytest.mark.parametrize("shape,tau", [((600, 3, 1000, 512, 64), 0.0),
+                                       ((1100, 2, 20000, 256, 64), 0.0),
+                                       ((1100, 2, 20000, 256, 64), 1.0)])
+def test_markov_draft_with_resident_e(shape, tau):
+    """Batches of four or more row blocks keep each CTA's E tile in shared memory
+    for the step (5 row blocks on 20 CTAs at r = 512, 9 on 144 CTAs at r = 256;
+    sampling with more than three requests per CTA)."""
+    rnd, orc = _draft_case(shape, tau, seed=295)
+    rep = compare_draft(rnd.tokens, rnd.conf, rnd.lse_d if tau > 0 else None,
+                        rnd.logp_d if tau > 0 else None, orc, tau, tol_rel=TOL_DRAFT)
+    print(f"{shape}: {rep.flagged} of {rep.compared} in the tie band")
+    assert rep.compared >= shape[0]
+    assert rep.flagged <= flag_budget(rep.compared)
+    assert dsp.dspark_device_status() == 0
+
+
 @pytest.mark.parametrize("shape,tau", [((3, 32, 520, 64, 64), 0.0), ((3, 32, 520, 64, 64), 1.0),
                                        ((37, 4, 1000, 128, 320), 0.05),
                                        ((37, 4, 1000, 128, 320), 4.0)])
