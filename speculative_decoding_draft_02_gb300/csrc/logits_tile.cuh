@@ -404,27 +404,53 @@ __device__ void block_logits(const bf16 *__restrict__ base_row, const bf16 *__re
   __syncthreads();
 }
 
-// Inside block b: the id with the largest score[j] + Gumbel(id, stream) (lowest
-// id on ties) among the ids with a finite score.  Called by one whole warp;
-// every lane gets the id (-1 when no id qualifies).  score is in shared memory.
-__device__ __forceinline__ int block_pick(const float *score, int b, int V, uint64_t seed,
-                                          uint32_t pos, uint32_t req, uint32_t stream) {
+// The Gumbels of block b's ids on `stream`: lane l < 16 holds those of ids
+// b * 64 + 4 l + t (t = 0..3).  They depend on no score, so a caller can draw
+// them while the scores are still being computed.
+struct BlockGumbels {
+  float g[4];
+};
+__device__ __forceinline__ BlockGumbels block_gumbels(int b, uint64_t seed, uint32_t pos,
+                                                      uint32_t req, uint32_t stream) {
+  const int lane = threadIdx.x & 31;
+  BlockGumbels out = {{0.f, 0.f, 0.f, 0.f}};
+  if (lane < GUMBEL_BLOCK / 4) {
+    const int v0 = b * GUMBEL_BLOCK + 4 * lane;
+    const uint4 w = rng_words4(seed, (uint32_t)(v0 >> 2), pos, req, stream);
+    out.g[0] = rng_gumbel(w.x);
+    out.g[1] = rng_gumbel(w.y);
+    out.g[2] = rng_gumbel(w.z);
+    out.g[3] = rng_gumbel(w.w);
+  }
+  return out;
+}
+
+// Inside block b: the id with the largest score[j] + Gumbel(id) (lowest id on
+// ties) among the ids with a finite score, given the block's Gumbels.  Called
+// by one whole warp; every lane gets the id (-1 when no id qualifies).  score
+// is in shared memory.
+__device__ __forceinline__ int block_pick(const float *score, int b, int V,
+                                          const BlockGumbels &gb) {
   const int lane = threadIdx.x & 31;
   float best = -INFINITY, d0 = 0.f, d1 = 0.f, d2 = 0.f;
   int idx = 0x7fffffff;
   if (lane < GUMBEL_BLOCK / 4) {
     const int v0 = b * GUMBEL_BLOCK + 4 * lane;
-    const uint4 w = rng_words4(seed, (uint32_t)(v0 >> 2), pos, req, stream);
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       const float sc = score[4 * lane + t];
       if (v0 + t < V && sc > -INFINITY) {
-        const float e = sc + rng_gumbel(ws[t]);
+        const float e = sc + gb.g[t];
         if (better(e, v0 + t, best, idx)) { best = e; idx = v0 + t; }
       }
     }
   }
   warp_merge(d0, d1, best, idx, d2);
   return best > -INFINITY ? idx : -1;
+}
+
+// The same draw with the Gumbels taken on `stream` here.
+__device__ __forceinline__ int block_pick(const float *score, int b, int V, uint64_t seed,
+                                          uint32_t pos, uint32_t req, uint32_t stream) {
+  return block_pick(score, b, V, block_gumbels(b, seed, pos, req, stream));
 }

@@ -297,12 +297,13 @@ __device__ __forceinline__ void tile_slice(const LoopArgs &a, int k, int i, bool
   }
 }
 
-// Logits of sampler block b, rebuilt by the RW warps of a row group:
-// out[j] = base_row[v] + E_row . W2t[v] for v = b * 64 + j (-inf past V).
-template <int RW>
-__device__ __forceinline__ void rebuild_block(const bf16 *__restrict__ base_row, const bf16 *E_row,
-                                              const bf16 *__restrict__ W2t, int b, int V, int r,
-                                              float *out, int wg, int lane) {
+// Markov bias of sampler block b, rebuilt by the RW warps of a row group:
+// out[j] = E_row . W2t[v] for v = b * 64 + j (-inf past V).  Every lane runs
+// hook() once, after its first W2t words are requested, to fill their latency.
+template <int RW, class Hook>
+__device__ __forceinline__ void rebuild_bias(const bf16 *E_row, const bf16 *__restrict__ W2t,
+                                             int b, int V, int r, float *out, int wg, int lane,
+                                             Hook hook) {
   // warp wg takes ids wg, wg + RW, wg + 2 RW, ... (RW need not divide 64), four
   // at a time: each lane has their W2t words of two passes in flight
   constexpr int CHK = 4;
@@ -332,17 +333,18 @@ __device__ __forceinline__ void rebuild_block(const bf16 *__restrict__ base_row,
         w0[u] = ok ? __ldg(rowp + c) : make_uint4(0, 0, 0, 0);
         w1[u] = (ok && two) ? __ldg(rowp + c + 32) : make_uint4(0, 0, 0, 0);
       }
+      if (t0 == 0 && c == lane) hook();
 #pragma unroll
       for (int u = 0; u < CHK; ++u) acc[u] = dot8_bf16(a1, w1[u], dot8_bf16(a0, w0[u], acc[u]));
     }
+    if (t0 == 0 && lane >= r8) hook();  // lanes that had no words to load
 #pragma unroll
     for (int u = 0; u < CHK; ++u) acc[u] = warp_sum(acc[u]);
     if (lane == 0) {
 #pragma unroll
       for (int u = 0; u < CHK; ++u) {
         const int v = b * GUMBEL_BLOCK + ids[u];
-        if (ids[u] < GUMBEL_BLOCK)
-          out[ids[u]] = v < V ? __bfloat162float(base_row[v]) + acc[u] : -INFINITY;
+        if (ids[u] < GUMBEL_BLOCK) out[ids[u]] = v < V ? acc[u] : -INFINITY;
       }
     }
   }
@@ -501,12 +503,26 @@ __device__ void row_phase(const LoopArgs &a, int k, Scratch<MODE, RW> &S, int g,
         const int nv = V - b * GUMBEL_BLOCK < GUMBEL_BLOCK ? V - b * GUMBEL_BLOCK : GUMBEL_BLOCK;
         bulk_prefetch_l2(a.W2t + (size_t)b * GUMBEL_BLOCK * r, (uint32_t)(nv * r) * 2u);
       }
-      rebuild_block<RW>(a.base + o * V, a.E + (size_t)i * r, a.W2t, b, V, r, S.score, wg, lane);
+      // warp 0 loads the block's base logits and draws its Gumbels while the
+      // group's first W2t words are on their way
+      const int v_lo = b * GUMBEL_BLOCK + lane, v_hi = v_lo + 32;
+      float base_lo = 0.f, base_hi = 0.f;
+      if (wg == 0) {
+        const bf16 *base_row = a.base + o * V;
+        if (v_lo < V) base_lo = __bfloat162float(__ldg(base_row + v_lo));
+        if (v_hi < V) base_hi = __bfloat162float(__ldg(base_row + v_hi));
+      }
+      BlockGumbels gum = {{0.f, 0.f, 0.f, 0.f}};
+      rebuild_bias<RW>(a.E + (size_t)i * r, a.W2t, b, V, r, S.score, wg, lane, [&]() {
+        if (wg == 0) gum = block_gumbels(b, a.seed, (uint32_t)k, (uint32_t)i, RNG_DRAFT);
+      });
       group_sync();
       if (wg == 0) {
-        for (int j = lane; j < GUMBEL_BLOCK; j += 32) S.score[j] *= a.inv_tau;
+        // the block's logits over tau: (Markov bias + base logit) / tau
+        S.score[lane] = v_lo < V ? (S.score[lane] + base_lo) * a.inv_tau : -INFINITY;
+        S.score[lane + 32] = v_hi < V ? (S.score[lane + 32] + base_hi) * a.inv_tau : -INFINITY;
         __syncwarp();
-        int t = block_pick(S.score, b, V, a.seed, (uint32_t)k, (uint32_t)i, RNG_DRAFT);
+        int t = block_pick(S.score, b, V, gum);
         if (t < 0) {
           if (lane == 0) dspark_set_status(DSPARK_ERR_TOKEN);
           t = b * GUMBEL_BLOCK;
