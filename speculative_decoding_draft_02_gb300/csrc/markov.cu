@@ -206,7 +206,8 @@ __global__ void __launch_bounds__(RP_THREADS) reduce_prep(
   }
 }
 
-// Row blocks (of 128 requests) from which the greedy loop keeps E resident.
+// Row blocks (of 128 requests) from which the loop keeps E resident (sampling
+// also at a single row block).
 constexpr int ERES_MIN_ROW_BLOCKS = 4;
 
 struct MarkovWs {
@@ -271,9 +272,14 @@ extern "C" int dspark_markov_draft(const dspark_dims *dims, const void *base_log
     const mloop::LoopGrid lg = mloop::loop_grid<MODE_SAMPLE>(R, V, sms);
     la.n_slots = lg.n_slots;
     const int num_m = (R + gemm::BM - 1) / gemm::BM;
-    if (num_m >= ERES_MIN_ROW_BLOCKS && lg.grid >= num_m && lg.grid % num_m == 0 &&
-        r <= mloop::ERES_KB * gemm::BK && R > lg.grid * (EW / 4))
+    const bool eres = lg.grid >= num_m && lg.grid % num_m == 0 && r <= mloop::ERES_KB * gemm::BK;
+    if (eres && num_m >= ERES_MIN_ROW_BLOCKS && R > lg.grid * (EW / 4))
       return mloop::launch_loop<MODE_SAMPLE, 2, true>(la, lg.grid, stream);
+    // resident E at one row block as well (four W2t stages): every CTA would
+    // otherwise re-read the same E tile from L2 for each of its tiles (R = 64,
+    // V = 151936: 273-275 against 284-286 us for 8 steps; at two row blocks,
+    // R = 256, it measured 276-279 against 274-275 us, so it stays off there)
+    if (eres && num_m == 1) return mloop::launch_loop<MODE_SAMPLE, EW, true>(la, lg.grid, stream);
     // warps per request in the row phase: as many as still cover R in one pass
     if (R <= lg.grid) return mloop::launch_loop<MODE_SAMPLE, EW>(la, lg.grid, stream);
     if (R <= lg.grid * 2) return mloop::launch_loop<MODE_SAMPLE, EW / 2>(la, lg.grid, stream);

@@ -112,12 +112,22 @@ struct RowScratch {
 template <int MODE, int RW>
 using Scratch = RowScratch<RW, MODE == MODE_SAMPLE ? GUMBEL_BLOCK : 1>;
 
-// Resident-E form of the loop (many row blocks): each CTA keeps its row block's
-// E (r / 64 k blocks of 128 x 64, up to r = 512) in shared memory for the whole
-// step, and only W2t streams through a ring of ERES_STAGES stages.  A greedy
-// 128 x 256 tile then moves 256 KB from L2 instead of 384 KB.
+// Resident-E form of the loop: each CTA keeps its row block's E (r / 64 k
+// blocks of 128 x 64, up to r = 512) in shared memory for the whole step, and
+// only W2t streams through a ring of eres_stages() stages: four where they fit
+// beside E and the row groups' scratch (sampling from four-warp groups up),
+// else three.  A greedy 128 x 256 tile then moves 256 KB from L2 instead of
+// 384 KB, a sampling 128 x 192 tile 192 KB instead of 320 KB.
 constexpr int ERES_KB = 8;
-constexpr int ERES_STAGES = 3;
+template <int MODE, int RW>
+constexpr int eres_stages() {
+  return 1024 + (size_t)ERES_KB * A_BYTES + 512 +
+                     sizeof(Scratch<MODE, RW>) * (LoopCfg<MODE>::EPI_WARPS / RW) +
+                     4 * (size_t)gemm::Geo<LoopCfg<MODE>::BN>::B_BYTES <=
+                 gemm::SMEM_LIMIT
+             ? 4
+             : 3;
+}
 
 // Bring `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2.
 __device__ __forceinline__ void bulk_prefetch_l2(const void *p, uint32_t bytes) {
@@ -572,7 +582,7 @@ __device__ void prologue_rows(const LoopArgs &a, Scr &S, int g, int wg, int lane
 template <int MODE, int RW, bool ERES>
 struct LoopSmem {
   using G = gemm::Geo<LoopCfg<MODE>::BN>;
-  static constexpr int NSTAGE = ERES ? ERES_STAGES : G::STAGES;
+  static constexpr int NSTAGE = ERES ? eres_stages<MODE, RW>() : G::STAGES;
   static constexpr size_t A_REGION = (size_t)(ERES ? ERES_KB : NSTAGE) * A_BYTES;
   static constexpr size_t B_REGION = (size_t)NSTAGE * G::B_BYTES;
   static constexpr size_t CTL = A_REGION + B_REGION;
