@@ -170,8 +170,8 @@ class ClockSampler:
 
 
 # Sources that define the LM-head kernel; a profile taken on other sources is stale.
-LM_HEAD_SOURCES = ["lm_head.cu", "umma_gemm_pair.cuh", "umma_gemm.cuh", "tcgen05.cuh",
-                   "common.cuh"]
+LM_HEAD_SOURCES = ["lm_head.cu", "umma_gemm_pair.cuh", "umma_gemm.cuh", "umma_skinny.cuh",
+                   "tcgen05.cuh", "common.cuh"]
 
 
 def kernel_source_hash(names):

@@ -11,6 +11,8 @@
 
 DSPARK_DECLARE_STATUS(s_status_lmhead)
 
+#include "umma_skinny.cuh"
+
 namespace {
 
 __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi) {
@@ -122,7 +124,15 @@ int dspark_lm_head_tc(const dspark_dims *dims, const void *h, const void *W_lm,
   // of the bf16 peak against 86% for the single-CTA kernel; at 512 rows
   // (V = 151936, d = 4096) 0.383 against 0.425 ms.  Below four row blocks a
   // pair would leave up to a quarter of its rows empty.
+  // Up to 16 rows, the swapped product: W_lm is the 128-row operand and h the
+  // 16-column one, so the ring holds twelve stages of W_lm instead of four
+  // 128 x 256 tiles beside a mostly empty 128-row tile of h.  V = 151936,
+  // d = 2560: 8 rows 132 against 165 us (0.87 against 0.69 of the copy
+  // peak), 16 rows 133 against 154 us; at 32 rows the 32-column form took
+  // 131 against 126 us, so from 17 rows on the row-tiled kernel stays.
   const int num_m = (epi.M + gemm::BM - 1) / gemm::BM;
+  if (epi.M <= 16)
+    return gemm::launch_skinny<16>(h, W_lm, epi.M, epi.N, dims->d, epi.C, stream);
   if (num_m >= 4) return gemm::launch_pair<4>(h, W_lm, epi.M, epi.N, dims->d, epi, stream);
   return gemm::launch<4, 256>(h, W_lm, epi.M, epi.N, dims->d, epi, stream);
 }
