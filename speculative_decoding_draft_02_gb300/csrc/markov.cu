@@ -272,14 +272,17 @@ extern "C" int dspark_markov_draft(const dspark_dims *dims, const void *base_log
     const mloop::LoopGrid lg = mloop::loop_grid<MODE_SAMPLE>(R, V, sms);
     la.n_slots = lg.n_slots;
     const int num_m = (R + gemm::BM - 1) / gemm::BM;
-    const bool eres = lg.grid >= num_m && lg.grid % num_m == 0 && r <= mloop::ERES_KB * gemm::BK;
+    const bool eres = lg.grid >= num_m && lg.grid % num_m == 0 && r <= 8 * gemm::BK;
     if (eres && num_m >= ERES_MIN_ROW_BLOCKS && R > lg.grid * (EW / 4))
-      return mloop::launch_loop<MODE_SAMPLE, 2, true>(la, lg.grid, stream);
-    // resident E at one row block as well (four W2t stages): every CTA would
-    // otherwise re-read the same E tile from L2 for each of its tiles (R = 64,
-    // V = 151936: 273-275 against 284-286 us for 8 steps; at two row blocks,
-    // R = 256, it measured 276-279 against 274-275 us, so it stays off there)
-    if (eres && num_m == 1) return mloop::launch_loop<MODE_SAMPLE, EW, true>(la, lg.grid, stream);
+      return mloop::launch_loop<MODE_SAMPLE, 2, 8>(la, lg.grid, stream);
+    // resident E at one row block as well: every CTA would otherwise re-read
+    // the same E tile from L2 for each of its tiles (R = 64, V = 151936, four
+    // W2t stages: 273-275 against 284-286 us for 8 steps; at two row blocks,
+    // R = 256, it measured 276-279 against 274-275 us, so it stays off there).
+    // With r <= 256 E takes half the room, and six W2t stages fit.
+    if (eres && num_m == 1)
+      return r <= 4 * gemm::BK ? mloop::launch_loop<MODE_SAMPLE, EW, 4>(la, lg.grid, stream)
+                               : mloop::launch_loop<MODE_SAMPLE, EW, 8>(la, lg.grid, stream);
     // warps per request in the row phase: as many as still cover R in one pass
     if (R <= lg.grid) return mloop::launch_loop<MODE_SAMPLE, EW>(la, lg.grid, stream);
     if (R <= lg.grid * 2) return mloop::launch_loop<MODE_SAMPLE, EW / 2>(la, lg.grid, stream);
@@ -295,9 +298,12 @@ extern "C" int dspark_markov_draft(const dspark_dims *dims, const void *base_log
   // (at four row blocks or more R exceeds two requests per CTA, so the row
   // phase takes one warp per request)
   const int num_m = (R + gemm::BM - 1) / gemm::BM;
-  if (num_m >= ERES_MIN_ROW_BLOCKS && lg.grid >= num_m && lg.grid % num_m == 0 &&
-      r <= mloop::ERES_KB * gemm::BK)
-    return mloop::launch_loop<MODE_GREEDY, 1, true>(la, lg.grid, stream);
+  const bool eres = lg.grid >= num_m && lg.grid % num_m == 0 && r <= 8 * gemm::BK;
+  if (eres && num_m >= ERES_MIN_ROW_BLOCKS)
+    return mloop::launch_loop<MODE_GREEDY, 1, 8>(la, lg.grid, stream);
+  // one row block with r <= 256: E (64 KB) resident beside five W2t stages
+  if (eres && num_m == 1 && r <= 4 * gemm::BK && R <= lg.grid * (EW / 4))
+    return mloop::launch_loop<MODE_GREEDY, 4, 4>(la, lg.grid, stream);
   if (R <= lg.grid * (EW / 4)) return mloop::launch_loop<MODE_GREEDY, 4>(la, lg.grid, stream);
   return mloop::launch_loop<MODE_GREEDY, 1>(la, lg.grid, stream);
 }

@@ -112,21 +112,19 @@ struct RowScratch {
 template <int MODE, int RW>
 using Scratch = RowScratch<RW, MODE == MODE_SAMPLE ? GUMBEL_BLOCK : 1>;
 
-// Resident-E form of the loop: each CTA keeps its row block's E (r / 64 k
-// blocks of 128 x 64, up to r = 512) in shared memory for the whole step, and
-// only W2t streams through a ring of eres_stages() stages: four where they fit
-// beside E and the row groups' scratch (sampling from four-warp groups up),
-// else three.  A greedy 128 x 256 tile then moves 256 KB from L2 instead of
-// 384 KB, a sampling 128 x 192 tile 192 KB instead of 320 KB.
-constexpr int ERES_KB = 8;
-template <int MODE, int RW>
+// Resident-E form of the loop (EKB > 0): each CTA keeps its row block's E (up
+// to EKB k blocks of 128 x 64: r <= 64 EKB, EKB = 4 or 8) in shared memory for
+// the whole step, and only W2t streams through a ring of eres_stages() stages,
+// as many as fit beside E and the row groups' scratch (up to six, at least
+// three).  A greedy 128 x 256 tile then moves 256 KB from L2 instead of 384 KB
+// (r = 512), a sampling 128 x 192 tile 192 KB instead of 320 KB.
+template <int MODE, int RW, int EKB>
 constexpr int eres_stages() {
-  return 1024 + (size_t)ERES_KB * A_BYTES + 512 +
-                     sizeof(Scratch<MODE, RW>) * (LoopCfg<MODE>::EPI_WARPS / RW) +
-                     4 * (size_t)gemm::Geo<LoopCfg<MODE>::BN>::B_BYTES <=
-                 gemm::SMEM_LIMIT
-             ? 4
-             : 3;
+  constexpr size_t fixed = 1024 + (size_t)EKB * A_BYTES + 512 +
+                           sizeof(Scratch<MODE, RW>) * (LoopCfg<MODE>::EPI_WARPS / RW);
+  constexpr size_t n = (gemm::SMEM_LIMIT - fixed) / gemm::Geo<LoopCfg<MODE>::BN>::B_BYTES;
+  static_assert(n >= 3, "resident E leaves room for three W2t stages");
+  return n > 6 ? 6 : (int)n;
 }
 
 // Bring `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2.
@@ -579,27 +577,28 @@ __device__ void prologue_rows(const LoopArgs &a, Scr &S, int g, int wg, int lane
 
 // Shared-memory geometry of a loop kernel: the A region (ring stages, or the
 // resident E), the W2t stages, then the barriers and the row groups' scratch.
-template <int MODE, int RW, bool ERES>
+template <int MODE, int RW, int EKB>
 struct LoopSmem {
   using G = gemm::Geo<LoopCfg<MODE>::BN>;
-  static constexpr int NSTAGE = ERES ? eres_stages<MODE, RW>() : G::STAGES;
-  static constexpr size_t A_REGION = (size_t)(ERES ? ERES_KB : NSTAGE) * A_BYTES;
+  static constexpr int NSTAGE = EKB ? eres_stages<MODE, RW, EKB>() : G::STAGES;
+  static constexpr size_t A_REGION = (size_t)(EKB ? EKB : NSTAGE) * A_BYTES;
   static constexpr size_t B_REGION = (size_t)NSTAGE * G::B_BYTES;
   static constexpr size_t CTL = A_REGION + B_REGION;
   static constexpr size_t BYTES = 1024 + CTL + 512 +
                                   sizeof(Scratch<MODE, RW>) * (LoopCfg<MODE>::EPI_WARPS / RW);
 };
 
-template <int MODE, int RW, bool ERES>
+template <int MODE, int RW, int EKB>
 __global__ void __launch_bounds__(64 + 32 * LoopCfg<MODE>::EPI_WARPS, 1) markov_loop_kernel(const __grid_constant__ CUtensorMap tma_a,
                        const __grid_constant__ CUtensorMap tma_b, const __grid_constant__ LoopArgs a) {
+  constexpr bool ERES = EKB > 0;  // E resident for the step
   constexpr int EPI_WARPS = LoopCfg<MODE>::EPI_WARPS;
   constexpr int EPI_THREADS = 32 * EPI_WARPS;
   constexpr int CG = EPI_WARPS / 4;  // column groups: threads per row in a tile
   constexpr int SLICE = LoopCfg<MODE>::SLICE;
   constexpr int RG = EPI_WARPS / RW;  // row groups per CTA
   using G = gemm::Geo<LoopCfg<MODE>::BN>;
-  using L = LoopSmem<MODE, RW, ERES>;
+  using L = LoopSmem<MODE, RW, EKB>;
   constexpr int BN = G::BN, STAGES = L::NSTAGE, B_BYTES = G::B_BYTES;
   constexpr int STAGE_BYTES = G::STAGE_BYTES;
   constexpr uint32_t TMEM_COLS = G::TMEM_COLS;
@@ -913,9 +912,9 @@ __global__ void __launch_bounds__(64 + 32 * LoopCfg<MODE>::EPI_WARPS, 1) markov_
   }
 }
 
-template <int MODE, int RW, bool ERES>
+template <int MODE, int RW, int EKB>
 constexpr size_t loop_smem_bytes() {
-  return LoopSmem<MODE, RW, ERES>::BYTES;
+  return LoopSmem<MODE, RW, EKB>::BYTES;
 }
 
 // Grid of the loop: at most one CTA per SM, a multiple of the M-block count
@@ -948,10 +947,12 @@ inline size_t loop_slots_max(int V) {
   return g > t ? g : t;
 }
 
-template <int MODE, int RW, bool ERES = false>
+// EKB: 0 (E streamed with W2t) or the k blocks of E kept resident (4 or 8,
+// r <= 64 EKB).
+template <int MODE, int RW, int EKB = 0>
 int launch_loop(const LoopArgs &args, int grid, cudaStream_t stream) {
-  auto kernel = markov_loop_kernel<MODE, RW, ERES>;
-  constexpr size_t smem = loop_smem_bytes<MODE, RW, ERES>();
+  auto kernel = markov_loop_kernel<MODE, RW, EKB>;
+  constexpr size_t smem = loop_smem_bytes<MODE, RW, EKB>();
   static_assert(smem <= gemm::SMEM_LIMIT, "shared memory of the loop kernel");
   CUtensorMap ta, tb;
   if (dspark_make_tmap_bf16(&ta, args.E, (uint64_t)args.R, (uint64_t)args.r, BM) != 0)

@@ -446,11 +446,14 @@ def test_markov_draft_row_groups(R):
 
 @pytest.mark.parametrize("shape,tau", [((600, 3, 1000, 512, 64), 0.0),
                                        ((1100, 2, 20000, 256, 64), 0.0),
-                                       ((1100, 2, 20000, 256, 64), 1.0)])
+                                       ((1100, 2, 20000, 256, 64), 1.0),
+                                       ((90, 3, 20000, 512, 64), 1.0)])
 def test_markov_draft_with_resident_e(shape, tau):
     """Batches of four or more row blocks keep each CTA's E tile in shared memory
     for the step (5 row blocks on 20 CTAs at r = 512, 9 on 144 CTAs at r = 256;
-    sampling with more than three requests per CTA)."""
+    sampling with more than three requests per CTA).  Sampling at one row block
+    keeps it too: eight k blocks of E at r = 512 here (four at r <= 256 in the
+    small sampled cases of test_markov_draft_matches_oracle)."""
     rnd, orc = _draft_case(shape, tau, seed=295)
     rep = compare_draft(rnd.tokens, rnd.conf, rnd.lse_d if tau > 0 else None,
                         rnd.logp_d if tau > 0 else None, orc, tau, tol_rel=TOL_DRAFT)
