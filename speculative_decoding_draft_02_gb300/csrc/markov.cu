@@ -206,8 +206,8 @@ __global__ void __launch_bounds__(RP_THREADS) reduce_prep(
   }
 }
 
-// Row blocks (of 128 requests) from which the loop keeps E resident (sampling
-// also at a single row block).
+// Row blocks (of 128 requests) from which the loop keeps E resident; it does at
+// a single row block too (sampling, and greedy with r <= 256).
 constexpr int ERES_MIN_ROW_BLOCKS = 4;
 
 struct MarkovWs {
