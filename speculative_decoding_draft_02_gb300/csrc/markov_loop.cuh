@@ -954,6 +954,7 @@ int launch_loop(const LoopArgs &args, int grid, cudaStream_t stream) {
   auto kernel = markov_loop_kernel<MODE, RW, EKB>;
   constexpr size_t smem = loop_smem_bytes<MODE, RW, EKB>();
   static_assert(smem <= gemm::SMEM_LIMIT, "shared memory of the loop kernel");
+  if (EKB && args.r > EKB * BK) return DSPARK_ERR_ARG;  // E must fit its resident room
   CUtensorMap ta, tb;
   if (dspark_make_tmap_bf16(&ta, args.E, (uint64_t)args.R, (uint64_t)args.r, BM) != 0)
     return DSPARK_ERR_CUDA;
