@@ -51,9 +51,11 @@ def _weights(R, G, V, r, d, seed):
 
 # ------------------------------------------------------------------ a1 ----
 
-# the last shapes have 17 and 5 row blocks of 128: the CTA-pair LM head (an odd
-# count leaves the last pair's second half empty)
-@pytest.mark.parametrize("shape", SHAPES + [(520, 4, 1000, 64, 128), (160, 4, 1000, 64, 128)])
+# 17 and 5 row blocks of 128: the CTA-pair LM head (an odd count leaves the
+# last pair's second half empty); 16 and 17 rows: the last size of the swapped-
+# operand kernel and the first of the row-tiled one
+@pytest.mark.parametrize("shape", SHAPES + [(520, 4, 1000, 64, 128), (160, 4, 1000, 64, 128),
+                                            (4, 4, 4104, 64, 128), (17, 1, 4104, 64, 128)])
 def test_lm_head_matches_oracle(shape):
     R, G, V, r, d = shape
     inp = _weights(R, G, V, r, d, seed=100 + V)
