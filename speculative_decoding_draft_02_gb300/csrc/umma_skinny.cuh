@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
-// C [M, V] (bf16, row-major) = X [M, K] . W [V, K]^T for 1 <= M <= NS, K a
+// C [M, V] (bf16, row-major) = X [M, K] . W [V, K]^T for 1 <= M <= 32, K a
 // multiple of 64; X, W and C 16-byte aligned.
 template <int NS>
 int launch_skinny(const void *X, const void *W, int M, int V, int K, bf16 *C,
